@@ -5,4 +5,4 @@ sm_103a); :mod:`attention_group_quantized_gb300.kvq` is its thin Python
 binding.  Importing this package does not load the library; the binding
 loads it on first use and raises if it is missing.
 """
-__all__ = ["kvq", "workloads"]
+__all__ = ["kvq"]

@@ -1,0 +1,221 @@
+// kvq_api.cu -- the C ABI of libkvq: argument validation, cache layout,
+// tensor-map encoding and dispatch to the kernels.  Nothing here allocates
+// device memory or synchronises; every launch goes to the caller's stream.
+#include <cstring>
+#include <cudaTypedefs.h>
+#include <mutex>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+
+CUresult encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                              uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes, uint32_t box0,
+                              uint32_t box1, CUtensorMapSwizzle swizzle) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (g_encode == nullptr) return CUDA_ERROR_NOT_FOUND;
+  const cuuint64_t dims[2] = {dim0, dim1};
+  const cuuint64_t strides[1] = {stride1_bytes};
+  const cuuint32_t box[2] = {box0, box1};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+static bool shape_ok(const kvq_cache& c) {
+  return c.B > 0 && c.Hkv > 0 && c.Hkv <= KVQ_MAX_HKV && c.Tcap > 0 && c.Tcap % KVQ_TILE_TOKENS == 0 &&
+         (c.D == 64 || c.D == 128) && c.head_bits != nullptr;
+}
+
+bool resolve_layout(const kvq_cache& c, HeadLayout* out) {
+  memset(out, 0, sizeof(*out));
+  if (!shape_ok(c)) return false;
+  const int64_t per_tok_base = static_cast<int64_t>(c.B) * c.Tcap;
+  int64_t off = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    const int want = pass == 0 ? 8 : 4;
+    if (pass == 1) out->off4 = off;
+    int idx = 0;
+    for (int h = 0; h < c.Hkv; ++h) {
+      const int b = c.head_bits[h];
+      if (b != 4 && b != 8) return false;
+      if (b != want) continue;
+      out->bits[h] = static_cast<int8_t>(b);
+      out->plane_idx[h] = idx++;
+      out->plane_off[h] = off;
+      off += per_tok_base * (c.D * b / 8);
+    }
+    (pass == 0 ? out->n8 : out->n4) = idx;
+  }
+  return true;
+}
+
+static int64_t codes_bytes(const kvq_cache& c) {
+  HeadLayout hl;
+  if (!resolve_layout(c, &hl)) return -1;
+  return hl.off4 + static_cast<int64_t>(hl.n4) * c.B * c.Tcap * (c.D / 2);
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" {
+
+int64_t kvq_cache_codes_bytes(const kvq_cache* cache) {
+  if (cache == nullptr) return -1;
+  return codes_bytes(*cache);
+}
+
+int64_t kvq_cache_sz_bytes(const kvq_cache* cache) {
+  if (cache == nullptr || !shape_ok(*cache)) return -1;
+  return static_cast<int64_t>(cache->Hkv) * cache->B * cache->Tcap * (cache->D / KVQ_GROUP) * 4;
+}
+
+int64_t kvq_cache_head_offset(const kvq_cache* cache, int32_t h) {
+  if (cache == nullptr) return -1;
+  HeadLayout hl;
+  if (!resolve_layout(*cache, &hl) || h < 0 || h >= cache->Hkv) return -1;
+  return hl.plane_off[h];
+}
+
+const char* kvq_status_str(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KVQ_ERR_CUDA: return "CUDA error";
+    case KVQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case KVQ_ERR_TIMEOUT: return "device wait timed out";
+    case KVQ_ERR_NONFINITE: return "non-finite input or fp16 overflow";
+  }
+  return "unknown status";
+}
+
+kvq_status kvq_quantize(const void* x, int64_t sx_b, int64_t sx_h, int64_t sx_t, int32_t t0, int32_t nt,
+                        const kvq_cache* dst, int32_t* dev_status, void* stream) {
+  if (dst == nullptr || x == nullptr || dst->codes == nullptr || dst->sz == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (dst->D != 64 && dst->D != 128 && dst->D > 0) return KVQ_ERR_UNSUPPORTED;
+  QuantizeArgs a;
+  if (!resolve_layout(*dst, &a.layout)) return KVQ_ERR_INVALID_ARG;
+  if (t0 < 0 || nt < 0 || static_cast<int64_t>(t0) + nt > dst->Tcap) return KVQ_ERR_INVALID_ARG;
+  if (sx_b < 0 || sx_h < 0 || sx_t < 0) return KVQ_ERR_INVALID_ARG;
+  // every row start must be 16-byte aligned (rows are read as 16-byte vectors)
+  if (!aligned16(x) || (sx_b % 8) || (sx_h % 8) || (sx_t % 8)) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(dst->codes) || !aligned16(dst->sz)) return KVQ_ERR_INVALID_ARG;
+  if (nt == 0) return KVQ_OK;
+  a.x = static_cast<const uint16_t*>(x);
+  a.sx_b = sx_b; a.sx_h = sx_h; a.sx_t = sx_t;
+  a.t0 = t0; a.nt = nt;
+  a.codes = dst->codes; a.sz = dst->sz;
+  a.B = dst->B; a.Hkv = dst->Hkv; a.Tcap = dst->Tcap; a.D = dst->D;
+  a.status = dev_status;
+  return launch_quantize(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+size_t kvq_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D) {
+  if (B <= 0 || Hkv <= 0 || Hq <= 0 || Hq % Hkv || (D != 64 && D != 128)) return 0;
+  return decode_workspace_bytes(B, Hq, Hkv, D, decode_num_ctas(D));
+}
+
+static bool same_cache_shape(const kvq_cache& a, const kvq_cache& b) {
+  if (a.B != b.B || a.Hkv != b.Hkv || a.Tcap != b.Tcap || a.D != b.D) return false;
+  if (a.head_bits == nullptr || b.head_bits == nullptr) return false;
+  for (int h = 0; h < a.Hkv && h < KVQ_MAX_HKV; ++h)
+    if (a.head_bits[h] != b.head_bits[h]) return false;
+  return true;
+}
+
+kvq_status kvq_decode_attention(const void* q, const kvq_cache* k, const kvq_cache* v, const int32_t* seq_lens,
+                                int32_t Hq, float softmax_scale, void* out, int32_t out_dtype, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || seq_lens == nullptr || out == nullptr)
+    return KVQ_ERR_INVALID_ARG;
+  if (k->codes == nullptr || k->sz == nullptr || v->codes == nullptr || v->sz == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (k->D > 0 && k->D != 64 && k->D != 128) return KVQ_ERR_UNSUPPORTED;
+  DecodeArgs a;
+  if (!resolve_layout(*k, &a.layout) || !same_cache_shape(*k, *v)) return KVQ_ERR_INVALID_ARG;
+  if (Hq <= 0 || Hq % k->Hkv) return KVQ_ERR_INVALID_ARG;
+  if (Hq / k->Hkv > 8) return KVQ_ERR_UNSUPPORTED;
+  if (out_dtype != KVQ_OUT_F32 && out_dtype != KVQ_OUT_BF16) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k->codes) || !aligned16(k->sz) || !aligned16(v->codes) || !aligned16(v->sz) ||
+      !aligned16(out) || (workspace != nullptr && !aligned16(workspace)) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return KVQ_ERR_INVALID_ARG;
+  // TMA row coordinates are 32-bit
+  if (static_cast<int64_t>(k->Hkv) * k->B * k->Tcap >= (int64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = k;
+  a.v = v;
+  a.seq_lens = seq_lens;
+  a.Hq = Hq;
+  a.softmax_scale = softmax_scale;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.ws = workspace;
+  a.ws_bytes = workspace_bytes;
+  a.status = dev_status;
+  return launch_decode(a, static_cast<cudaStream_t>(stream));
+}
+
+kvq_status kvq_prefill_attention(const void* q, const void* k, const void* v, int32_t B, int32_t Hq, int32_t Hkv,
+                                 int32_t S, int32_t D, int32_t causal, float softmax_scale,
+                                 const uint8_t* tile_mask, int32_t tile, const kvq_cache* k_cache,
+                                 const kvq_cache* v_cache, void* out, int32_t out_dtype, int32_t* dev_status,
+                                 void* stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || k_cache == nullptr || v_cache == nullptr || out == nullptr)
+    return KVQ_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || Hq % Hkv) return KVQ_ERR_INVALID_ARG;
+  if (causal != 1 || tile != 128 || D != 128 || S % 128) return KVQ_ERR_UNSUPPORTED;
+  if (out_dtype != KVQ_OUT_F32 && out_dtype != KVQ_OUT_BF16) return KVQ_ERR_INVALID_ARG;
+  PrefillArgs a;
+  if (!resolve_layout(*k_cache, &a.layout) || !same_cache_shape(*k_cache, *v_cache)) return KVQ_ERR_INVALID_ARG;
+  if (k_cache->B != B || k_cache->Hkv != Hkv || k_cache->D != D || k_cache->Tcap < S) return KVQ_ERR_INVALID_ARG;
+  if (a.layout.n4 != 0) return KVQ_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(k_cache->codes) ||
+      !aligned16(k_cache->sz) || !aligned16(v_cache->codes) || !aligned16(v_cache->sz))
+    return KVQ_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t sx_t = D, sx_h = static_cast<int64_t>(S) * D, sx_b = sx_h * Hkv;
+  kvq_status s = kvq_quantize(k, sx_b, sx_h, sx_t, 0, S, k_cache, dev_status, stream);
+  if (s != KVQ_OK) return s;
+  s = kvq_quantize(v, sx_b, sx_h, sx_t, 0, S, v_cache, dev_status, stream);
+  if (s != KVQ_OK) return s;
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = k_cache;
+  a.v = v_cache;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.S = S; a.D = D;
+  a.softmax_scale = softmax_scale;
+  a.tile_mask = tile_mask;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.status = dev_status;
+  return launch_prefill(a, st);
+}
+
+}  // extern "C"

@@ -1,0 +1,185 @@
+// kvq_device.cuh -- small device helpers shared by the kvq kernels (sm_103a):
+// status reporting, a wall-clock bound for every wait, mbarriers, bulk and
+// tensor TMA copies, warp-level fp16 tensor-core products and the bit tricks
+// that turn stored integer codes into exact fp16 values.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+// ---------------------------------------------------------------------------
+// status
+// ---------------------------------------------------------------------------
+
+// First error wins: a later error never overwrites an earlier one.
+__device__ __forceinline__ void report(int32_t* status, int32_t code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Every spin in these kernels gives up after this long and reports a timeout.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// ---------------------------------------------------------------------------
+// mbarrier (shared memory, CTA scope)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(phase)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false (and reports
+// KVQ_ERR_TIMEOUT) if the phase did not complete within kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase, int32_t* status) {
+  if (mbar_try_wait(bar, phase)) return true;
+  const uint64_t t0 = global_ns();
+  uint32_t n = 0;
+  while (!mbar_try_wait(bar, phase)) {
+    if ((++n & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) {
+      report(status, KVQ_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// TMA: 1D bulk copy and 2D tensor copy into shared memory, completing on an
+// mbarrier (transaction bytes).
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_2d_g2s(void* dst, const void* tmap, int32_t x, int32_t y,
+                                           uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// warp-level tensor-core product D = A(16x16 fp16) * B(16x8 fp16) + C (fp32)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---------------------------------------------------------------------------
+// codes -> fp16.  An fp16 whose top byte is 0x64 and low byte is c has the
+// value 1024 + c exactly (exponent 2^10, ten mantissa bits), for 0 <= c < 1024.
+// Subtracting (1024 + z) in fp16 then gives the exact integer c - z.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// bytes 0,1 of w -> half2(1024 + w.b0, 1024 + w.b1)
+__device__ __forceinline__ uint32_t bytes01_biased(uint32_t w) { return prmt(w, 0x64646464u, 0x5140u); }
+// bytes 2,3 of w -> half2(1024 + w.b2, 1024 + w.b3)
+__device__ __forceinline__ uint32_t bytes23_biased(uint32_t w) { return prmt(w, 0x64646464u, 0x7362u); }
+// nibbles at bits [0,4) and [16,20) of w -> half2(1024 + lo, 1024 + hi)
+__device__ __forceinline__ uint32_t nib_biased(uint32_t w) { return (w & 0x000F000Fu) | 0x64006400u; }
+
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float half_lo(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
+}
+__device__ __forceinline__ float half_hi(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+// (1024 + z) broadcast to both halves, from a scale/zero word (zero in the high half)
+__device__ __forceinline__ uint32_t zero_biased2(uint32_t sz) {
+  __half z = __ushort_as_half(static_cast<unsigned short>(sz >> 16));
+  __half zb = __hadd(z, __ushort_as_half(0x6400));  // exact: z is an integer <= 255
+  __half2 r = __halves2half2(zb, zb);
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+// half2((1024 + z_a), (1024 + z_b)) from two scale/zero words
+__device__ __forceinline__ uint32_t zero_biased_pair(uint32_t sz_a, uint32_t sz_b) {
+  uint32_t zz = prmt(sz_a, sz_b, 0x7632u);  // high halves: z_a | z_b << 16
+  __half2 r = __hadd2(*reinterpret_cast<__half2*>(&zz), __halves2half2(__ushort_as_half(0x6400),
+                                                                      __ushort_as_half(0x6400)));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+}  // namespace kvq

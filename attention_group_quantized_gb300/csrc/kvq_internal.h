@@ -1,0 +1,77 @@
+// kvq_internal.h -- launch interfaces between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+// Resolved per-head layout of a cache: where each head's code plane starts,
+// its bit-width and its index among the planes of the same bit-width.
+struct HeadLayout {
+  int64_t plane_off[KVQ_MAX_HKV];   // byte offset of the head's code plane
+  int32_t plane_idx[KVQ_MAX_HKV];   // index among planes of equal bit-width
+  int8_t bits[KVQ_MAX_HKV];
+  int32_t n8, n4;                   // number of 8-bit / 4-bit heads
+  int64_t off4;                     // byte offset of the first 4-bit plane
+};
+
+bool resolve_layout(const kvq_cache& c, HeadLayout* out);
+
+struct QuantizeArgs {
+  const uint16_t* x;
+  int64_t sx_b, sx_h, sx_t;
+  int32_t t0, nt;
+  uint8_t* codes;
+  uint32_t* sz;
+  int32_t B, Hkv, Tcap, D;
+  int32_t* status;
+  HeadLayout layout;
+};
+cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t stream);
+
+struct DecodeArgs {
+  const uint16_t* q;
+  const kvq_cache* k;
+  const kvq_cache* v;
+  HeadLayout layout;                // shared by K and V
+  const int32_t* seq_lens;
+  int32_t Hq;
+  float softmax_scale;
+  void* out;
+  int32_t out_dtype;
+  void* ws;
+  size_t ws_bytes;
+  int32_t* status;
+};
+// Number of persistent split CTAs on the current device for head dim D.
+int decode_num_ctas(int D);
+size_t decode_workspace_bytes(int B, int Hq, int Hkv, int D, int num_ctas);
+kvq_status launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+struct PrefillArgs {
+  const uint16_t* q;
+  const kvq_cache* k;
+  const kvq_cache* v;
+  HeadLayout layout;
+  int32_t B, Hq, Hkv, S, D;
+  float softmax_scale;
+  const uint8_t* tile_mask;
+  void* out;
+  int32_t out_dtype;
+  int32_t* status;
+};
+kvq_status launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+// cuTensorMapEncodeTiled, resolved from the driver at first use (no link to
+// libcuda, so the library loads on machines without a GPU driver).
+CUresult encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,
+                              uint64_t dim0, uint64_t dim1, uint64_t stride1_bytes,
+                              uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle);
+
+int device_sm_count();
+
+}  // namespace kvq

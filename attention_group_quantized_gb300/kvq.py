@@ -1,0 +1,175 @@
+"""Thin Python binding of libkvq (the C ABI declared in include/kvq.h).
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels.  PyTorch supplies device memory and streams.  If the
+library has not been built, :func:`lib` raises -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libkvq.so")
+
+KVQ_OK = 0
+STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error",
+                4: "workspace", 5: "timeout", 6: "non-finite"}
+OUT_F32 = 0
+OUT_BF16 = 1
+GROUP = 32
+TILE_TOKENS = 64
+
+# every symbol include/kvq.h declares
+EXPORTS = ("kvq_cache_codes_bytes", "kvq_cache_sz_bytes", "kvq_cache_head_offset", "kvq_quantize",
+           "kvq_decode_workspace_bytes", "kvq_decode_attention", "kvq_prefill_attention",
+           "kvq_status_str")
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({status})")
+        self.status = status
+
+
+class CCache(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("sz", ctypes.c_void_p), ("head_bits", ctypes.c_void_p),
+                ("B", ctypes.c_int32), ("Hkv", ctypes.c_int32), ("Tcap", ctypes.c_int32),
+                ("D", ctypes.c_int32)]
+
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libkvq.so (once).  Raises if it is missing: there is no CPU path."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libkvq.so not found at {LIB_PATH}; build it with "
+                               "attention_group_quantized_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I32, I64, F32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        CP = ctypes.POINTER(CCache)
+        L.kvq_cache_codes_bytes.argtypes = [CP]; L.kvq_cache_codes_bytes.restype = I64
+        L.kvq_cache_sz_bytes.argtypes = [CP]; L.kvq_cache_sz_bytes.restype = I64
+        L.kvq_cache_head_offset.argtypes = [CP, I32]; L.kvq_cache_head_offset.restype = I64
+        L.kvq_quantize.argtypes = [P, I64, I64, I64, I32, I32, CP, P, P]; L.kvq_quantize.restype = I32
+        L.kvq_decode_workspace_bytes.argtypes = [I32, I32, I32, I32]; L.kvq_decode_workspace_bytes.restype = SZ
+        L.kvq_decode_attention.argtypes = [P, CP, CP, P, I32, F32, P, I32, P, SZ, P, P]
+        L.kvq_decode_attention.restype = I32
+        L.kvq_prefill_attention.argtypes = [P, P, P, I32, I32, I32, I32, I32, I32, F32, P, I32, CP, CP, P, I32,
+                                            P, P]
+        L.kvq_prefill_attention.restype = I32
+        L.kvq_status_str.argtypes = [I32]; L.kvq_status_str.restype = ctypes.c_char_p
+        _LIB = L
+    return _LIB
+
+
+def _check(status: int, what: str):
+    if status != KVQ_OK:
+        raise KvqError(status, what)
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+@dataclass
+class QuantCache:
+    """A quantised K or V cache in libkvq's layout, backed by torch tensors."""
+    codes: "object"           # torch.uint8 [codes_bytes]
+    sz: "object"              # torch.int32 [Hkv*B*Tcap*D/32] (fp16 scale | fp16 zero << 16)
+    head_bits: np.ndarray     # int8 [Hkv] (host)
+    B: int
+    Hkv: int
+    Tcap: int
+    D: int
+
+    def c_struct(self) -> CCache:
+        hb = np.ascontiguousarray(self.head_bits, dtype=np.int8)
+        self.head_bits = hb
+        return CCache(self.codes.data_ptr(), self.sz.data_ptr(), hb.ctypes.data, self.B, self.Hkv,
+                      self.Tcap, self.D)
+
+    def head_offset(self, h: int) -> int:
+        cs = self.c_struct()
+        return int(lib().kvq_cache_head_offset(ctypes.byref(cs), h))
+
+
+def cache_nbytes(head_bits: Sequence[int], B: int, Tcap: int, D: int):
+    """(codes bytes, sz bytes) of a cache with this shape."""
+    hb = np.ascontiguousarray(head_bits, dtype=np.int8)
+    cs = CCache(None, None, hb.ctypes.data, B, len(hb), Tcap, D)
+    nc = int(lib().kvq_cache_codes_bytes(ctypes.byref(cs)))
+    ns = int(lib().kvq_cache_sz_bytes(ctypes.byref(cs)))
+    if nc < 0 or ns < 0:
+        raise KvqError(1, "cache shape")
+    return nc, ns
+
+
+def empty_cache(head_bits: Sequence[int], B: int, Tcap: int, D: int, device="cuda") -> QuantCache:
+    import torch
+    nc, ns = cache_nbytes(head_bits, B, Tcap, D)
+    codes = torch.empty(nc, dtype=torch.uint8, device=device)
+    sz = torch.empty(ns // 4, dtype=torch.int32, device=device)
+    return QuantCache(codes, sz, np.asarray(head_bits, np.int8), B, len(head_bits), Tcap, D)
+
+
+def quantize(x, cache: QuantCache, t0: int = 0, status=None, stream=None):
+    """Quantise bf16 x[B][Hkv][T][D] (strided, channels contiguous) into cache positions t0.."""
+    assert x.dtype.itemsize == 2 and x.stride(-1) == 1
+    cs = cache.c_struct()
+    st = lib().kvq_quantize(x.data_ptr(), x.stride(0), x.stride(1), x.stride(2), t0, x.shape[2],
+                            ctypes.byref(cs), status.data_ptr() if status is not None else None,
+                            _stream_ptr(stream))
+    _check(st, "kvq_quantize")
+
+
+def decode_workspace_bytes(B: int, Hq: int, Hkv: int, D: int) -> int:
+    return int(lib().kvq_decode_workspace_bytes(B, Hq, Hkv, D))
+
+
+def decode_attention(q, k: QuantCache, v: QuantCache, seq_lens, softmax_scale: float = 0.0,
+                     out=None, out_dtype: int = OUT_F32, workspace=None, status=None, stream=None):
+    """Decode attention: q bf16 [B][Hq][D] over the caches; returns out [B][Hq][D]."""
+    import torch
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32 if out_dtype == OUT_F32 else torch.bfloat16,
+                          device=q.device)
+    if workspace is None:
+        n = decode_workspace_bytes(B, Hq, k.Hkv, D)
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+    kc, vc = k.c_struct(), v.c_struct()
+    st = lib().kvq_decode_attention(q.data_ptr(), ctypes.byref(kc), ctypes.byref(vc), seq_lens.data_ptr(),
+                                    Hq, float(softmax_scale), out.data_ptr(), out_dtype,
+                                    workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                    status.data_ptr() if status is not None else None, _stream_ptr(stream))
+    _check(st, "kvq_decode_attention")
+    return out
+
+
+def prefill_attention(q, k, v, k_cache: QuantCache, v_cache: QuantCache, softmax_scale: float = 0.0,
+                      tile_mask=None, out=None, out_dtype: int = OUT_F32, status=None, stream=None):
+    """Causal prefill: q bf16 [B][Hq][S][D], k/v bf16 [B][Hkv][S][D]; fills the caches, returns out."""
+    import torch
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    if out is None:
+        out = torch.empty((B, Hq, S, D), dtype=torch.float32 if out_dtype == OUT_F32 else torch.bfloat16,
+                          device=q.device)
+    kc, vc = k_cache.c_struct(), v_cache.c_struct()
+    st = lib().kvq_prefill_attention(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, Hq, Hkv, S, D, 1,
+                                     float(softmax_scale),
+                                     tile_mask.data_ptr() if tile_mask is not None else None, 128,
+                                     ctypes.byref(kc), ctypes.byref(vc), out.data_ptr(), out_dtype,
+                                     status.data_ptr() if status is not None else None, _stream_ptr(stream))
+    _check(st, "kvq_prefill_attention")
+    return out

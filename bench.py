@@ -1,0 +1,396 @@
+"""Benchmark: quantised-KV decode attention HBM GB/s on one GB300 (per rank).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kvq|reference]
+                    [--workload decode_gqa] [--no-cpu-baseline] [--no-prefill]
+
+A step is one decode-attention call (split-K pass + log-sum-exp merge) of the
+whole batch over its quantised cache, resident in HBM; the cache is
+quantised once, untimed, by kvq_quantize.  Between timed steps L2 is flushed
+by a memset of twice its size, outside the per-step CUDA events.  ``value``
+is algorithmic cache bytes (codes plus scale/zero words of K and V) per
+second over all ranks.  Under torchrun each rank runs its own batch
+(independent sequences: weak scaling, no collective on the data path).
+
+Also reported: ``e2e`` (the same metric through the C ABI with the step's
+new inputs copied from pinned host memory and the output read back every
+step), ``roofline`` for the split kernel, the CPU oracle timed on a bounded
+sample (``cpu_baseline``), clocks sampled during the timed region, and the
+causal prefill workload's TFLOP/s when the prefill kernel is available.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    found = {}
+    if os.path.exists(path):
+        try:
+            data = json.load(open(path))
+
+            def walk(d):
+                if isinstance(d, dict):
+                    for k, v in d.items():
+                        if isinstance(v, (int, float)) and k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                            found.setdefault(k, float(v))
+                        else:
+                            walk(v)
+                elif isinstance(d, list):
+                    for v in d:
+                        walk(v)
+            walk(data)
+        except Exception:
+            found = {}
+    hbm = found.get("hbm_gbs")
+    bf = found.get("bf16_tflops")
+    bfs = found.get("bf16_tflops_sustained")
+    return {
+        "hbm_gbs": hbm or FALLBACK_HBM_GBS, "hbm_src": "of measured" if hbm else "of fallback",
+        "bf16_tflops": bf or FALLBACK_BF16_TFLOPS, "bf16_src": "of measured" if bf else "of fallback",
+        "bf16_tflops_sustained": bfs or bf or 1700.0,
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1])); mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _traffic_from_profile(kernel_src: str, workload: str):
+    """DRAM bytes per launch recorded by the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    for line in open(path):
+        if "=" in line and not line.lstrip().startswith("#"):
+            k, v = line.split("=", 1)
+            kv[k.strip()] = v.strip()
+    src = open(os.path.join(ROOT, "attention_group_quantized_gb300", "csrc", kernel_src), "rb").read()
+    if kv.get("source_sha256") != hashlib.sha256(src).hexdigest():
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def _oracle_subprocess(workload: str, seconds: float):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-m", "oracle.timing", "--workload", workload, "--seconds", str(seconds)],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        return {"error": r.stderr.strip().splitlines()[-1:] or ["failed"]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def decode_bytes(inp) -> int:
+    D = inp.D
+    tot = 0
+    for b in range(inp.B):
+        for h in range(inp.Hkv):
+            tot += 2 * int(inp.seq_lens[b]) * (D * int(inp.head_bits[h]) // 8 + 4 * (D // 32))
+    return tot
+
+
+def run_reference(args, rank):
+    """Reference arm: the CPU oracle, as it stands, on a bounded sample (rank 0 only)."""
+    if rank != 0:
+        return
+    import kvq_workloads as W
+    name = W.NAMED[args.workload]().name
+    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    vals = []
+    last = None
+    for i in range(args.warmup + args.steps):
+        r = _oracle_subprocess(args.workload, per_step)
+        if "error" in r:
+            print(json.dumps({"impl": "reference", "unavailable": f"oracle run failed: {r['error']}"}))
+            return
+        if i >= args.warmup:
+            vals.append(r["value"])
+        last = r
+    v = statistics.mean(vals)
+    line = {"impl": "reference", "metric": "quant-KV decode attn HBM GB/s", "value": v, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded, kvq_workloads)",
+            "config": {"workload": name},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": last["cores"], "kind": "oracle",
+                             "sample": last["sample"]},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def bench_prefill(torch, kvq, W, peaks, steps, warmup, dev):
+    """Causal prefill workload (quantise K/V + tile-masked attention): TFLOP/s."""
+    import numpy as np
+    inp = W.prefill_causal()
+    B, Hq, Hkv, S, D = inp.B, inp.Hq, inp.Hkv, inp.S, inp.D
+    todev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    q, k, v = todev(inp.q), todev(inp.k), todev(inp.v)
+    mask = torch.from_numpy(inp.tile_mask).to(dev)
+    kc = kvq.empty_cache(inp.head_bits, B, S, D, device=dev)
+    vc = kvq.empty_cache(inp.head_bits, B, S, D, device=dev)
+    out = torch.empty((B, Hq, S, D), dtype=torch.bfloat16, device=dev)
+    try:
+        kvq.prefill_attention(q, k, v, kc, vc, inp.softmax_scale, mask, out=out, out_dtype=kvq.OUT_BF16)
+    except kvq.KvqError as e:
+        return {"unavailable": str(e)}
+    n_t = S // 128
+    kept = int(np.tril(inp.tile_mask, -1).sum())
+    flops = 4.0 * D * Hq * B * (kept * 128 * 128 + n_t * 128 * 129 / 2)
+    for _ in range(warmup):
+        kvq.prefill_attention(q, k, v, kc, vc, inp.softmax_scale, mask, out=out, out_dtype=kvq.OUT_BF16)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        kvq.prefill_attention(q, k, v, kc, vc, inp.softmax_scale, mask, out=out, out_dtype=kvq.OUT_BF16)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / 1e3)
+    t = statistics.mean(times)
+    tf = flops / t / 1e12
+    return {"workload": inp.name, "value": tf, "unit": "TFLOP/s", "ms_per_step": t * 1e3,
+            "algorithmic_flop": flops,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["bf16_tflops"], "peak_src": peaks["bf16_src"],
+                         "note": "time includes the two quantise launches of the same call"}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    ap.add_argument("--workload", default="decode_gqa")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import numpy as np
+    import torch
+
+    import kvq_workloads as W
+    from attention_group_quantized_gb300 import kvq
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    kvq.lib()   # fail loudly if the library is missing
+    peaks = _peaks()
+
+    inp = W.NAMED[args.workload]()
+    B, Hq, Hkv, D, Tcap = inp.B, inp.Hq, inp.Hkv, inp.D, inp.Tcap
+    todev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    kc = kvq.empty_cache(inp.head_bits, B, Tcap, D, device=dev)
+    vc = kvq.empty_cache(inp.head_bits, B, Tcap, D, device=dev)
+    kd, vd = todev(inp.k), todev(inp.v)
+    kvq.quantize(kd, kc)
+    kvq.quantize(vd, vc)
+    del kd, vd
+    q = todev(inp.q)
+    sl = torch.from_numpy(inp.seq_lens).to(dev)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(16, kvq.decode_workspace_bytes(B, Hq, Hkv, D)), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    bytes_per_step = decode_bytes(inp)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kvq.decode_attention(q, kc, vc, sl, inp.softmax_scale, out=out, workspace=ws, status=status)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    per = [s.elapsed_time(e) / 1e3 for s, e in zip(starts, ends)]
+    t_total = sum(per)
+    if dist:
+        tt = torch.tensor([t_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_total = float(tt.item())
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    value = bytes_per_step * world * args.steps / t_total / 1e9
+    avg = t_total / args.steps
+    achieved = bytes_per_step / avg / 1e9
+
+    # e2e: new query + new K/V token from pinned host memory, quantise-append, decode, read back
+    pin = lambda t: t.pin_memory()
+    h_q = pin(torch.from_numpy(np.ascontiguousarray(inp.q).view(np.int16)).view(torch.bfloat16))
+    last = Tcap - 1
+    h_k = pin(torch.from_numpy(np.ascontiguousarray(inp.k[:, :, last:last + 1]).view(np.int16)).view(torch.bfloat16))
+    h_v = pin(torch.from_numpy(np.ascontiguousarray(inp.v[:, :, last:last + 1]).view(np.int16)).view(torch.bfloat16))
+    h_out = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
+    d_k, d_v = torch.empty_like(h_k, device=dev), torch.empty_like(h_v, device=dev)
+    out16 = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    e2e_ok = bool(np.all(inp.seq_lens == Tcap))
+
+    def e2e_step():
+        q.copy_(h_q, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        kvq.quantize(d_k, kc, last)
+        kvq.quantize(d_v, vc, last)
+        kvq.decode_attention(q, kc, vc, sl, inp.softmax_scale, out=out16, out_dtype=kvq.OUT_BF16, workspace=ws)
+        h_out.copy_(out16, non_blocking=True)
+
+    e2e = None
+    if e2e_ok:
+        for _ in range(args.warmup):
+            flush.zero_()
+            e2e_step()
+        torch.cuda.synchronize()
+        et = []
+        for i in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            e2e_step()
+            e1.record(stream)
+            e1.synchronize()
+            et.append(e0.elapsed_time(e1) / 1e3)
+        te = sum(et)
+        if dist:
+            tt = torch.tensor([te], dtype=torch.float64, device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            te = float(tt.item())
+        e2e = {"value": bytes_per_step * world * args.steps / te / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": int(h_q.numel() * 2 + h_k.numel() * 2 + h_v.numel() * 2),
+               "d2h_bytes_per_step": int(h_out.numel() * 2),
+               "ms_per_step": te / args.steps * 1e3,
+               "step": "H2D q + new-token K/V, kvq_quantize x2 (append), kvq_decode_attention (bf16 out), D2H out"}
+
+    prefill = None
+    if not args.no_prefill and rank == 0:
+        del flush
+        torch.cuda.empty_cache()
+        prefill = bench_prefill(torch, kvq, W, peaks, max(3, min(args.steps, 10)), 3, dev)
+
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        cpu = _oracle_subprocess(args.workload, 15.0)
+        if "error" not in cpu:
+            cpu = {"value": cpu["value"], "unit": cpu["unit"], "cores": cpu["cores"], "kind": "oracle",
+                   "sample": cpu["sample"]}
+
+    if rank == 0:
+        traffic = _traffic_from_profile("kvq_decode.cu", args.workload)
+        line = {
+            "metric": "quant-KV decode attn HBM GB/s (% of peak); prefill attn TFLOP/s (% of peak)",
+            "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": avg * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "u8/u4 codes, f16 mma, f32 accumulate", "data": "synthetic (seeded, kvq_workloads)",
+            "config": {"workload": inp.name, "B": B, "Hq": Hq, "Hkv": Hkv, "D": D, "context": int(Tcap),
+                       "bits": [int(b) for b in inp.head_bits],
+                       "l2": "flushed between timed steps (memset of 2x L2), outside the step events",
+                       "per_rank": "each rank decodes its own batch (independent sequences)"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                         "kernel": "decode_split_kernel (event time also covers its merge launch)",
+                         "algorithmic_bytes_per_launch": bytes_per_step, "peak_src": peaks["hbm_src"]},
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": clk.summary(),
+            "gpu_launches": 2 * args.steps,
+            "prefill": prefill,
+        }
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,180 @@
+/*
+ * kvq.h -- C ABI of libkvq: group-quantised KV-cache attention on GB300 (sm_103a).
+ *
+ * The method (source pages: 《分块稀疏注意力与KV Cache量化：长文本推理显存优化实践》,
+ * xdnf.cn, here "P4"; and 《一只"兔子"如何搅动大模型推理赛道的底层逻辑》, m.xxqk.cn, "P1"):
+ *   - the KV cache is stored as integer codes, quantised in groups of 32
+ *     adjacent head_dim channels, each group with its own scale and zero point
+ *     (P4 §2.4 "KV Cache分组量化"; group size 32 from the hook in P4 §3.2);
+ *   - attention softmax(Q K^T / sqrt(d)) V (P1 §3.1) is computed tile by tile
+ *     with an online softmax whose running max and normaliser are merged
+ *     across tiles (P4 §2.2);
+ *   - dequantisation happens inside the attention read, not as a separate pass
+ *     (P4 §1.3);
+ *   - prefill may skip whole key tiles with a block-sparse mask (P4 §1.3, §2.3).
+ *
+ * Conventions for every call:
+ *   - Ownership: the caller owns every buffer.  The library never allocates or
+ *     frees memory, never synchronises, and launches only on `stream`
+ *     (a cudaStream_t; NULL = the legacy default stream).  All calls are
+ *     asynchronous with respect to the host.
+ *   - Errors: argument problems are detected on the host; the call returns a
+ *     status and launches nothing.  A failed launch returns KVQ_ERR_CUDA.
+ *   - Device status: conditions only the device can see (non-finite input,
+ *     fp16 scale overflow, a sequence length beyond capacity, a bounded wait
+ *     that timed out) are written to the optional device word `dev_status`
+ *     (first error wins; the caller zeroes it and reads it after its own
+ *     synchronisation).  NULL disables the report.
+ *   - bf16 tensors are raw 16-bit bfloat16 values; fp16 values are IEEE binary16.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvq_status {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned buffer, ... */
+  KVQ_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. D not 64/128) */
+  KVQ_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+  KVQ_ERR_WORKSPACE = 4,     /* workspace missing or too small */
+  KVQ_ERR_TIMEOUT = 5,       /* (device) a bounded wait gave up */
+  KVQ_ERR_NONFINITE = 6      /* (device) non-finite input or fp16 overflow */
+} kvq_status;
+
+#define KVQ_GROUP 32          /* channels per quantisation group (P4 §3.2) */
+#define KVQ_MAX_HKV 64        /* most KV heads a cache may have */
+#define KVQ_TILE_TOKENS 64    /* cache capacity granularity */
+#define KVQ_OUT_F32 0
+#define KVQ_OUT_BF16 1
+
+/*
+ * A quantised KV cache (one for K, one for V).  Group quantisation of P4 §2.4:
+ * per (sequence b, KV head h, token t, group g of 32 channels) one fp16 scale
+ * s and one fp16 integer zero point z; each channel value x is stored as the
+ * code c with x_hat = (c - z) * s.  Per-head bit-width (P4 §2.4: sensitive
+ * heads keep more bits) is 8 (one code per byte) or 4 (two codes per byte,
+ * even channel in the low nibble).
+ *
+ * Layout (fixed by the library; all device memory, 16-byte aligned):
+ *   codes: one plane per KV head.  Planes of 8-bit heads come first, in head
+ *          order, then planes of 4-bit heads, in head order.  A plane is
+ *          [B][Tcap][D*bits/8] bytes, row-major.  kvq_cache_head_offset()
+ *          gives a plane's byte offset; kvq_cache_codes_bytes() the total.
+ *   sz:    [Hkv][B][Tcap][D/32] 32-bit words; low 16 bits = fp16 scale,
+ *          high 16 bits = fp16 zero point.  kvq_cache_sz_bytes() is the size.
+ * head_bits is a HOST array of Hkv entries, each 4 or 8; it must stay valid
+ * for the duration of each call that takes the cache.  Tcap must be a
+ * multiple of KVQ_TILE_TOKENS; D is 64 or 128.
+ */
+typedef struct kvq_cache {
+  uint8_t* codes;
+  uint32_t* sz;
+  const int8_t* head_bits;
+  int32_t B, Hkv, Tcap, D;
+} kvq_cache;
+
+/* Total bytes of the code planes / the scale-zero words; -1 on invalid shape. */
+KVQ_API int64_t kvq_cache_codes_bytes(const kvq_cache* cache);
+KVQ_API int64_t kvq_cache_sz_bytes(const kvq_cache* cache);
+/* Byte offset of KV head h's code plane within `codes`; -1 on invalid input. */
+KVQ_API int64_t kvq_cache_head_offset(const kvq_cache* cache, int32_t h);
+
+/*
+ * kvq_quantize -- quantise-on-write (P4 §2.4, group 32 per P4 §3.2).
+ *
+ * x: device bf16, element (b, h, t, d) at x[b*sx_b + h*sx_h + t*sx_t + d]
+ *    (element strides; channels contiguous; every row 16-byte aligned), for
+ *    b < dst->B, h < dst->Hkv, t < nt.
+ * Writes cache positions t0 .. t0+nt-1 of every (b, h) of `dst`.
+ * Per group of 32 channels, qmax = 2^bits - 1, all arithmetic IEEE fp32:
+ *   lo = min(0, min x), hi = max(0, max x), r = hi - lo;
+ *   r == 0: s = 1, z = 0, codes 0;
+ *   else s = fp16 rounded up from r / qmax, z = clamp(rne(-lo / s), 0, qmax),
+ *        c = clamp(rne(x / s) + z, 0, qmax)   (rne = round half to even).
+ * A non-finite input or a scale beyond fp16 range reports KVQ_ERR_NONFINITE
+ * in dev_status; that group's stored values are then unspecified.
+ */
+KVQ_API kvq_status kvq_quantize(const void* x, int64_t sx_b, int64_t sx_h, int64_t sx_t,
+                        int32_t t0, int32_t nt, const kvq_cache* dst,
+                        int32_t* dev_status, void* stream);
+
+/*
+ * Workspace bytes kvq_decode_attention needs for this shape on the CURRENT
+ * device (the split count depends on its SM count).  0 on invalid shape.
+ */
+KVQ_API size_t kvq_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D);
+
+/*
+ * kvq_decode_attention -- one query token per (sequence, query head) over the
+ * quantised cache, dequantised inside the attention read (P4 §1.3), tiled
+ * online softmax (P4 §2.2) split across CTAs, then a log-sum-exp merge.
+ *
+ * q:        device bf16 [B][Hq][D], contiguous, 16-byte aligned.
+ * k, v:     caches with identical B, Hkv, Tcap, D and head_bits.
+ * seq_lens: device int32 [B]; sequence b attends cache tokens 0 .. len_b-1.
+ *           len_b == 0 gives a zero output row; len_b outside [0, Tcap]
+ *           reports KVQ_ERR_INVALID_ARG in dev_status and is clamped.
+ * Hq:       query heads; Hq % Hkv == 0 and Hq / Hkv <= 8.  Query head h
+ *           reads KV head h / (Hq / Hkv).
+ * softmax_scale: multiplies Q.K; <= 0 selects 1/sqrt(D).
+ * out:      device [B][Hq][D], fp32 (out_dtype KVQ_OUT_F32) or bf16 (KVQ_OUT_BF16).
+ * workspace: device scratch of >= kvq_decode_workspace_bytes(B, Hq, Hkv, D)
+ *           bytes, 16-byte aligned; its contents need no initialisation.
+ *           Calls that share a workspace must be ordered on the GPU.
+ * q values must lie within fp16 range (|q| < 65504): the kernel's tensor-core
+ * products take Q in fp16 (exact for bf16 values in that range).
+ */
+KVQ_API kvq_status kvq_decode_attention(const void* q, const kvq_cache* k, const kvq_cache* v,
+                                const int32_t* seq_lens, int32_t Hq, float softmax_scale,
+                                void* out, int32_t out_dtype,
+                                void* workspace, size_t workspace_bytes,
+                                int32_t* dev_status, void* stream);
+
+/*
+ * kvq_prefill_attention -- causal prefill over a group-quantised KV cache.
+ *
+ * Quantises K and V into k_cache / v_cache (positions 0 .. S-1, exactly as
+ * kvq_quantize), then computes, per query head h and query position i,
+ *   O[i] = softmax_j(scale * Q[i] . K_hat[j]) V_hat[j]
+ * over keys j <= i (P1 §3.1 with the causal rule), where K_hat, V_hat are the
+ * dequantised cache rows, tile by tile with an online softmax (P4 §2.2).
+ * With a tile mask (P4 §1.3, §2.3: skipped blocks are not computed), key tile
+ * kt < query tile qt takes part only if tile_mask[qt * nT + kt] != 0, where
+ * nT = S / tile; the keys of a skipped tile are left out of the softmax.
+ * Diagonal tiles are always computed with the element-wise causal rule.
+ *
+ * q:    device bf16 [B][Hq][S][D]; k, v: device bf16 [B][Hkv][S][D];
+ *       contiguous, 16-byte aligned.
+ * causal must be 1; tile must be 128; S a multiple of 128; D == 128;
+ * Hq % Hkv == 0; caches 8-bit for every head, Tcap >= S.
+ * tile_mask: device uint8 [nT][nT] or NULL (dense causal).
+ * out:  device [B][Hq][S][D], fp32 or bf16.
+ */
+KVQ_API kvq_status kvq_prefill_attention(const void* q, const void* k, const void* v,
+                                 int32_t B, int32_t Hq, int32_t Hkv, int32_t S, int32_t D,
+                                 int32_t causal, float softmax_scale,
+                                 const uint8_t* tile_mask, int32_t tile,
+                                 const kvq_cache* k_cache, const kvq_cache* v_cache,
+                                 void* out, int32_t out_dtype,
+                                 int32_t* dev_status, void* stream);
+
+/* Static, human-readable name of a status code. */
+KVQ_API const char* kvq_status_str(kvq_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -1,0 +1,111 @@
+"""CPU-only checks of the C ABI: the library loads, exports every declared
+symbol, reports cache layout sizes, and rejects bad arguments before any
+device work (no GPU needed: validation returns before a launch)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from attention_group_quantized_gb300 import kvq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(kvq.LIB_PATH):
+        from attention_group_quantized_gb300 import build
+        build.build()
+    return kvq.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    declared = _declared_functions()
+    assert set(declared) == set(kvq.EXPORTS)
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for s in range(7):
+        assert L.kvq_status_str(s)
+    assert L.kvq_status_str(99) == b"unknown status"
+
+
+def test_cache_layout_sizes(L):
+    hb = np.array([8, 4, 4, 8], np.int8)
+    B, Tcap, D = 3, 128, 128
+    nc, ns = kvq.cache_nbytes(hb, B, Tcap, D)
+    assert nc == B * Tcap * (2 * 128 + 2 * 64)
+    assert ns == 4 * B * Tcap * 4 * 4
+    cs = kvq.CCache(None, None, hb.ctypes.data, B, 4, Tcap, D)
+    offs = [L.kvq_cache_head_offset(ctypes.byref(cs), h) for h in range(4)]
+    plane8, plane4 = B * Tcap * 128, B * Tcap * 64
+    # 8-bit planes first in head order, then 4-bit planes in head order
+    assert offs == [0, 2 * plane8, 2 * plane8 + plane4, plane8]
+    assert L.kvq_cache_head_offset(ctypes.byref(cs), 4) == -1
+
+
+def test_cache_layout_rejects_bad_shapes(L):
+    hb = np.array([8, 5], np.int8)
+    cs = kvq.CCache(None, None, hb.ctypes.data, 1, 2, 64, 128)
+    assert L.kvq_cache_codes_bytes(ctypes.byref(cs)) == -1
+    hb = np.array([8], np.int8)
+    for B, Tcap, D in [(0, 64, 128), (1, 100, 128), (1, 64, 96)]:
+        cs = kvq.CCache(None, None, hb.ctypes.data, B, 1, Tcap, D)
+        assert L.kvq_cache_codes_bytes(ctypes.byref(cs)) == -1
+
+
+def _cache(hb, B=1, Tcap=64, D=128, codes=0x1000, sz=0x2000):
+    hb = np.asarray(hb, np.int8)
+    return kvq.CCache(codes, sz, hb.ctypes.data, B, len(hb), Tcap, D), hb
+
+
+def test_quantize_validation_without_launch(L):
+    c, hb = _cache([8])
+    P = ctypes.byref
+    assert L.kvq_quantize(None, 0, 0, 128, 0, 1, P(c), None, None) == 1
+    assert L.kvq_quantize(0x3000, 0, 0, 128, 0, 65, P(c), None, None) == 1        # past capacity
+    assert L.kvq_quantize(0x3000, 0, 0, 128, -1, 1, P(c), None, None) == 1
+    assert L.kvq_quantize(0x3002, 0, 0, 128, 0, 1, P(c), None, None) == 1        # misaligned rows
+    assert L.kvq_quantize(0x3000, 0, 0, 100, 0, 1, P(c), None, None) == 1        # row stride not 16 B
+    c2, hb2 = _cache([8], D=96)
+    assert L.kvq_quantize(0x3000, 0, 0, 96, 0, 1, P(c2), None, None) == 2
+    assert L.kvq_quantize(0x3000, 0, 0, 128, 0, 0, P(c), None, None) == 0        # nothing to do
+
+
+def test_decode_validation_without_launch(L):
+    k, hk = _cache([8, 8])
+    v, hv = _cache([8, 8])
+    P = ctypes.byref
+    q, lens, out, ws = 0x4000, 0x5000, 0x6000, 0x7000
+    assert L.kvq_decode_attention(None, P(k), P(v), lens, 8, 0.0, out, 0, ws, 1 << 20, None, None) == 1
+    assert L.kvq_decode_attention(q, P(k), P(v), lens, 7, 0.0, out, 0, ws, 1 << 20, None, None) == 1   # Hq % Hkv
+    assert L.kvq_decode_attention(q, P(k), P(v), lens, 32, 0.0, out, 0, ws, 1 << 20, None, None) == 2  # 16 per KV
+    assert L.kvq_decode_attention(q, P(k), P(v), lens, 8, 0.0, out, 5, ws, 1 << 20, None, None) == 1   # dtype
+    v2, hv2 = _cache([8, 4])
+    assert L.kvq_decode_attention(q, P(k), P(v2), lens, 8, 0.0, out, 0, ws, 1 << 20, None, None) == 1  # bits differ
+    assert L.kvq_decode_attention(q + 8, P(k), P(v), lens, 8, 0.0, out, 0, ws, 1 << 20, None, None) == 1
+
+
+def test_prefill_validation_without_launch(L):
+    k, hk = _cache([8, 8], Tcap=256)
+    v, hv = _cache([8, 8], Tcap=256)
+    P = ctypes.byref
+    a = 0x8000
+    assert L.kvq_prefill_attention(a, a, a, 1, 4, 2, 256, 128, 0, 0.0, None, 128, P(k), P(v), a, 0, None, None) == 2
+    assert L.kvq_prefill_attention(a, a, a, 1, 4, 2, 256, 128, 1, 0.0, None, 64, P(k), P(v), a, 0, None, None) == 2
+    assert L.kvq_prefill_attention(a, a, a, 1, 4, 2, 200, 128, 1, 0.0, None, 128, P(k), P(v), a, 0, None, None) == 2
+    assert L.kvq_prefill_attention(a, a, a, 1, 4, 2, 512, 128, 1, 0.0, None, 128, P(k), P(v), a, 0, None, None) == 1
+    assert L.kvq_prefill_attention(a, a, a, 1, 3, 2, 256, 128, 1, 0.0, None, 128, P(k), P(v), a, 0, None, None) == 1
+    k4, _ = _cache([8, 4], Tcap=256)
+    v4, _ = _cache([8, 4], Tcap=256)
+    assert L.kvq_prefill_attention(a, a, a, 1, 4, 2, 256, 128, 1, 0.0, None, 128, P(k4), P(v4), a, 0, None, None) == 2

@@ -1,0 +1,240 @@
+"""GPU parity of kvq_quantize and kvq_decode_attention against the oracle.
+
+Codes, scales and zero points must be bit-exact; attention outputs must
+satisfy |o - ref| <= 2e-3 + 2e-3 |ref| against the fp64 oracle fed the same
+dequantised cache.  Small cases are compared element by element (several
+64-token tiles and ragged tails); the full-size workloads are compared on
+sampled rows the oracle can compute one by one.
+"""
+import numpy as np
+import pytest
+
+from oracle import kvq_oracle as O
+import kvq_workloads as W
+from tests import kvq_testutil as U
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from attention_group_quantized_gb300 import kvq
+    kvq.lib()
+
+
+def _kvq():
+    from attention_group_quantized_gb300 import kvq
+    return kvq
+
+
+def _quantized_caches(inp: W.DecodeInputs, fill_garbage=True):
+    kvq = _kvq()
+    B, Hkv, Tcap, D = inp.B, inp.Hkv, inp.Tcap, inp.D
+    kc = kvq.empty_cache(inp.head_bits, B, Tcap, D)
+    vc = kvq.empty_cache(inp.head_bits, B, Tcap, D)
+    if fill_garbage:   # stale cache contents past each sequence must never matter
+        for c in (kc, vc):
+            c.codes.fill_(0xA5)
+            c.sz.fill_(-1)       # fp16 NaN scale and zero
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kd, vd = U.to_dev_bf16(inp.k), U.to_dev_bf16(inp.v)
+    kvq.quantize(kd, kc, 0, status)
+    kvq.quantize(vd, vc, 0, status)
+    return kc, vc, status
+
+
+def _check_cache_exact(cache, bits_in: np.ndarray, head_bits, lens):
+    """Bit-exact comparison of the cache rows that hold live tokens."""
+    planes, scale, zero = U.read_cache(cache, bits_in.shape[2])
+    o_planes, o_scale, o_zero, deq = U.oracle_quantize(bits_in, head_bits)
+    for b, L in enumerate(lens):
+        for h in range(len(head_bits)):
+            assert np.array_equal(planes[h][b, :L], o_planes[h][b, :L]), (b, h)
+        assert np.array_equal(scale[b, :, :L].view(np.uint16), o_scale[b, :, :L].view(np.uint16)), b
+        assert np.array_equal(zero[b, :, :L].view(np.uint16), o_zero[b, :, :L].view(np.uint16)), b
+    return deq
+
+
+def _run_decode_case(inp: W.DecodeInputs, out_dtype=0):
+    kvq = _kvq()
+    kc, vc, status = _quantized_caches(inp)
+    lens = inp.seq_lens
+    deq_k = _check_cache_exact(kc, inp.k, inp.head_bits, lens)
+    deq_v = _check_cache_exact(vc, inp.v, inp.head_bits, lens)
+    q = U.to_dev_bf16(inp.q)
+    sl = torch.from_numpy(lens.astype(np.int32)).cuda()
+    out = kvq.decode_attention(q, kc, vc, sl, inp.softmax_scale, out_dtype=out_dtype, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = out.float().cpu().numpy()
+    ref = O.decode_attention(inp.q, deq_k, deq_v, lens, inp.softmax_scale)
+    return U.assert_close(got, ref, inp.name)
+
+
+SMALL = [
+    # name, seed, B, Hq, Hkv, D, Tcap, lens, bits
+    ("gqa_int8_ragged", 11, 2, 8, 2, 128, 1024, [1000, 77], "8"),
+    ("int4_ragged", 12, 3, 8, 2, 128, 2048, [1, 1500, 2048], "4"),
+    ("mixed_heads", 13, 2, 16, 4, 128, 640, [640, 333], "mixed"),
+    ("d64_int8_mha", 14, 2, 4, 4, 64, 512, [512, 129], "8"),
+    ("d64_int4_gqa2", 15, 2, 8, 4, 64, 256, [31, 255], "4"),
+    ("edge_lengths", 16, 9, 8, 1, 128, 192, [0, 1, 31, 33, 63, 64, 65, 127, 192], "8"),
+    ("many_sequences", 17, 40, 4, 1, 128, 256, list(np.random.default_rng(0).integers(0, 257, 40)), "mixed"),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_decode_small_parity(case):
+    name, seed, B, Hq, Hkv, D, Tcap, lens, bits = case
+    inp = W.make_decode(name, seed, B, Hq, Hkv, D, Tcap, lens=list(lens), bits=bits,
+                        outliers_per_head=2, outlier_head_mult=8.0)
+    _run_decode_case(inp)
+
+
+def test_decode_bf16_output():
+    inp = W.make_decode("bf16_out", 21, 2, 8, 2, 128, 512, lens=[512, 300], bits="8")
+    _run_decode_case(inp, out_dtype=1)
+
+
+def test_decode_tiny_workload_includes_quantize():
+    inp = W.decode_tiny()
+    _run_decode_case(inp)
+
+
+def test_quantize_strided_input_and_offset_positions():
+    """Quantise a strided view into cache positions t0.. ; bit-exact against the oracle."""
+    kvq = _kvq()
+    rng = np.random.default_rng(5)
+    B, Hkv, T, D, Tcap, t0 = 2, 3, 100, 128, 256, 64
+    x = W.bf16_bits(rng.standard_normal((B, T, Hkv, D)).astype(np.float32) * 3)
+    xd = U.to_dev_bf16(x).permute(0, 2, 1, 3)          # [B][Hkv][T][D] view, strides (T*Hkv*D, D, Hkv*D, 1)
+    for hb in ([8, 8, 8], [4, 8, 4]):
+        c = kvq.empty_cache(np.array(hb, np.int8), B, Tcap, D)
+        kvq.quantize(xd, c, t0)
+        torch.cuda.synchronize()
+        planes, scale, zero = U.read_cache(c, Tcap)
+        o_planes, o_scale, o_zero, _ = U.oracle_quantize(np.ascontiguousarray(x.transpose(0, 2, 1, 3)), hb)
+        for h in range(Hkv):
+            assert np.array_equal(planes[h][:, t0:t0 + T], o_planes[h])
+        assert np.array_equal(scale[:, :, t0:t0 + T].view(np.uint16), o_scale.view(np.uint16))
+        assert np.array_equal(zero[:, :, t0:t0 + T].view(np.uint16), o_zero.view(np.uint16))
+
+
+def test_quantize_special_groups_bit_exact():
+    """All-zero, constant, one-sided, tiny, huge and tie-producing groups."""
+    kvq = _kvq()
+    rng = np.random.default_rng(8)
+    rows = [np.zeros(128), np.full(128, 3.25), -np.abs(rng.standard_normal(128)) - 1,
+            np.abs(rng.standard_normal(128)) * 1e-6, rng.standard_normal(128) * 3e4,
+            np.repeat([-1.0, 3.0, 0.0, 0.5], 32), (np.arange(128) % 16 - 7.5) * 0.125]
+    x = W.bf16_bits(np.stack(rows).astype(np.float32))[None, None]   # [1][1][7][128]
+    for bits in (8, 4):
+        c = kvq.empty_cache(np.array([bits], np.int8), 1, 64, 128)
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        kvq.quantize(U.to_dev_bf16(x), c, 0, status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        planes, scale, zero = U.read_cache(c, 7)
+        o_planes, o_scale, o_zero, _ = U.oracle_quantize(x, [bits])
+        assert np.array_equal(planes[0], o_planes[0])
+        assert np.array_equal(scale.view(np.uint16), o_scale.view(np.uint16))
+        assert np.array_equal(zero.view(np.uint16), o_zero.view(np.uint16))
+
+
+def test_quantize_reports_nonfinite():
+    kvq = _kvq()
+    x = np.zeros((1, 1, 1, 128), np.float32)
+    x[0, 0, 0, 5] = np.inf
+    c = kvq.empty_cache(np.array([8], np.int8), 1, 64, 128)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq.quantize(U.to_dev_bf16(W.bf16_bits(x)), c, 0, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 6
+
+
+def test_decode_reports_length_beyond_capacity():
+    kvq = _kvq()
+    inp = W.make_decode("too_long", 3, 1, 4, 1, 128, 128, lens=[128], bits="8")
+    kc, vc, status = _quantized_caches(inp)
+    sl = torch.tensor([129], dtype=torch.int32, device="cuda")
+    kvq.decode_attention(U.to_dev_bf16(inp.q), kc, vc, sl, 0.0, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+
+
+def test_decode_workspace_too_small_is_rejected():
+    kvq = _kvq()
+    inp = W.make_decode("ws", 3, 1, 4, 1, 128, 128, lens=[128], bits="8")
+    kc, vc, _ = _quantized_caches(inp)
+    sl = torch.tensor([128], dtype=torch.int32, device="cuda")
+    ws = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.decode_attention(U.to_dev_bf16(inp.q), kc, vc, sl, 0.0, workspace=ws)
+    assert e.value.status == 4
+
+
+def test_decode_output_guard_bytes_untouched():
+    kvq = _kvq()
+    inp = W.make_decode("guard", 4, 3, 8, 2, 128, 256, lens=[256, 10, 200], bits="mixed")
+    kc, vc, status = _quantized_caches(inp)
+    n = 3 * 8 * 128
+    buf = torch.full((n + 64,), 12345.0, dtype=torch.float32, device="cuda")
+    out = buf[:n].view(3, 8, 128)
+    kvq.decode_attention(U.to_dev_bf16(inp.q), kc, vc, torch.from_numpy(inp.seq_lens).cuda(), 0.0, out=out)
+    torch.cuda.synchronize()
+    assert torch.all(buf[n:] == 12345.0)
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads: sampled rows
+# ---------------------------------------------------------------------------
+
+def _full_size_check(inp: W.DecodeInputs, n_rows=6, n_tok_rows=2048, seed=0):
+    kvq = _kvq()
+    kc, vc, status = _quantized_caches(inp, fill_garbage=False)
+    q = U.to_dev_bf16(inp.q)
+    sl = torch.from_numpy(inp.seq_lens).cuda()
+    out = kvq.decode_attention(q, kc, vc, sl, inp.softmax_scale, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = out.cpu().numpy()
+    rng = np.random.default_rng(seed)
+    B, Hq, Hkv, D = inp.B, inp.Hq, inp.Hkv, inp.D
+    rep = Hq // Hkv
+    kp, ks, kz = U.read_cache(kc, inp.Tcap)
+    vp, vs, vz = U.read_cache(vc, inp.Tcap)
+    # bit-exact quantisation on sampled token rows
+    for _ in range(4):
+        b = int(rng.integers(B)); h = int(rng.integers(Hkv))
+        L = int(inp.seq_lens[b])
+        rows = rng.integers(0, L, min(n_tok_rows, L))
+        for src, planes, sc, zz in ((inp.k, kp, ks, kz), (inp.v, vp, vs, vz)):
+            op, osc, oz, _ = U.oracle_quantize(src[b:b + 1, h:h + 1, rows], inp.head_bits[h:h + 1])
+            assert np.array_equal(planes[h][b, rows], op[0][0])
+            assert np.array_equal(sc[b, h, rows].view(np.uint16), osc[0, 0].view(np.uint16))
+            assert np.array_equal(zz[b, h, rows].view(np.uint16), oz[0, 0].view(np.uint16))
+    # attention on sampled (sequence, query head) rows
+    for _ in range(n_rows):
+        b = int(rng.integers(B)); hq = int(rng.integers(Hq)); kv = hq // rep
+        L = int(inp.seq_lens[b])
+        _, _, _, kd = U.oracle_quantize(inp.k[b:b + 1, kv:kv + 1, :L], inp.head_bits[kv:kv + 1])
+        _, _, _, vd = U.oracle_quantize(inp.v[b:b + 1, kv:kv + 1, :L], inp.head_bits[kv:kv + 1])
+        qf = O.bf16_to_f32(inp.q[b, hq]).astype(np.float64)
+        ref = O.attention(qf[None], kd[0, 0], vd[0, 0], inp.softmax_scale)[0]
+        U.assert_close(got[b, hq], ref, f"{inp.name} b={b} hq={hq}")
+
+
+def test_full_decode_gqa():
+    _full_size_check(W.decode_gqa())
+
+
+def test_full_decode_long_ragged():
+    _full_size_check(W.decode_long_ragged(), n_rows=4)
+
+
+def test_full_decode_mixed():
+    _full_size_check(W.decode_mixed(), n_rows=4)

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 from oracle import kvq_oracle as O
-from attention_group_quantized_gb300 import workloads as W
+import kvq_workloads as W
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 
