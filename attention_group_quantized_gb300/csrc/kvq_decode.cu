@@ -13,14 +13,19 @@
 //    into equal contiguous ranges, one per persistent CTA (SMs x CTAs/SM), so
 //    ragged lengths cost no load imbalance; each CTA emits one partial
 //    (o, lse) per segment piece it touched.
-//  * Each tile's codes arrive by TMA (2D tensor copies with hardware swizzle,
-//    so the fragment reads below are bank-conflict free) and its scale/zero
-//    words by 1D bulk copies, into a 4-stage mbarrier ring.
+//  * A producer warp streams each tile's codes by TMA (2D tensor copies with
+//    hardware swizzle, so the fragment reads below are bank-conflict free)
+//    and its scale/zero words by 1D bulk copies into a 3-stage ring; per-slot
+//    full/empty mbarriers let the four consumer warps run independently.
 //  * The products run on the tensor cores with exact integer operands: a code
 //    byte becomes the fp16 value 1024 + c by a byte permute, and one fp16
-//    subtraction of (1024 + z) gives c - z exactly.  Q.K(c - z) is summed per
-//    group of 32 channels and scaled by the group's fp32 scale; for P.V the
-//    scale is folded into the probability operand (P * s in fp16).
+//    subtraction of (1024 + z) gives c - z exactly.
+//      S = Q K^T: rows = the query heads of the KV head, columns = tokens;
+//        Q.(c - z) is summed per group of 32 channels and scaled by the
+//        group's fp32 scale.
+//      O^T = V^T P^T: rows = channels, columns = query heads; the channel's
+//        scale is applied in fp16 ((c - z) * s, one rounding), and P comes
+//        straight from the S accumulator registers (same fragment layout).
 //  * One CTA serves all query heads of a KV head, so every cache byte is read
 //    once for the whole GQA group.
 #include <cfloat>
@@ -32,9 +37,10 @@ namespace kvq {
 namespace {
 
 constexpr int kTile = 64;       // tokens per pipeline stage
-constexpr int kWarps = 4;       // each warp owns 16 tokens of a tile
-constexpr int kStages = 4;
-constexpr int kMaxRep = 8;      // query heads per KV head (rows of the MMA)
+constexpr int kWarps = 4;       // consumer warps; each owns 16 tokens of a tile
+constexpr int kThreads = (kWarps + 1) * 32;
+constexpr int kStages = 3;
+constexpr int kMaxRep = 8;      // query heads per KV head
 
 struct DParams {
   CUtensorMap tm_k8, tm_k4, tm_v8, tm_v4;
@@ -60,12 +66,11 @@ struct Smem {
   static constexpr int kCodeBytes = kTile * D;          // room for an 8-bit tile
   static constexpr int kSzBytes = kTile * G * 4;
   static constexpr int kStageBytes = 2 * kCodeBytes + 2 * kSzBytes;
-  // layout: [stages][kc | vc | ksz | vsz], merge scratch, barriers, prefix array
-  static constexpr int kStagesBytes = kStages * kStageBytes;
+  // a finished slot doubles as the merge scratch of a piece end
   static constexpr int kMergeO = kWarps * kMaxRep * D * 4;
-  static constexpr int kMergeML = kWarps * kMaxRep * 2 * 4;
-  static constexpr int kBars = kStages * 8;
-  static constexpr int kFixed = kStagesBytes + kMergeO + kMergeML + kBars;
+  static_assert(kMergeO + kWarps * kMaxRep * 8 <= kStageBytes, "merge scratch must fit a stage");
+  static constexpr int kBars = (2 * kStages + 1) * 8;
+  static constexpr int kFixed = kStages * kStageBytes + kBars;
   static size_t bytes(int B) { return 1024 + kFixed + static_cast<size_t>(B + 1) * 4 * 2; }
 };
 
@@ -85,8 +90,8 @@ __device__ __forceinline__ uint32_t lds32(const uint8_t* base, uint32_t off) {
 __device__ __forceinline__ uint2 lds64(const uint8_t* base, uint32_t off) {
   return *reinterpret_cast<const uint2*>(base + off);
 }
-__device__ __forceinline__ uint32_t lds16(const uint8_t* base, uint32_t off) {
-  return *reinterpret_cast<const uint16_t*>(base + off);
+__device__ __forceinline__ uint4 lds128(const uint8_t* base, uint32_t off) {
+  return *reinterpret_cast<const uint4*>(base + off);
 }
 
 // Position in the flat work list: sequence b, KV head, tile index i.
@@ -106,14 +111,13 @@ __device__ __forceinline__ void advance(Cursor& c, const int32_t* pre, int B, in
 }
 
 __device__ __forceinline__ Cursor locate(int64_t f, const int32_t* pre, int B, int Hkv) {
-  // largest b with Hkv * pre[b] <= f (and a non-empty sequence)
+  // largest b with Hkv * pre[b] <= f; it is a non-empty sequence because f < Hkv * pre[B]
   int lo = 0, hi = B - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (static_cast<int64_t>(Hkv) * pre[mid] <= f) lo = mid; else hi = mid - 1;
   }
-  int b = lo;
-  while (pre[b + 1] == pre[b]) ++b;  // skip empty sequences sharing the same prefix
+  const int b = lo;
   const int n = pre[b + 1] - pre[b];
   const int64_t off = f - static_cast<int64_t>(Hkv) * pre[b];
   Cursor c;
@@ -123,8 +127,8 @@ __device__ __forceinline__ Cursor locate(int64_t f, const int32_t* pre, int B, i
   return c;
 }
 
-// Q fragments (A operand rows = query heads of the group, zero above rep),
-// channel order matching the code unpacking of the given bit-width.
+// Q fragments for S = Q K^T (A operand rows = query heads of the group, zero
+// from rep up), channel order matching the code unpacking of the bit-width.
 template <int D>
 __device__ __forceinline__ void load_q(uint32_t (&qa)[D / 32][2][2], const DParams& p, int b, int kvh,
                                        int bits, int g, int t) {
@@ -149,7 +153,7 @@ __device__ __forceinline__ void load_q(uint32_t (&qa)[D / 32][2][2], const DPara
 #pragma unroll
       for (int i = 0; i < 8; ++i) f[i] = 0.0f;
     }
-    if (bits == 8) {  // byte order: half 0 = ch 0..3, half 1 = ch 4..7
+    if (bits == 8) {  // byte order: k-step 0 = ch 0..3, k-step 1 = ch 4..7
       qa[grp][0][0] = pack_half2(f[0], f[1]);
       qa[grp][0][1] = pack_half2(f[2], f[3]);
       qa[grp][1][0] = pack_half2(f[4], f[5]);
@@ -163,9 +167,9 @@ __device__ __forceinline__ void load_q(uint32_t (&qa)[D / 32][2][2], const DPara
   }
 }
 
-// Scores of one warp's 16 tokens for its head row g: S[j][e] is token
-// 8j + 2t + e of the warp's slice, summed per group and scaled by that
-// token's group scale.
+// Scores of one warp's 16 tokens for head row g: S[j][e] belongs to token
+// 16w + 8j + 2t + e of the tile.  Thread (g, t) feeds the codes of token
+// 16w + 8j + g (B operand) and receives the scores of tokens 8j + 2t + e.
 template <int D, int BITS>
 __device__ __forceinline__ void qk_tile(float (&S)[2][2], const uint32_t (&qa)[D / 32][2][2],
                                         const uint8_t* kc, const uint32_t* ksz, int w, int g, int t) {
@@ -173,13 +177,28 @@ __device__ __forceinline__ void qk_tile(float (&S)[2][2], const uint32_t (&qa)[D
   constexpr int R = D * BITS / 8;
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    S[j][0] = 0.0f;
-    S[j][1] = 0.0f;
-    const int row = 16 * w + 8 * j + g;         // token whose codes this thread feeds
-    const int ta = 16 * w + 8 * j + 2 * t;      // tokens whose scores this thread receives
+    const int row = 16 * w + 8 * j + g;
+    const int ta = 16 * w + 8 * j + 2 * t;
+    uint32_t zrow[G], s0[G], s1[G];
+    if constexpr (G == 4) {
+      const uint4 a = *reinterpret_cast<const uint4*>(ksz + row * 4);
+      const uint4 b0 = *reinterpret_cast<const uint4*>(ksz + ta * 4);
+      const uint4 b1 = *reinterpret_cast<const uint4*>(ksz + (ta + 1) * 4);
+      zrow[0] = a.x; zrow[1] = a.y; zrow[2] = a.z; zrow[3] = a.w;
+      s0[0] = b0.x; s0[1] = b0.y; s0[2] = b0.z; s0[3] = b0.w;
+      s1[0] = b1.x; s1[1] = b1.y; s1[2] = b1.z; s1[3] = b1.w;
+    } else {
+      const uint2 a = *reinterpret_cast<const uint2*>(ksz + row * 2);
+      const uint2 b0 = *reinterpret_cast<const uint2*>(ksz + ta * 2);
+      const uint2 b1 = *reinterpret_cast<const uint2*>(ksz + (ta + 1) * 2);
+      zrow[0] = a.x; zrow[1] = a.y;
+      s0[0] = b0.x; s0[1] = b0.y;
+      s1[0] = b1.x; s1[1] = b1.y;
+    }
+    float acc0 = 0.0f, acc1 = 0.0f;
 #pragma unroll
     for (int grp = 0; grp < G; ++grp) {
-      const uint32_t zb = zero_biased2(ksz[row * G + grp]);
+      const uint32_t zb = zero_biased2(zrow[grp]);
       float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       if constexpr (BITS == 8) {
         const uint2 cw = lds64(kc, swz<R>(row, grp * 32 + t * 8));
@@ -194,93 +213,151 @@ __device__ __forceinline__ void qk_tile(float (&S)[2][2], const uint32_t (&qa)[D
         mma_16816(c, qa[grp][1][0], 0u, qa[grp][1][1], 0u, hsub2_u32(nib_biased(cw >> 8), zb),
                   hsub2_u32(nib_biased(cw >> 12), zb));
       }
-      S[j][0] = fmaf(half_lo(ksz[ta * G + grp]), c[0], S[j][0]);
-      S[j][1] = fmaf(half_lo(ksz[(ta + 1) * G + grp]), c[1], S[j][1]);
+      acc0 = fmaf(half_lo(s0[grp]), c[0], acc0);
+      acc1 = fmaf(half_lo(s1[grp]), c[1], acc1);
     }
+    S[j][0] = acc0;
+    S[j][1] = acc1;
   }
 }
 
-// O[4*grp + q] += (P * s_v) (c_v - z_v) for the warp's 16 tokens.  Thread
-// (g, t) feeds channel 32*grp + 4*g + q of tokens 2t, 2t+1 (k = 0..7) and
-// 8+2t, 9+2t (k = 8..15); its accumulators hold channels 32*grp + 8t + q
-// (c0) and 32*grp + 8t + 4 + q (c1) of head g.
+// O^T[ch][h] += V_hat^T[ch][tok] P^T[tok][h] over the warp's 16 tokens.
+// A operand (rows = channels, k = tokens): thread (g, t) supplies channels
+// CPT*g + m (row g of m-tile m) and CPT*g + CPT/2 + m (row g + 8), CPT = D/8,
+// of tokens 2t, 2t+1 (k 0..7) and 8+2t, 9+2t (k 8..15).  B operand (k =
+// tokens, n = heads) is P straight from the score fragments.  Accumulator
+// O[m]: c0/c1 = heads 2t, 2t+1 of the row-g channel, c2/c3 of the row-(g+8)
+// channel.  Tokens past the sequence end read as s = 0, z = 0, so stale
+// cache words cannot poison O.
 template <int D, int BITS>
-__device__ __forceinline__ void pv_tile(float (&O)[D / 8][4], const float (&P)[2][2], const uint8_t* vc,
-                                        const uint32_t* vsz, const bool (&valid)[2][2], int w, int g,
-                                        int t) {
+__device__ __forceinline__ void pv_tile(float (&O)[D / 16][4], const uint32_t (&pb)[2], const uint8_t* vc,
+                                        const uint32_t* vsz, const bool (&valid)[2][2], int w, int g, int t) {
   constexpr int G = D / 32;
   constexpr int R = D * BITS / 8;
+  constexpr int CPT = D / 8;            // channels per thread (16 or 8)
+  constexpr int HALF = CPT / 2;         // channels per row half = m-tiles
+  const int grp = (g * CPT) / 32;       // all of a thread's channels share one group
   int rows[2][2];
+  uint32_t word[2][2];
 #pragma unroll
   for (int j = 0; j < 2; ++j)
 #pragma unroll
-    for (int e = 0; e < 2; ++e) rows[j][e] = 16 * w + 8 * j + 2 * t + e;
+    for (int e = 0; e < 2; ++e) {
+      rows[j][e] = 16 * w + 8 * j + 2 * t + e;
+      word[j][e] = valid[j][e] ? vsz[rows[j][e] * G + grp] : 0u;
+    }
+  // (s_a, s_b) and (1024 + z_a, 1024 + z_b) for the token pairs j = 0, 1
+  uint32_t s2[2], zb[2];
 #pragma unroll
-  for (int grp = 0; grp < G; ++grp) {
-    uint32_t wz[2][2];
-    float s[2][2];
+  for (int j = 0; j < 2; ++j) {
+    s2[j] = prmt(word[j][0], word[j][1], 0x5410u);
+    zb[j] = zero_biased_pair(word[j][0], word[j][1]);
+  }
+  // exact (c - z) then one fp16 rounding of (c - z) * s, for a token pair
+  auto deq = [&](uint32_t biased, int j) -> uint32_t {
+    uint32_t d = hsub2_u32(biased, zb[j]);
+    __half2 r = __hmul2(*reinterpret_cast<__half2*>(&d), *reinterpret_cast<const __half2*>(&s2[j]));
+    return *reinterpret_cast<uint32_t*>(&r);
+  };
+  uint32_t A[2][2][HALF];   // [token pair j][row half][m]
+  if constexpr (BITS == 8) {
+    // per token: CPT bytes = channels [CPT*g, CPT*g + CPT), word wi = channels 4wi .. 4wi+3
+    uint32_t wv[2][2][CPT / 4];
 #pragma unroll
     for (int j = 0; j < 2; ++j)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        // tokens past the sequence end may hold stale words: force s = 0, z = 0
-        const uint32_t word = valid[j][e] ? vsz[rows[j][e] * G + grp] : 0u;
-        wz[j][e] = word;
-        s[j][e] = half_lo(word);
+        if constexpr (CPT == 16) {
+          const uint4 v = lds128(vc, swz<R>(rows[j][e], g * 16));
+          wv[j][e][0] = v.x; wv[j][e][1] = v.y; wv[j][e][2] = v.z; wv[j][e][3] = v.w;
+        } else {
+          const uint2 v = lds64(vc, swz<R>(rows[j][e], g * 8));
+          wv[j][e][0] = v.x; wv[j][e][1] = v.y;
+        }
       }
-    const uint32_t a0 = pack_half2(P[0][0] * s[0][0], P[0][1] * s[0][1]);
-    const uint32_t a2 = pack_half2(P[1][0] * s[1][0], P[1][1] * s[1][1]);
-    const uint32_t zb0 = zero_biased_pair(wz[0][0], wz[0][1]);
-    const uint32_t zb1 = zero_biased_pair(wz[1][0], wz[1][1]);
-    if constexpr (BITS == 8) {
-      const uint32_t w00 = lds32(vc, swz<R>(rows[0][0], grp * 32 + g * 4));
-      const uint32_t w01 = lds32(vc, swz<R>(rows[0][1], grp * 32 + g * 4));
-      const uint32_t w10 = lds32(vc, swz<R>(rows[1][0], grp * 32 + g * 4));
-      const uint32_t w11 = lds32(vc, swz<R>(rows[1][1], grp * 32 + g * 4));
-      const uint32_t x0 = prmt(w00, w01, 0x5140u), x1 = prmt(w00, w01, 0x7362u);
-      const uint32_t y0 = prmt(w10, w11, 0x5140u), y1 = prmt(w10, w11, 0x7362u);
-      mma_16816(O[4 * grp + 0], a0, 0u, a2, 0u, hsub2_u32(bytes01_biased(x0), zb0),
-                hsub2_u32(bytes01_biased(y0), zb1));
-      mma_16816(O[4 * grp + 1], a0, 0u, a2, 0u, hsub2_u32(bytes23_biased(x0), zb0),
-                hsub2_u32(bytes23_biased(y0), zb1));
-      mma_16816(O[4 * grp + 2], a0, 0u, a2, 0u, hsub2_u32(bytes01_biased(x1), zb0),
-                hsub2_u32(bytes01_biased(y1), zb1));
-      mma_16816(O[4 * grp + 3], a0, 0u, a2, 0u, hsub2_u32(bytes23_biased(x1), zb0),
-                hsub2_u32(bytes23_biased(y1), zb1));
-    } else {
-      const uint32_t x = lds16(vc, swz<R>(rows[0][0], grp * 16 + g * 2)) |
-                         (lds16(vc, swz<R>(rows[0][1], grp * 16 + g * 2)) << 16);
-      const uint32_t y = lds16(vc, swz<R>(rows[1][0], grp * 16 + g * 2)) |
-                         (lds16(vc, swz<R>(rows[1][1], grp * 16 + g * 2)) << 16);
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        mma_16816(O[4 * grp + q], a0, 0u, a2, 0u, hsub2_u32(nib_biased(x >> (4 * q)), zb0),
-                  hsub2_u32(nib_biased(y >> (4 * q)), zb1));
-    }
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+        for (int wq = 0; wq < HALF / 4; ++wq) {
+          const int wi = hr * (HALF / 4) + wq;
+          const uint32_t x0 = prmt(wv[j][0][wi], wv[j][1][wi], 0x5140u);  // bytes 0,1 of both tokens
+          const uint32_t x1 = prmt(wv[j][0][wi], wv[j][1][wi], 0x7362u);  // bytes 2,3
+          A[j][hr][4 * wq + 0] = deq(bytes01_biased(x0), j);
+          A[j][hr][4 * wq + 1] = deq(bytes23_biased(x0), j);
+          A[j][hr][4 * wq + 2] = deq(bytes01_biased(x1), j);
+          A[j][hr][4 * wq + 3] = deq(bytes23_biased(x1), j);
+        }
+  } else {
+    // per token: CPT/2 bytes; nibble n of the thread's chunk = channel CPT*g + n
+    uint32_t wv[2][2][CPT / 8];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        if constexpr (CPT == 16) {
+          const uint2 v = lds64(vc, swz<R>(rows[j][e], g * 8));
+          wv[j][e][0] = v.x; wv[j][e][1] = v.y;
+        } else {
+          wv[j][e][0] = lds32(vc, swz<R>(rows[j][e], g * 4));
+        }
+      }
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int base = hr * HALF;                  // first nibble of this row half
+        const int sh = (base % 8) * 4;
+        const uint32_t a0 = wv[j][0][base / 8] >> sh, a1 = wv[j][1][base / 8] >> sh;
+        const uint32_t ev0 = a0 & 0x0F0F0F0Fu, ev1 = a1 & 0x0F0F0F0Fu;                // nibbles 0,2,4,6
+        const uint32_t od0 = (a0 >> 4) & 0x0F0F0F0Fu, od1 = (a1 >> 4) & 0x0F0F0F0Fu;  // nibbles 1,3,5,7
+        const uint32_t e01 = prmt(ev0, ev1, 0x5140u), o01 = prmt(od0, od1, 0x5140u);
+        A[j][hr][0] = deq(bytes01_biased(e01), j);
+        A[j][hr][1] = deq(bytes01_biased(o01), j);
+        A[j][hr][2] = deq(bytes23_biased(e01), j);
+        A[j][hr][3] = deq(bytes23_biased(o01), j);
+        if constexpr (HALF == 8) {
+          const uint32_t e23 = prmt(ev0, ev1, 0x7362u), o23 = prmt(od0, od1, 0x7362u);
+          A[j][hr][4] = deq(bytes01_biased(e23), j);
+          A[j][hr][5] = deq(bytes01_biased(o23), j);
+          A[j][hr][6] = deq(bytes23_biased(e23), j);
+          A[j][hr][7] = deq(bytes23_biased(o23), j);
+        }
+      }
   }
+#pragma unroll
+  for (int m = 0; m < HALF; ++m) mma_16816(O[m], A[0][0][m], A[0][1][m], A[1][0][m], A[1][1][m], pb[0], pb[1]);
 }
 
 template <int D>
-__global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant__ DParams p) {
+__global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const __grid_constant__ DParams p) {
   using L = Smem<D>;
   constexpr int G = D / 32;
+  constexpr int CPT = D / 8;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* m_o = reinterpret_cast<float*>(smem + L::kStagesBytes);
-  float* m_ml = reinterpret_cast<float*>(smem + L::kStagesBytes + L::kMergeO);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kStagesBytes + L::kMergeO + L::kMergeML);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * L::kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* gbar = empty + kStages;       // consumer-group barrier for piece ends
   int32_t* pre = reinterpret_cast<int32_t*>(smem + L::kFixed);
   int32_t* lens = pre + (p.B + 1);
+
+  // let the merge grid get scheduled early; it waits for this grid's completion itself
+  asm volatile("griddepcontrol.launch_dependents;");
 
   const int tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int B = p.B, Hkv = p.Hkv;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
+    }
+    mbar_init(gbar, kWarps);
     fence_barrier_init();
   }
-  // per-sequence tile counts and their prefix sums (warp 0)
   for (int b = tid; b < B; b += blockDim.x) {
     int L0 = p.seq_lens[b];
     if (L0 < 0 || L0 > p.Tcap) {
@@ -290,7 +367,7 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant
     lens[b] = L0;
   }
   __syncthreads();
-  if (w == 0) {
+  if (w == 0) {  // per-sequence tile counts and their prefix sums
     int carry = 0;
     for (int b0 = 0; b0 < B; b0 += 32) {
       const int b = b0 + lane;
@@ -316,51 +393,61 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant
   const int ntiles = static_cast<int>(f1 - f0);
   if (ntiles <= 0) return;
 
-  // ---- producer: thread 0 keeps kStages-1 tiles in flight ----
-  Cursor pc = locate(f0, pre, B, Hkv);
-  auto issue = [&](int k, const Cursor& c) {
-    uint8_t* st = smem + (k % kStages) * L::kStageBytes;
-    const int bits = p.bits[c.kvh];
-    const int R = D * bits / 8;
-    const int32_t row0 = (p.plane[c.kvh] * B + c.b) * p.Tcap + c.i * kTile;
-    const int64_t szoff = (static_cast<int64_t>(c.kvh) * B + c.b) * p.Tcap + static_cast<int64_t>(c.i) * kTile;
-    uint64_t* bar = &full[k % kStages];
-    mbar_arrive_expect_tx(bar, 2 * kTile * R + 2 * L::kSzBytes);
-    tma_2d_g2s(st, bits == 8 ? &p.tm_k8 : &p.tm_k4, 0, row0, bar);
-    tma_2d_g2s(st + L::kCodeBytes, bits == 8 ? &p.tm_v8 : &p.tm_v4, 0, row0, bar);
-    bulk_g2s(st + 2 * L::kCodeBytes, p.k_sz + szoff * G, L::kSzBytes, bar);
-    bulk_g2s(st + 2 * L::kCodeBytes + L::kSzBytes, p.v_sz + szoff * G, L::kSzBytes, bar);
-  };
-  if (tid == 0) {
-    for (int k = 0; k < kStages - 1 && k < ntiles; ++k) {
-      issue(k, pc);
+  if (w == kWarps) {
+    // ---------------- producer warp: one thread streams the tiles ----------------
+    if (lane != 0) return;
+    Cursor pc = locate(f0, pre, B, Hkv);
+    for (int k = 0; k < ntiles; ++k) {
+      const int slot = k % kStages;
+      if (k >= kStages && !mbar_wait(&empty[slot], ((k / kStages) - 1) & 1, p.status)) return;
+      uint8_t* st = smem + slot * L::kStageBytes;
+      const int bits = p.bits[pc.kvh];
+      const int R = D * bits / 8;
+      const int32_t row0 = (p.plane[pc.kvh] * B + pc.b) * p.Tcap + pc.i * kTile;
+      const int64_t szoff = (static_cast<int64_t>(pc.kvh) * B + pc.b) * p.Tcap + static_cast<int64_t>(pc.i) * kTile;
+      uint64_t* bar = &full[slot];
+      mbar_arrive_expect_tx(bar, 2 * kTile * R + 2 * L::kSzBytes);
+      tma_2d_g2s(st, bits == 8 ? &p.tm_k8 : &p.tm_k4, 0, row0, bar);
+      tma_2d_g2s(st + L::kCodeBytes, bits == 8 ? &p.tm_v8 : &p.tm_v4, 0, row0, bar);
+      bulk_g2s(st + 2 * L::kCodeBytes, p.k_sz + szoff * G, L::kSzBytes, bar);
+      bulk_g2s(st + 2 * L::kCodeBytes + L::kSzBytes, p.v_sz + szoff * G, L::kSzBytes, bar);
       advance(pc, pre, B, Hkv);
     }
+    return;
   }
 
-  // ---- consumers: all four warps ----
+  // ---------------- consumers: four warps ----------------
   Cursor cc = locate(f0, pre, B, Hkv);
   uint32_t qa[G][2][2];
-  float O[D / 8][4];
+  float O[D / 16][4];
   float m_run = -INFINITY, l_run = 0.0f;
   bool piece_start = true;
+  bool ok = true;
+  uint32_t gphase = 0;
+  // bounded barrier among the four consumer warps (a plain bar.sync could wait forever
+  // if one warp left after a timed-out wait)
+  auto group_sync = [&]() {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(gbar);
+    ok = ok && mbar_wait(gbar, gphase & 1, p.status);
+    ++gphase;
+    __syncwarp();
+  };
 
   for (int k = 0; k < ntiles; ++k) {
-    if (tid == 0 && k + kStages - 1 < ntiles) {
-      issue(k + kStages - 1, pc);
-      advance(pc, pre, B, Hkv);
-    }
+    const int slot = k % kStages;
     const int bits = p.bits[cc.kvh];
     const int n_b = pre[cc.b + 1] - pre[cc.b];
     if (piece_start) {
       load_q<D>(qa, p, cc.b, cc.kvh, bits, g, t);
 #pragma unroll
-      for (int i = 0; i < D / 8; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.0f;
+      for (int i = 0; i < D / 16; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.0f;
       m_run = -INFINITY;
       l_run = 0.0f;
     }
-    const bool ok = mbar_wait(&full[k % kStages], (k / kStages) & 1, p.status);
-    const uint8_t* st = smem + (k % kStages) * L::kStageBytes;
+    ok = ok && mbar_wait(&full[slot], (k / kStages) & 1, p.status);
+    if (!ok) break;   // a timed-out wait ends this warp (status already set)
+    uint8_t* st = smem + slot * L::kStageBytes;
     const uint8_t* kc = st;
     const uint8_t* vc = st + L::kCodeBytes;
     const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + 2 * L::kCodeBytes);
@@ -370,7 +457,7 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant
     if (bits == 8) qk_tile<D, 8>(S, qa, kc, ksz, w, g, t);
     else qk_tile<D, 4>(S, qa, kc, ksz, w, g, t);
 
-    // mask past the sequence end, move to the log2 domain, online softmax
+    // mask past the sequence end, move to the log2 domain, online softmax per head row g
     const int len = lens[cc.b];
     bool valid[2][2];
     float mx = -INFINITY;
@@ -399,37 +486,46 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant
     l_run = l_run * alpha + psum;
     m_run = m_new;
     if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+      // O^T columns are heads 2t, 2t+1; their factors live in rows g = 2t, 2t+1
+      const float a0 = __shfl_sync(0xffffffffu, alpha, (2 * t) << 2);
+      const float a1 = __shfl_sync(0xffffffffu, alpha, (2 * t + 1) << 2);
 #pragma unroll
-      for (int i = 0; i < D / 8; ++i) {
-        O[i][0] *= alpha;
-        O[i][1] *= alpha;
+      for (int i = 0; i < D / 16; ++i) {
+        O[i][0] *= a0; O[i][1] *= a1;
+        O[i][2] *= a0; O[i][3] *= a1;
       }
     }
-    if (bits == 8) pv_tile<D, 8>(O, P, vc, vsz, valid, w, g, t);
-    else pv_tile<D, 4>(O, P, vc, vsz, valid, w, g, t);
+    const uint32_t pb[2] = {pack_half2(P[0][0], P[0][1]), pack_half2(P[1][0], P[1][1])};
+    if (bits == 8) pv_tile<D, 8>(O, pb, vc, vsz, valid, w, g, t);
+    else pv_tile<D, 4>(O, pb, vc, vsz, valid, w, g, t);
 
     // ---- end of a piece: merge the four warps and write the partial ----
     const bool piece_end = (cc.i == n_b - 1) || (k == ntiles - 1);
     if (piece_end) {
       float l_tot = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
       l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
-      if (g < p.rep) {
-        if (t == 0) {
-          m_ml[(w * kMaxRep + g) * 2 + 0] = m_run;
-          m_ml[(w * kMaxRep + g) * 2 + 1] = l_tot;
-        }
-        float* dst = m_o + (w * kMaxRep + g) * D;
-#pragma unroll
-        for (int grp = 0; grp < G; ++grp)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            dst[grp * 32 + 8 * t + q] = O[4 * grp + q][0];
-            dst[grp * 32 + 8 * t + 4 + q] = O[4 * grp + q][1];
-          }
+      float* m_o = reinterpret_cast<float*>(st);                 // this slot, once every warp is done with it
+      float* m_ml = reinterpret_cast<float*>(st + L::kMergeO);
+      group_sync();
+      if (t == 0 && g < p.rep) {
+        m_ml[(w * kMaxRep + g) * 2 + 0] = m_run;
+        m_ml[(w * kMaxRep + g) * 2 + 1] = l_tot;
       }
-      __syncthreads();
-      const int slot = cc.b * Hkv + cc.kvh + blockIdx.x;
-      for (int idx = tid; idx < p.rep * D; idx += blockDim.x) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int h = 2 * t + e;
+        if (h < p.rep) {
+          float* dst = m_o + (w * kMaxRep + h) * D;
+#pragma unroll
+          for (int m = 0; m < D / 16; ++m) {
+            dst[CPT * g + m] = O[m][e];
+            dst[CPT * g + CPT / 2 + m] = O[m][2 + e];
+          }
+        }
+      }
+      group_sync();
+      const int slotw = cc.b * Hkv + cc.kvh + blockIdx.x;
+      for (int idx = tid; idx < p.rep * D; idx += kWarps * 32) {
         const int h = idx / D, ch = idx % D;
         float M = -INFINITY;
 #pragma unroll
@@ -444,15 +540,18 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant
           }
         }
         const bool any = M != -INFINITY && Lsum > 0.0f;
-        p.ws_o[(static_cast<int64_t>(slot) * p.rep + h) * D + ch] = any ? o / Lsum : 0.0f;
-        if (ch == 0) p.ws_lse[static_cast<int64_t>(slot) * p.rep + h] = any ? M + __log2f(Lsum) : -INFINITY;
+        p.ws_o[(static_cast<int64_t>(slotw) * p.rep + h) * D + ch] = any ? o / Lsum : 0.0f;
+        if (ch == 0) p.ws_lse[static_cast<int64_t>(slotw) * p.rep + h] = any ? M + __log2f(Lsum) : -INFINITY;
       }
+      group_sync();                                              // scratch read before the slot is refilled
       piece_start = true;
     } else {
       piece_start = false;
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
     advance(cc, pre, B, Hkv);
-    if (__syncthreads_or(!ok)) break;  // a timed-out wait ends the CTA (status already set)
+    if (!ok) break;
   }
 }
 
@@ -460,6 +559,7 @@ __global__ void __launch_bounds__(128) decode_split_kernel(const __grid_constant
 template <int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant__ DParams p) {
   constexpr int V = D / 32;  // channels per lane
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (gw >= p.B * p.Hq) return;
@@ -477,24 +577,38 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant
     const int64_t last = start + n_b - 1;
     const int c0 = static_cast<int>(((start + 1) * C - 1) / N);
     const int c1 = static_cast<int>(((last + 1) * C - 1) / N);
-    const int seg = b * Hkv + kvh;
-    float M = -INFINITY, Lsum = 0.0f;
-    for (int c = c0; c <= c1; ++c) {
-      if (N * (c + 1) / C == N * c / C) continue;  // CTA with an empty range
-      const int64_t slot = seg + c;
-      const float lse = p.ws_lse[slot * p.rep + r];
-      if (lse == -INFINITY) continue;
-      const float* o = p.ws_o + (slot * p.rep + r) * D + lane * V;
-      const float M2 = fmaxf(M, lse);
-      const float a = fast_exp2(M - M2), bb = fast_exp2(lse - M2);
-#pragma unroll
-      for (int i = 0; i < V; ++i) acc[i] = acc[i] * a + o[i] * bb;
-      Lsum = Lsum * a + bb;
-      M = M2;
+    const int64_t seg = static_cast<int64_t>(b) * Hkv + kvh;
+    // pass 1: pieces spread over the lanes -> the largest lse
+    float M = -INFINITY;
+    for (int c = c0 + lane; c <= c1; c += 32) {
+      if (N * (c + 1) / C == N * c / C) continue;  // a CTA with an empty range wrote nothing
+      M = fmaxf(M, p.ws_lse[(seg + c) * p.rep + r]);
     }
-    if (Lsum > 0.0f) {
 #pragma unroll
-      for (int i = 0; i < V; ++i) acc[i] /= Lsum;
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    // pass 2: weighted sum of the partial outputs (loads independent of each other)
+    float Lsum = 0.0f;
+    if (M != -INFINITY) {
+      for (int c = c0; c <= c1; ++c) {
+        if (N * (c + 1) / C == N * c / C) continue;
+        const int64_t slot = seg + c;
+        const float lse = p.ws_lse[slot * p.rep + r];
+        const float wgt = lse == -INFINITY ? 0.0f : fast_exp2(lse - M);
+        const float* o = p.ws_o + (slot * p.rep + r) * D + lane * V;
+        if constexpr (V == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(o);
+          acc[0] = fmaf(wgt, v.x, acc[0]); acc[1] = fmaf(wgt, v.y, acc[1]);
+          acc[2] = fmaf(wgt, v.z, acc[2]); acc[3] = fmaf(wgt, v.w, acc[3]);
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(o);
+          acc[0] = fmaf(wgt, v.x, acc[0]); acc[1] = fmaf(wgt, v.y, acc[1]);
+        }
+        Lsum += wgt;
+      }
+      if (Lsum > 0.0f) {
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] /= Lsum;
+      }
     }
   }
   const int64_t orow = (static_cast<int64_t>(b) * p.Hq + hq) * D + lane * V;
@@ -511,17 +625,40 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant
 
 template <int D>
 int ctas_per_sm() {
-  static int cached = -1;
-  if (cached < 0) {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev] == 0) {
     int n = 0;
     const size_t sm = Smem<D>::bytes(64);
     cudaFuncSetAttribute(decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(Smem<D>::bytes(4096)));
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<D>, 128, sm) != cudaSuccess || n < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<D>, kThreads, sm) != cudaSuccess ||
+        n < 1)
       n = 1;
-    cached = n;
+    cached[dev] = n;
   }
-  return cached;
+  return cached[dev];
+}
+
+template <int D>
+cudaError_t launch_pair(const DParams& p, int C, int B, int Hq, cudaStream_t stream) {
+  decode_split_kernel<D><<<C, kThreads, Smem<D>::bytes(B), stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // the merge may start while the split grid drains (programmatic dependent launch);
+  // it waits for the split grid's completion before reading the partials
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((B * Hq + 3) / 4);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, p);
 }
 
 }  // namespace
@@ -544,10 +681,10 @@ kvq_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const kvq_cache& K = *a.k;
   const kvq_cache& Vc = *a.v;
   const int D = K.D, B = K.B, Hkv = K.Hkv, Tcap = K.Tcap;
+  if (B > 4096) return KVQ_ERR_UNSUPPORTED;  // dynamic shared memory was sized for B <= 4096
   const int C = decode_num_ctas(D);
   const size_t need = decode_workspace_bytes(B, a.Hq, Hkv, D, C);
   if (a.ws == nullptr || a.ws_bytes < need) return KVQ_ERR_WORKSPACE;
-  if (B > 4096) return KVQ_ERR_UNSUPPORTED;  // dynamic shared memory was sized for B <= 4096
 
   DParams p;
   memset(&p, 0, sizeof(p));
@@ -586,19 +723,8 @@ kvq_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.plane[h] = hl.plane_idx[h];
     p.bits[h] = hl.bits[h];
   }
-  const int merge_blocks = (B * a.Hq + 3) / 4;
-  if (D == 128) {
-    const size_t sm = Smem<128>::bytes(B);
-    decode_split_kernel<128><<<C, 128, sm, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
-    decode_merge_kernel<128><<<merge_blocks, 128, 0, stream>>>(p);
-  } else {
-    const size_t sm = Smem<64>::bytes(B);
-    decode_split_kernel<64><<<C, 128, sm, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
-    decode_merge_kernel<64><<<merge_blocks, 128, 0, stream>>>(p);
-  }
-  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+  const cudaError_t e = D == 128 ? launch_pair<128>(p, C, B, a.Hq, stream) : launch_pair<64>(p, C, B, a.Hq, stream);
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
 }  // namespace kvq
