@@ -6,26 +6,34 @@
 // dequantisation happens inside the attention read (same page, §1.3).  The
 // keys are visited tile by tile with an online softmax carrying the running
 // max and normaliser (same page, §2.2); splits of the key range run on
-// different CTAs and a second pass merges them by log-sum-exp.
+// different CTAs and are merged by log-sum-exp.
 //
-// GB300 design (HBM-bound):
+// GB300 design (HBM-bound; the aim is few instructions per cache byte):
 //  * Stream-K split: the (sequence, KV head, 64-token tile) work list is cut
 //    into equal contiguous ranges, one per persistent CTA (SMs x CTAs/SM), so
 //    ragged lengths cost no load imbalance; each CTA emits one partial
-//    (o, lse) per segment piece it touched.
+//    (o, lse) per segment piece it touched, and the CTA that completes a
+//    segment (a per-segment arrival counter) merges its pieces in place -- no
+//    second kernel.  A segment held by one CTA is written out directly.
 //  * A producer warp streams each tile's codes by TMA (2D tensor copies with
-//    hardware swizzle, so the fragment reads below are bank-conflict free)
-//    and its scale/zero words by 1D bulk copies into a 3-stage ring; per-slot
-//    full/empty mbarriers let the four consumer warps run independently.
-//  * The products run on the tensor cores with exact integer operands: a code
-//    byte becomes the fp16 value 1024 + c by a byte permute, and one fp16
-//    subtraction of (1024 + z) gives c - z exactly.
-//      S = Q K^T: rows = the query heads of the KV head, columns = tokens;
-//        Q.(c - z) is summed per group of 32 channels and scaled by the
-//        group's fp32 scale.
-//      O^T = V^T P^T: rows = channels, columns = query heads; the channel's
-//        scale is applied in fp16 ((c - z) * s, one rounding), and P comes
-//        straight from the S accumulator registers (same fragment layout).
+//    hardware swizzle) and its scale/zero words by 1D bulk copies into a
+//    3-stage ring, then turns the scale/zero words into per-tile tables
+//    (fp32 scales, zero terms, tokens past the sequence end zeroed) so the
+//    four consumer warps do no per-group conversions.
+//  * The products run on the tensor cores with exact operands: a code byte
+//    becomes the fp16 value 1024 + c by one byte permute.
+//      S = Q K^T (rows = the query heads of the KV head, columns = tokens),
+//        per group g of 32 channels: C_g = Q.(1024 + c), then
+//        S += s_g C_g - (1024 + z_g) s_g sum_g(Q), which equals s_g Q.(c - z_g).
+//      O^T = V^T P^T (rows = channels, columns = query heads): each MMA's rows
+//        lie in one group g, so its B operand is P * s_g (one fp16 rounding);
+//        A is 1024 + c, and one extra MMA per group accumulates
+//        sum_tok (1024 + z_g) P s_g into a spare row, subtracted at the end.
+//  * Fragments come from the swizzled code tiles by ldmatrix: K as stored
+//    (token rows), V transposed, so each register holds two tokens of two
+//    channels and one byte permute yields a (token, token) pair of a channel.
+//    Every lane's row addresses are fixed, and the swizzle keeps all eight
+//    rows of each 8x8 matrix in distinct banks.
 //  * One CTA serves all query heads of a KV head, so every cache byte is read
 //    once for the whole GQA group.
 #include <cfloat>
@@ -38,8 +46,15 @@ namespace {
 
 constexpr int kTile = 64;       // tokens per pipeline stage
 constexpr int kWarps = 4;       // consumer warps; each owns 16 tokens of a tile
-constexpr int kThreads = (kWarps + 1) * 32;
-constexpr int kStages = 3;
+constexpr int kThreads = (kWarps + 2) * 32;   // + TMA issuer warp + table builder warp
+// pipeline depth and CTAs per SM (tunable at build time)
+#ifndef KVQ_DECODE_STAGES
+#define KVQ_DECODE_STAGES 4
+#endif
+#ifndef KVQ_DECODE_MIN_BLOCKS
+#define KVQ_DECODE_MIN_BLOCKS 2
+#endif
+constexpr int kStages = KVQ_DECODE_STAGES;
 constexpr int kMaxRep = 8;      // query heads per KV head
 
 struct DParams {
@@ -48,7 +63,7 @@ struct DParams {
   const uint32_t* v_sz;
   const uint16_t* q;
   const int32_t* seq_lens;
-  int32_t* ws_pre;      // [B+1] tile prefix sums, written by CTA 0 for the merge
+  int32_t* ws_cnt;      // [B*Hkv] pieces written per segment; zero between calls
   float* ws_lse;        // [slots][rep]
   float* ws_o;          // [slots][rep][D]
   void* out;
@@ -65,14 +80,26 @@ struct Smem {
   static constexpr int G = D / 32;
   static constexpr int kCodeBytes = kTile * D;          // room for an 8-bit tile
   static constexpr int kSzBytes = kTile * G * 4;
-  static constexpr int kStageBytes = 2 * kCodeBytes + 2 * kSzBytes;
+  // offsets inside a stage
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kCodeBytes;
+  static constexpr int kOffKsz = 2 * kCodeBytes;
+  static constexpr int kOffVsz = kOffKsz + kSzBytes;
+  static constexpr int kOffKt = kOffVsz + kSzBytes;        // float2 [G][64 tok]: (s, (1024 + z) s)
+  static constexpr int kOffVtS = kOffKt + kTile * G * 8;   // float [G][64 tok] s
+  static constexpr int kOffVtZ = kOffVtS + kTile * G * 4;  // u16   [G][64 tok] fp16 (1024 + z)
+  static constexpr int kOffMeta = kOffVtZ + kTile * G * 2; // int4 {b, kvh, i | flags, len}
+  static constexpr int kStageBytes = ((kOffMeta + 16 + 1023) / 1024) * 1024;
   // a finished slot doubles as the merge scratch of a piece end
   static constexpr int kMergeO = kWarps * kMaxRep * D * 4;
-  static_assert(kMergeO + kWarps * kMaxRep * 8 <= kStageBytes, "merge scratch must fit a stage");
-  static constexpr int kBars = (2 * kStages + 1) * 8;
+  static_assert(kMergeO + kWarps * kMaxRep * 8 + 16 <= kStageBytes, "merge scratch must fit a stage");
+  static constexpr int kBars = (3 * kStages + 1) * 8;
   static constexpr int kFixed = kStages * kStageBytes + kBars;
   static size_t bytes(int B) { return 1024 + kFixed + static_cast<size_t>(B + 1) * 4 * 2; }
 };
+
+constexpr int kFlagStart = 1 << 30;
+constexpr int kFlagEnd = 1 << 29;
 
 // Byte offset of (row, byte) inside a TMA tile written with the swizzle mode
 // matching its row pitch R (128B, 64B or 32B): the 16-byte chunk index is
@@ -82,16 +109,6 @@ __device__ __forceinline__ uint32_t swz(int row, int byte) {
   if constexpr (R == 128) return row * 128 + ((((byte >> 4) ^ (row & 7)) << 4) | (byte & 15));
   if constexpr (R == 64) return row * 64 + ((((byte >> 4) ^ ((row >> 1) & 3)) << 4) | (byte & 15));
   return row * 32 + ((((byte >> 4) ^ ((row >> 2) & 1)) << 4) | (byte & 15));
-}
-
-__device__ __forceinline__ uint32_t lds32(const uint8_t* base, uint32_t off) {
-  return *reinterpret_cast<const uint32_t*>(base + off);
-}
-__device__ __forceinline__ uint2 lds64(const uint8_t* base, uint32_t off) {
-  return *reinterpret_cast<const uint2*>(base + off);
-}
-__device__ __forceinline__ uint4 lds128(const uint8_t* base, uint32_t off) {
-  return *reinterpret_cast<const uint4*>(base + off);
 }
 
 // Position in the flat work list: sequence b, KV head, tile index i.
@@ -127,224 +144,331 @@ __device__ __forceinline__ Cursor locate(int64_t f, const int32_t* pre, int B, i
   return c;
 }
 
-// Q fragments for S = Q K^T (A operand rows = query heads of the group, zero
-// from rep up), channel order matching the code unpacking of the bit-width.
+// Per-thread shared-memory offsets (from a stage base) of the ldmatrix rows this
+// lane supplies; they do not change from tile to tile.
+//   K (non-transposed): lane l -> token row 16w + (l & 7) (+8 per n-tile), chunk (l >> 3) (+4)
+//   V (transposed):     lane l -> token row 16w + 8(m >> 1) + (l & 7), chunk 2*grp + (m & 1)
+//                       for 8-bit codes, chunk 2*gi + (m & 1) for 4-bit codes, m = l >> 3
+struct LaneAddr {
+  uint32_t k8, k4, v8, v4;
+};
+
+// For the other chunks of the same row the swizzled offset only changes by an
+// XOR: chunk c + 4 flips address bit 6, the next group of V flips bit 5.
 template <int D>
-__device__ __forceinline__ void load_q(uint32_t (&qa)[D / 32][2][2], const DParams& p, int b, int kvh,
-                                       int bits, int g, int t) {
+__device__ __forceinline__ LaneAddr lane_addr(int w, int lane) {
+  constexpr int R8 = D, R4 = D / 2;
+  LaneAddr a;
+  const int r = 16 * w + (lane & 7);
+  const int m = lane >> 3;
+  a.k8 = swz<R8>(r, 16 * m);
+  a.k4 = swz<R4>(r, 16 * (m & (R4 / 16 - 1)));
+  const int vr = 16 * w + 8 * (m >> 1) + (lane & 7);
+  a.v8 = swz<R8>(vr, 16 * (m & 1));
+  a.v4 = swz<R4>(vr, 16 * (m & 1));
+  return a;
+}
+
+// Q fragments of S = Q K^T (A operand rows = the group's query heads, zero from
+// rep up) in the channel order of the code unpacking, and per-group sums of
+// the same fp16 values (reduced over the quad).
+//   8-bit: k-step s (16 channels): cols 2t,2t+1 <-> ch 16s + 4t + {0,1},
+//          cols 2t+8, 2t+9 <-> ch 16s + 4t + {2,3}
+//   4-bit: k-steps 2g, 2g+1 of group g: ch 32g + 8t + {(0,4),(1,5)} and {(2,6),(3,7)}
+template <int D>
+__device__ __forceinline__ void load_q(uint32_t (&qa)[D / 16][2], float (&qsum)[D / 32], const DParams& p,
+                                       int b, int kvh, int bits, int g, int t) {
   constexpr int G = D / 32;
+  const uint16_t* src = p.q + (static_cast<int64_t>(b) * p.Hq + kvh * p.rep + g) * D;
+  bool ok = true;
 #pragma unroll
   for (int grp = 0; grp < G; ++grp) {
-    float f[8];
+    float f[8];   // 8-bit: ch 32grp + {4t..4t+3, 16+4t..16+4t+3}; 4-bit: ch 32grp + 8t + 0..7
     if (g < p.rep) {
-      const uint16_t* src = p.q + (static_cast<int64_t>(b) * p.Hq + kvh * p.rep + g) * D + grp * 32 + t * 8;
-      const uint4 raw = *reinterpret_cast<const uint4*>(src);
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      uint32_t w[4];
+      if (bits == 8) {
+        const uint2 a = *reinterpret_cast<const uint2*>(src + grp * 32 + 4 * t);
+        const uint2 c = *reinterpret_cast<const uint2*>(src + grp * 32 + 16 + 4 * t);
+        w[0] = a.x; w[1] = a.y; w[2] = c.x; w[3] = c.y;
+      } else {
+        const uint4 a = *reinterpret_cast<const uint4*>(src + grp * 32 + 8 * t);
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         f[2 * i] = __uint_as_float(w[i] << 16);
         f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
       }
-      bool ok = true;
 #pragma unroll
       for (int i = 0; i < 8; ++i) ok &= fabsf(f[i]) < 65504.0f;
-      if (!ok) report(p.status, KVQ_ERR_NONFINITE);
     } else {
 #pragma unroll
       for (int i = 0; i < 8; ++i) f[i] = 0.0f;
     }
-    if (bits == 8) {  // byte order: k-step 0 = ch 0..3, k-step 1 = ch 4..7
-      qa[grp][0][0] = pack_half2(f[0], f[1]);
-      qa[grp][0][1] = pack_half2(f[2], f[3]);
-      qa[grp][1][0] = pack_half2(f[4], f[5]);
-      qa[grp][1][1] = pack_half2(f[6], f[7]);
-    } else {          // nibble order: (0,4)(1,5) then (2,6)(3,7)
-      qa[grp][0][0] = pack_half2(f[0], f[4]);
-      qa[grp][0][1] = pack_half2(f[1], f[5]);
-      qa[grp][1][0] = pack_half2(f[2], f[6]);
-      qa[grp][1][1] = pack_half2(f[3], f[7]);
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += __half2float(__float2half_rn(f[i]));
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    qsum[grp] = s;
+    if (bits == 8) {
+      qa[2 * grp][0] = pack_half2(f[0], f[1]);
+      qa[2 * grp][1] = pack_half2(f[2], f[3]);
+      qa[2 * grp + 1][0] = pack_half2(f[4], f[5]);
+      qa[2 * grp + 1][1] = pack_half2(f[6], f[7]);
+    } else {
+      qa[2 * grp][0] = pack_half2(f[0], f[4]);
+      qa[2 * grp][1] = pack_half2(f[1], f[5]);
+      qa[2 * grp + 1][0] = pack_half2(f[2], f[6]);
+      qa[2 * grp + 1][1] = pack_half2(f[3], f[7]);
     }
   }
+  if (!ok) report(p.status, KVQ_ERR_NONFINITE);
 }
 
-// Scores of one warp's 16 tokens for head row g: S[j][e] belongs to token
-// 16w + 8j + 2t + e of the tile.  Thread (g, t) feeds the codes of token
-// 16w + 8j + g (B operand) and receives the scores of tokens 8j + 2t + e.
+// Scores of the warp's 16 tokens for head row g: S[j][e] is token 16w + 8j + 2t + e.
+// The B operand (k = channels, n = tokens) comes by ldmatrix from the swizzled
+// code tile; per group the products are rescaled with the tile's tables.
 template <int D, int BITS>
-__device__ __forceinline__ void qk_tile(float (&S)[2][2], const uint32_t (&qa)[D / 32][2][2],
-                                        const uint8_t* kc, const uint32_t* ksz, int w, int g, int t) {
+__device__ __forceinline__ void qk_tile(float (&S)[2][2], const uint32_t (&qa)[D / 16][2],
+                                        const float (&qsum)[D / 32], uint32_t st_s, const uint8_t* st,
+                                        const LaneAddr& la, int w, int t) {
+  using L = Smem<D>;
   constexpr int G = D / 32;
-  constexpr int R = D * BITS / 8;
+  const float2* kt = reinterpret_cast<const float2*>(st + L::kOffKt);
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    const int row = 16 * w + 8 * j + g;
-    const int ta = 16 * w + 8 * j + 2 * t;
-    uint32_t zrow[G], s0[G], s1[G];
-    if constexpr (G == 4) {
-      const uint4 a = *reinterpret_cast<const uint4*>(ksz + row * 4);
-      const uint4 b0 = *reinterpret_cast<const uint4*>(ksz + ta * 4);
-      const uint4 b1 = *reinterpret_cast<const uint4*>(ksz + (ta + 1) * 4);
-      zrow[0] = a.x; zrow[1] = a.y; zrow[2] = a.z; zrow[3] = a.w;
-      s0[0] = b0.x; s0[1] = b0.y; s0[2] = b0.z; s0[3] = b0.w;
-      s1[0] = b1.x; s1[1] = b1.y; s1[2] = b1.z; s1[3] = b1.w;
-    } else {
-      const uint2 a = *reinterpret_cast<const uint2*>(ksz + row * 2);
-      const uint2 b0 = *reinterpret_cast<const uint2*>(ksz + ta * 2);
-      const uint2 b1 = *reinterpret_cast<const uint2*>(ksz + (ta + 1) * 2);
-      zrow[0] = a.x; zrow[1] = a.y;
-      s0[0] = b0.x; s0[1] = b0.y;
-      s1[0] = b1.x; s1[1] = b1.y;
-    }
+    const int tok = 16 * w + 8 * j + 2 * t;
     float acc0 = 0.0f, acc1 = 0.0f;
+    // one ldmatrix covers 4 chunks: 8-bit -> groups 2h, 2h+1; 4-bit -> groups 0..3
 #pragma unroll
-    for (int grp = 0; grp < G; ++grp) {
-      const uint32_t zb = zero_biased2(zrow[grp]);
-      float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int h = 0; h < (BITS == 8 ? G / 2 : 1); ++h) {
+      uint32_t r[4];
       if constexpr (BITS == 8) {
-        const uint2 cw = lds64(kc, swz<R>(row, grp * 32 + t * 8));
-        mma_16816(c, qa[grp][0][0], 0u, qa[grp][0][1], 0u, hsub2_u32(bytes01_biased(cw.x), zb),
-                  hsub2_u32(bytes23_biased(cw.x), zb));
-        mma_16816(c, qa[grp][1][0], 0u, qa[grp][1][1], 0u, hsub2_u32(bytes01_biased(cw.y), zb),
-                  hsub2_u32(bytes23_biased(cw.y), zb));
+        ldsm_x4(r, st_s + L::kOffK + (la.k8 ^ (h << 6)) + j * 8 * D);
+      } else if constexpr (D == 128) {
+        ldsm_x4(r, st_s + L::kOffK + la.k4 + j * 8 * (D / 2));
       } else {
-        const uint32_t cw = lds32(kc, swz<R>(row, grp * 16 + t * 4));
-        mma_16816(c, qa[grp][0][0], 0u, qa[grp][0][1], 0u, hsub2_u32(nib_biased(cw), zb),
-                  hsub2_u32(nib_biased(cw >> 4), zb));
-        mma_16816(c, qa[grp][1][0], 0u, qa[grp][1][1], 0u, hsub2_u32(nib_biased(cw >> 8), zb),
-                  hsub2_u32(nib_biased(cw >> 12), zb));
+        uint32_t r2[2];
+        ldsm_x2(r2, st_s + L::kOffK + la.k4 + j * 8 * (D / 2));
+        r[0] = r2[0]; r[1] = r2[1]; r[2] = 0u; r[3] = 0u;
       }
-      acc0 = fmaf(half_lo(s0[grp]), c[0], acc0);
-      acc1 = fmaf(half_lo(s1[grp]), c[1], acc1);
+#pragma unroll
+      for (int gg = 0; gg < (BITS == 8 ? 2 : G); ++gg) {
+        const int grp = BITS == 8 ? 2 * h + gg : gg;
+        float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        if constexpr (BITS == 8) {
+          mma_16816(c, qa[2 * grp][0], 0u, qa[2 * grp][1], 0u, bytes01_biased(r[2 * gg]),
+                    bytes23_biased(r[2 * gg]));
+          mma_16816(c, qa[2 * grp + 1][0], 0u, qa[2 * grp + 1][1], 0u, bytes01_biased(r[2 * gg + 1]),
+                    bytes23_biased(r[2 * gg + 1]));
+        } else {
+          const uint32_t cw = r[gg];
+          mma_16816(c, qa[2 * grp][0], 0u, qa[2 * grp][1], 0u, nib_biased(cw), nib_biased(cw >> 4));
+          mma_16816(c, qa[2 * grp + 1][0], 0u, qa[2 * grp + 1][1], 0u, nib_biased(cw >> 8), nib_biased(cw >> 12));
+        }
+        const float4 sz = *reinterpret_cast<const float4*>(kt + grp * kTile + tok);  // tokens tok, tok+1
+        acc0 = fmaf(sz.x, c[0], fmaf(-sz.y, qsum[grp], acc0));
+        acc1 = fmaf(sz.z, c[1], fmaf(-sz.w, qsum[grp], acc1));
+      }
     }
     S[j][0] = acc0;
     S[j][1] = acc1;
   }
 }
 
-// O^T[ch][h] += V_hat^T[ch][tok] P^T[tok][h] over the warp's 16 tokens.
-// A operand (rows = channels, k = tokens): thread (g, t) supplies channels
-// CPT*g + m (row g of m-tile m) and CPT*g + CPT/2 + m (row g + 8), CPT = D/8,
-// of tokens 2t, 2t+1 (k 0..7) and 8+2t, 9+2t (k 8..15).  B operand (k =
-// tokens, n = heads) is P straight from the score fragments.  Accumulator
-// O[m]: c0/c1 = heads 2t, 2t+1 of the row-g channel, c2/c3 of the row-(g+8)
-// channel.  Tokens past the sequence end read as s = 0, z = 0, so stale
-// cache words cannot poison O.
+// O^T[ch][h] += (1024 + c)[ch][tok] (P s_g)[tok][h] over the warp's 16 tokens,
+// and Z[g][h] += (1024 + z_g)[tok] (P s_g)[tok][h] in row g of a spare tile.
+// A operand (rows = channels, k = tokens 2t, 2t+1 | 8+2t, 9+2t) by transposed
+// ldmatrix from the swizzled code tile.  Row -> channel of m-tile 2*grp + mh:
+//   8-bit: row r < 8 -> 32grp + 2r + mh, row r >= 8 -> 32grp + 16 + 2(r-8) + mh
+//   4-bit: row r < 8 -> 32grp + 4r + 2mh, row r >= 8 -> 32grp + 4(r-8) + 2mh + 1
+// Accumulators hold heads 2t (c0, c2) and 2t+1 (c1, c3).
 template <int D, int BITS>
-__device__ __forceinline__ void pv_tile(float (&O)[D / 16][4], const uint32_t (&pb)[2], const uint8_t* vc,
-                                        const uint32_t* vsz, const bool (&valid)[2][2], int w, int g, int t) {
+__device__ __forceinline__ void pv_tile(float (&O)[D / 16][4], float (&Z)[4], const float (&P)[2][2],
+                                        uint32_t st_s, const uint8_t* st, const LaneAddr& la, int w, int g,
+                                        int t) {
+  using L = Smem<D>;
   constexpr int G = D / 32;
-  constexpr int R = D * BITS / 8;
-  constexpr int CPT = D / 8;            // channels per thread (16 or 8)
-  constexpr int HALF = CPT / 2;         // channels per row half = m-tiles
-  const int grp = (g * CPT) / 32;       // all of a thread's channels share one group
-  int rows[2][2];
-  uint32_t word[2][2];
+  const float* vts = reinterpret_cast<const float*>(st + L::kOffVtS);
+  const uint8_t* vtz = st + L::kOffVtZ;
+  const int tok = 16 * w + 2 * t;
+  uint32_t rv4[2][4];
+  if constexpr (BITS == 4) {
+    ldsm_x4_t(rv4[0], st_s + L::kOffV + la.v4);
+    if constexpr (G == 4) ldsm_x4_t(rv4[1], st_s + L::kOffV + (la.v4 ^ 32u));
+  }
 #pragma unroll
-  for (int j = 0; j < 2; ++j)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      rows[j][e] = 16 * w + 8 * j + 2 * t + e;
-      word[j][e] = valid[j][e] ? vsz[rows[j][e] * G + grp] : 0u;
+  for (int grp = 0; grp < G; ++grp) {
+    const float2 sa = *reinterpret_cast<const float2*>(vts + grp * kTile + tok);
+    const float2 sb = *reinterpret_cast<const float2*>(vts + grp * kTile + tok + 8);
+    const uint32_t b0 = pack_half2(P[0][0] * sa.x, P[0][1] * sa.y);
+    const uint32_t b1 = pack_half2(P[1][0] * sb.x, P[1][1] * sb.y);
+    if constexpr (BITS == 8) {
+      uint32_t r[4];   // (tok 0-7, ch 0-15), (tok 0-7, ch 16-31), (tok 8-15, ch 0-15), (tok 8-15, ch 16-31)
+      ldsm_x4_t(r, st_s + L::kOffV + (la.v8 ^ (static_cast<uint32_t>(grp) << 5)));
+      mma_16816(O[2 * grp + 0], bytes02_biased(r[0]), bytes02_biased(r[1]), bytes02_biased(r[2]),
+                bytes02_biased(r[3]), b0, b1);
+      mma_16816(O[2 * grp + 1], bytes13_biased(r[0]), bytes13_biased(r[1]), bytes13_biased(r[2]),
+                bytes13_biased(r[3]), b0, b1);
+    } else {
+      // matrices of ldmatrix (gi = grp/2): (group 2gi, tok 0-7), (2gi+1, 0-7), (2gi, 8-15), (2gi+1, 8-15)
+      const uint32_t lo = rv4[grp >> 1][grp & 1], hi = rv4[grp >> 1][2 + (grp & 1)];
+      mma_16816(O[2 * grp + 0], nib_biased(lo), nib_biased(lo >> 4), nib_biased(hi), nib_biased(hi >> 4), b0, b1);
+      mma_16816(O[2 * grp + 1], nib_biased(lo >> 8), nib_biased(lo >> 12), nib_biased(hi >> 8),
+                nib_biased(hi >> 12), b0, b1);
     }
-  // (s_a, s_b) and (1024 + z_a, 1024 + z_b) for the token pairs j = 0, 1
-  uint32_t s2[2], zb[2];
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    s2[j] = prmt(word[j][0], word[j][1], 0x5410u);
-    zb[j] = zero_biased_pair(word[j][0], word[j][1]);
+    const uint32_t za = g == grp ? *reinterpret_cast<const uint32_t*>(vtz + (grp * kTile + tok) * 2) : 0u;
+    const uint32_t zb = g == grp ? *reinterpret_cast<const uint32_t*>(vtz + (grp * kTile + tok + 8) * 2) : 0u;
+    mma_16816(Z, za, 0u, zb, 0u, b0, b1);
   }
-  // exact (c - z) then one fp16 rounding of (c - z) * s, for a token pair
-  auto deq = [&](uint32_t biased, int j) -> uint32_t {
-    uint32_t d = hsub2_u32(biased, zb[j]);
-    __half2 r = __hmul2(*reinterpret_cast<__half2*>(&d), *reinterpret_cast<const __half2*>(&s2[j]));
-    return *reinterpret_cast<uint32_t*>(&r);
-  };
-  uint32_t A[2][2][HALF];   // [token pair j][row half][m]
-  if constexpr (BITS == 8) {
-    // per token: CPT bytes = channels [CPT*g, CPT*g + CPT), word wi = channels 4wi .. 4wi+3
-    uint32_t wv[2][2][CPT / 4];
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        if constexpr (CPT == 16) {
-          const uint4 v = lds128(vc, swz<R>(rows[j][e], g * 16));
-          wv[j][e][0] = v.x; wv[j][e][1] = v.y; wv[j][e][2] = v.z; wv[j][e][3] = v.w;
-        } else {
-          const uint2 v = lds64(vc, swz<R>(rows[j][e], g * 8));
-          wv[j][e][0] = v.x; wv[j][e][1] = v.y;
-        }
-      }
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr)
-#pragma unroll
-        for (int wq = 0; wq < HALF / 4; ++wq) {
-          const int wi = hr * (HALF / 4) + wq;
-          const uint32_t x0 = prmt(wv[j][0][wi], wv[j][1][wi], 0x5140u);  // bytes 0,1 of both tokens
-          const uint32_t x1 = prmt(wv[j][0][wi], wv[j][1][wi], 0x7362u);  // bytes 2,3
-          A[j][hr][4 * wq + 0] = deq(bytes01_biased(x0), j);
-          A[j][hr][4 * wq + 1] = deq(bytes23_biased(x0), j);
-          A[j][hr][4 * wq + 2] = deq(bytes01_biased(x1), j);
-          A[j][hr][4 * wq + 3] = deq(bytes23_biased(x1), j);
-        }
-  } else {
-    // per token: CPT/2 bytes; nibble n of the thread's chunk = channel CPT*g + n
-    uint32_t wv[2][2][CPT / 8];
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        if constexpr (CPT == 16) {
-          const uint2 v = lds64(vc, swz<R>(rows[j][e], g * 8));
-          wv[j][e][0] = v.x; wv[j][e][1] = v.y;
-        } else {
-          wv[j][e][0] = lds32(vc, swz<R>(rows[j][e], g * 4));
-        }
-      }
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int base = hr * HALF;                  // first nibble of this row half
-        const int sh = (base % 8) * 4;
-        const uint32_t a0 = wv[j][0][base / 8] >> sh, a1 = wv[j][1][base / 8] >> sh;
-        const uint32_t ev0 = a0 & 0x0F0F0F0Fu, ev1 = a1 & 0x0F0F0F0Fu;                // nibbles 0,2,4,6
-        const uint32_t od0 = (a0 >> 4) & 0x0F0F0F0Fu, od1 = (a1 >> 4) & 0x0F0F0F0Fu;  // nibbles 1,3,5,7
-        const uint32_t e01 = prmt(ev0, ev1, 0x5140u), o01 = prmt(od0, od1, 0x5140u);
-        A[j][hr][0] = deq(bytes01_biased(e01), j);
-        A[j][hr][1] = deq(bytes01_biased(o01), j);
-        A[j][hr][2] = deq(bytes23_biased(e01), j);
-        A[j][hr][3] = deq(bytes23_biased(o01), j);
-        if constexpr (HALF == 8) {
-          const uint32_t e23 = prmt(ev0, ev1, 0x7362u), o23 = prmt(od0, od1, 0x7362u);
-          A[j][hr][4] = deq(bytes01_biased(e23), j);
-          A[j][hr][5] = deq(bytes01_biased(o23), j);
-          A[j][hr][6] = deq(bytes23_biased(e23), j);
-          A[j][hr][7] = deq(bytes23_biased(o23), j);
-        }
-      }
+}
+
+// channel held by accumulator row half (0: rows < 8, 1: rows >= 8) of m-tile (grp, mh), thread row g
+template <int BITS>
+__device__ __forceinline__ int acc_channel(int grp, int mh, int half, int g) {
+  if constexpr (BITS == 8) return 32 * grp + 16 * half + 2 * g + mh;
+  return 32 * grp + 4 * g + 2 * mh + half;
+}
+
+__device__ __forceinline__ void store_out(const DParams& p, int64_t i, float v) {
+  if (p.out_dtype == KVQ_OUT_F32) reinterpret_cast<float*>(p.out)[i] = v;
+  else reinterpret_cast<__nv_bfloat16*>(p.out)[i] = __float2bfloat16_rn(v);
+}
+
+// Bounded barrier among the four consumer warps (tid < 128).  A plain bar.sync
+// could wait forever if one warp left after a timed-out wait.
+__device__ __forceinline__ void consumer_sync(uint64_t* gbar, uint32_t* gphase, bool* ok, int32_t* status) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(gbar);
+  *ok = *ok && mbar_wait(gbar, *gphase & 1, status);
+  ++*gphase;
+  __syncwarp();
+}
+
+// Whether CTA c of the stream-K split got an empty tile range (only possible
+// when there are fewer tiles than CTAs).
+__device__ __forceinline__ bool cta_empty(int64_t N, int C, int c) { return N * (c + 1) / C == N * c / C; }
+
+// End of a piece (kept out of line: it is rare and would otherwise crowd the
+// hot loop's registers).  m_o[w][h][ch], m_ml[w][h] = (max, sum) hold the four
+// consumer warps' states.  A segment held by this CTA alone is normalised and
+// written out; otherwise the CTA's partial (o, lse) goes to the workspace and
+// the CTA whose arrival completes the segment merges all its pieces.
+template <int D>
+__device__ __noinline__ uint32_t finish_piece(const DParams* pp, float* m_o, float* m_ml, int cb, int ckvh,
+                                              const int32_t* pre, int64_t N, int C, int tid, uint64_t* gbar,
+                                              uint32_t gphase_in, bool ok_in) {
+  uint32_t gph = gphase_in;
+  bool okv = ok_in;
+  uint32_t* gphase = &gph;
+  bool* ok = &okv;
+  const DParams& p = *pp;
+  const int Hkv = p.Hkv, rep = p.rep;
+  int* info = reinterpret_cast<int*>(m_ml + kWarps * kMaxRep * 2);   // [c0, c1, npieces, last]
+  const int seg = cb * Hkv + ckvh;
+  if (tid == 0) {
+    const int n_b = pre[cb + 1] - pre[cb];
+    const int64_t start = static_cast<int64_t>(Hkv) * pre[cb] + static_cast<int64_t>(ckvh) * n_b;
+    const int c0 = static_cast<int>(((start + 1) * C - 1) / N);
+    const int c1 = static_cast<int>(((start + n_b) * C - 1) / N);
+    int np = c1 - c0 + 1;
+    if (N < C) {  // some CTAs may have empty ranges: count the ones that wrote a piece
+      np = 0;
+      for (int c = c0; c <= c1; ++c) np += cta_empty(N, C, c) ? 0 : 1;
+    }
+    info[0] = c0; info[1] = c1; info[2] = np;
   }
+  consumer_sync(gbar, gphase, ok, p.status);
+  const int c0 = info[0], c1 = info[1], npieces = info[2];
+  const int64_t orow0 = (static_cast<int64_t>(cb) * p.Hq + ckvh * rep) * D;
+  const bool whole = c0 == c1;
+  const int64_t slot = static_cast<int64_t>(seg) + blockIdx.x;
+  for (int idx = tid; idx < rep * D; idx += kWarps * 32) {
+    const int h = idx / D, ch = idx % D;
+    float M = -INFINITY;
 #pragma unroll
-  for (int m = 0; m < HALF; ++m) mma_16816(O[m], A[0][0][m], A[0][1][m], A[1][0][m], A[1][1][m], pb[0], pb[1]);
+    for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, m_ml[(ww * kMaxRep + h) * 2]);
+    float Lsum = 0.0f, o = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int ww = 0; ww < kWarps; ++ww) {
+        const float sc = fast_exp2(m_ml[(ww * kMaxRep + h) * 2] - M);
+        Lsum += m_ml[(ww * kMaxRep + h) * 2 + 1] * sc;
+        o += m_o[(ww * kMaxRep + h) * D + ch] * sc;
+      }
+    }
+    const bool any = M != -INFINITY && Lsum > 0.0f;
+    if (whole) {
+      store_out(p, orow0 + idx, any ? o / Lsum : 0.0f);
+    } else {
+      p.ws_o[(slot * rep + h) * D + ch] = any ? o / Lsum : 0.0f;
+      if (ch == 0) p.ws_lse[slot * rep + h] = any ? M + __log2f(Lsum) : -INFINITY;
+    }
+  }
+  if (whole) {
+    consumer_sync(gbar, gphase, ok, p.status);
+    return (gph << 1) | (okv ? 1u : 0u);
+  }
+  // publish the piece (each writer fences its own stores), then count the arrivals
+  __threadfence();
+  consumer_sync(gbar, gphase, ok, p.status);
+  if (tid == 0) info[3] = (atomicAdd(&p.ws_cnt[seg], 1) + 1 == npieces) ? 1 : 0;
+  consumer_sync(gbar, gphase, ok, p.status);
+  if (info[3] != 1) return (gph << 1) | (okv ? 1u : 0u);
+  __threadfence();
+  // the segment is complete: one online log-sum-exp pass over its pieces, four
+  // channels per thread, eight pieces of loads in flight
+  const bool check = N < C;
+  for (int i4 = tid; i4 < rep * (D / 4); i4 += kWarps * 32) {
+    const int h = i4 / (D / 4), ch = (i4 % (D / 4)) * 4;
+    float M = -INFINITY, Lsum = 0.0f;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int cb8 = c0; cb8 <= c1; cb8 += 8) {
+      float lse[8];
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int c = cb8 + u;
+        const bool live = c <= c1 && !(check && cta_empty(N, C, c));
+        const int64_t sl = static_cast<int64_t>(seg) + (live ? c : c0);
+        lse[u] = live ? __ldcg(p.ws_lse + sl * rep + h) : -INFINITY;
+        v[u] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (sl * rep + h) * D + ch));
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (lse[u] == -INFINITY) continue;
+        const float M2 = fmaxf(M, lse[u]);
+        const float a = fast_exp2(M - M2), bw = fast_exp2(lse[u] - M2);
+        acc.x = acc.x * a + bw * v[u].x; acc.y = acc.y * a + bw * v[u].y;
+        acc.z = acc.z * a + bw * v[u].z; acc.w = acc.w * a + bw * v[u].w;
+        Lsum = Lsum * a + bw;
+        M = M2;
+      }
+    }
+    const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
+    const int64_t o0 = orow0 + static_cast<int64_t>(h) * D + ch;
+    store_out(p, o0 + 0, acc.x * inv);
+    store_out(p, o0 + 1, acc.y * inv);
+    store_out(p, o0 + 2, acc.z * inv);
+    store_out(p, o0 + 3, acc.w * inv);
+  }
+  if (tid == 0) p.ws_cnt[seg] = 0;   // ready for the next call
+  return (gph << 1) | (okv ? 1u : 0u);
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const __grid_constant__ DParams p) {
+__global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_kernel(const __grid_constant__ DParams p) {
   using L = Smem<D>;
   constexpr int G = D / 32;
-  constexpr int CPT = D / 8;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * L::kStageBytes);
-  uint64_t* empty = full + kStages;
+  uint64_t* ready = full + kStages;
+  uint64_t* empty = ready + kStages;
   uint64_t* gbar = empty + kStages;       // consumer-group barrier for piece ends
   int32_t* pre = reinterpret_cast<int32_t*>(smem + L::kFixed);
   int32_t* lens = pre + (p.B + 1);
-
-  // let the merge grid get scheduled early; it waits for this grid's completion itself
-  asm volatile("griddepcontrol.launch_dependents;");
 
   const int tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
@@ -353,6 +477,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const __grid_
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
+      mbar_init(&ready[s], 1);
       mbar_init(&empty[s], kWarps);
     }
     mbar_init(gbar, kWarps);
@@ -383,8 +508,14 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const __grid_
     if (lane == 0) pre[0] = 0;
   }
   __syncthreads();
-  if (blockIdx.x == 0)
-    for (int b = tid; b <= B; b += blockDim.x) p.ws_pre[b] = pre[b];
+  // sequences of length 0 get a zero output row (no CTA visits them)
+  for (int idx = blockIdx.x * blockDim.x + tid; idx < B * p.Hq * D; idx += gridDim.x * blockDim.x) {
+    const int b = idx / (p.Hq * D);
+    if (lens[b] == 0) {
+      if (p.out_dtype == KVQ_OUT_F32) reinterpret_cast<float*>(p.out)[idx] = 0.0f;
+      else reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(0.0f);
+    }
+  }
 
   const int64_t N = static_cast<int64_t>(Hkv) * pre[B];
   const int C = p.num_ctas;
@@ -394,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const __grid_
   if (ntiles <= 0) return;
 
   if (w == kWarps) {
-    // ---------------- producer warp: one thread streams the tiles ----------------
+    // ---------------- TMA issuer warp: lane 0 keeps kStages tiles in flight ----------------
     if (lane != 0) return;
     Cursor pc = locate(f0, pre, B, Hkv);
     for (int k = 0; k < ntiles; ++k) {
@@ -407,66 +538,95 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const __grid_
       const int64_t szoff = (static_cast<int64_t>(pc.kvh) * B + pc.b) * p.Tcap + static_cast<int64_t>(pc.i) * kTile;
       uint64_t* bar = &full[slot];
       mbar_arrive_expect_tx(bar, 2 * kTile * R + 2 * L::kSzBytes);
-      tma_2d_g2s(st, bits == 8 ? &p.tm_k8 : &p.tm_k4, 0, row0, bar);
-      tma_2d_g2s(st + L::kCodeBytes, bits == 8 ? &p.tm_v8 : &p.tm_v4, 0, row0, bar);
-      bulk_g2s(st + 2 * L::kCodeBytes, p.k_sz + szoff * G, L::kSzBytes, bar);
-      bulk_g2s(st + 2 * L::kCodeBytes + L::kSzBytes, p.v_sz + szoff * G, L::kSzBytes, bar);
+      tma_2d_g2s(st + L::kOffK, bits == 8 ? &p.tm_k8 : &p.tm_k4, 0, row0, bar);
+      tma_2d_g2s(st + L::kOffV, bits == 8 ? &p.tm_v8 : &p.tm_v4, 0, row0, bar);
+      bulk_g2s(st + L::kOffKsz, p.k_sz + szoff * G, L::kSzBytes, bar);
+      bulk_g2s(st + L::kOffVsz, p.v_sz + szoff * G, L::kSzBytes, bar);
       advance(pc, pre, B, Hkv);
+    }
+    return;
+  }
+  if (w == kWarps + 1) {
+    // ---------------- table warp: per landed tile, scale/zero words -> consumer tables ----------------
+    Cursor tc = locate(f0, pre, B, Hkv);
+    for (int kk = 0; kk < ntiles; ++kk) {
+      const int slot = kk % kStages;
+      const bool okw = mbar_wait(&full[slot], (kk / kStages) & 1, p.status);
+      if (!__all_sync(0xffffffffu, okw)) return;
+      uint8_t* st = smem + slot * L::kStageBytes;
+      const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + L::kOffKsz);
+      const uint32_t* vsz = reinterpret_cast<const uint32_t*>(st + L::kOffVsz);
+      float2* kt = reinterpret_cast<float2*>(st + L::kOffKt);
+      float* vts = reinterpret_cast<float*>(st + L::kOffVtS);
+      uint16_t* vtz = reinterpret_cast<uint16_t*>(st + L::kOffVtZ);
+      const int len = lens[tc.b];
+      // tables in [group][token] order: consecutive lanes take consecutive tokens
+#pragma unroll 4
+      for (int e = lane; e < kTile * G; e += 32) {
+        const int grp = e / kTile, tok = e % kTile;
+        const bool valid = tc.i * kTile + tok < len;
+        const uint32_t kw = valid ? ksz[tok * G + grp] : 0u;
+        const uint32_t vw = valid ? vsz[tok * G + grp] : 0u;
+        const float ks = half_lo(kw);
+        kt[e] = make_float2(ks, (1024.0f + half_hi(kw)) * ks);
+        vts[e] = half_lo(vw);
+        vtz[e] = static_cast<unsigned short>(zero_biased2(vw) & 0xFFFFu);
+      }
+      if (lane == 0) {
+        const int n_b = pre[tc.b + 1] - pre[tc.b];
+        int flags = tc.i;
+        if (tc.i == 0 || kk == 0) flags |= kFlagStart;
+        if (tc.i == n_b - 1 || kk == ntiles - 1) flags |= kFlagEnd;
+        *reinterpret_cast<int4*>(st + L::kOffMeta) = make_int4(tc.b, tc.kvh, flags, len);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ready[slot]);
+      advance(tc, pre, B, Hkv);
     }
     return;
   }
 
   // ---------------- consumers: four warps ----------------
-  Cursor cc = locate(f0, pre, B, Hkv);
-  uint32_t qa[G][2][2];
+  const LaneAddr la = lane_addr<D>(w, lane);
+  uint32_t qa[D / 16][2];
+  float qsum[G];
   float O[D / 16][4];
+  float Z[4];
   float m_run = -INFINITY, l_run = 0.0f;
-  bool piece_start = true;
   bool ok = true;
   uint32_t gphase = 0;
-  // bounded barrier among the four consumer warps (a plain bar.sync could wait forever
-  // if one warp left after a timed-out wait)
-  auto group_sync = [&]() {
-    __syncwarp();
-    if (lane == 0) mbar_arrive(gbar);
-    ok = ok && mbar_wait(gbar, gphase & 1, p.status);
-    ++gphase;
-    __syncwarp();
-  };
+  auto group_sync = [&]() { consumer_sync(gbar, &gphase, &ok, p.status); };
 
   for (int k = 0; k < ntiles; ++k) {
     const int slot = k % kStages;
-    const int bits = p.bits[cc.kvh];
-    const int n_b = pre[cc.b + 1] - pre[cc.b];
-    if (piece_start) {
-      load_q<D>(qa, p, cc.b, cc.kvh, bits, g, t);
+    ok = ok && mbar_wait(&ready[slot], (k / kStages) & 1, p.status);
+    if (!ok) break;   // a timed-out wait ends this warp (status already set)
+    uint8_t* st = smem + slot * L::kStageBytes;
+    const uint32_t st_s = smem_u32(st);
+    const int4 meta = *reinterpret_cast<const int4*>(st + L::kOffMeta);
+    const int cb = meta.x, ckvh = meta.y, ci = meta.z & 0xFFFFFF, len = meta.w;
+    const int bits = p.bits[ckvh];
+    if (meta.z & kFlagStart) {
+      load_q<D>(qa, qsum, p, cb, ckvh, bits, g, t);
 #pragma unroll
       for (int i = 0; i < D / 16; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.0f;
+      Z[0] = Z[1] = Z[2] = Z[3] = 0.0f;
       m_run = -INFINITY;
       l_run = 0.0f;
     }
-    ok = ok && mbar_wait(&full[slot], (k / kStages) & 1, p.status);
-    if (!ok) break;   // a timed-out wait ends this warp (status already set)
-    uint8_t* st = smem + slot * L::kStageBytes;
-    const uint8_t* kc = st;
-    const uint8_t* vc = st + L::kCodeBytes;
-    const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + 2 * L::kCodeBytes);
-    const uint32_t* vsz = reinterpret_cast<const uint32_t*>(st + 2 * L::kCodeBytes + L::kSzBytes);
 
     float S[2][2];
-    if (bits == 8) qk_tile<D, 8>(S, qa, kc, ksz, w, g, t);
-    else qk_tile<D, 4>(S, qa, kc, ksz, w, g, t);
+    if (bits == 8) qk_tile<D, 8>(S, qa, qsum, st_s, st, la, w, t);
+    else qk_tile<D, 4>(S, qa, qsum, st_s, st, la, w, t);
 
     // mask past the sequence end, move to the log2 domain, online softmax per head row g
-    const int len = lens[cc.b];
-    bool valid[2][2];
     float mx = -INFINITY;
+    const int tok0 = ci * kTile + 16 * w + 2 * t;
 #pragma unroll
     for (int j = 0; j < 2; ++j)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        valid[j][e] = cc.i * kTile + 16 * w + 8 * j + 2 * t + e < len;
-        S[j][e] = valid[j][e] ? S[j][e] * p.scale_log2 : -INFINITY;
+        S[j][e] = tok0 + 8 * j + e < len ? S[j][e] * p.scale_log2 : -INFINITY;
         mx = fmaxf(mx, S[j][e]);
       }
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -486,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const __grid_
     l_run = l_run * alpha + psum;
     m_run = m_new;
     if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-      // O^T columns are heads 2t, 2t+1; their factors live in rows g = 2t, 2t+1
+      // accumulator columns are heads 2t, 2t+1; their factors live in rows g = 2t, 2t+1
       const float a0 = __shfl_sync(0xffffffffu, alpha, (2 * t) << 2);
       const float a1 = __shfl_sync(0xffffffffu, alpha, (2 * t + 1) << 2);
 #pragma unroll
@@ -494,14 +654,13 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const __grid_
         O[i][0] *= a0; O[i][1] *= a1;
         O[i][2] *= a0; O[i][3] *= a1;
       }
+      Z[0] *= a0; Z[1] *= a1; Z[2] *= a0; Z[3] *= a1;
     }
-    const uint32_t pb[2] = {pack_half2(P[0][0], P[0][1]), pack_half2(P[1][0], P[1][1])};
-    if (bits == 8) pv_tile<D, 8>(O, pb, vc, vsz, valid, w, g, t);
-    else pv_tile<D, 4>(O, pb, vc, vsz, valid, w, g, t);
+    if (bits == 8) pv_tile<D, 8>(O, Z, P, st_s, st, la, w, g, t);
+    else pv_tile<D, 4>(O, Z, P, st_s, st, la, w, g, t);
 
-    // ---- end of a piece: merge the four warps and write the partial ----
-    const bool piece_end = (cc.i == n_b - 1) || (k == ntiles - 1);
-    if (piece_end) {
+    // ---- end of a piece: hand the four warps' states to the (out-of-line) merge ----
+    if (meta.z & kFlagEnd) {
       float l_tot = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
       l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
       float* m_o = reinterpret_cast<float*>(st);                 // this slot, once every warp is done with it
@@ -512,114 +671,34 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const __grid_
         m_ml[(w * kMaxRep + g) * 2 + 1] = l_tot;
       }
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int h = 2 * t + e;
-        if (h < p.rep) {
-          float* dst = m_o + (w * kMaxRep + h) * D;
+      for (int grp = 0; grp < G; ++grp) {
+        // zero-point term of group grp for heads 2t, 2t+1 sits in row grp of Z
+        const float r0 = __shfl_sync(0xffffffffu, Z[0], grp * 4 + t);
+        const float r1 = __shfl_sync(0xffffffffu, Z[1], grp * 4 + t);
 #pragma unroll
-          for (int m = 0; m < D / 16; ++m) {
-            dst[CPT * g + m] = O[m][e];
-            dst[CPT * g + CPT / 2 + m] = O[m][2 + e];
+        for (int e = 0; e < 2; ++e) {
+          const int h = 2 * t + e;
+          const float r = e ? r1 : r0;
+          if (h < p.rep) {
+            float* dst = m_o + (w * kMaxRep + h) * D;
+#pragma unroll
+            for (int mh = 0; mh < 2; ++mh)
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                const int ch = bits == 8 ? acc_channel<8>(grp, mh, half, g) : acc_channel<4>(grp, mh, half, g);
+                dst[ch] = O[2 * grp + mh][2 * half + e] - r;
+              }
           }
         }
       }
       group_sync();
-      const int slotw = cc.b * Hkv + cc.kvh + blockIdx.x;
-      for (int idx = tid; idx < p.rep * D; idx += kWarps * 32) {
-        const int h = idx / D, ch = idx % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, m_ml[(ww * kMaxRep + h) * 2]);
-        float Lsum = 0.0f, o = 0.0f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int ww = 0; ww < kWarps; ++ww) {
-            const float sc = fast_exp2(m_ml[(ww * kMaxRep + h) * 2] - M);
-            Lsum += m_ml[(ww * kMaxRep + h) * 2 + 1] * sc;
-            o += m_o[(ww * kMaxRep + h) * D + ch] * sc;
-          }
-        }
-        const bool any = M != -INFINITY && Lsum > 0.0f;
-        p.ws_o[(static_cast<int64_t>(slotw) * p.rep + h) * D + ch] = any ? o / Lsum : 0.0f;
-        if (ch == 0) p.ws_lse[static_cast<int64_t>(slotw) * p.rep + h] = any ? M + __log2f(Lsum) : -INFINITY;
-      }
-      group_sync();                                              // scratch read before the slot is refilled
-      piece_start = true;
-    } else {
-      piece_start = false;
+      const uint32_t st_ret = finish_piece<D>(&p, m_o, m_ml, cb, ckvh, pre, N, C, tid, gbar, gphase, ok);
+      gphase = st_ret >> 1;
+      ok = (st_ret & 1u) != 0;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
-    advance(cc, pre, B, Hkv);
     if (!ok) break;
-  }
-}
-
-// One warp per (sequence, query head): log-sum-exp merge of the partials.
-template <int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const __grid_constant__ DParams p) {
-  constexpr int V = D / 32;  // channels per lane
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (gw >= p.B * p.Hq) return;
-  const int b = gw / p.Hq, hq = gw % p.Hq;
-  const int kvh = hq / p.rep, r = hq % p.rep;
-  const int B = p.B, Hkv = p.Hkv, C = p.num_ctas;
-  const int32_t* pre = p.ws_pre;
-  const int n_b = pre[b + 1] - pre[b];
-  float acc[V];
-#pragma unroll
-  for (int i = 0; i < V; ++i) acc[i] = 0.0f;
-  if (n_b > 0) {
-    const int64_t N = static_cast<int64_t>(Hkv) * pre[B];
-    const int64_t start = static_cast<int64_t>(Hkv) * pre[b] + static_cast<int64_t>(kvh) * n_b;
-    const int64_t last = start + n_b - 1;
-    const int c0 = static_cast<int>(((start + 1) * C - 1) / N);
-    const int c1 = static_cast<int>(((last + 1) * C - 1) / N);
-    const int64_t seg = static_cast<int64_t>(b) * Hkv + kvh;
-    // pass 1: pieces spread over the lanes -> the largest lse
-    float M = -INFINITY;
-    for (int c = c0 + lane; c <= c1; c += 32) {
-      if (N * (c + 1) / C == N * c / C) continue;  // a CTA with an empty range wrote nothing
-      M = fmaxf(M, p.ws_lse[(seg + c) * p.rep + r]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    // pass 2: weighted sum of the partial outputs (loads independent of each other)
-    float Lsum = 0.0f;
-    if (M != -INFINITY) {
-      for (int c = c0; c <= c1; ++c) {
-        if (N * (c + 1) / C == N * c / C) continue;
-        const int64_t slot = seg + c;
-        const float lse = p.ws_lse[slot * p.rep + r];
-        const float wgt = lse == -INFINITY ? 0.0f : fast_exp2(lse - M);
-        const float* o = p.ws_o + (slot * p.rep + r) * D + lane * V;
-        if constexpr (V == 4) {
-          const float4 v = *reinterpret_cast<const float4*>(o);
-          acc[0] = fmaf(wgt, v.x, acc[0]); acc[1] = fmaf(wgt, v.y, acc[1]);
-          acc[2] = fmaf(wgt, v.z, acc[2]); acc[3] = fmaf(wgt, v.w, acc[3]);
-        } else {
-          const float2 v = *reinterpret_cast<const float2*>(o);
-          acc[0] = fmaf(wgt, v.x, acc[0]); acc[1] = fmaf(wgt, v.y, acc[1]);
-        }
-        Lsum += wgt;
-      }
-      if (Lsum > 0.0f) {
-#pragma unroll
-        for (int i = 0; i < V; ++i) acc[i] /= Lsum;
-      }
-    }
-  }
-  const int64_t orow = (static_cast<int64_t>(b) * p.Hq + hq) * D + lane * V;
-  if (p.out_dtype == KVQ_OUT_F32) {
-    float* o = reinterpret_cast<float*>(p.out) + orow;
-#pragma unroll
-    for (int i = 0; i < V; ++i) o[i] = acc[i];
-  } else {
-    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + orow;
-#pragma unroll
-    for (int i = 0; i < V; ++i) o[i] = __float2bfloat16_rn(acc[i]);
   }
 }
 
@@ -642,23 +721,9 @@ int ctas_per_sm() {
 }
 
 template <int D>
-cudaError_t launch_pair(const DParams& p, int C, int B, int Hq, cudaStream_t stream) {
+cudaError_t launch_split(const DParams& p, int C, int B, cudaStream_t stream) {
   decode_split_kernel<D><<<C, kThreads, Smem<D>::bytes(B), stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  // the merge may start while the split grid drains (programmatic dependent launch);
-  // it waits for the split grid's completion before reading the partials
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((B * Hq + 3) / 4);
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, p);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -668,13 +733,13 @@ int decode_num_ctas(int D) {
   return device_sm_count() * per;
 }
 
-// workspace: [pre: B+1 int32, padded to 16 B][lse: slots*rep f32, padded][o: slots*rep*D f32]
+// workspace: [cnt: B*Hkv int32, padded to 16 B][lse: slots*rep f32, padded][o: slots*rep*D f32]
 static size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
 size_t decode_workspace_bytes(int B, int Hq, int Hkv, int D, int num_ctas) {
   const size_t rep = static_cast<size_t>(Hq / Hkv);
   const size_t slots = static_cast<size_t>(B) * Hkv + num_ctas;
-  return align16((B + 1) * 4) + align16(slots * rep * 4) + slots * rep * D * 4;
+  return align16(static_cast<size_t>(B) * Hkv * 4) + align16(slots * rep * 4) + slots * rep * D * 4;
 }
 
 kvq_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
@@ -710,9 +775,10 @@ kvq_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const int rep = a.Hq / Hkv;
   const size_t slots = static_cast<size_t>(B) * Hkv + C;
   uint8_t* ws = static_cast<uint8_t*>(a.ws);
-  p.ws_pre = reinterpret_cast<int32_t*>(ws);
-  p.ws_lse = reinterpret_cast<float*>(ws + align16((B + 1) * 4));
-  p.ws_o = reinterpret_cast<float*>(ws + align16((B + 1) * 4) + align16(slots * rep * 4));
+  const size_t cnt_bytes = align16(static_cast<size_t>(B) * Hkv * 4);
+  p.ws_cnt = reinterpret_cast<int32_t*>(ws);
+  p.ws_lse = reinterpret_cast<float*>(ws + cnt_bytes);
+  p.ws_o = reinterpret_cast<float*>(ws + cnt_bytes + align16(slots * rep * 4));
   p.out = a.out;
   p.status = a.status;
   p.out_dtype = a.out_dtype;
@@ -723,7 +789,7 @@ kvq_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.plane[h] = hl.plane_idx[h];
     p.bits[h] = hl.bits[h];
   }
-  const cudaError_t e = D == 128 ? launch_pair<128>(p, C, B, a.Hq, stream) : launch_pair<64>(p, C, B, a.Hq, stream);
+  const cudaError_t e = D == 128 ? launch_split<128>(p, C, B, stream) : launch_split<64>(p, C, B, stream);
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

@@ -127,6 +127,26 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 }
 
 // ---------------------------------------------------------------------------
+// ldmatrix: lane l supplies the shared address of row (l & 7) of matrix (l >> 3);
+// thread (g = lane/4, t = lane%4) receives, per matrix, the 16-bit elements
+// (row g, cols 2t, 2t+1), or with .trans (rows 2t, 2t+1, col g).
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t saddr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], uint32_t saddr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(saddr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t saddr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr));
+}
+
+// ---------------------------------------------------------------------------
 // codes -> fp16.  An fp16 whose top byte is 0x64 and low byte is c has the
 // value 1024 + c exactly (exponent 2^10, ten mantissa bits), for 0 <= c < 1024.
 // Subtracting (1024 + z) in fp16 then gives the exact integer c - z.
@@ -142,6 +162,9 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 __device__ __forceinline__ uint32_t bytes01_biased(uint32_t w) { return prmt(w, 0x64646464u, 0x5140u); }
 // bytes 2,3 of w -> half2(1024 + w.b2, 1024 + w.b3)
 __device__ __forceinline__ uint32_t bytes23_biased(uint32_t w) { return prmt(w, 0x64646464u, 0x7362u); }
+// bytes 0,2 of w -> half2(1024 + w.b0, 1024 + w.b2); bytes 1,3 likewise
+__device__ __forceinline__ uint32_t bytes02_biased(uint32_t w) { return prmt(w, 0x64646464u, 0x5240u); }
+__device__ __forceinline__ uint32_t bytes13_biased(uint32_t w) { return prmt(w, 0x64646464u, 0x5341u); }
 // nibbles at bits [0,4) and [16,20) of w -> half2(1024 + lo, 1024 + hi)
 __device__ __forceinline__ uint32_t nib_biased(uint32_t w) { return (w & 0x000F000Fu) | 0x64006400u; }
 

@@ -74,36 +74,60 @@ __device__ __forceinline__ bool tile_kept(const PParams& p, int qt, int kt) {
   return kt == qt || p.tile_mask == nullptr || p.tile_mask[qt * p.nT + kt] != 0;
 }
 
-// fp16 K_hat / V_hat tile writer: codes of 128 tokens x 128 channels -> swizzled fp16
-__device__ __forceinline__ void dequant_tile(uint8_t* dst, const uint8_t* codes, const uint32_t* sz, int wt) {
-  // wt: thread index within the warpgroup (0..127)
-  const int c8 = wt & 7;          // 16-channel chunk
-  const int kb = c8 >> 2;         // 64-channel block
-  const int ch2 = (c8 & 3) * 2;   // first 16-byte chunk of this thread inside the 128-byte row
-#pragma unroll 2
+// One 128-token x 128-channel code tile (K or V) of the dequant warpgroup,
+// held in registers between its global loads and its conversion.  Thread wt
+// (0..127), iteration it (0..7): k-block kb = it & 1 (64 channels), row
+// 32 * (it >> 1) + 8 * (wt >> 5) + ((wt & 31) >> 2), 16 channels from
+// chunk c8 = 4 * kb + (wt & 3).  A quarter warp then stores two adjacent rows,
+// whose swizzled chunks never share banks.
+struct CodeRegs {
+  uint4 c[8];
+  uint32_t sz[8];
+};
+
+__device__ __forceinline__ int dq_row(int it, int wt) { return 32 * (it >> 1) + 8 * (wt >> 5) + ((wt & 31) >> 2); }
+__device__ __forceinline__ int dq_c8(int it, int wt) { return 4 * (it & 1) + (wt & 3); }
+
+__device__ __forceinline__ void load_codes(CodeRegs& r, const uint8_t* codes, const uint32_t* sz, int wt) {
+#pragma unroll
   for (int it = 0; it < 8; ++it) {
-    const int row = it * 16 + (wt >> 3);
-    const uint4 cw = *reinterpret_cast<const uint4*>(codes + static_cast<size_t>(row) * kD + c8 * 16);
-    const uint32_t word = sz[row * 4 + (c8 >> 1)];
+    const int row = dq_row(it, wt), c8 = dq_c8(it, wt);
+    r.c[it] = __ldg(reinterpret_cast<const uint4*>(codes + static_cast<size_t>(row) * kD + c8 * 16));
+    r.sz[it] = __ldg(sz + row * 4 + (c8 >> 1));
+  }
+}
+
+// fp16 K_hat / V_hat = (c - z) * s (exact difference, one rounding) into the
+// 128-byte-swizzled K-major operand layout: [2 k-blocks][128 rows][128 B].
+__device__ __forceinline__ void store_dequant(uint8_t* dst, const CodeRegs& r, int wt) {
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int row = dq_row(it, wt), c8 = dq_c8(it, wt);
+    const uint32_t word = r.sz[it];
     const uint32_t zb = zero_biased2(word);
     const uint32_t s2 = (word & 0xFFFFu) | (word << 16);
     const __half2 sh = *reinterpret_cast<const __half2*>(&s2);
     uint32_t o[8];
-    const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+    const uint32_t w[4] = {r.c[it].x, r.c[it].y, r.c[it].z, r.c[it].w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       uint32_t lo = hsub2_u32(bytes01_biased(w[i]), zb);
       uint32_t hi = hsub2_u32(bytes23_biased(w[i]), zb);
-      __half2 a = __hmul2(*reinterpret_cast<__half2*>(&lo), sh);
-      __half2 b = __hmul2(*reinterpret_cast<__half2*>(&hi), sh);
-      o[2 * i] = *reinterpret_cast<uint32_t*>(&a);
-      o[2 * i + 1] = *reinterpret_cast<uint32_t*>(&b);
+      __half2 x = __hmul2(*reinterpret_cast<__half2*>(&lo), sh);
+      __half2 y = __hmul2(*reinterpret_cast<__half2*>(&hi), sh);
+      o[2 * i] = *reinterpret_cast<uint32_t*>(&x);
+      o[2 * i + 1] = *reinterpret_cast<uint32_t*>(&y);
     }
+    const int kb = c8 >> 2, ch2 = (c8 & 3) * 2, sw = row & 7;
     uint8_t* rowp = dst + kb * (kT * 128) + row * 128;
-    const int sw = row & 7;
     *reinterpret_cast<uint4*>(rowp + ((ch2 ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
     *reinterpret_cast<uint4*>(rowp + (((ch2 + 1) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
   }
+}
+
+__device__ __forceinline__ int next_kept(const PParams& p, int qt, int kt) {
+  while (kt <= qt && !tile_kept(p, qt, kt)) ++kt;
+  return kt;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PParams p) {
@@ -243,21 +267,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     if (lane == 0) mbar_arrive(&bar[B_QREADY]);
 
     const size_t plane = static_cast<size_t>(kvh) * p.B * p.Tcap + static_cast<size_t>(b) * p.Tcap;
-    int j = 0;
-    for (int kt = 0; kt <= qt; ++kt) {
-      if (!tile_kept(p, qt, kt)) continue;
+    const uint8_t* kcodes = p.kcodes + plane * kD;
+    const uint8_t* vcodes = p.vcodes + plane * kD;
+    const uint32_t* ksz = p.ksz + plane * 4;
+    const uint32_t* vsz = p.vsz + plane * 4;
+    // two register sets: while one part (K or V of a tile) is converted, the
+    // next part's codes are already on their way from L2 / HBM
+    CodeRegs ra, rb;
+    int kt = next_kept(p, qt, 0);
+    if (kt <= qt) load_codes(ra, kcodes + static_cast<size_t>(kt) * kT * kD, ksz + kt * kT * 4, wt);
+    for (int j = 0; kt <= qt; ++j) {
       const int st = j & 1;
+      const int kt_next = next_kept(p, qt, kt + 1);
+      load_codes(rb, vcodes + static_cast<size_t>(kt) * kT * kD, vsz + kt * kT * 4, wt);
       if (j >= 2 && !mbar_wait(&bar[B_KVEMPTY0 + st], ((j >> 1) - 1) & 1, p.status)) return;
-      const size_t row0 = plane + static_cast<size_t>(kt) * kT;
-      dequant_tile(smem + kOff_K + st * kQBytes, p.kcodes + row0 * kD, p.ksz + row0 * 4, wt);
+      store_dequant(smem + kOff_K + st * kQBytes, ra, wt);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[B_KFULL0 + st]);
-      dequant_tile(smem + kOff_V + st * kQBytes, p.vcodes + row0 * kD, p.vsz + row0 * 4, wt);
+      if (kt_next <= qt)
+        load_codes(ra, kcodes + static_cast<size_t>(kt_next) * kT * kD, ksz + kt_next * kT * 4, wt);
+      store_dequant(smem + kOff_V + st * kQBytes, rb, wt);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[B_VFULL0 + st]);
-      ++j;
+      kt = kt_next;
     }
     return;
   }

@@ -136,6 +136,13 @@ def decode_workspace_bytes(B: int, Hq: int, Hkv: int, D: int) -> int:
     return int(lib().kvq_decode_workspace_bytes(B, Hq, Hkv, D))
 
 
+def decode_workspace(B: int, Hq: int, Hkv: int, D: int, device="cuda"):
+    """A zero-filled decode workspace (the library keeps it zeroed between calls)."""
+    import torch
+    n = decode_workspace_bytes(B, Hq, Hkv, D)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
+
+
 def decode_attention(q, k: QuantCache, v: QuantCache, seq_lens, softmax_scale: float = 0.0,
                      out=None, out_dtype: int = OUT_F32, workspace=None, status=None, stream=None):
     """Decode attention: q bf16 [B][Hq][D] over the caches; returns out [B][Hq][D]."""
@@ -145,8 +152,7 @@ def decode_attention(q, k: QuantCache, v: QuantCache, seq_lens, softmax_scale: f
         out = torch.empty((B, Hq, D), dtype=torch.float32 if out_dtype == OUT_F32 else torch.bfloat16,
                           device=q.device)
     if workspace is None:
-        n = decode_workspace_bytes(B, Hq, k.Hkv, D)
-        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+        workspace = decode_workspace(B, Hq, k.Hkv, D, q.device)
     kc, vc = k.c_struct(), v.c_struct()
     st = lib().kvq_decode_attention(q.data_ptr(), ctypes.byref(kc), ctypes.byref(vc), seq_lens.data_ptr(),
                                     Hq, float(softmax_scale), out.data_ptr(), out_dtype,

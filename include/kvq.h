@@ -131,8 +131,11 @@ KVQ_API size_t kvq_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, in
  * softmax_scale: multiplies Q.K; <= 0 selects 1/sqrt(D).
  * out:      device [B][Hq][D], fp32 (out_dtype KVQ_OUT_F32) or bf16 (KVQ_OUT_BF16).
  * workspace: device scratch of >= kvq_decode_workspace_bytes(B, Hq, Hkv, D)
- *           bytes, 16-byte aligned; its contents need no initialisation.
- *           Calls that share a workspace must be ordered on the GPU.
+ *           bytes, 16-byte aligned.  Zero-fill it once before its first use
+ *           (e.g. cudaMemsetAsync): it holds per-segment arrival counters that
+ *           every successful call leaves at zero again.  After a call that
+ *           reported a device error, zero-fill it again.  Calls that share a
+ *           workspace must be ordered on the GPU.
  * q values must lie within fp16 range (|q| < 65504): the kernel's tensor-core
  * products take Q in fp16 (exact for bf16 values in that range).
  */

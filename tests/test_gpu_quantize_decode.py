@@ -238,3 +238,22 @@ def test_full_decode_long_ragged():
 
 def test_full_decode_mixed():
     _full_size_check(W.decode_mixed(), n_rows=4)
+
+
+def test_decode_workspace_reused_across_calls():
+    """The arrival counters in the workspace are back at zero after every call."""
+    kvq = _kvq()
+    ws = kvq.decode_workspace(6, 8, 2, 128)
+    for i, lens in enumerate(([1000, 77, 512, 0, 3, 640], [64, 65, 1024, 1, 900, 333], [1024] * 6)):
+        inp = W.make_decode(f"reuse{i}", 40 + i, 6, 8, 2, 128, 1024, lens=lens, bits="8")
+        kc, vc, status = _quantized_caches(inp)
+        out = kvq.decode_attention(U.to_dev_bf16(inp.q), kc, vc, torch.from_numpy(inp.seq_lens).cuda(),
+                                   inp.softmax_scale, workspace=ws, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        _, _, _, kd = U.oracle_quantize(inp.k, inp.head_bits)
+        _, _, _, vd = U.oracle_quantize(inp.v, inp.head_bits)
+        ref = O.decode_attention(inp.q, kd, vd, inp.seq_lens, inp.softmax_scale)
+        U.assert_close(out.cpu().numpy(), ref, f"reuse call {i}")
+    n_cnt = 6 * 2 * 4
+    assert int(ws[:n_cnt].sum().item()) == 0
