@@ -736,6 +736,8 @@ int decode_num_ctas(int D) {
 // workspace: [cnt: B*Hkv int32, padded to 16 B][lse: slots*rep f32, padded][o: slots*rep*D f32]
 static size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
+size_t decode_workspace_counter_bytes(int B, int Hkv) { return align16(static_cast<size_t>(B) * Hkv * 4); }
+
 size_t decode_workspace_bytes(int B, int Hq, int Hkv, int D, int num_ctas) {
   const size_t rep = static_cast<size_t>(Hq / Hkv);
   const size_t slots = static_cast<size_t>(B) * Hkv + num_ctas;

@@ -50,6 +50,8 @@ struct DecodeArgs {
 // Number of persistent split CTAs on the current device for head dim D.
 int decode_num_ctas(int D);
 size_t decode_workspace_bytes(int B, int Hq, int Hkv, int D, int num_ctas);
+// Leading bytes of a decode workspace that hold its arrival counters.
+size_t decode_workspace_counter_bytes(int B, int Hkv);
 kvq_status launch_decode(const DecodeArgs& a, cudaStream_t stream);
 
 struct PrefillArgs {

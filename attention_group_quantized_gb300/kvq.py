@@ -27,7 +27,7 @@ TILE_TOKENS = 64
 # every symbol include/kvq.h declares
 EXPORTS = ("kvq_cache_codes_bytes", "kvq_cache_sz_bytes", "kvq_cache_head_offset", "kvq_quantize",
            "kvq_decode_workspace_bytes", "kvq_decode_attention", "kvq_prefill_attention",
-           "kvq_status_str")
+           "kvq_decode_attention_noalloc", "kvq_status_str")
 
 
 class KvqError(RuntimeError):
@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
         L.kvq_prefill_attention.argtypes = [P, P, P, I32, I32, I32, I32, I32, I32, F32, P, I32, CP, CP, P, I32,
                                             P, P]
         L.kvq_prefill_attention.restype = I32
+        L.kvq_decode_attention_noalloc.argtypes = [P, CP, CP, P, I32, F32, P, I32, P, P]
+        L.kvq_decode_attention_noalloc.restype = I32
         L.kvq_status_str.argtypes = [I32]; L.kvq_status_str.restype = ctypes.c_char_p
         _LIB = L
     return _LIB
@@ -159,6 +161,27 @@ def decode_attention(q, k: QuantCache, v: QuantCache, seq_lens, softmax_scale: f
                                     workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                     status.data_ptr() if status is not None else None, _stream_ptr(stream))
     _check(st, "kvq_decode_attention")
+    return out
+
+
+def decode_attention_noalloc(q, k: QuantCache, v: QuantCache, seq_lens, softmax_scale: float = 0.0,
+                             out=None, out_dtype: int = OUT_F32, status=None, stream=None):
+    """Decode attention with the library's built-in scratch (no workspace argument).
+
+    For callers that cannot allocate device memory; the output buffer must be
+    given by the caller in that case (``out``).  Calls on one device share the
+    scratch, so they must be ordered on the GPU.
+    """
+    import torch
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32 if out_dtype == OUT_F32 else torch.bfloat16,
+                          device=q.device)
+    kc, vc = k.c_struct(), v.c_struct()
+    st = lib().kvq_decode_attention_noalloc(q.data_ptr(), ctypes.byref(kc), ctypes.byref(vc), seq_lens.data_ptr(),
+                                            Hq, float(softmax_scale), out.data_ptr(), out_dtype,
+                                            status.data_ptr() if status is not None else None, _stream_ptr(stream))
+    _check(st, "kvq_decode_attention_noalloc")
     return out
 
 

@@ -173,6 +173,31 @@ KVQ_API kvq_status kvq_prefill_attention(const void* q, const void* k, const voi
                                  void* out, int32_t out_dtype,
                                  int32_t* dev_status, void* stream);
 
+/*
+ * kvq_decode_attention_noalloc -- kvq_decode_attention for callers that may
+ * not allocate device memory (for example code running inside another
+ * framework's memory pool, or a plugin whose host forbids cudaMalloc at call
+ * time).  The source pages have no counterpart to this call.
+ *
+ * Arguments and results are those of kvq_decode_attention, minus the
+ * workspace: the split scratch is a fixed array of 4 MiB compiled into the
+ * library, present on every GPU that loads it until the process exits.  A
+ * shape whose kvq_decode_workspace_bytes() exceeds 4 MiB returns
+ * KVQ_ERR_WORKSPACE and launches nothing.  The call allocates nothing; it
+ * clears the array's arrival counters with an asynchronous memset on `stream`
+ * before the decode launch.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * Every call on a device shares the one array, so calls whose executions
+ * overlap on the GPU (different streams, no ordering between them) race and
+ * give wrong results; order them.
+ */
+KVQ_API kvq_status kvq_decode_attention_noalloc(const void* q, const kvq_cache* k, const kvq_cache* v,
+                                                const int32_t* seq_lens, int32_t Hq, float softmax_scale,
+                                                void* out, int32_t out_dtype,
+                                                int32_t* dev_status, void* stream);
+
 /* Static, human-readable name of a status code. */
 KVQ_API const char* kvq_status_str(kvq_status status);
 
