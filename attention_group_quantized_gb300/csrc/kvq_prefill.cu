@@ -168,10 +168,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
+  // Registers: the CTA is launched with 128 per thread (checked on the host).
+  // Each warpgroup resets its own limit at the top of its branch:
+  //   TMA/MMA 128 -> 80 (frees 6144), softmax x2 128 -> 120 (frees 2048),
+  //   dequant 128 -> 192 (takes 8192): 128 x (80 + 192 + 120 + 120) = 65536
+  // = 512 x 128, and per sub-partition (one warp of each warpgroup)
+  // 32 x (80 + 192 + 120 + 120) = 16384, its whole register file.
+
   // number of kept key tiles (identical in every role)
   int n_kept = 0;
   for (int kt = 0; kt <= qt; ++kt) n_kept += tile_kept(p, qt, kt) ? 1 : 0;
 
+  if (warp < 4) {
+  tc::reg_dealloc<80>();
   if (warp == 0) {
     // ---------------- Q by TMA, then wait for the end and free TMEM ----------------
     if (lane == 0) {
@@ -242,9 +251,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     return;
   }
 
-  if (warp < 4) return;   // warps 2, 3: no role
+  return;   // warps 2, 3: no role
+  }
 
   if (warp < 8) {
+    tc::reg_alloc<192>();
     // ---------------- dequant warpgroup ----------------
     const int wt = threadIdx.x - 128;
     if (!mbar_wait(&bar[B_QFULL], 0, p.status)) return;
@@ -297,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   }
 
   // ---------------- softmax warpgroups ----------------
+  tc::reg_dealloc<120>();
   const int h = (warp - 8) >> 2;            // head slot 0 or 1
   if (h >= nh) return;
   const int q4 = warp & 3;                  // TMEM lane quarter
@@ -313,17 +325,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const bool diag = kt == qt;
     ok = mbar_wait(&bar[B_SFULL0 + h], j & 1, p.status);
     tc::fence_after_sync();
-    // pass 1: row max
+    // pass 1: row max (the causal rule only applies on the diagonal tile)
     float mx = -INFINITY;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t v[32];
       tc::ld_32x32b_x32(s_addr + c * 32, v);
       tc::wait_ld();
+      if (!diag) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const bool masked = diag && (c * 32 + i > r);
-        mx = masked ? mx : fmaxf(mx, __uint_as_float(v[i]));
+        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(v[i]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mx = (c * 32 + i > r) ? mx : fmaxf(mx, __uint_as_float(v[i]));
       }
     }
     const float m_tile = mx * sl2;
@@ -333,28 +347,33 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       alpha = (m_run == -INFINITY) ? 0.0f : fast_exp2(m_run - m_use);
       m_run = m_use;
     }
-    // pass 2: P = 2^(S*scale_log2 - m), written over the first half of S as fp16 pairs
+    // pass 2: P = 2^(S*scale_log2 - m) as fp16 pairs, written over the part of S
+    // already read (columns 16c.. of P after S columns 32c.. were loaded)
     float psum = 0.0f;
 #pragma unroll
-    for (int cp = 0; cp < 2; ++cp) {
-      uint32_t pk[32];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int c = cp * 2 + half;
-        uint32_t v[32];
-        tc::ld_32x32b_x32(s_addr + c * 32, v);
-        tc::wait_ld();
+    for (int c = 0; c < 4; ++c) {
+      uint32_t v[32];
+      uint32_t pk[16];
+      tc::ld_32x32b_x32(s_addr + c * 32, v);
+      tc::wait_ld();
+      if (!diag) {
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const bool m0 = diag && (c * 32 + i > r);
-          const bool m1 = diag && (c * 32 + i + 1 > r);
-          const float p0 = m0 ? 0.0f : fast_exp2(fmaf(__uint_as_float(v[i]), sl2, -m_use));
-          const float p1 = m1 ? 0.0f : fast_exp2(fmaf(__uint_as_float(v[i + 1]), sl2, -m_use));
+          const float p0 = fast_exp2(fmaf(__uint_as_float(v[i]), sl2, -m_use));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(v[i + 1]), sl2, -m_use));
           psum += p0 + p1;
-          pk[half * 16 + i / 2] = pack_half2(p0, p1);
+          pk[i / 2] = pack_half2(p0, p1);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float p0 = (c * 32 + i > r) ? 0.0f : fast_exp2(fmaf(__uint_as_float(v[i]), sl2, -m_use));
+          const float p1 = (c * 32 + i + 1 > r) ? 0.0f : fast_exp2(fmaf(__uint_as_float(v[i + 1]), sl2, -m_use));
+          psum += p0 + p1;
+          pk[i / 2] = pack_half2(p0, p1);
         }
       }
-      tc::st_32x32b_x32(s_addr + cp * 32, pk);
+      tc::st_32x32b_x16(s_addr + c * 16, pk);
     }
     l_run = l_run * alpha + psum;
     // rescale O (rare): needs the previous P.V product finished
@@ -414,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 }
 
 bool g_attr_set = false;
+int g_regs_ok = -1;   // the register split above assumes 128 registers per thread at launch
 
 }  // namespace
 
@@ -439,6 +459,11 @@ kvq_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.nT = a.S / kT;
   const float scale = a.softmax_scale > 0.0f ? a.softmax_scale : 1.0f / sqrtf(static_cast<float>(kD));
   p.scale_log2 = scale * 1.4426950408889634f;
+  if (g_regs_ok < 0) {
+    cudaFuncAttributes fa;
+    g_regs_ok = (cudaFuncGetAttributes(&fa, prefill_kernel) == cudaSuccess && fa.numRegs == 128) ? 1 : 0;
+  }
+  if (g_regs_ok != 1) return KVQ_ERR_UNSUPPORTED;
   if (!g_attr_set) {
     if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
       return KVQ_ERR_CUDA;
