@@ -184,6 +184,92 @@ def run_reference(args, rank):
     print(json.dumps(line))
 
 
+def time_decode(torch, kvq, inp, dev, l2, steps, warmup, dist=None, keep=False, busy_s=0.0, sampler=None):
+    """Back-to-back decode steps over cache copies larger than 3x L2 together.
+
+    Returns the total device time of `steps` steps (max over ranks) and the
+    algorithmic bytes per step; with keep=True also the device buffers.
+    """
+    import numpy as np
+    B, Hq, Hkv, D, Tcap = inp.B, inp.Hq, inp.Hkv, inp.D, inp.Tcap
+    todev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    nbytes = decode_bytes(inp)
+    n_copies = max(2, -(-3 * l2 // max(nbytes, 1)))
+    kd, vd = todev(inp.k), todev(inp.v)
+    caches = []
+    for _ in range(n_copies):
+        kc = kvq.empty_cache(inp.head_bits, B, Tcap, D, device=dev)
+        vc = kvq.empty_cache(inp.head_bits, B, Tcap, D, device=dev)
+        kvq.quantize(kd, kc)
+        kvq.quantize(vd, vc)
+        caches.append((kc, vc))
+    del kd, vd
+    q = todev(inp.q)
+    sl = torch.from_numpy(inp.seq_lens).to(dev)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    ws = kvq.decode_workspace(B, Hq, Hkv, D, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        kc_i, vc_i = caches[i % n_copies]
+        kvq.decode_attention(q, kc_i, vc_i, sl, inp.softmax_scale, out=out, workspace=ws, status=status)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    clk = sampler() if sampler else None
+    if clk:
+        clk.__enter__()
+    # sustained load (untimed) right before the timed steps, so clock samples
+    # taken around them see the GPU in the same state
+    t_busy = time.time()
+    while time.time() - t_busy < busy_s:
+        for i in range(200):
+            step(i)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clk:
+        clk.__exit__(None, None, None)
+    t_total = t0.elapsed_time(t1) / 1e3
+    if dist:
+        tt = torch.tensor([t_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_total = float(tt.item())
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    res = {"t_total": t_total, "bytes": nbytes, "n_copies": n_copies, "clk": clk}
+    if keep:
+        res.update(caches=caches, q=q, sl=sl, ws=ws)
+    return res
+
+
+def bench_extra_decodes(torch, kvq, W, peaks, dev, steps, warmup):
+    """The other decode workloads, measured the same way (context for the main line)."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    res = {}
+    for name in ("decode_long_ragged", "decode_mixed", "decode_tiny"):
+        inp = W.NAMED[name]()
+        d = time_decode(torch, kvq, inp, dev, l2, steps, warmup)
+        avg = d["t_total"] / steps
+        gbs = d["bytes"] / avg / 1e9
+        res[inp.name] = {"GB/s": round(gbs, 1), "us_per_step": round(avg * 1e6, 2),
+                         "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4), "bytes_per_step": d["bytes"]}
+        del d
+        torch.cuda.empty_cache()
+    return res
+
+
 def bench_prefill(torch, kvq, W, peaks, steps, warmup, dev):
     """Causal prefill workload (quantise K/V + tile-masked attention): TFLOP/s."""
     import numpy as np
@@ -231,6 +317,9 @@ def main():
     ap.add_argument("--workload", default="decode_gqa")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the other decode workloads")
+    ap.add_argument("--busy-seconds", type=float, default=1.0,
+                    help="untimed sustained decode steps before the timed ones, under the clock sampler")
     ap.add_argument("--only-prefill", action="store_true",
                     help="run only the causal prefill workload and print its JSON object")
     args = ap.parse_args()
@@ -266,60 +355,17 @@ def main():
 
     inp = W.NAMED[args.workload]()
     B, Hq, Hkv, D, Tcap = inp.B, inp.Hq, inp.Hkv, inp.D, inp.Tcap
-    todev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
-    # Several copies of the quantised cache, visited in turn, so the bytes one step
-    # reads were not read by the previous steps (together more than 3x L2): the
-    # steps run back to back with no L2 flush and no host gap between them.
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    bytes_per_step = decode_bytes(inp)
-    n_copies = max(2, -(-3 * l2 // bytes_per_step))
-    kd, vd = todev(inp.k), todev(inp.v)
-    caches = []
-    for _ in range(n_copies):
-        kc = kvq.empty_cache(inp.head_bits, B, Tcap, D, device=dev)
-        vc = kvq.empty_cache(inp.head_bits, B, Tcap, D, device=dev)
-        kvq.quantize(kd, kc)
-        kvq.quantize(vd, vc)
-        caches.append((kc, vc))
-    del kd, vd
-    kc, vc = caches[0]
-    q = todev(inp.q)
-    sl = torch.from_numpy(inp.seq_lens).to(dev)
-    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
-    ws = kvq.decode_workspace(B, Hq, Hkv, D, dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def step(i):
-        kc_i, vc_i = caches[i % n_copies]
-        kvq.decode_attention(q, kc_i, vc_i, sl, inp.softmax_scale, out=out, workspace=ws, status=status)
-
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        t_start.record(stream)
-        for i in range(args.steps):
-            step(i)
-        t_end.record(stream)
-        torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_total = t_start.elapsed_time(t_end) / 1e3
-    if dist:
-        tt = torch.tensor([t_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_total = float(tt.item())
-    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    d = time_decode(torch, kvq, inp, dev, l2, args.steps, args.warmup, dist, keep=True, busy_s=args.busy_seconds,
+                    sampler=lambda: ClockSampler(local))
+    clk = d["clk"]
+    caches, n_copies, q, sl, ws = d["caches"], d["n_copies"], d["q"], d["sl"], d["ws"]
+    bytes_per_step = d["bytes"]
+    t_total = d["t_total"]
     value = bytes_per_step * world * args.steps / t_total / 1e9
     avg = t_total / args.steps
     achieved = bytes_per_step / avg / 1e9
+    stream = torch.cuda.current_stream()
 
     # e2e: new query + new K/V token from pinned host memory, quantise-append, decode, read back
     pin = lambda t: t.pin_memory()
@@ -366,11 +412,14 @@ def main():
                "ms_per_step": te / args.steps * 1e3,
                "step": "H2D q + new-token K/V, kvq_quantize x2 (append), kvq_decode_attention (bf16 out), D2H out"}
 
+    del caches, d
+    torch.cuda.empty_cache()
     prefill = None
     if not args.no_prefill and rank == 0:
-        del caches
-        torch.cuda.empty_cache()
         prefill = bench_prefill(torch, kvq, W, peaks, max(3, min(args.steps, 10)), 3, dev)
+    extras = None
+    if not args.no_extras and rank == 0:
+        extras = bench_extra_decodes(torch, kvq, W, peaks, dev, args.steps, args.warmup)
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
@@ -400,6 +449,7 @@ def main():
             "clocks": clk.summary(),
             "gpu_launches": args.steps,
             "prefill": prefill,
+            "other_decode_workloads": extras,
         }
         print(json.dumps(line))
     if dist:
