@@ -15,11 +15,18 @@
 //    (o, lse) per segment piece it touched, and the CTA that completes a
 //    segment (a per-segment arrival counter) merges its pieces in place -- no
 //    second kernel.  A segment held by one CTA is written out directly.
-//  * A producer warp streams each tile's codes by TMA (2D tensor copies with
+//  * Eight warps in two warpgroups.  Warps 0-3 consume tiles, 16 tokens
+//    each, two tiles of a piece per step for more independent work per
+//    warp.  Warp 4 streams each tile's codes by TMA (2D tensor copies with
 //    hardware swizzle) and its scale/zero words by 1D bulk copies into a
-//    3-stage ring, then turns the scale/zero words into per-tile tables
-//    (fp32 scales, zero terms, tokens past the sequence end zeroed) so the
-//    four consumer warps do no per-group conversions.
+//    kStages-deep ring.  Warps 5 and 7 (even and odd tiles) turn the
+//    scale/zero words of each landed tile into tables (fp32 scales carrying
+//    the softmax scale, zero terms, tokens past the sequence end zeroed) so
+//    the consumers do no per-group conversions.  Warp 6 runs piece ends
+//    other than the CTA's last -- combining the consumers' states, writing
+//    the partial, counting arrivals, merging -- while the consumers go on
+//    with the next tiles; the last piece the consumers finish themselves.
+//    setmaxnreg moves registers from the helper warpgroup to the consumers.
 //  * The products run on the tensor cores with exact operands: a code byte
 //    becomes the fp16 value 1024 + c by one byte permute.
 //      S = Q K^T (rows = the query heads of the KV head, columns = tokens),
@@ -40,13 +47,22 @@
 
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
+#include "kvq_tc.cuh"
 
 namespace kvq {
 namespace {
 
 constexpr int kTile = 64;       // tokens per pipeline stage
 constexpr int kWarps = 4;       // consumer warps; each owns 16 tokens of a tile
-constexpr int kThreads = (kWarps + 2) * 32;   // + TMA issuer warp + table builder warp
+// two warpgroups: the consumers, then TMA issuer, table builder, epilogue and one idle warp
+constexpr int kThreads = 2 * kWarps * 32;
+// setmaxnreg split of the 128 registers a thread is launched with (tunable at build time)
+#ifndef KVQ_DECODE_CONSUMER_REGS
+#define KVQ_DECODE_CONSUMER_REGS 160
+#endif
+constexpr int kConsumerRegs = KVQ_DECODE_CONSUMER_REGS;
+constexpr int kHelperRegs = 256 - kConsumerRegs;
+static_assert(kWarps * (kConsumerRegs + kHelperRegs) == 2 * kWarps * 128, "register split must use the launch allocation");
 // pipeline depth and CTAs per SM (tunable at build time)
 #ifndef KVQ_DECODE_STAGES
 #define KVQ_DECODE_STAGES 4
@@ -75,6 +91,15 @@ struct DParams {
   int8_t bits[KVQ_MAX_HKV];
 };
 
+// Hand-off buffer from the consumer warps to the epilogue warp at a piece end.
+template <int D>
+struct EpiBuf {
+  float o[kWarps][kMaxRep][D];     // unnormalised output per consumer warp and head
+  float ml[kWarps][kMaxRep][2];    // (running max, sum) per consumer warp and head, log2 domain
+  int4 info;                       // sequence, KV head
+  int flag[2];                     // last-arrival flags: epilogue warp, consumer warps
+};
+
 template <int D>
 struct Smem {
   static constexpr int G = D / 32;
@@ -83,23 +108,27 @@ struct Smem {
   // offsets inside a stage
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kCodeBytes;
-  static constexpr int kOffKsz = 2 * kCodeBytes;
-  static constexpr int kOffVsz = kOffKsz + kSzBytes;
-  static constexpr int kOffKt = kOffVsz + kSzBytes;        // float2 [G][64 tok]: (s, (1024 + z) s)
+  static constexpr int kOffKsz = 2 * kCodeBytes;          // raw K scale/zero words [64 tok][G] ...
+  static constexpr int kOffVsz = kOffKsz + kSzBytes;       // ... and V's, both replaced by
+  static constexpr int kOffKt = kOffKsz;                   // float2 [G][64 tok]: (s, (1024 + z) s) scaled
   static constexpr int kOffVtS = kOffKt + kTile * G * 8;   // float [G][64 tok] s
   static constexpr int kOffVtZ = kOffVtS + kTile * G * 4;  // u16   [G][64 tok] fp16 (1024 + z)
   static constexpr int kOffMeta = kOffVtZ + kTile * G * 2; // int4 {b, kvh, i | flags, len}
-  static constexpr int kStageBytes = ((kOffMeta + 16 + 1023) / 1024) * 1024;
-  // a finished slot doubles as the merge scratch of a piece end
-  static constexpr int kMergeO = kWarps * kMaxRep * D * 4;
-  static_assert(kMergeO + kWarps * kMaxRep * 8 + 16 <= kStageBytes, "merge scratch must fit a stage");
-  static constexpr int kBars = (3 * kStages + 1) * 8;
-  static constexpr int kFixed = kStages * kStageBytes + kBars;
+  static constexpr int kOffQ = kOffMeta + 16;              // bf16 [rep][D]: the piece's queries (first tile)
+  static constexpr int kStageBytes = ((kOffQ + kMaxRep * D * 2 + 1023) / 1024) * 1024;
+  static_assert(kOffKt + kTile * G * 8 == kOffVsz + kSzBytes, "the K table exactly covers the raw words");
+  static constexpr int kOffEpi = kStages * kStageBytes;                       // EpiBuf<D>
+  static constexpr int kOffBars = kOffEpi + ((static_cast<int>(sizeof(EpiBuf<D>)) + 15) / 16) * 16;
+  static constexpr int kBars = (3 * kStages + 3) * 8;
+  static constexpr int kFixed = kOffBars + kBars;
   static size_t bytes(int B) { return 1024 + kFixed + static_cast<size_t>(B + 1) * 4 * 2; }
 };
 
-constexpr int kFlagStart = 1 << 30;
-constexpr int kFlagEnd = 1 << 29;
+// tile flags (meta.z): tile index in bits 0-23, then
+constexpr int kFlag4 = 1 << 24;      // the KV head is stored with 4-bit codes
+constexpr int kFlagFull = 1 << 25;   // every token of the tile is inside the sequence
+constexpr int kFlagEnd = 1 << 29;    // last tile of a piece
+constexpr int kFlagStart = 1 << 30;  // first tile of a piece
 
 // Byte offset of (row, byte) inside a TMA tile written with the swizzle mode
 // matching its row pitch R (128B, 64B or 32B): the 16-byte chunk index is
@@ -177,9 +206,9 @@ __device__ __forceinline__ LaneAddr lane_addr(int w, int lane) {
 //   4-bit: k-steps 2g, 2g+1 of group g: ch 32g + 8t + {(0,4),(1,5)} and {(2,6),(3,7)}
 template <int D>
 __device__ __forceinline__ void load_q(uint32_t (&qa)[D / 16][2], float (&qsum)[D / 32], const DParams& p,
-                                       int b, int kvh, int bits, int g, int t) {
+                                       const uint16_t* qs, int bits, int g, int t) {
   constexpr int G = D / 32;
-  const uint16_t* src = p.q + (static_cast<int64_t>(b) * p.Hq + kvh * p.rep + g) * D;
+  const uint16_t* src = qs + g * D;
   bool ok = true;
 #pragma unroll
   for (int grp = 0; grp < G; ++grp) {
@@ -256,15 +285,15 @@ __device__ __forceinline__ void qk_tile(float (&S)[2][2], const uint32_t (&qa)[D
 #pragma unroll
       for (int gg = 0; gg < (BITS == 8 ? 2 : G); ++gg) {
         const int grp = BITS == 8 ? 2 * h + gg : gg;
-        float c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float c[4];
         if constexpr (BITS == 8) {
-          mma_16816(c, qa[2 * grp][0], 0u, qa[2 * grp][1], 0u, bytes01_biased(r[2 * gg]),
-                    bytes23_biased(r[2 * gg]));
+          mma_16816_z(c, qa[2 * grp][0], 0u, qa[2 * grp][1], 0u, bytes01_biased(r[2 * gg]),
+                      bytes23_biased(r[2 * gg]));
           mma_16816(c, qa[2 * grp + 1][0], 0u, qa[2 * grp + 1][1], 0u, bytes01_biased(r[2 * gg + 1]),
                     bytes23_biased(r[2 * gg + 1]));
         } else {
           const uint32_t cw = r[gg];
-          mma_16816(c, qa[2 * grp][0], 0u, qa[2 * grp][1], 0u, nib_biased(cw), nib_biased(cw >> 4));
+          mma_16816_z(c, qa[2 * grp][0], 0u, qa[2 * grp][1], 0u, nib_biased(cw), nib_biased(cw >> 4));
           mma_16816(c, qa[2 * grp + 1][0], 0u, qa[2 * grp + 1][1], 0u, nib_biased(cw >> 8), nib_biased(cw >> 12));
         }
         const float4 sz = *reinterpret_cast<const float4*>(kt + grp * kTile + tok);  // tokens tok, tok+1
@@ -331,112 +360,158 @@ __device__ __forceinline__ int acc_channel(int grp, int mh, int half, int g) {
   return 32 * grp + 4 * g + 2 * mh + half;
 }
 
-__device__ __forceinline__ void store_out(const DParams& p, int64_t i, float v) {
-  if (p.out_dtype == KVQ_OUT_F32) reinterpret_cast<float*>(p.out)[i] = v;
-  else reinterpret_cast<__nv_bfloat16*>(p.out)[i] = __float2bfloat16_rn(v);
-}
-
-// Bounded barrier among the four consumer warps (tid < 128).  A plain bar.sync
-// could wait forever if one warp left after a timed-out wait.
-__device__ __forceinline__ void consumer_sync(uint64_t* gbar, uint32_t* gphase, bool* ok, int32_t* status) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(gbar);
-  *ok = *ok && mbar_wait(gbar, *gphase & 1, status);
-  ++*gphase;
-  __syncwarp();
-}
-
 // Whether CTA c of the stream-K split got an empty tile range (only possible
 // when there are fewer tiles than CTAs).
 __device__ __forceinline__ bool cta_empty(int64_t N, int C, int c) { return N * (c + 1) / C == N * c / C; }
 
-// End of a piece (kept out of line: it is rare and would otherwise crowd the
-// hot loop's registers).  m_o[w][h][ch], m_ml[w][h] = (max, sum) hold the four
-// consumer warps' states.  A segment held by this CTA alone is normalised and
-// written out; otherwise the CTA's partial (o, lse) goes to the workspace and
-// the CTA whose arrival completes the segment merges all its pieces.
+// Sequences of length 0 get a zero output row (no CTA visits them); one warp
+// per CTA writes its share of the rows.
 template <int D>
-__device__ __noinline__ uint32_t finish_piece(const DParams* pp, float* m_o, float* m_ml, int cb, int ckvh,
-                                              const int32_t* pre, int64_t N, int C, int tid, uint64_t* gbar,
-                                              uint32_t gphase_in, bool ok_in) {
-  uint32_t gph = gphase_in;
-  bool okv = ok_in;
-  uint32_t* gphase = &gph;
-  bool* ok = &okv;
-  const DParams& p = *pp;
-  const int Hkv = p.Hkv, rep = p.rep;
-  int* info = reinterpret_cast<int*>(m_ml + kWarps * kMaxRep * 2);   // [c0, c1, npieces, last]
-  const int seg = cb * Hkv + ckvh;
-  if (tid == 0) {
-    const int n_b = pre[cb + 1] - pre[cb];
-    const int64_t start = static_cast<int64_t>(Hkv) * pre[cb] + static_cast<int64_t>(ckvh) * n_b;
-    const int c0 = static_cast<int>(((start + 1) * C - 1) / N);
-    const int c1 = static_cast<int>(((start + n_b) * C - 1) / N);
-    int np = c1 - c0 + 1;
-    if (N < C) {  // some CTAs may have empty ranges: count the ones that wrote a piece
-      np = 0;
-      for (int c = c0; c <= c1; ++c) np += cta_empty(N, C, c) ? 0 : 1;
+__device__ __forceinline__ void zero_empty_rows(const DParams& p, const int32_t* lens, int lane) {
+  const int n = p.B * p.Hq * D;
+  for (int idx = blockIdx.x * 32 + lane; idx < n; idx += gridDim.x * 32) {
+    const int b = idx / (p.Hq * D);
+    if (lens[b] == 0) {
+      if (p.out_dtype == KVQ_OUT_F32) reinterpret_cast<float*>(p.out)[idx] = 0.0f;
+      else reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(0.0f);
     }
-    info[0] = c0; info[1] = c1; info[2] = np;
   }
-  consumer_sync(gbar, gphase, ok, p.status);
-  const int c0 = info[0], c1 = info[1], npieces = info[2];
-  const int64_t orow0 = (static_cast<int64_t>(cb) * p.Hq + ckvh * rep) * D;
+}
+
+// Number of pieces (runs of tiles inside one segment) in a CTA's tile range.
+__device__ __forceinline__ int count_pieces(int64_t f0, int ntiles, const int32_t* pre, int B, int Hkv) {
+  Cursor c = locate(f0, pre, B, Hkv);
+  int left = ntiles, n = 0;
+  while (left > 0) {
+    const int nb = pre[c.b + 1] - pre[c.b];
+    const int take = min(left, nb - c.i);
+    left -= take;
+    ++n;
+    c.i = nb - 1;
+    advance(c, pre, B, Hkv);
+  }
+  return n;
+}
+
+__device__ __forceinline__ void store_out4(const DParams& p, int64_t i, float4 v) {
+  if (p.out_dtype == KVQ_OUT_F32) {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + i) = v;
+  } else {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&a);
+    u.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p.out) + i) = u;
+  }
+}
+
+// Thread-group synchronisation for segment_end: the epilogue warp uses
+// __syncwarp; the four consumer warps a bounded mbarrier round (a plain
+// bar.sync could wait forever if one warp left after a timed-out wait).
+struct WarpSync {
+  __device__ __forceinline__ void operator()() const { __syncwarp(); }
+};
+struct ConsumerSync {
+  uint64_t* bar;
+  uint32_t* phase;
+  bool* ok;
+  int32_t* status;
+  __device__ __forceinline__ void operator()() const {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+    *ok = *ok && mbar_wait(bar, *phase & 1, status);
+    ++*phase;
+    __syncwarp();
+  }
+};
+
+// End of a piece.  The four consumer warps' states (running max and sum per
+// head, unnormalised o per head and channel) sit in the hand-off buffer.  A
+// segment held by this CTA alone is normalised and written out; otherwise the
+// CTA's partial (o, lse) goes to the workspace and the CTA whose arrival
+// completes the segment merges all its pieces by log-sum-exp.  Run by
+// `nthr` threads (tid = 0 .. nthr-1) that `sync` joins; `epi_empty`, if
+// given, is arrived once the buffer has been read.
+template <int D, int MB, class Sync>
+__device__ __forceinline__ void segment_end(const DParams& p, const EpiBuf<D>* eb, int* flag, int cb, int ckvh,
+                                            const int32_t* pre, int64_t N, int C, int tid, int nthr,
+                                            const Sync& sync, uint64_t* epi_empty) {
+  const int Hkv = p.Hkv, rep = p.rep;
+  const int seg = cb * Hkv + ckvh;
+  const int n_b = pre[cb + 1] - pre[cb];
+  const int64_t start = static_cast<int64_t>(Hkv) * pre[cb] + static_cast<int64_t>(ckvh) * n_b;
+  // CTAs holding the first and the last tile of the segment
+  const int c0 = static_cast<int>(((start + 1) * C - 1) / N);
+  const int c1 = static_cast<int>(((start + n_b) * C - 1) / N);
   const bool whole = c0 == c1;
+  const int64_t orow0 = (static_cast<int64_t>(cb) * p.Hq + ckvh * rep) * D;
   const int64_t slot = static_cast<int64_t>(seg) + blockIdx.x;
-  for (int idx = tid; idx < rep * D; idx += kWarps * 32) {
-    const int h = idx / D, ch = idx % D;
+  for (int i4 = tid; i4 < rep * (D / 4); i4 += nthr) {
+    const int h = i4 / (D / 4), ch = (i4 % (D / 4)) * 4;
     float M = -INFINITY;
 #pragma unroll
-    for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, m_ml[(ww * kMaxRep + h) * 2]);
-    float Lsum = 0.0f, o = 0.0f;
+    for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, eb->ml[ww][h][0]);
+    float Lsum = 0.0f;
+    float4 o = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if (M != -INFINITY) {
 #pragma unroll
       for (int ww = 0; ww < kWarps; ++ww) {
-        const float sc = fast_exp2(m_ml[(ww * kMaxRep + h) * 2] - M);
-        Lsum += m_ml[(ww * kMaxRep + h) * 2 + 1] * sc;
-        o += m_o[(ww * kMaxRep + h) * D + ch] * sc;
+        const float sc = fast_exp2(eb->ml[ww][h][0] - M);
+        Lsum += eb->ml[ww][h][1] * sc;
+        const float4 v = *reinterpret_cast<const float4*>(&eb->o[ww][h][ch]);
+        o.x += v.x * sc; o.y += v.y * sc; o.z += v.z * sc; o.w += v.w * sc;
       }
     }
     const bool any = M != -INFINITY && Lsum > 0.0f;
+    const float inv = any ? 1.0f / Lsum : 0.0f;
+    o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
     if (whole) {
-      store_out(p, orow0 + idx, any ? o / Lsum : 0.0f);
+      store_out4(p, orow0 + static_cast<int64_t>(h) * D + ch, o);
     } else {
-      p.ws_o[(slot * rep + h) * D + ch] = any ? o / Lsum : 0.0f;
+      *reinterpret_cast<float4*>(p.ws_o + (slot * rep + h) * D + ch) = o;
       if (ch == 0) p.ws_lse[slot * rep + h] = any ? M + __log2f(Lsum) : -INFINITY;
     }
   }
-  if (whole) {
-    consumer_sync(gbar, gphase, ok, p.status);
-    return (gph << 1) | (okv ? 1u : 0u);
+  if (epi_empty != nullptr || !whole) sync();   // the group's reads of eb / stores are done
+  if (epi_empty != nullptr && tid == 0) mbar_arrive(epi_empty);   // the consumers may refill the buffer
+  if (whole) return;
+  // publish the piece and count the arrivals: after the group barrier, the
+  // leader's fence orders every member's partial stores (fences are
+  // cumulative) before its atomic; the last arriver's second fence orders the
+  // other pieces before the group's reads below
+  const bool check = N < C;   // some CTAs may have empty ranges
+  if (tid == 0) {
+    int np = c1 - c0 + 1;
+    if (check) {
+      np = 0;
+      for (int c = c0; c <= c1; ++c) np += cta_empty(N, C, c) ? 0 : 1;
+    }
+    __threadfence();
+    const int last = (atomicAdd(&p.ws_cnt[seg], 1) + 1 == np) ? 1 : 0;
+    if (last) __threadfence();
+    *flag = last;
   }
-  // publish the piece (each writer fences its own stores), then count the arrivals
-  __threadfence();
-  consumer_sync(gbar, gphase, ok, p.status);
-  if (tid == 0) info[3] = (atomicAdd(&p.ws_cnt[seg], 1) + 1 == npieces) ? 1 : 0;
-  consumer_sync(gbar, gphase, ok, p.status);
-  if (info[3] != 1) return (gph << 1) | (okv ? 1u : 0u);
-  __threadfence();
-  // the segment is complete: one online log-sum-exp pass over its pieces, four
-  // channels per thread, eight pieces of loads in flight
-  const bool check = N < C;
-  for (int i4 = tid; i4 < rep * (D / 4); i4 += kWarps * 32) {
+  sync();
+  if (*flag != 1) return;
+  // the segment is complete: one online log-sum-exp pass over its pieces,
+  // four channels per thread, MB pieces of loads in flight
+  for (int i4 = tid; i4 < rep * (D / 4); i4 += nthr) {
     const int h = i4 / (D / 4), ch = (i4 % (D / 4)) * 4;
     float M = -INFINITY, Lsum = 0.0f;
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    for (int cb8 = c0; cb8 <= c1; cb8 += 8) {
-      float lse[8];
-      float4 v[8];
+    for (int cb4 = c0; cb4 <= c1; cb4 += MB) {
+      float lse[MB];
+      float4 v[MB];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int c = cb8 + u;
+      for (int u = 0; u < MB; ++u) {
+        const int c = cb4 + u;
         const bool live = c <= c1 && !(check && cta_empty(N, C, c));
         const int64_t sl = static_cast<int64_t>(seg) + (live ? c : c0);
         lse[u] = live ? __ldcg(p.ws_lse + sl * rep + h) : -INFINITY;
         v[u] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (sl * rep + h) * D + ch));
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
+      for (int u = 0; u < MB; ++u) {
         if (lse[u] == -INFINITY) continue;
         const float M2 = fmaxf(M, lse[u]);
         const float a = fast_exp2(M - M2), bw = fast_exp2(lse[u] - M2);
@@ -447,14 +522,71 @@ __device__ __noinline__ uint32_t finish_piece(const DParams* pp, float* m_o, flo
       }
     }
     const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
-    const int64_t o0 = orow0 + static_cast<int64_t>(h) * D + ch;
-    store_out(p, o0 + 0, acc.x * inv);
-    store_out(p, o0 + 1, acc.y * inv);
-    store_out(p, o0 + 2, acc.z * inv);
-    store_out(p, o0 + 3, acc.w * inv);
+    acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+    store_out4(p, orow0 + static_cast<int64_t>(h) * D + ch, acc);
   }
   if (tid == 0) p.ws_cnt[seg] = 0;   // ready for the next call
-  return (gph << 1) | (okv ? 1u : 0u);
+}
+
+// One consumer step over NT tiles (1, or 2 of the same piece) for the warp's
+// 16 tokens of each: scores, one online-softmax update over all of them, and
+// the P.V products.
+template <int D, int BITS, int NT>
+__device__ __forceinline__ void consume_tiles(const uint32_t (&st_s)[NT], const uint8_t* const (&st)[NT],
+                                              const int (&flags)[NT], int len, const uint32_t (&qa)[D / 16][2],
+                                              const float (&qsum)[D / 32], float (&O)[D / 16][4], float (&Z)[4],
+                                              float& m_run, float& l_run, const LaneAddr& la, int w, int g,
+                                              int t) {
+  float S[NT][2][2];   // log2-domain scores (the table carries the softmax scale)
+#pragma unroll
+  for (int u = 0; u < NT; ++u) qk_tile<D, BITS>(S[u], qa, qsum, st_s[u], st[u], la, w, t);
+  // mask past the sequence end (only the last tile of a sequence)
+#pragma unroll
+  for (int u = 0; u < NT; ++u) {
+    if (!(flags[u] & kFlagFull)) {
+      const int tok0 = (flags[u] & 0xFFFFFF) * kTile + 16 * w + 2 * t;
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          if (tok0 + 8 * j + e >= len) S[u][j][e] = -INFINITY;
+    }
+  }
+  // online softmax per head row g
+  float mx = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < NT; ++u) mx = fmaxf(mx, fmaxf(fmaxf(S[u][0][0], S[u][0][1]), fmaxf(S[u][1][0], S[u][1][1])));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  const float m_new = fmaxf(m_run, mx);
+  const float m_use = m_new == -INFINITY ? 0.0f : m_new;
+  const float alpha = fast_exp2(m_run - m_use);
+  float P[NT][2][2];
+  float psum = 0.0f;
+#pragma unroll
+  for (int u = 0; u < NT; ++u)
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        P[u][j][e] = fast_exp2(S[u][j][e] - m_use);
+        psum += P[u][j][e];
+      }
+  l_run = l_run * alpha + psum;
+  m_run = m_new;
+  if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+    // accumulator columns are heads 2t, 2t+1; their factors live in rows g = 2t, 2t+1
+    const float a0 = __shfl_sync(0xffffffffu, alpha, (2 * t) << 2);
+    const float a1 = __shfl_sync(0xffffffffu, alpha, (2 * t + 1) << 2);
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+      O[i][0] *= a0; O[i][1] *= a1;
+      O[i][2] *= a0; O[i][3] *= a1;
+    }
+    Z[0] *= a0; Z[1] *= a1; Z[2] *= a0; Z[3] *= a1;
+  }
+#pragma unroll
+  for (int u = 0; u < NT; ++u) pv_tile<D, BITS>(O, Z, P[u], st_s[u], st[u], la, w, g, t);
 }
 
 template <int D>
@@ -463,10 +595,13 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
   constexpr int G = D / 32;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * L::kStageBytes);
+  EpiBuf<D>* eb = reinterpret_cast<EpiBuf<D>*>(smem + L::kOffEpi);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kOffBars);
   uint64_t* ready = full + kStages;
   uint64_t* empty = ready + kStages;
-  uint64_t* gbar = empty + kStages;       // consumer-group barrier for piece ends
+  uint64_t* epi_full = empty + kStages;    // consumers -> epilogue: a piece's states are in eb
+  uint64_t* epi_empty = epi_full + 1;      // epilogue -> consumers: eb may be overwritten
+  uint64_t* gbar = epi_empty + 1;          // consumer-group barrier for the final piece
   int32_t* pre = reinterpret_cast<int32_t*>(smem + L::kFixed);
   int32_t* lens = pre + (p.B + 1);
 
@@ -480,9 +615,22 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
       mbar_init(&ready[s], 1);
       mbar_init(&empty[s], kWarps);
     }
+    mbar_init(epi_full, kWarps);
+    mbar_init(epi_empty, 1);
     mbar_init(gbar, kWarps);
     fence_barrier_init();
   }
+  if (tid == kWarps * 32) {
+    prefetch_tmap(&p.tm_k8);
+    prefetch_tmap(&p.tm_v8);
+    prefetch_tmap(&p.tm_k4);
+    prefetch_tmap(&p.tm_v4);
+  }
+  // With programmatic dependent launch this kernel may start while the
+  // previous kernel in the stream is finishing: wait for it (and its memory)
+  // before the first global access, then let the next one start early.
+  grid_dependency_wait();
+  grid_launch_dependents();
   for (int b = tid; b < B; b += blockDim.x) {
     int L0 = p.seq_lens[b];
     if (L0 < 0 || L0 > p.Tcap) {
@@ -508,85 +656,125 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
     if (lane == 0) pre[0] = 0;
   }
   __syncthreads();
-  // sequences of length 0 get a zero output row (no CTA visits them)
-  for (int idx = blockIdx.x * blockDim.x + tid; idx < B * p.Hq * D; idx += gridDim.x * blockDim.x) {
-    const int b = idx / (p.Hq * D);
-    if (lens[b] == 0) {
-      if (p.out_dtype == KVQ_OUT_F32) reinterpret_cast<float*>(p.out)[idx] = 0.0f;
-      else reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(0.0f);
-    }
-  }
 
   const int64_t N = static_cast<int64_t>(Hkv) * pre[B];
   const int C = p.num_ctas;
   const int64_t f0 = N * blockIdx.x / C;
   const int64_t f1 = N * (blockIdx.x + 1) / C;
   const int ntiles = static_cast<int>(f1 - f0);
-  if (ntiles <= 0) return;
-
-  if (w == kWarps) {
-    // ---------------- TMA issuer warp: lane 0 keeps kStages tiles in flight ----------------
-    if (lane != 0) return;
-    Cursor pc = locate(f0, pre, B, Hkv);
-    for (int k = 0; k < ntiles; ++k) {
-      const int slot = k % kStages;
-      if (k >= kStages && !mbar_wait(&empty[slot], ((k / kStages) - 1) & 1, p.status)) return;
-      uint8_t* st = smem + slot * L::kStageBytes;
-      const int bits = p.bits[pc.kvh];
-      const int R = D * bits / 8;
-      const int32_t row0 = (p.plane[pc.kvh] * B + pc.b) * p.Tcap + pc.i * kTile;
-      const int64_t szoff = (static_cast<int64_t>(pc.kvh) * B + pc.b) * p.Tcap + static_cast<int64_t>(pc.i) * kTile;
-      uint64_t* bar = &full[slot];
-      mbar_arrive_expect_tx(bar, 2 * kTile * R + 2 * L::kSzBytes);
-      tma_2d_g2s(st + L::kOffK, bits == 8 ? &p.tm_k8 : &p.tm_k4, 0, row0, bar);
-      tma_2d_g2s(st + L::kOffV, bits == 8 ? &p.tm_v8 : &p.tm_v4, 0, row0, bar);
-      bulk_g2s(st + L::kOffKsz, p.k_sz + szoff * G, L::kSzBytes, bar);
-      bulk_g2s(st + L::kOffVsz, p.v_sz + szoff * G, L::kSzBytes, bar);
-      advance(pc, pre, B, Hkv);
-    }
+  if (ntiles <= 0) {
+    if (w == 0) zero_empty_rows<D>(p, lens, lane);
     return;
   }
-  if (w == kWarps + 1) {
-    // ---------------- table warp: per landed tile, scale/zero words -> consumer tables ----------------
-    Cursor tc = locate(f0, pre, B, Hkv);
-    for (int kk = 0; kk < ntiles; ++kk) {
-      const int slot = kk % kStages;
-      const bool okw = mbar_wait(&full[slot], (kk / kStages) & 1, p.status);
-      if (!__all_sync(0xffffffffu, okw)) return;
-      uint8_t* st = smem + slot * L::kStageBytes;
-      const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + L::kOffKsz);
-      const uint32_t* vsz = reinterpret_cast<const uint32_t*>(st + L::kOffVsz);
-      float2* kt = reinterpret_cast<float2*>(st + L::kOffKt);
-      float* vts = reinterpret_cast<float*>(st + L::kOffVtS);
-      uint16_t* vtz = reinterpret_cast<uint16_t*>(st + L::kOffVtZ);
-      const int len = lens[tc.b];
-      // tables in [group][token] order: consecutive lanes take consecutive tokens
-#pragma unroll 4
-      for (int e = lane; e < kTile * G; e += 32) {
-        const int grp = e / kTile, tok = e % kTile;
-        const bool valid = tc.i * kTile + tok < len;
-        const uint32_t kw = valid ? ksz[tok * G + grp] : 0u;
-        const uint32_t vw = valid ? vsz[tok * G + grp] : 0u;
-        const float ks = half_lo(kw);
-        kt[e] = make_float2(ks, (1024.0f + half_hi(kw)) * ks);
-        vts[e] = half_lo(vw);
-        vtz[e] = static_cast<unsigned short>(zero_biased2(vw) & 0xFFFFu);
+
+  // Registers: launched with 128 per thread (checked on the host); the
+  // consumer warpgroup takes kConsumerRegs, the helper warpgroup keeps
+  // kHelperRegs: 4 x (kConsumerRegs + kHelperRegs) = 8 x 128, and per
+  // sub-partition 32 x (kConsumerRegs + kHelperRegs) x 2 CTAs = 16384, its
+  // whole register file.
+  if (w >= kWarps) {
+    tc::reg_dealloc<kHelperRegs>();
+    if (w == kWarps) {
+      // ---------------- TMA issuer warp: lane 0 keeps kStages tiles in flight ----------------
+      if (lane != 0) return;
+      Cursor pc = locate(f0, pre, B, Hkv);
+      for (int k = 0; k < ntiles; ++k) {
+        const int slot = k % kStages;
+        if (k >= kStages && !mbar_wait(&empty[slot], ((k / kStages) - 1) & 1, p.status)) return;
+        uint8_t* st = smem + slot * L::kStageBytes;
+        const int bits = p.bits[pc.kvh];
+        const int R = D * bits / 8;
+        const int32_t row0 = (p.plane[pc.kvh] * B + pc.b) * p.Tcap + pc.i * kTile;
+        const int64_t szoff =
+            (static_cast<int64_t>(pc.kvh) * B + pc.b) * p.Tcap + static_cast<int64_t>(pc.i) * kTile;
+        uint64_t* bar = &full[slot];
+        const bool first = pc.i == 0 || k == 0;
+        const uint32_t qbytes = first ? static_cast<uint32_t>(p.rep * D * 2) : 0u;
+        mbar_arrive_expect_tx(bar, 2 * kTile * R + 2 * L::kSzBytes + qbytes);
+        if (first)
+          bulk_g2s(st + L::kOffQ, p.q + (static_cast<int64_t>(pc.b) * p.Hq + pc.kvh * p.rep) * D, qbytes, bar);
+        tma_2d_g2s(st + L::kOffK, bits == 8 ? &p.tm_k8 : &p.tm_k4, 0, row0, bar);
+        tma_2d_g2s(st + L::kOffV, bits == 8 ? &p.tm_v8 : &p.tm_v4, 0, row0, bar);
+        bulk_g2s(st + L::kOffKsz, p.k_sz + szoff * G, L::kSzBytes, bar);
+        bulk_g2s(st + L::kOffVsz, p.v_sz + szoff * G, L::kSzBytes, bar);
+        advance(pc, pre, B, Hkv);
       }
-      if (lane == 0) {
-        const int n_b = pre[tc.b + 1] - pre[tc.b];
-        int flags = tc.i;
-        if (tc.i == 0 || kk == 0) flags |= kFlagStart;
-        if (tc.i == n_b - 1 || kk == ntiles - 1) flags |= kFlagEnd;
-        *reinterpret_cast<int4*>(st + L::kOffMeta) = make_int4(tc.b, tc.kvh, flags, len);
+      return;
+    }
+    if (w == kWarps + 1 || w == kWarps + 3) {
+      // ---------------- two table warps (even / odd tiles): scale/zero words -> consumer tables ----------------
+      const int par = w == kWarps + 1 ? 0 : 1;
+      if (par >= ntiles) return;
+      Cursor tc = locate(f0 + par, pre, B, Hkv);
+      const float sl2 = p.scale_log2;
+      for (int kk = par; kk < ntiles; kk += 2) {
+        const int slot = kk % kStages;
+        const bool okw = mbar_wait(&full[slot], (kk / kStages) & 1, p.status);
+        if (!__all_sync(0xffffffffu, okw)) return;
+        uint8_t* st = smem + slot * L::kStageBytes;
+        const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + L::kOffKsz);
+        const uint32_t* vsz = reinterpret_cast<const uint32_t*>(st + L::kOffVsz);
+        float2* kt = reinterpret_cast<float2*>(st + L::kOffKt);
+        float* vts = reinterpret_cast<float*>(st + L::kOffVtS);
+        uint16_t* vtz = reinterpret_cast<uint16_t*>(st + L::kOffVtZ);
+        const int len = lens[tc.b];
+        // tables in [group][token] order: consecutive lanes take consecutive
+        // tokens; the K scale carries the softmax scale (log2 domain).  The K
+        // table overwrites the raw words, so all of them are read first.
+        constexpr int kPer = kTile * G / 32;
+        uint32_t kw[kPer], vw[kPer];
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int e = lane + 32 * i;
+          const int grp = e / kTile, tok = e % kTile;
+          const bool valid = tc.i * kTile + tok < len;
+          kw[i] = valid ? ksz[tok * G + grp] : 0u;
+          vw[i] = valid ? vsz[tok * G + grp] : 0u;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int e = lane + 32 * i;
+          const float ks = half_lo(kw[i]) * sl2;
+          kt[e] = make_float2(ks, (1024.0f + half_hi(kw[i])) * ks);
+          vts[e] = half_lo(vw[i]);
+          vtz[e] = static_cast<unsigned short>(zero_biased2(vw[i]) & 0xFFFFu);
+        }
+        // the raw-word area is refilled by TMA (async proxy) once the stage is released
+        fence_proxy_async_smem();
+        if (lane == 0) {
+          const int n_b = pre[tc.b + 1] - pre[tc.b];
+          int flags = tc.i;
+          if (p.bits[tc.kvh] == 4) flags |= kFlag4;
+          if ((tc.i + 1) * kTile <= len) flags |= kFlagFull;
+          if (tc.i == 0 || kk == 0) flags |= kFlagStart;
+          if (tc.i == n_b - 1 || kk == ntiles - 1) flags |= kFlagEnd;
+          *reinterpret_cast<int4*>(st + L::kOffMeta) = make_int4(tc.b, tc.kvh, flags, len);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ready[slot]);
+        advance(tc, pre, B, Hkv);
+        if (kk + 2 < ntiles) advance(tc, pre, B, Hkv);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ready[slot]);
-      advance(tc, pre, B, Hkv);
+      return;
+    }
+    if (w == kWarps + 2) {
+      // ---------------- epilogue warp: every piece end but the CTA's last ----------------
+      zero_empty_rows<D>(p, lens, lane);
+      const int npieces = count_pieces(f0, ntiles, pre, B, Hkv);
+      for (int e = 0; e + 1 < npieces; ++e) {
+        const bool okw = mbar_wait(epi_full, e & 1, p.status);
+        if (!__all_sync(0xffffffffu, okw)) return;
+        const int4 info = eb->info;
+        segment_end<D, 4>(p, eb, &eb->flag[0], info.x, info.y, pre, N, C, lane, 32, WarpSync{}, epi_empty);
+      }
+      return;
     }
     return;
   }
 
   // ---------------- consumers: four warps ----------------
+  tc::reg_alloc<kConsumerRegs>();
   const LaneAddr la = lane_addr<D>(w, lane);
   uint32_t qa[D / 16][2];
   float qsum[G];
@@ -594,81 +782,59 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
   float Z[4];
   float m_run = -INFINITY, l_run = 0.0f;
   bool ok = true;
+  int n_end = 0;
   uint32_t gphase = 0;
-  auto group_sync = [&]() { consumer_sync(gbar, &gphase, &ok, p.status); };
 
-  for (int k = 0; k < ntiles; ++k) {
+  for (int k = 0; k < ntiles;) {
     const int slot = k % kStages;
     ok = ok && mbar_wait(&ready[slot], (k / kStages) & 1, p.status);
     if (!ok) break;   // a timed-out wait ends this warp (status already set)
-    uint8_t* st = smem + slot * L::kStageBytes;
-    const uint32_t st_s = smem_u32(st);
-    const int4 meta = *reinterpret_cast<const int4*>(st + L::kOffMeta);
-    const int cb = meta.x, ckvh = meta.y, ci = meta.z & 0xFFFFFF, len = meta.w;
-    const int bits = p.bits[ckvh];
+    const uint8_t* st0 = smem + slot * L::kStageBytes;
+    const int4 meta = *reinterpret_cast<const int4*>(st0 + L::kOffMeta);
+    const int cb = meta.x, ckvh = meta.y, len = meta.w;
+    const bool four = (meta.z & kFlag4) != 0;
     if (meta.z & kFlagStart) {
-      load_q<D>(qa, qsum, p, cb, ckvh, bits, g, t);
+      load_q<D>(qa, qsum, p, reinterpret_cast<const uint16_t*>(st0 + L::kOffQ), four ? 4 : 8, g, t);
 #pragma unroll
       for (int i = 0; i < D / 16; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.0f;
       Z[0] = Z[1] = Z[2] = Z[3] = 0.0f;
       m_run = -INFINITY;
       l_run = 0.0f;
     }
-
-    float S[2][2];
-    if (bits == 8) qk_tile<D, 8>(S, qa, qsum, st_s, st, la, w, t);
-    else qk_tile<D, 4>(S, qa, qsum, st_s, st, la, w, t);
-
-    // mask past the sequence end, move to the log2 domain, online softmax per head row g
-    float mx = -INFINITY;
-    const int tok0 = ci * kTile + 16 * w + 2 * t;
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        S[j][e] = tok0 + 8 * j + e < len ? S[j][e] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, S[j][e]);
-      }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float m_new = fmaxf(m_run, mx);
-    const float m_use = m_new == -INFINITY ? 0.0f : m_new;
-    const float alpha = fast_exp2(m_run - m_use);
-    float P[2][2];
-    float psum = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        P[j][e] = fast_exp2(S[j][e] - m_use);
-        psum += P[j][e];
-      }
-    l_run = l_run * alpha + psum;
-    m_run = m_new;
-    if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-      // accumulator columns are heads 2t, 2t+1; their factors live in rows g = 2t, 2t+1
-      const float a0 = __shfl_sync(0xffffffffu, alpha, (2 * t) << 2);
-      const float a1 = __shfl_sync(0xffffffffu, alpha, (2 * t + 1) << 2);
-#pragma unroll
-      for (int i = 0; i < D / 16; ++i) {
-        O[i][0] *= a0; O[i][1] *= a1;
-        O[i][2] *= a0; O[i][3] *= a1;
-      }
-      Z[0] *= a0; Z[1] *= a1; Z[2] *= a0; Z[3] *= a1;
+    int fend, nt;
+    if (!(meta.z & kFlagEnd)) {
+      // the next tile belongs to the same piece: take both in one step
+      const int slot1 = (k + 1) % kStages;
+      ok = ok && mbar_wait(&ready[slot1], ((k + 1) / kStages) & 1, p.status);
+      if (!ok) break;
+      const uint8_t* st1 = smem + slot1 * L::kStageBytes;
+      const int f1 = reinterpret_cast<const int4*>(st1 + L::kOffMeta)->z;
+      const uint32_t ss[2] = {smem_u32(st0), smem_u32(st1)};
+      const uint8_t* const sp[2] = {st0, st1};
+      const int ff[2] = {meta.z, f1};
+      if (!four) consume_tiles<D, 8, 2>(ss, sp, ff, len, qa, qsum, O, Z, m_run, l_run, la, w, g, t);
+      else consume_tiles<D, 4, 2>(ss, sp, ff, len, qa, qsum, O, Z, m_run, l_run, la, w, g, t);
+      fend = f1;
+      nt = 2;
+    } else {
+      const uint32_t ss[1] = {smem_u32(st0)};
+      const uint8_t* const sp[1] = {st0};
+      const int ff[1] = {meta.z};
+      if (!four) consume_tiles<D, 8, 1>(ss, sp, ff, len, qa, qsum, O, Z, m_run, l_run, la, w, g, t);
+      else consume_tiles<D, 4, 1>(ss, sp, ff, len, qa, qsum, O, Z, m_run, l_run, la, w, g, t);
+      fend = meta.z;
+      nt = 1;
     }
-    if (bits == 8) pv_tile<D, 8>(O, Z, P, st_s, st, la, w, g, t);
-    else pv_tile<D, 4>(O, Z, P, st_s, st, la, w, g, t);
 
-    // ---- end of a piece: hand the four warps' states to the (out-of-line) merge ----
-    if (meta.z & kFlagEnd) {
+    // ---- end of a piece: the warps' states go to the hand-off buffer ----
+    if (fend & kFlagEnd) {
       float l_tot = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
       l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
-      float* m_o = reinterpret_cast<float*>(st);                 // this slot, once every warp is done with it
-      float* m_ml = reinterpret_cast<float*>(st + L::kMergeO);
-      group_sync();
+      if (n_end > 0) ok = ok && mbar_wait(epi_empty, (n_end - 1) & 1, p.status);
+      if (!ok) break;
       if (t == 0 && g < p.rep) {
-        m_ml[(w * kMaxRep + g) * 2 + 0] = m_run;
-        m_ml[(w * kMaxRep + g) * 2 + 1] = l_tot;
+        eb->ml[w][g][0] = m_run;
+        eb->ml[w][g][1] = l_tot;
       }
 #pragma unroll
       for (int grp = 0; grp < G; ++grp) {
@@ -680,25 +846,37 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
           const int h = 2 * t + e;
           const float r = e ? r1 : r0;
           if (h < p.rep) {
-            float* dst = m_o + (w * kMaxRep + h) * D;
+            float* dst = eb->o[w][h];
 #pragma unroll
             for (int mh = 0; mh < 2; ++mh)
 #pragma unroll
               for (int half = 0; half < 2; ++half) {
-                const int ch = bits == 8 ? acc_channel<8>(grp, mh, half, g) : acc_channel<4>(grp, mh, half, g);
+                const int ch = four ? acc_channel<4>(grp, mh, half, g) : acc_channel<8>(grp, mh, half, g);
                 dst[ch] = O[2 * grp + mh][2 * half + e] - r;
               }
           }
         }
       }
-      group_sync();
-      const uint32_t st_ret = finish_piece<D>(&p, m_o, m_ml, cb, ckvh, pre, N, C, tid, gbar, gphase, ok);
-      gphase = st_ret >> 1;
-      ok = (st_ret & 1u) != 0;
+      ++n_end;
+      if (k + nt < ntiles) {
+        // not the CTA's last piece: the epilogue warp takes it from here
+        if (w == 0 && lane == 0) eb->info = make_int4(cb, ckvh, 0, 0);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(epi_full);
+      } else {
+        // the last piece: the CTA has no more tiles, so the four consumer
+        // warps finish it themselves
+        const ConsumerSync cs{gbar, &gphase, &ok, p.status};
+        cs();
+        segment_end<D, 4>(p, eb, &eb->flag[1], cb, ckvh, pre, N, C, tid, kWarps * 32, cs, nullptr);
+      }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
-    if (!ok) break;
+    if (lane == 0) {
+      mbar_arrive(&empty[slot]);
+      if (nt == 2) mbar_arrive(&empty[(k + 1) % kStages]);
+    }
+    k += nt;
   }
 }
 
@@ -720,10 +898,34 @@ int ctas_per_sm() {
   return cached[dev];
 }
 
+// The register split inside the kernel assumes 128 registers per thread at
+// launch; any other count would make the consumers' setmaxnreg wait forever.
+template <int D>
+bool regs_ok() {
+  static int cached = -1;
+  if (cached < 0) {
+    cudaFuncAttributes fa;
+    cached = (cudaFuncGetAttributes(&fa, decode_split_kernel<D>) == cudaSuccess && fa.numRegs == 128) ? 1 : 0;
+  }
+  return cached == 1;
+}
+
+// Launched with programmatic stream serialization: the kernel's CTAs may be
+// scheduled while the previous kernel of the stream drains; the kernel waits
+// for it (griddepcontrol.wait) before its first global memory access.
 template <int D>
 cudaError_t launch_split(const DParams& p, int C, int B, cudaStream_t stream) {
-  decode_split_kernel<D><<<C, kThreads, Smem<D>::bytes(B), stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(C));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Smem<D>::bytes(B);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_split_kernel<D>, p);
 }
 
 }  // namespace
@@ -749,6 +951,7 @@ kvq_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const kvq_cache& Vc = *a.v;
   const int D = K.D, B = K.B, Hkv = K.Hkv, Tcap = K.Tcap;
   if (B > 4096) return KVQ_ERR_UNSUPPORTED;  // dynamic shared memory was sized for B <= 4096
+  if (!(D == 128 ? regs_ok<128>() : regs_ok<64>())) return KVQ_ERR_UNSUPPORTED;
   const int C = decode_num_ctas(D);
   const size_t need = decode_workspace_bytes(B, a.Hq, Hkv, D, C);
   if (a.ws == nullptr || a.ws_bytes < need) return KVQ_ERR_WORKSPACE;
