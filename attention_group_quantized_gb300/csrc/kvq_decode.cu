@@ -36,6 +36,11 @@
 //        lie in one group g, so its B operand is P * s_g (one fp16 rounding);
 //        A is 1024 + c, and one extra MMA per group accumulates
 //        sum_tok (1024 + z_g) P s_g into a spare row, subtracted at the end.
+//        That row must go through the same sequence of MMAs as the output
+//        accumulators (one accumulator, same order): the tensor core's fp32
+//        accumulation then rounds the large common 1024 * sum(P s_g) part the
+//        same way on both sides and it cancels; a differently split sum
+//        leaves an error about ten times larger.
 //  * Fragments come from the swizzled code tiles by ldmatrix: K as stored
 //    (token rows), V transposed, so each register holds two tokens of two
 //    channels and one byte permute yields a (token, token) pair of a channel.
@@ -71,6 +76,10 @@ static_assert(kWarps * (kConsumerRegs + kHelperRegs) == 2 * kWarps * 128, "regis
 #define KVQ_DECODE_MIN_BLOCKS 2
 #endif
 constexpr int kStages = KVQ_DECODE_STAGES;
+#ifndef KVQ_DECODE_WARM
+#define KVQ_DECODE_WARM 4
+#endif
+constexpr int kWarm = KVQ_DECODE_WARM;
 constexpr int kMaxRep = 8;      // query heads per KV head
 
 struct DParams {
@@ -322,6 +331,12 @@ __device__ __forceinline__ void pv_tile(float (&O)[D / 16][4], float (&Z)[4], co
   const float* vts = reinterpret_cast<const float*>(st + L::kOffVtS);
   const uint8_t* vtz = st + L::kOffVtZ;
   const int tok = 16 * w + 2 * t;
+  // row g of the zero-term product carries group g: lanes with g < G load it once
+  uint32_t zown_a = 0u, zown_b = 0u;
+  if (g < G) {
+    zown_a = *reinterpret_cast<const uint32_t*>(vtz + (g * kTile + tok) * 2);
+    zown_b = *reinterpret_cast<const uint32_t*>(vtz + (g * kTile + tok + 8) * 2);
+  }
   uint32_t rv4[2][4];
   if constexpr (BITS == 4) {
     ldsm_x4_t(rv4[0], st_s + L::kOffV + la.v4);
@@ -347,8 +362,8 @@ __device__ __forceinline__ void pv_tile(float (&O)[D / 16][4], float (&Z)[4], co
       mma_16816(O[2 * grp + 1], nib_biased(lo >> 8), nib_biased(lo >> 12), nib_biased(hi >> 8),
                 nib_biased(hi >> 12), b0, b1);
     }
-    const uint32_t za = g == grp ? *reinterpret_cast<const uint32_t*>(vtz + (grp * kTile + tok) * 2) : 0u;
-    const uint32_t zb = g == grp ? *reinterpret_cast<const uint32_t*>(vtz + (grp * kTile + tok + 8) * 2) : 0u;
+    const uint32_t za = g == grp ? zown_a : 0u;
+    const uint32_t zb = g == grp ? zown_b : 0u;
     mma_16816(Z, za, 0u, zb, 0u, b0, b1);
   }
 }
@@ -359,10 +374,6 @@ __device__ __forceinline__ int acc_channel(int grp, int mh, int half, int g) {
   if constexpr (BITS == 8) return 32 * grp + 16 * half + 2 * g + mh;
   return 32 * grp + 4 * g + 2 * mh + half;
 }
-
-// Whether CTA c of the stream-K split got an empty tile range (only possible
-// when there are fewer tiles than CTAs).
-__device__ __forceinline__ bool cta_empty(int64_t N, int C, int c) { return N * (c + 1) / C == N * c / C; }
 
 // Sequences of length 0 get a zero output row (no CTA visits them); one warp
 // per CTA writes its share of the rows.
@@ -375,6 +386,18 @@ __device__ __forceinline__ void zero_empty_rows(const DParams& p, const int32_t*
       if (p.out_dtype == KVQ_OUT_F32) reinterpret_cast<float*>(p.out)[idx] = 0.0f;
       else reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(0.0f);
     }
+  }
+}
+
+// The G scale/zero words of one token (16 or 8 bytes, aligned).
+template <int G>
+__device__ __forceinline__ void load_words(uint32_t (&w)[G], const uint32_t* src) {
+  if constexpr (G == 4) {
+    const uint4 v = *reinterpret_cast<const uint4*>(src);
+    w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+  } else {
+    const uint2 v = *reinterpret_cast<const uint2*>(src);
+    w[0] = v.x; w[1] = v.y;
   }
 }
 
@@ -479,13 +502,8 @@ __device__ __forceinline__ void segment_end(const DParams& p, const EpiBuf<D>* e
   // leader's fence orders every member's partial stores (fences are
   // cumulative) before its atomic; the last arriver's second fence orders the
   // other pieces before the group's reads below
-  const bool check = N < C;   // some CTAs may have empty ranges
   if (tid == 0) {
-    int np = c1 - c0 + 1;
-    if (check) {
-      np = 0;
-      for (int c = c0; c <= c1; ++c) np += cta_empty(N, C, c) ? 0 : 1;
-    }
+    const int np = c1 - c0 + 1;   // every split CTA owns at least one tile
     __threadfence();
     const int last = (atomicAdd(&p.ws_cnt[seg], 1) + 1 == np) ? 1 : 0;
     if (last) __threadfence();
@@ -493,8 +511,8 @@ __device__ __forceinline__ void segment_end(const DParams& p, const EpiBuf<D>* e
   }
   sync();
   if (*flag != 1) return;
-  // the segment is complete: one online log-sum-exp pass over its pieces,
-  // four channels per thread, MB pieces of loads in flight
+  // the segment is complete: log-sum-exp over its pieces, four channels per
+  // thread, MB pieces per round with all their loads in flight together
   for (int i4 = tid; i4 < rep * (D / 4); i4 += nthr) {
     const int h = i4 / (D / 4), ch = (i4 % (D / 4)) * 4;
     float M = -INFINITY, Lsum = 0.0f;
@@ -505,21 +523,25 @@ __device__ __forceinline__ void segment_end(const DParams& p, const EpiBuf<D>* e
 #pragma unroll
       for (int u = 0; u < MB; ++u) {
         const int c = cb4 + u;
-        const bool live = c <= c1 && !(check && cta_empty(N, C, c));
+        const bool live = c <= c1;
         const int64_t sl = static_cast<int64_t>(seg) + (live ? c : c0);
         lse[u] = live ? __ldcg(p.ws_lse + sl * rep + h) : -INFINITY;
         v[u] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (sl * rep + h) * D + ch));
       }
+      float Mr = M;
+#pragma unroll
+      for (int u = 0; u < MB; ++u) Mr = fmaxf(Mr, lse[u]);
+      if (Mr == -INFINITY) continue;   // no piece with weight yet
+      const float a = M == -INFINITY ? 0.0f : fast_exp2(M - Mr);
+      acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
+      Lsum *= a;
 #pragma unroll
       for (int u = 0; u < MB; ++u) {
-        if (lse[u] == -INFINITY) continue;
-        const float M2 = fmaxf(M, lse[u]);
-        const float a = fast_exp2(M - M2), bw = fast_exp2(lse[u] - M2);
-        acc.x = acc.x * a + bw * v[u].x; acc.y = acc.y * a + bw * v[u].y;
-        acc.z = acc.z * a + bw * v[u].z; acc.w = acc.w * a + bw * v[u].w;
-        Lsum = Lsum * a + bw;
-        M = M2;
+        const float bw = lse[u] == -INFINITY ? 0.0f : fast_exp2(lse[u] - Mr);
+        acc.x += bw * v[u].x; acc.y += bw * v[u].y; acc.z += bw * v[u].z; acc.w += bw * v[u].w;
+        Lsum += bw;
       }
+      M = Mr;
     }
     const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
     acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
@@ -658,9 +680,12 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
   __syncthreads();
 
   const int64_t N = static_cast<int64_t>(Hkv) * pre[B];
-  const int C = p.num_ctas;
-  const int64_t f0 = N * blockIdx.x / C;
-  const int64_t f1 = N * (blockIdx.x + 1) / C;
+  // never more split CTAs than tiles: every CTA of the split then owns at
+  // least one tile, and a segment's pieces are those of CTAs c0 .. c1
+  const int C = N < p.num_ctas ? static_cast<int>(N) : p.num_ctas;
+  const bool in_split = static_cast<int>(blockIdx.x) < C;
+  const int64_t f0 = in_split ? N * blockIdx.x / C : 0;
+  const int64_t f1 = in_split ? N * (blockIdx.x + 1) / C : 0;
   const int ntiles = static_cast<int>(f1 - f0);
   if (ntiles <= 0) {
     if (w == 0) zero_empty_rows<D>(p, lens, lane);
@@ -681,6 +706,8 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
       for (int k = 0; k < ntiles; ++k) {
         const int slot = k % kStages;
         if (k >= kStages && !mbar_wait(&empty[slot], ((k / kStages) - 1) & 1, p.status)) return;
+        // start with kWarm tiles so the first one lands early, the rest once it has
+        if (k == kWarm && kWarm < kStages && !mbar_wait(&full[0], 0, p.status)) return;
         uint8_t* st = smem + slot * L::kStageBytes;
         const int bits = p.bits[pc.kvh];
         const int R = D * bits / 8;
@@ -714,31 +741,34 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
         uint8_t* st = smem + slot * L::kStageBytes;
         const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + L::kOffKsz);
         const uint32_t* vsz = reinterpret_cast<const uint32_t*>(st + L::kOffVsz);
-        float2* kt = reinterpret_cast<float2*>(st + L::kOffKt);
-        float* vts = reinterpret_cast<float*>(st + L::kOffVtS);
-        uint16_t* vtz = reinterpret_cast<uint16_t*>(st + L::kOffVtZ);
         const int len = lens[tc.b];
-        // tables in [group][token] order: consecutive lanes take consecutive
-        // tokens; the K scale carries the softmax scale (log2 domain).  The K
-        // table overwrites the raw words, so all of them are read first.
-        constexpr int kPer = kTile * G / 32;
-        uint32_t kw[kPer], vw[kPer];
+        // Lane l takes tokens 2l and 2l+1 (all G groups of each: the raw words
+        // are [token][group]); the tables are [group][token], so each lane
+        // writes its two tokens' entries of a group with one store.  The K
+        // scale carries the softmax scale (log2 domain).  The K table
+        // overwrites the raw words, so all of them are read first.
+        const int t0 = 2 * lane;
+        uint32_t kw[2][G], vw[2][G];
+        load_words<G>(kw[0], ksz + t0 * G);
+        load_words<G>(kw[1], ksz + (t0 + 1) * G);
+        load_words<G>(vw[0], vsz + t0 * G);
+        load_words<G>(vw[1], vsz + (t0 + 1) * G);
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-          const int e = lane + 32 * i;
-          const int grp = e / kTile, tok = e % kTile;
-          const bool valid = tc.i * kTile + tok < len;
-          kw[i] = valid ? ksz[tok * G + grp] : 0u;
-          vw[i] = valid ? vsz[tok * G + grp] : 0u;
-        }
+        for (int u = 0; u < 2; ++u)
+          if (tc.i * kTile + t0 + u >= len) {   // past the sequence end: zero scales
+#pragma unroll
+            for (int grp = 0; grp < G; ++grp) kw[u][grp] = vw[u][grp] = 0u;
+          }
         __syncwarp();
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) {
-          const int e = lane + 32 * i;
-          const float ks = half_lo(kw[i]) * sl2;
-          kt[e] = make_float2(ks, (1024.0f + half_hi(kw[i])) * ks);
-          vts[e] = half_lo(vw[i]);
-          vtz[e] = static_cast<unsigned short>(zero_biased2(vw[i]) & 0xFFFFu);
+        for (int grp = 0; grp < G; ++grp) {
+          const float ks0 = half_lo(kw[0][grp]) * sl2, ks1 = half_lo(kw[1][grp]) * sl2;
+          *reinterpret_cast<float4*>(st + L::kOffKt + (grp * kTile + t0) * 8) =
+              make_float4(ks0, (1024.0f + half_hi(kw[0][grp])) * ks0, ks1, (1024.0f + half_hi(kw[1][grp])) * ks1);
+          *reinterpret_cast<float2*>(st + L::kOffVtS + (grp * kTile + t0) * 4) =
+              make_float2(half_lo(vw[0][grp]), half_lo(vw[1][grp]));
+          *reinterpret_cast<uint32_t*>(st + L::kOffVtZ + (grp * kTile + t0) * 2) =
+              zero_biased_pair(vw[0][grp], vw[1][grp]);
         }
         // the raw-word area is refilled by TMA (async proxy) once the stage is released
         fence_proxy_async_smem();
@@ -766,7 +796,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
         const bool okw = mbar_wait(epi_full, e & 1, p.status);
         if (!__all_sync(0xffffffffu, okw)) return;
         const int4 info = eb->info;
-        segment_end<D, 4>(p, eb, &eb->flag[0], info.x, info.y, pre, N, C, lane, 32, WarpSync{}, epi_empty);
+        segment_end<D, 8>(p, eb, &eb->flag[0], info.x, info.y, pre, N, C, lane, 32, WarpSync{}, epi_empty);
       }
       return;
     }
@@ -868,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
         // warps finish it themselves
         const ConsumerSync cs{gbar, &gphase, &ok, p.status};
         cs();
-        segment_end<D, 4>(p, eb, &eb->flag[1], cb, ckvh, pre, N, C, tid, kWarps * 32, cs, nullptr);
+        segment_end<D, 8>(p, eb, &eb->flag[1], cb, ckvh, pre, N, C, tid, kWarps * 32, cs, nullptr);
       }
     }
     __syncwarp();
