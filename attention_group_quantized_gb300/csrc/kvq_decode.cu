@@ -52,6 +52,7 @@
 
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
+#include "kvq_split.cuh"
 #include "kvq_tc.cuh"
 
 namespace kvq {
@@ -149,38 +150,10 @@ __device__ __forceinline__ uint32_t swz(int row, int byte) {
   return row * 32 + ((((byte >> 4) ^ ((row >> 2) & 1)) << 4) | (byte & 15));
 }
 
-// Position in the flat work list: sequence b, KV head, tile index i.
-struct Cursor {
-  int b, kvh, i;
-};
-
-__device__ __forceinline__ void advance(Cursor& c, const int32_t* pre, int B, int Hkv) {
-  const int n = pre[c.b + 1] - pre[c.b];
-  if (++c.i < n) return;
-  c.i = 0;
-  if (++c.kvh < Hkv) return;
-  c.kvh = 0;
-  do {
-    ++c.b;
-  } while (c.b < B && pre[c.b + 1] == pre[c.b]);
-}
-
-__device__ __forceinline__ Cursor locate(int64_t f, const int32_t* pre, int B, int Hkv) {
-  // largest b with Hkv * pre[b] <= f; it is a non-empty sequence because f < Hkv * pre[B]
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (static_cast<int64_t>(Hkv) * pre[mid] <= f) lo = mid; else hi = mid - 1;
-  }
-  const int b = lo;
-  const int n = pre[b + 1] - pre[b];
-  const int64_t off = f - static_cast<int64_t>(Hkv) * pre[b];
-  Cursor c;
-  c.b = b;
-  c.kvh = static_cast<int>(off / n);
-  c.i = static_cast<int>(off % n);
-  return c;
-}
+using split::Cursor;
+using split::advance;
+using split::locate;
+using split::count_pieces;
 
 // Per-thread shared-memory offsets (from a stage base) of the ldmatrix rows this
 // lane supplies; they do not change from tile to tile.
@@ -401,21 +374,6 @@ __device__ __forceinline__ void load_words(uint32_t (&w)[G], const uint32_t* src
   }
 }
 
-// Number of pieces (runs of tiles inside one segment) in a CTA's tile range.
-__device__ __forceinline__ int count_pieces(int64_t f0, int ntiles, const int32_t* pre, int B, int Hkv) {
-  Cursor c = locate(f0, pre, B, Hkv);
-  int left = ntiles, n = 0;
-  while (left > 0) {
-    const int nb = pre[c.b + 1] - pre[c.b];
-    const int take = min(left, nb - c.i);
-    left -= take;
-    ++n;
-    c.i = nb - 1;
-    advance(c, pre, B, Hkv);
-  }
-  return n;
-}
-
 __device__ __forceinline__ void store_out4(const DParams& p, int64_t i, float4 v) {
   if (p.out_dtype == KVQ_OUT_F32) {
     *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + i) = v;
@@ -461,11 +419,8 @@ __device__ __forceinline__ void segment_end(const DParams& p, const EpiBuf<D>* e
                                             const Sync& sync, uint64_t* epi_empty) {
   const int Hkv = p.Hkv, rep = p.rep;
   const int seg = cb * Hkv + ckvh;
-  const int n_b = pre[cb + 1] - pre[cb];
-  const int64_t start = static_cast<int64_t>(Hkv) * pre[cb] + static_cast<int64_t>(ckvh) * n_b;
-  // CTAs holding the first and the last tile of the segment
-  const int c0 = static_cast<int>(((start + 1) * C - 1) / N);
-  const int c1 = static_cast<int>(((start + n_b) * C - 1) / N);
+  int c0, c1;   // CTAs holding the first and the last tile of the segment
+  split::segment_ctas(pre, Hkv, cb, ckvh, N, C, &c0, &c1);
   const bool whole = c0 == c1;
   const int64_t orow0 = (static_cast<int64_t>(cb) * p.Hq + ckvh * rep) * D;
   const int64_t slot = static_cast<int64_t>(seg) + blockIdx.x;
