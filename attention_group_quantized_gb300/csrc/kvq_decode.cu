@@ -120,9 +120,13 @@ struct Smem {
   static constexpr int kOffV = kCodeBytes;
   static constexpr int kOffKsz = 2 * kCodeBytes;          // raw K scale/zero words [64 tok][G] ...
   static constexpr int kOffVsz = kOffKsz + kSzBytes;       // ... and V's, both replaced by
-  static constexpr int kOffKt = kOffKsz;                   // float2 [G][64 tok]: (s, (1024 + z) s) scaled
-  static constexpr int kOffVtS = kOffKt + kTile * G * 8;   // float [G][64 tok] s
-  static constexpr int kOffVtZ = kOffVtS + kTile * G * 4;  // u16   [G][64 tok] fp16 (1024 + z)
+  // K table, float4 [G][4 warps][8 rows r]: (s, (1024 + z) s) of tokens 16w + r
+  // and 16w + r + 8, the scale carrying the softmax scale
+  static constexpr int kOffKt = kOffKsz;
+  // V tables, uint2 [G][4 warps][4 columns c]: half2 pairs of tokens
+  // (16w + 2c, 16w + 2c + 1) and (16w + 8 + 2c, 16w + 9 + 2c): s, and (1024 + z)
+  static constexpr int kOffVtS = kOffKt + kTile * G * 8;
+  static constexpr int kOffVtZ = kOffVtS + kTile * G * 2;
   static constexpr int kOffMeta = kOffVtZ + kTile * G * 2; // int4 {b, kvh, i | flags, len}
   static constexpr int kOffQ = kOffMeta + 16;              // bf16 [rep][D]: the piece's queries (first tile)
   static constexpr int kStageBytes = ((kOffQ + kMaxRep * D * 2 + 1023) / 1024) * 1024;
@@ -156,33 +160,33 @@ using split::locate;
 using split::count_pieces;
 
 // Per-thread shared-memory offsets (from a stage base) of the ldmatrix rows this
-// lane supplies; they do not change from tile to tile.
-//   K (non-transposed): lane l -> token row 16w + (l & 7) (+8 per n-tile), chunk (l >> 3) (+4)
-//   V (transposed):     lane l -> token row 16w + 8(m >> 1) + (l & 7), chunk 2*grp + (m & 1)
-//                       for 8-bit codes, chunk 2*gi + (m & 1) for 4-bit codes, m = l >> 3
+// lane supplies; they do not change from tile to tile.  m = l >> 3 is the
+// matrix the lane addresses.
+//   K (as stored):  token row 16w + 8(m & 1) + (l & 7), chunk (m >> 1)
+//   V (transposed): token row 16w + 8(m >> 1) + (l & 7), chunk (m & 1)
 struct LaneAddr {
   uint32_t k8, k4, v8, v4;
 };
 
-// For the other chunks of the same row the swizzled offset only changes by an
-// XOR: chunk c + 4 flips address bit 6, the next group of V flips bit 5.
+// Other chunks of the same row differ only by an XOR of the swizzled offset:
+// two chunks further flips address bit 5, one group of V codes further too.
 template <int D>
 __device__ __forceinline__ LaneAddr lane_addr(int w, int lane) {
   constexpr int R8 = D, R4 = D / 2;
   LaneAddr a;
-  const int r = 16 * w + (lane & 7);
   const int m = lane >> 3;
-  a.k8 = swz<R8>(r, 16 * m);
-  a.k4 = swz<R4>(r, 16 * (m & (R4 / 16 - 1)));
+  const int r = 16 * w + 8 * (m & 1) + (lane & 7);
+  a.k8 = swz<R8>(r, 16 * (m >> 1));
+  a.k4 = swz<R4>(r, 16 * (m >> 1));
   const int vr = 16 * w + 8 * (m >> 1) + (lane & 7);
   a.v8 = swz<R8>(vr, 16 * (m & 1));
   a.v4 = swz<R4>(vr, 16 * (m & 1));
   return a;
 }
 
-// Q fragments of S = Q K^T (A operand rows = the group's query heads, zero from
-// rep up) in the channel order of the code unpacking, and per-group sums of
-// the same fp16 values (reduced over the quad).
+// Q fragments of S^T = K Q^T (B operand columns = the group's query heads,
+// zero from rep up) in the channel order of the code unpacking, and per-group
+// sums of the same fp16 values for head g (reduced over the quad).
 //   8-bit: k-step s (16 channels): cols 2t,2t+1 <-> ch 16s + 4t + {0,1},
 //          cols 2t+8, 2t+9 <-> ch 16s + 4t + {2,3}
 //   4-bit: k-steps 2g, 2g+1 of group g: ch 32g + 8t + {(0,4),(1,5)} and {(2,6),(3,7)}
@@ -237,79 +241,76 @@ __device__ __forceinline__ void load_q(uint32_t (&qa)[D / 16][2], float (&qsum)[
   if (!ok) report(p.status, KVQ_ERR_NONFINITE);
 }
 
-// Scores of the warp's 16 tokens for head row g: S[j][e] is token 16w + 8j + 2t + e.
-// The B operand (k = channels, n = tokens) comes by ldmatrix from the swizzled
-// code tile; per group the products are rescaled with the tile's tables.
+// Scores of the warp's 16 tokens: S^T = K Q^T with the tokens as the MMA rows
+// and the query heads as its columns, so S[0], S[1] are token 16w + g with
+// heads 2t, 2t+1 and S[2], S[3] token 16w + g + 8.  The A operand comes by
+// ldmatrix from the swizzled code tile (a register holds four channels of one
+// token); per group the product is rescaled with the tile's K table:
+// S += s C_g - (1024 + z) s sum_g(q).
 template <int D, int BITS>
-__device__ __forceinline__ void qk_tile(float (&S)[2][2], const uint32_t (&qa)[D / 16][2],
-                                        const float (&qsum)[D / 32], uint32_t st_s, const uint8_t* st,
-                                        const LaneAddr& la, int w, int t) {
+__device__ __forceinline__ void qk_tile(float (&S)[4], const uint32_t (&qa)[D / 16][2], const float (&qs)[D / 32][2],
+                                        uint32_t st_s, const uint8_t* st, const LaneAddr& la, int w, int g) {
   using L = Smem<D>;
   constexpr int G = D / 32;
-  const float2* kt = reinterpret_cast<const float2*>(st + L::kOffKt);
+  const float4* kt = reinterpret_cast<const float4*>(st + L::kOffKt) + w * 8 + g;
+  float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  // one ldmatrix: tokens 0-7 and 8-15 of two chunks; 8-bit: the two chunks of
+  // group pr, 4-bit: groups 2pr and 2pr + 1
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int tok = 16 * w + 8 * j + 2 * t;
-    float acc0 = 0.0f, acc1 = 0.0f;
-    // one ldmatrix covers 4 chunks: 8-bit -> groups 2h, 2h+1; 4-bit -> groups 0..3
-#pragma unroll
-    for (int h = 0; h < (BITS == 8 ? G / 2 : 1); ++h) {
-      uint32_t r[4];
-      if constexpr (BITS == 8) {
-        ldsm_x4(r, st_s + L::kOffK + (la.k8 ^ (h << 6)) + j * 8 * D);
-      } else if constexpr (D == 128) {
-        ldsm_x4(r, st_s + L::kOffK + la.k4 + j * 8 * (D / 2));
-      } else {
-        uint32_t r2[2];
-        ldsm_x2(r2, st_s + L::kOffK + la.k4 + j * 8 * (D / 2));
-        r[0] = r2[0]; r[1] = r2[1]; r[2] = 0u; r[3] = 0u;
-      }
-#pragma unroll
-      for (int gg = 0; gg < (BITS == 8 ? 2 : G); ++gg) {
-        const int grp = BITS == 8 ? 2 * h + gg : gg;
-        float c[4];
-        if constexpr (BITS == 8) {
-          mma_16816_z(c, qa[2 * grp][0], 0u, qa[2 * grp][1], 0u, bytes01_biased(r[2 * gg]),
-                      bytes23_biased(r[2 * gg]));
-          mma_16816(c, qa[2 * grp + 1][0], 0u, qa[2 * grp + 1][1], 0u, bytes01_biased(r[2 * gg + 1]),
-                    bytes23_biased(r[2 * gg + 1]));
-        } else {
-          const uint32_t cw = r[gg];
-          mma_16816_z(c, qa[2 * grp][0], 0u, qa[2 * grp][1], 0u, nib_biased(cw), nib_biased(cw >> 4));
-          mma_16816(c, qa[2 * grp + 1][0], 0u, qa[2 * grp + 1][1], 0u, nib_biased(cw >> 8), nib_biased(cw >> 12));
-        }
-        const float4 sz = *reinterpret_cast<const float4*>(kt + grp * kTile + tok);  // tokens tok, tok+1
-        acc0 = fmaf(sz.x, c[0], fmaf(-sz.y, qsum[grp], acc0));
-        acc1 = fmaf(sz.z, c[1], fmaf(-sz.w, qsum[grp], acc1));
-      }
+  for (int pr = 0; pr < (BITS == 8 ? G : (G + 1) / 2); ++pr) {
+    uint32_t r[4];
+    if constexpr (BITS == 8) {
+      ldsm_x4(r, st_s + L::kOffK + (la.k8 ^ (static_cast<uint32_t>(pr) << 5)));
+    } else {
+      ldsm_x4(r, st_s + L::kOffK + (la.k4 ^ (static_cast<uint32_t>(pr) << 5)));
     }
-    S[j][0] = acc0;
-    S[j][1] = acc1;
+#pragma unroll
+    for (int gg = 0; gg < (BITS == 8 ? 1 : 2); ++gg) {
+      const int grp = BITS == 8 ? pr : 2 * pr + gg;
+      float c[4];
+      if constexpr (BITS == 8) {
+        mma_16816_z(c, bytes01_biased(r[0]), bytes01_biased(r[1]), bytes23_biased(r[0]), bytes23_biased(r[1]),
+                    qa[2 * grp][0], qa[2 * grp][1]);
+        mma_16816(c, bytes01_biased(r[2]), bytes01_biased(r[3]), bytes23_biased(r[2]), bytes23_biased(r[3]),
+                  qa[2 * grp + 1][0], qa[2 * grp + 1][1]);
+      } else {
+        const uint32_t w0 = r[2 * gg], w1 = r[2 * gg + 1];
+        mma_16816_z(c, nib_biased(w0), nib_biased(w1), nib_biased(w0 >> 4), nib_biased(w1 >> 4), qa[2 * grp][0],
+                    qa[2 * grp][1]);
+        mma_16816(c, nib_biased(w0 >> 8), nib_biased(w1 >> 8), nib_biased(w0 >> 12), nib_biased(w1 >> 12),
+                  qa[2 * grp + 1][0], qa[2 * grp + 1][1]);
+      }
+      const float4 sz = kt[grp * 32];   // tokens g and g + 8
+      acc[0] = fmaf(sz.x, c[0], fmaf(-sz.y, qs[grp][0], acc[0]));
+      acc[1] = fmaf(sz.x, c[1], fmaf(-sz.y, qs[grp][1], acc[1]));
+      acc[2] = fmaf(sz.z, c[2], fmaf(-sz.w, qs[grp][0], acc[2]));
+      acc[3] = fmaf(sz.z, c[3], fmaf(-sz.w, qs[grp][1], acc[3]));
+    }
   }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) S[i] = acc[i];
 }
 
 // O^T[ch][h] += (1024 + c)[ch][tok] (P s_g)[tok][h] over the warp's 16 tokens,
-// and Z[g][h] += (1024 + z_g)[tok] (P s_g)[tok][h] in row g of a spare tile.
-// A operand (rows = channels, k = tokens 2t, 2t+1 | 8+2t, 9+2t) by transposed
-// ldmatrix from the swizzled code tile.  Row -> channel of m-tile 2*grp + mh:
+// and Z[g & 1][g][h] += (1024 + z_g)[tok] (P s_g)[tok][h] in row g of a spare
+// tile (two accumulators, even and odd groups: each row sees the same MMAs
+// with nonzero terms, in the same order, as the output rows of its group).
+// pb = P^T as the B operand: tokens 2t, 2t+1 | 8+2t, 9+2t of head g, fp16.
+// A operand (rows = channels, k = tokens) by transposed ldmatrix from the
+// swizzled code tile.  Row -> channel of m-tile 2*grp + mh:
 //   8-bit: row r < 8 -> 32grp + 2r + mh, row r >= 8 -> 32grp + 16 + 2(r-8) + mh
 //   4-bit: row r < 8 -> 32grp + 4r + 2mh, row r >= 8 -> 32grp + 4(r-8) + 2mh + 1
 // Accumulators hold heads 2t (c0, c2) and 2t+1 (c1, c3).
 template <int D, int BITS>
-__device__ __forceinline__ void pv_tile(float (&O)[D / 16][4], float (&Z)[4], const float (&P)[2][2],
+__device__ __forceinline__ void pv_tile(float (&O)[D / 16][4], float (&Z)[2][4], const uint32_t (&pb)[2],
                                         uint32_t st_s, const uint8_t* st, const LaneAddr& la, int w, int g,
                                         int t) {
   using L = Smem<D>;
   constexpr int G = D / 32;
-  const float* vts = reinterpret_cast<const float*>(st + L::kOffVtS);
-  const uint8_t* vtz = st + L::kOffVtZ;
-  const int tok = 16 * w + 2 * t;
+  const uint2* vts = reinterpret_cast<const uint2*>(st + L::kOffVtS) + w * 4 + t;
   // row g of the zero-term product carries group g: lanes with g < G load it once
-  uint32_t zown_a = 0u, zown_b = 0u;
-  if (g < G) {
-    zown_a = *reinterpret_cast<const uint32_t*>(vtz + (g * kTile + tok) * 2);
-    zown_b = *reinterpret_cast<const uint32_t*>(vtz + (g * kTile + tok + 8) * 2);
-  }
+  uint2 zown = make_uint2(0u, 0u);
+  if (g < G) zown = reinterpret_cast<const uint2*>(st + L::kOffVtZ)[(g * 4 + w) * 4 + t];
   uint32_t rv4[2][4];
   if constexpr (BITS == 4) {
     ldsm_x4_t(rv4[0], st_s + L::kOffV + la.v4);
@@ -317,10 +318,9 @@ __device__ __forceinline__ void pv_tile(float (&O)[D / 16][4], float (&Z)[4], co
   }
 #pragma unroll
   for (int grp = 0; grp < G; ++grp) {
-    const float2 sa = *reinterpret_cast<const float2*>(vts + grp * kTile + tok);
-    const float2 sb = *reinterpret_cast<const float2*>(vts + grp * kTile + tok + 8);
-    const uint32_t b0 = pack_half2(P[0][0] * sa.x, P[0][1] * sa.y);
-    const uint32_t b1 = pack_half2(P[1][0] * sb.x, P[1][1] * sb.y);
+    const uint2 sv = vts[grp * 16];   // s_g of tokens 2t, 2t+1 | 8+2t, 9+2t
+    const uint32_t b0 = hmul2_u32(pb[0], sv.x);
+    const uint32_t b1 = hmul2_u32(pb[1], sv.y);
     if constexpr (BITS == 8) {
       uint32_t r[4];   // (tok 0-7, ch 0-15), (tok 0-7, ch 16-31), (tok 8-15, ch 0-15), (tok 8-15, ch 16-31)
       ldsm_x4_t(r, st_s + L::kOffV + (la.v8 ^ (static_cast<uint32_t>(grp) << 5)));
@@ -335,9 +335,9 @@ __device__ __forceinline__ void pv_tile(float (&O)[D / 16][4], float (&Z)[4], co
       mma_16816(O[2 * grp + 1], nib_biased(lo >> 8), nib_biased(lo >> 12), nib_biased(hi >> 8),
                 nib_biased(hi >> 12), b0, b1);
     }
-    const uint32_t za = g == grp ? zown_a : 0u;
-    const uint32_t zb = g == grp ? zown_b : 0u;
-    mma_16816(Z, za, 0u, zb, 0u, b0, b1);
+    const uint32_t za = g == grp ? zown.x : 0u;
+    const uint32_t zb = g == grp ? zown.y : 0u;
+    mma_16816(Z[grp & 1], za, 0u, zb, 0u, b0, b1);
   }
 }
 
@@ -507,63 +507,73 @@ __device__ __forceinline__ void segment_end(const DParams& p, const EpiBuf<D>* e
 
 // One consumer step over NT tiles (1, or 2 of the same piece) for the warp's
 // 16 tokens of each: scores, one online-softmax update over all of them, and
-// the P.V products.
+// the P.V products.  lim[u] = tokens of tile u inside the sequence.  The
+// running max m_run and the per-lane partial sums l_run are those of heads
+// 2t, 2t+1 -- the same heads as the lane's output accumulator columns.
 template <int D, int BITS, int NT>
 __device__ __forceinline__ void consume_tiles(const uint32_t (&st_s)[NT], const uint8_t* const (&st)[NT],
-                                              const int (&flags)[NT], int len, const uint32_t (&qa)[D / 16][2],
-                                              const float (&qsum)[D / 32], float (&O)[D / 16][4], float (&Z)[4],
-                                              float& m_run, float& l_run, const LaneAddr& la, int w, int g,
-                                              int t) {
-  float S[NT][2][2];   // log2-domain scores (the table carries the softmax scale)
+                                              const int (&lim)[NT], const uint32_t (&qa)[D / 16][2],
+                                              const float (&qs)[D / 32][2], float (&O)[D / 16][4],
+                                              float (&Z)[2][4], float (&m_run)[2], float (&l_run)[2],
+                                              const LaneAddr& la, int w, int g, int t) {
+  float S[NT][4];   // log2-domain scores (the table carries the softmax scale)
 #pragma unroll
-  for (int u = 0; u < NT; ++u) qk_tile<D, BITS>(S[u], qa, qsum, st_s[u], st[u], la, w, t);
+  for (int u = 0; u < NT; ++u) qk_tile<D, BITS>(S[u], qa, qs, st_s[u], st[u], la, w, g);
   // mask past the sequence end (only the last tile of a sequence)
+  const int r0 = 16 * w + g;
 #pragma unroll
   for (int u = 0; u < NT; ++u) {
-    if (!(flags[u] & kFlagFull)) {
-      const int tok0 = (flags[u] & 0xFFFFFF) * kTile + 16 * w + 2 * t;
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-          if (tok0 + 8 * j + e >= len) S[u][j][e] = -INFINITY;
-    }
+    if (r0 >= lim[u]) S[u][0] = S[u][1] = -INFINITY;
+    if (r0 + 8 >= lim[u]) S[u][2] = S[u][3] = -INFINITY;
   }
-  // online softmax per head row g
-  float mx = -INFINITY;
+  // online softmax for heads 2t, 2t+1: the max over the warp's tokens (rows g)
+  float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-  for (int u = 0; u < NT; ++u) mx = fmaxf(mx, fmaxf(fmaxf(S[u][0][0], S[u][0][1]), fmaxf(S[u][1][0], S[u][1][1])));
-  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-  const float m_new = fmaxf(m_run, mx);
-  const float m_use = m_new == -INFINITY ? 0.0f : m_new;
-  const float alpha = fast_exp2(m_run - m_use);
-  float P[NT][2][2];
-  float psum = 0.0f;
+  for (int u = 0; u < NT; ++u) {
+    mx0 = fmaxf(mx0, fmaxf(S[u][0], S[u][2]));
+    mx1 = fmaxf(mx1, fmaxf(S[u][1], S[u][3]));
+  }
 #pragma unroll
-  for (int u = 0; u < NT; ++u)
+  for (int o = 4; o < 32; o <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+  }
+  const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+  const float mu0 = mn0 == -INFINITY ? 0.0f : mn0, mu1 = mn1 == -INFINITY ? 0.0f : mn1;
+  const float a0 = fast_exp2(m_run[0] - mu0), a1 = fast_exp2(m_run[1] - mu1);
+  float P[NT][4];
+  float ps0 = 0.0f, ps1 = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        P[u][j][e] = fast_exp2(S[u][j][e] - m_use);
-        psum += P[u][j][e];
-      }
-  l_run = l_run * alpha + psum;
-  m_run = m_new;
-  if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-    // accumulator columns are heads 2t, 2t+1; their factors live in rows g = 2t, 2t+1
-    const float a0 = __shfl_sync(0xffffffffu, alpha, (2 * t) << 2);
-    const float a1 = __shfl_sync(0xffffffffu, alpha, (2 * t + 1) << 2);
+  for (int u = 0; u < NT; ++u) {
+    P[u][0] = fast_exp2(S[u][0] - mu0);
+    P[u][1] = fast_exp2(S[u][1] - mu1);
+    P[u][2] = fast_exp2(S[u][2] - mu0);
+    P[u][3] = fast_exp2(S[u][3] - mu1);
+    ps0 += P[u][0] + P[u][2];
+    ps1 += P[u][1] + P[u][3];
+  }
+  l_run[0] = l_run[0] * a0 + ps0;
+  l_run[1] = l_run[1] * a1 + ps1;
+  m_run[0] = mn0;
+  m_run[1] = mn1;
+  if (__any_sync(0xffffffffu, a0 != 1.0f || a1 != 1.0f)) {
 #pragma unroll
     for (int i = 0; i < D / 16; ++i) {
       O[i][0] *= a0; O[i][1] *= a1;
       O[i][2] *= a0; O[i][3] *= a1;
     }
-    Z[0] *= a0; Z[1] *= a1; Z[2] *= a0; Z[3] *= a1;
-  }
 #pragma unroll
-  for (int u = 0; u < NT; ++u) pv_tile<D, BITS>(O, Z, P[u], st_s[u], st[u], la, w, g, t);
+    for (int z = 0; z < 2; ++z) {
+      Z[z][0] *= a0; Z[z][1] *= a1; Z[z][2] *= a0; Z[z][3] *= a1;
+    }
+  }
+  // P^T as the B operand of the products: transpose the (token, head) pairs
+  // of tokens g and g + 8 into (head g; tokens 2t, 2t+1) and (8+2t, 9+2t)
+#pragma unroll
+  for (int u = 0; u < NT; ++u) {
+    const uint32_t pb[2] = {movm_trans(pack_half2(P[u][0], P[u][1])), movm_trans(pack_half2(P[u][2], P[u][3]))};
+    pv_tile<D, BITS>(O, Z, pb, st_s[u], st[u], la, w, g, t);
+  }
 }
 
 template <int D>
@@ -698,11 +708,14 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
         const uint32_t* vsz = reinterpret_cast<const uint32_t*>(st + L::kOffVsz);
         const int len = lens[tc.b];
         // Lane l takes tokens 2l and 2l+1 (all G groups of each: the raw words
-        // are [token][group]); the tables are [group][token], so each lane
-        // writes its two tokens' entries of a group with one store.  The K
+        // are [token][group]) and writes their entries in the consumers'
+        // fragment order: warp l/8; K table rows 2(l%4) and 2(l%4)+1, slot
+        // (l/4)%2 of the float4; V tables column l%4, slot (l/4)%2.  The K
         // scale carries the softmax scale (log2 domain).  The K table
         // overwrites the raw words, so all of them are read first.
         const int t0 = 2 * lane;
+        const int kslot = ((lane >> 3) * 8 + 2 * (lane & 3)) * 2 + ((lane >> 2) & 1);   // float2 index in group 0
+        const int vslot = ((lane >> 3) * 4 + (lane & 3)) * 2 + ((lane >> 2) & 1);       // u32 index in group 0
         uint32_t kw[2][G], vw[2][G];
         load_words<G>(kw[0], ksz + t0 * G);
         load_words<G>(kw[1], ksz + (t0 + 1) * G);
@@ -715,15 +728,16 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
             for (int grp = 0; grp < G; ++grp) kw[u][grp] = vw[u][grp] = 0u;
           }
         __syncwarp();
+        float2* ktab = reinterpret_cast<float2*>(st + L::kOffKt);
+        uint32_t* vts = reinterpret_cast<uint32_t*>(st + L::kOffVtS);
+        uint32_t* vtz = reinterpret_cast<uint32_t*>(st + L::kOffVtZ);
 #pragma unroll
         for (int grp = 0; grp < G; ++grp) {
           const float ks0 = half_lo(kw[0][grp]) * sl2, ks1 = half_lo(kw[1][grp]) * sl2;
-          *reinterpret_cast<float4*>(st + L::kOffKt + (grp * kTile + t0) * 8) =
-              make_float4(ks0, (1024.0f + half_hi(kw[0][grp])) * ks0, ks1, (1024.0f + half_hi(kw[1][grp])) * ks1);
-          *reinterpret_cast<float2*>(st + L::kOffVtS + (grp * kTile + t0) * 4) =
-              make_float2(half_lo(vw[0][grp]), half_lo(vw[1][grp]));
-          *reinterpret_cast<uint32_t*>(st + L::kOffVtZ + (grp * kTile + t0) * 2) =
-              zero_biased_pair(vw[0][grp], vw[1][grp]);
+          ktab[grp * kTile + kslot] = make_float2(ks0, (1024.0f + half_hi(kw[0][grp])) * ks0);
+          ktab[grp * kTile + kslot + 2] = make_float2(ks1, (1024.0f + half_hi(kw[1][grp])) * ks1);
+          vts[grp * (kTile / 2) + vslot] = scale_pair(vw[0][grp], vw[1][grp]);
+          vtz[grp * (kTile / 2) + vslot] = zero_biased_pair(vw[0][grp], vw[1][grp]);
         }
         // the raw-word area is refilled by TMA (async proxy) once the stage is released
         fence_proxy_async_smem();
@@ -762,10 +776,10 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
   tc::reg_alloc<kConsumerRegs>();
   const LaneAddr la = lane_addr<D>(w, lane);
   uint32_t qa[D / 16][2];
-  float qsum[G];
+  float qs[G][2];   // per-group sums of q for heads 2t, 2t+1
   float O[D / 16][4];
-  float Z[4];
-  float m_run = -INFINITY, l_run = 0.0f;
+  float Z[2][4];
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
   bool ok = true;
   int n_end = 0;
   uint32_t gphase = 0;
@@ -779,13 +793,22 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
     const int cb = meta.x, ckvh = meta.y, len = meta.w;
     const bool four = (meta.z & kFlag4) != 0;
     if (meta.z & kFlagStart) {
+      float qsum[G];
       load_q<D>(qa, qsum, p, reinterpret_cast<const uint16_t*>(st0 + L::kOffQ), four ? 4 : 8, g, t);
 #pragma unroll
+      for (int grp = 0; grp < G; ++grp) {
+        qs[grp][0] = __shfl_sync(0xffffffffu, qsum[grp], (2 * t) << 2);
+        qs[grp][1] = __shfl_sync(0xffffffffu, qsum[grp], (2 * t + 1) << 2);
+      }
+#pragma unroll
       for (int i = 0; i < D / 16; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.0f;
-      Z[0] = Z[1] = Z[2] = Z[3] = 0.0f;
-      m_run = -INFINITY;
-      l_run = 0.0f;
+#pragma unroll
+      for (int z = 0; z < 2; ++z) Z[z][0] = Z[z][1] = Z[z][2] = Z[z][3] = 0.0f;
+      m_run[0] = m_run[1] = -INFINITY;
+      l_run[0] = l_run[1] = 0.0f;
     }
+    // tokens of a tile inside the sequence
+    auto tile_lim = [len](int f) { return (f & kFlagFull) ? kTile : len - (f & 0xFFFFFF) * kTile; };
     int fend, nt;
     if (!(meta.z & kFlagEnd)) {
       // the next tile belongs to the same piece: take both in one step
@@ -796,36 +819,45 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
       const int f1 = reinterpret_cast<const int4*>(st1 + L::kOffMeta)->z;
       const uint32_t ss[2] = {smem_u32(st0), smem_u32(st1)};
       const uint8_t* const sp[2] = {st0, st1};
-      const int ff[2] = {meta.z, f1};
-      if (!four) consume_tiles<D, 8, 2>(ss, sp, ff, len, qa, qsum, O, Z, m_run, l_run, la, w, g, t);
-      else consume_tiles<D, 4, 2>(ss, sp, ff, len, qa, qsum, O, Z, m_run, l_run, la, w, g, t);
+      const int lim[2] = {tile_lim(meta.z), tile_lim(f1)};
+      if (!four) consume_tiles<D, 8, 2>(ss, sp, lim, qa, qs, O, Z, m_run, l_run, la, w, g, t);
+      else consume_tiles<D, 4, 2>(ss, sp, lim, qa, qs, O, Z, m_run, l_run, la, w, g, t);
       fend = f1;
       nt = 2;
     } else {
       const uint32_t ss[1] = {smem_u32(st0)};
       const uint8_t* const sp[1] = {st0};
-      const int ff[1] = {meta.z};
-      if (!four) consume_tiles<D, 8, 1>(ss, sp, ff, len, qa, qsum, O, Z, m_run, l_run, la, w, g, t);
-      else consume_tiles<D, 4, 1>(ss, sp, ff, len, qa, qsum, O, Z, m_run, l_run, la, w, g, t);
+      const int lim[1] = {tile_lim(meta.z)};
+      if (!four) consume_tiles<D, 8, 1>(ss, sp, lim, qa, qs, O, Z, m_run, l_run, la, w, g, t);
+      else consume_tiles<D, 4, 1>(ss, sp, lim, qa, qs, O, Z, m_run, l_run, la, w, g, t);
       fend = meta.z;
       nt = 1;
     }
 
     // ---- end of a piece: the warps' states go to the hand-off buffer ----
     if (fend & kFlagEnd) {
-      float l_tot = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
-      l_tot += __shfl_xor_sync(0xffffffffu, l_tot, 2);
+      // sums over the warp's tokens (rows g) for heads 2t, 2t+1
+      float l_tot[2] = {l_run[0], l_run[1]};
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        l_tot[0] += __shfl_xor_sync(0xffffffffu, l_tot[0], o);
+        l_tot[1] += __shfl_xor_sync(0xffffffffu, l_tot[1], o);
+      }
       if (n_end > 0) ok = ok && mbar_wait(epi_empty, (n_end - 1) & 1, p.status);
       if (!ok) break;
-      if (t == 0 && g < p.rep) {
-        eb->ml[w][g][0] = m_run;
-        eb->ml[w][g][1] = l_tot;
+      if (g == 0) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          if (2 * t + e < p.rep) {
+            eb->ml[w][2 * t + e][0] = m_run[e];
+            eb->ml[w][2 * t + e][1] = l_tot[e];
+          }
       }
 #pragma unroll
       for (int grp = 0; grp < G; ++grp) {
-        // zero-point term of group grp for heads 2t, 2t+1 sits in row grp of Z
-        const float r0 = __shfl_sync(0xffffffffu, Z[0], grp * 4 + t);
-        const float r1 = __shfl_sync(0xffffffffu, Z[1], grp * 4 + t);
+        // zero-point term of group grp for heads 2t, 2t+1 sits in row grp of Z[grp & 1]
+        const float r0 = __shfl_sync(0xffffffffu, Z[grp & 1][0], grp * 4 + t);
+        const float r1 = __shfl_sync(0xffffffffu, Z[grp & 1][1], grp * 4 + t);
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int h = 2 * t + e;

@@ -194,6 +194,20 @@ __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// Transpose of an 8x8 matrix of 16-bit elements held one register per lane
+// (lane l: row l/4, columns 2(l%4), 2(l%4)+1): afterwards the lane holds
+// row l/4, columns 2(l%4), 2(l%4)+1 of the transposed matrix.
+__device__ __forceinline__ uint32_t movm_trans(uint32_t x) {
+  uint32_t y;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -212,6 +226,8 @@ __device__ __forceinline__ uint32_t zero_biased2(uint32_t sz) {
   __half2 r = __halves2half2(zb, zb);
   return *reinterpret_cast<uint32_t*>(&r);
 }
+// half2(s_a, s_b): the fp16 scales of two scale/zero words
+__device__ __forceinline__ uint32_t scale_pair(uint32_t sz_a, uint32_t sz_b) { return prmt(sz_a, sz_b, 0x5410u); }
 // half2((1024 + z_a), (1024 + z_b)) from two scale/zero words
 __device__ __forceinline__ uint32_t zero_biased_pair(uint32_t sz_a, uint32_t sz_b) {
   uint32_t zz = prmt(sz_a, sz_b, 0x7632u);  // high halves: z_a | z_b << 16
