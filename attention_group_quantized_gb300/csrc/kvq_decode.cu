@@ -667,6 +667,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
     if (w == kWarps) {
       // ---------------- TMA issuer warp: lane 0 keeps kStages tiles in flight ----------------
       if (lane != 0) return;
+      const uint64_t pol = l2_evict_first_policy();   // the cache is streamed once per call
       Cursor pc = locate(f0, pre, B, Hkv);
       for (int k = 0; k < ntiles; ++k) {
         const int slot = k % kStages;
@@ -685,10 +686,10 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
         mbar_arrive_expect_tx(bar, 2 * kTile * R + 2 * L::kSzBytes + qbytes);
         if (first)
           bulk_g2s(st + L::kOffQ, p.q + (static_cast<int64_t>(pc.b) * p.Hq + pc.kvh * p.rep) * D, qbytes, bar);
-        tma_2d_g2s(st + L::kOffK, bits == 8 ? &p.tm_k8 : &p.tm_k4, 0, row0, bar);
-        tma_2d_g2s(st + L::kOffV, bits == 8 ? &p.tm_v8 : &p.tm_v4, 0, row0, bar);
-        bulk_g2s(st + L::kOffKsz, p.k_sz + szoff * G, L::kSzBytes, bar);
-        bulk_g2s(st + L::kOffVsz, p.v_sz + szoff * G, L::kSzBytes, bar);
+        tma_2d_g2s_hint(st + L::kOffK, bits == 8 ? &p.tm_k8 : &p.tm_k4, 0, row0, bar, pol);
+        tma_2d_g2s_hint(st + L::kOffV, bits == 8 ? &p.tm_v8 : &p.tm_v4, 0, row0, bar, pol);
+        bulk_g2s_hint(st + L::kOffKsz, p.k_sz + szoff * G, L::kSzBytes, bar, pol);
+        bulk_g2s_hint(st + L::kOffVsz, p.v_sz + szoff * G, L::kSzBytes, bar, pol);
         advance(pc, pre, B, Hkv);
       }
       return;
