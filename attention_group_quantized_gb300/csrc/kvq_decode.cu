@@ -526,21 +526,40 @@ __device__ __forceinline__ void consume_tiles(const uint32_t (&st_s)[NT], const 
     if (r0 >= lim[u]) S[u][0] = S[u][1] = -INFINITY;
     if (r0 + 8 >= lim[u]) S[u][2] = S[u][3] = -INFINITY;
   }
-  // online softmax for heads 2t, 2t+1: the max over the warp's tokens (rows g)
+  // online softmax for heads 2t, 2t+1: the max over the warp's tokens (rows g).
+  // While no score exceeds the running max the max is unchanged and so is
+  // every factor: the warp reduction and the rescale run only when some lane
+  // sees a larger score (the results are the same either way).
   float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
   for (int u = 0; u < NT; ++u) {
     mx0 = fmaxf(mx0, fmaxf(S[u][0], S[u][2]));
     mx1 = fmaxf(mx1, fmaxf(S[u][1], S[u][3]));
   }
+  float a0 = 1.0f, a1 = 1.0f;
+  if (__any_sync(0xffffffffu, mx0 > m_run[0] || mx1 > m_run[1])) {
 #pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+    a0 = fast_exp2(m_run[0] - (mn0 == -INFINITY ? 0.0f : mn0));
+    a1 = fast_exp2(m_run[1] - (mn1 == -INFINITY ? 0.0f : mn1));
+    m_run[0] = mn0;
+    m_run[1] = mn1;
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+      O[i][0] *= a0; O[i][1] *= a1;
+      O[i][2] *= a0; O[i][3] *= a1;
+    }
+#pragma unroll
+    for (int z = 0; z < 2; ++z) {
+      Z[z][0] *= a0; Z[z][1] *= a1; Z[z][2] *= a0; Z[z][3] *= a1;
+    }
   }
-  const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-  const float mu0 = mn0 == -INFINITY ? 0.0f : mn0, mu1 = mn1 == -INFINITY ? 0.0f : mn1;
-  const float a0 = fast_exp2(m_run[0] - mu0), a1 = fast_exp2(m_run[1] - mu1);
+  const float mu0 = m_run[0] == -INFINITY ? 0.0f : m_run[0];
+  const float mu1 = m_run[1] == -INFINITY ? 0.0f : m_run[1];
   float P[NT][4];
   float ps0 = 0.0f, ps1 = 0.0f;
 #pragma unroll
@@ -554,19 +573,6 @@ __device__ __forceinline__ void consume_tiles(const uint32_t (&st_s)[NT], const 
   }
   l_run[0] = l_run[0] * a0 + ps0;
   l_run[1] = l_run[1] * a1 + ps1;
-  m_run[0] = mn0;
-  m_run[1] = mn1;
-  if (__any_sync(0xffffffffu, a0 != 1.0f || a1 != 1.0f)) {
-#pragma unroll
-    for (int i = 0; i < D / 16; ++i) {
-      O[i][0] *= a0; O[i][1] *= a1;
-      O[i][2] *= a0; O[i][3] *= a1;
-    }
-#pragma unroll
-    for (int z = 0; z < 2; ++z) {
-      Z[z][0] *= a0; Z[z][1] *= a1; Z[z][2] *= a0; Z[z][3] *= a1;
-    }
-  }
   // P^T as the B operand of the products: transpose the (token, head) pairs
   // of tokens g and g + 8 into (head g; tokens 2t, 2t+1) and (8+2t, 9+2t)
 #pragma unroll
