@@ -29,23 +29,29 @@
 //    setmaxnreg moves registers from the helper warpgroup to the consumers.
 //  * The products run on the tensor cores with exact operands: a code byte
 //    becomes the fp16 value 1024 + c by one byte permute.
-//      S = Q K^T (rows = the query heads of the KV head, columns = tokens),
-//        per group g of 32 channels: C_g = Q.(1024 + c), then
-//        S += s_g C_g - (1024 + z_g) s_g sum_g(Q), which equals s_g Q.(c - z_g).
+//      S^T = K Q^T (rows = 16 tokens per warp, columns = the query heads of
+//        the KV head), per group g of 32 channels: C_g = (1024 + c).Q, then
+//        S += s_g C_g - (1024 + z_g) s_g sum_g(Q), which equals s_g (c - z_g).Q.
+//        Each lane then holds two tokens of heads 2t, 2t+1 -- the same heads as
+//        its output columns below, so the softmax factors need no shuffles.
 //      O^T = V^T P^T (rows = channels, columns = query heads): each MMA's rows
-//        lie in one group g, so its B operand is P * s_g (one fp16 rounding);
-//        A is 1024 + c, and one extra MMA per group accumulates
-//        sum_tok (1024 + z_g) P s_g into a spare row, subtracted at the end.
-//        That row must go through the same sequence of MMAs as the output
-//        accumulators (one accumulator, same order): the tensor core's fp32
-//        accumulation then rounds the large common 1024 * sum(P s_g) part the
-//        same way on both sides and it cancels; a differently split sum
-//        leaves an error about ten times larger.
+//        lie in one group g, so its B operand is P^T * s_g (P rounded to fp16,
+//        transposed in registers by movmatrix, times the fp16 scale); A is
+//        1024 + c, and one extra MMA per group accumulates
+//        sum_tok (1024 + z_g) P s_g into row g of a spare tile, subtracted at
+//        the end.  Each such row must see the same MMAs with nonzero terms, in
+//        the same order, as the output rows of its group (two spare tiles, even
+//        and odd groups, keep that): the tensor core's fp32 accumulation then
+//        rounds the large common 1024 * sum(P s_g) part the same way on both
+//        sides and it cancels; a differently split sum leaves an error about
+//        ten times larger.
 //  * Fragments come from the swizzled code tiles by ldmatrix: K as stored
-//    (token rows), V transposed, so each register holds two tokens of two
-//    channels and one byte permute yields a (token, token) pair of a channel.
-//    Every lane's row addresses are fixed, and the swizzle keeps all eight
-//    rows of each 8x8 matrix in distinct banks.
+//    (token rows, a register holds four channels of one token), V transposed
+//    (a register holds two tokens of two channels).  Every lane's row
+//    addresses are fixed, and the swizzle keeps all eight rows of each 8x8
+//    matrix in distinct banks.
+//  * The cache is streamed with an L2 evict-first policy: it is read once per
+//    call, and the small buffers the next call needs stay in L2.
 //  * One CTA serves all query heads of a KV head, so every cache byte is read
 //    once for the whole GQA group.
 #include <cfloat>
