@@ -183,6 +183,122 @@ kvq_status kvq_decode_attention(const void* q, const kvq_cache* k, const kvq_cac
   return launch_decode(a, static_cast<cudaStream_t>(stream));
 }
 
+}  // extern "C"
+
+// One decode step; with q_src set, the append launch also copies q_bytes
+// from q_src (any device-visible memory) to q, the decode's query buffer.
+static kvq_status decode_step_impl(const void* q, const void* q_src, size_t q_bytes, const void* k_new,
+                                   const void* v_new, const kvq_cache* k, const kvq_cache* v,
+                                   const int32_t* seq_lens, int32_t Hq, float softmax_scale, void* out,
+                                   int32_t out_dtype, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                   void* stream) {
+  if (k_new == nullptr || v_new == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_INVALID_ARG;
+  // every check of the decode call first, so that nothing is appended unless both launches are valid
+  if (q == nullptr || k == nullptr || v == nullptr || seq_lens == nullptr || out == nullptr)
+    return KVQ_ERR_INVALID_ARG;
+  if (k->codes == nullptr || k->sz == nullptr || v->codes == nullptr || v->sz == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (k->D > 0 && k->D != 64 && k->D != 128) return KVQ_ERR_UNSUPPORTED;
+  AppendArgs a;
+  if (!resolve_layout(*k, &a.layout) || !same_cache_shape(*k, *v)) return KVQ_ERR_INVALID_ARG;
+  if (Hq <= 0 || Hq % k->Hkv) return KVQ_ERR_INVALID_ARG;
+  if (Hq / k->Hkv > 8) return KVQ_ERR_UNSUPPORTED;
+  if (out_dtype != KVQ_OUT_F32 && out_dtype != KVQ_OUT_BF16) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k->codes) || !aligned16(k->sz) || !aligned16(v->codes) || !aligned16(v->sz) ||
+      !aligned16(out) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return KVQ_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(k->Hkv) * k->B * k->Tcap >= (int64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
+  if (k->B > 4096) return KVQ_ERR_UNSUPPORTED;   // the decode kernel's shared memory holds up to 4096 lengths
+  const size_t need = kvq_decode_workspace_bytes(k->B, Hq, k->Hkv, k->D);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return KVQ_ERR_WORKSPACE;
+  if (q_src != nullptr && (!aligned16(q_src) || (q_bytes & 15u))) return KVQ_ERR_INVALID_ARG;
+  a.q_src = q_src;
+  a.q_dst = const_cast<void*>(q);
+  a.q_bytes = q_src != nullptr ? q_bytes : 0;
+  a.k_new = static_cast<const uint16_t*>(k_new);
+  a.v_new = static_cast<const uint16_t*>(v_new);
+  a.k_codes = k->codes; a.k_sz = k->sz;
+  a.v_codes = v->codes; a.v_sz = v->sz;
+  a.seq_lens = seq_lens;
+  a.B = k->B; a.Hkv = k->Hkv; a.Tcap = k->Tcap; a.D = k->D;
+  a.status = dev_status;
+  if (launch_append(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  return kvq_decode_attention(q, k, v, seq_lens, Hq, softmax_scale, out, out_dtype, workspace, workspace_bytes,
+                              dev_status, stream);
+}
+
+extern "C" {
+
+kvq_status kvq_decode_step(const void* q, const void* k_new, const void* v_new, const kvq_cache* k,
+                           const kvq_cache* v, const int32_t* seq_lens, int32_t Hq, float softmax_scale, void* out,
+                           int32_t out_dtype, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                           void* stream) {
+  return decode_step_impl(q, nullptr, 0, k_new, v_new, k, v, seq_lens, Hq, softmax_scale, out, out_dtype, workspace,
+                          workspace_bytes, dev_status, stream);
+}
+
+static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Device address of pinned (page-locked, mapped) host memory, or null for
+// pageable memory.  With unified addressing the GPU reads and writes such
+// memory in place over the host link.
+static void* pinned_device_view(const void* host) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, host) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return nullptr;
+  return at.devicePointer;
+}
+
+size_t kvq_decode_step_staging_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t out_dtype) {
+  if (B <= 0 || Hkv <= 0 || Hq <= 0 || Hq % Hkv || (D != 64 && D != 128)) return 0;
+  if (out_dtype != KVQ_OUT_F32 && out_dtype != KVQ_OUT_BF16) return 0;
+  const size_t q = static_cast<size_t>(B) * Hq * D * 2, kv = static_cast<size_t>(B) * Hkv * D * 2;
+  const size_t o = static_cast<size_t>(B) * Hq * D * (out_dtype == KVQ_OUT_F32 ? 4 : 2);
+  return round256(q) + 2 * round256(kv) + round256(o);
+}
+
+kvq_status kvq_decode_step_host(const void* q_host, const void* k_new_host, const void* v_new_host,
+                                const kvq_cache* k, const kvq_cache* v, const int32_t* seq_lens, int32_t Hq,
+                                float softmax_scale, void* out_host, int32_t out_dtype, void* staging,
+                                size_t staging_bytes, void* workspace, size_t workspace_bytes,
+                                int32_t* dev_status, void* stream) {
+  if (q_host == nullptr || k_new_host == nullptr || v_new_host == nullptr || out_host == nullptr || k == nullptr ||
+      staging == nullptr)
+    return KVQ_ERR_INVALID_ARG;
+  const size_t need = kvq_decode_step_staging_bytes(k->B, Hq, k->Hkv, k->D, out_dtype);
+  if (need == 0) return KVQ_ERR_INVALID_ARG;
+  if (staging_bytes < need || (reinterpret_cast<uintptr_t>(staging) & 255u)) return KVQ_ERR_INVALID_ARG;
+  const size_t qb = static_cast<size_t>(k->B) * Hq * k->D * 2, kvb = static_cast<size_t>(k->B) * k->Hkv * k->D * 2;
+  const size_t ob = static_cast<size_t>(k->B) * Hq * k->D * (out_dtype == KVQ_OUT_F32 ? 4 : 2);
+  uint8_t* st = static_cast<uint8_t*>(staging);
+  uint8_t* d_q = st;
+  uint8_t* d_k = d_q + round256(qb);
+  uint8_t* d_v = d_k + round256(kvb);
+  uint8_t* d_o = d_v + round256(kvb);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Pinned host buffers: no copy calls.  The append launch reads the new
+  // K/V rows in place and stages q; the decode writes the output in place.
+  void* p_q = pinned_device_view(q_host);
+  void* p_k = p_q ? pinned_device_view(k_new_host) : nullptr;
+  void* p_v = p_k ? pinned_device_view(v_new_host) : nullptr;
+  void* p_o = p_v ? pinned_device_view(out_host) : nullptr;
+  if (p_o != nullptr && aligned16(p_q) && aligned16(p_k) && aligned16(p_v) && aligned16(p_o))
+    return decode_step_impl(d_q, p_q, qb, p_k, p_v, k, v, seq_lens, Hq, softmax_scale, p_o, out_dtype, workspace,
+                            workspace_bytes, dev_status, stream);
+  // pageable memory: asynchronous copies through the staging buffer
+  if (cudaMemcpyAsync(d_q, q_host, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(d_k, k_new_host, kvb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(d_v, v_new_host, kvb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  const kvq_status r = decode_step_impl(d_q, nullptr, 0, d_k, d_v, k, v, seq_lens, Hq, softmax_scale, d_o, out_dtype,
+                                        workspace, workspace_bytes, dev_status, stream);
+  if (r != KVQ_OK) return r;
+  return cudaMemcpyAsync(out_host, d_o, ob, cudaMemcpyDeviceToHost, s) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
 kvq_status kvq_prefill_attention(const void* q, const void* k, const void* v, int32_t B, int32_t Hq, int32_t Hkv,
                                  int32_t S, int32_t D, int32_t causal, float softmax_scale,
                                  const uint8_t* tile_mask, int32_t tile, const kvq_cache* k_cache,

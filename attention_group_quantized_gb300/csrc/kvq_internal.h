@@ -33,6 +33,25 @@ struct QuantizeArgs {
 };
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t stream);
 
+// The new token of every (sequence, KV head) of K and V, written at cache
+// position seq_lens[b] - 1 (one launch for both caches).
+struct AppendArgs {
+  const void* q_src = nullptr;      // optional copy of q (q_bytes, a multiple of 16) into q_dst,
+  void* q_dst = nullptr;            // done by the same launch
+  size_t q_bytes = 0;
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  uint8_t* k_codes;
+  uint32_t* k_sz;
+  uint8_t* v_codes;
+  uint32_t* v_sz;
+  const int32_t* seq_lens;
+  int32_t B, Hkv, Tcap, D;
+  int32_t* status;
+  HeadLayout layout;                // shared by K and V
+};
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
+
 struct DecodeArgs {
   const uint16_t* q;
   const kvq_cache* k;

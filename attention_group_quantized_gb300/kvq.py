@@ -27,7 +27,8 @@ TILE_TOKENS = 64
 # every symbol include/kvq.h declares
 EXPORTS = ("kvq_cache_codes_bytes", "kvq_cache_sz_bytes", "kvq_cache_head_offset", "kvq_quantize",
            "kvq_decode_workspace_bytes", "kvq_decode_attention", "kvq_prefill_attention",
-           "kvq_decode_attention_noalloc", "kvq_status_str")
+           "kvq_decode_attention_noalloc", "kvq_decode_step", "kvq_decode_step_staging_bytes",
+           "kvq_decode_step_host", "kvq_status_str")
 
 
 class KvqError(RuntimeError):
@@ -67,6 +68,12 @@ def lib() -> ctypes.CDLL:
         L.kvq_prefill_attention.restype = I32
         L.kvq_decode_attention_noalloc.argtypes = [P, CP, CP, P, I32, F32, P, I32, P, P]
         L.kvq_decode_attention_noalloc.restype = I32
+        L.kvq_decode_step.argtypes = [P, P, P, CP, CP, P, I32, F32, P, I32, P, SZ, P, P]
+        L.kvq_decode_step.restype = I32
+        L.kvq_decode_step_staging_bytes.argtypes = [I32, I32, I32, I32, I32]
+        L.kvq_decode_step_staging_bytes.restype = SZ
+        L.kvq_decode_step_host.argtypes = [P, P, P, CP, CP, P, I32, F32, P, I32, P, SZ, P, SZ, P, P]
+        L.kvq_decode_step_host.restype = I32
         L.kvq_status_str.argtypes = [I32]; L.kvq_status_str.restype = ctypes.c_char_p
         _LIB = L
     return _LIB
@@ -95,10 +102,17 @@ class QuantCache:
     D: int
 
     def c_struct(self) -> CCache:
+        """The C view of the cache, rebuilt only when a backing buffer changed."""
+        key = (self.codes.data_ptr(), self.sz.data_ptr(), id(self.head_bits), self.B, self.Hkv, self.Tcap, self.D)
+        cached = self.__dict__.get("_c_view")
+        if cached is not None and cached[0] == key:
+            return cached[1]
         hb = np.ascontiguousarray(self.head_bits, dtype=np.int8)
         self.head_bits = hb
-        return CCache(self.codes.data_ptr(), self.sz.data_ptr(), hb.ctypes.data, self.B, self.Hkv,
-                      self.Tcap, self.D)
+        cs = CCache(self.codes.data_ptr(), self.sz.data_ptr(), hb.ctypes.data, self.B, self.Hkv, self.Tcap, self.D)
+        key = (self.codes.data_ptr(), self.sz.data_ptr(), id(hb), self.B, self.Hkv, self.Tcap, self.D)
+        self.__dict__["_c_view"] = (key, cs, hb)
+        return cs
 
     def head_offset(self, h: int) -> int:
         cs = self.c_struct()
@@ -183,6 +197,85 @@ def decode_attention_noalloc(q, k: QuantCache, v: QuantCache, seq_lens, softmax_
                                             status.data_ptr() if status is not None else None, _stream_ptr(stream))
     _check(st, "kvq_decode_attention_noalloc")
     return out
+
+
+def decode_step(q, k_new, v_new, k: QuantCache, v: QuantCache, seq_lens, softmax_scale: float = 0.0,
+                out=None, out_dtype: int = OUT_F32, workspace=None, status=None, stream=None):
+    """One decode step: append k_new/v_new bf16 [B][Hkv][D] at position seq_lens[b] - 1 of the
+    caches, then attend q bf16 [B][Hq][D] over seq_lens[b] tokens; returns out [B][Hq][D]."""
+    import torch
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32 if out_dtype == OUT_F32 else torch.bfloat16,
+                          device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, k.Hkv, D, q.device)
+    kc, vc = k.c_struct(), v.c_struct()
+    st = lib().kvq_decode_step(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), ctypes.byref(kc), ctypes.byref(vc),
+                               seq_lens.data_ptr(), Hq, float(softmax_scale), out.data_ptr(), out_dtype,
+                               workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                               status.data_ptr() if status is not None else None, _stream_ptr(stream))
+    _check(st, "kvq_decode_step")
+    return out
+
+
+def decode_step_staging(B: int, Hq: int, Hkv: int, D: int, out_dtype: int = OUT_F32, device="cuda"):
+    """Device staging buffer for decode_step_host (256-byte aligned)."""
+    import torch
+    n = int(lib().kvq_decode_step_staging_bytes(B, Hq, Hkv, D, out_dtype))
+    if n == 0:
+        raise KvqError(1, "kvq_decode_step_staging_bytes: invalid shape")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def decode_step_host(q_host, k_new_host, v_new_host, k: QuantCache, v: QuantCache, seq_lens, out_host,
+                     softmax_scale: float = 0.0, out_dtype: int = OUT_F32, staging=None, workspace=None,
+                     status=None, stream=None):
+    """decode_step with the inputs (q_host, k_new_host, v_new_host, bf16 CPU tensors) and the
+    output (out_host, CPU tensor of out_dtype) in host memory.  With pinned tensors the launches
+    read and write them in place; otherwise they are copied through `staging`.  Everything is
+    enqueued on `stream`; out_host is valid after a synchronisation."""
+    B, Hq, D = q_host.shape
+    dev = k.codes.device
+    if staging is None:
+        staging = decode_step_staging(B, Hq, k.Hkv, D, out_dtype, dev)
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, k.Hkv, D, dev)
+    kc, vc = k.c_struct(), v.c_struct()
+    st = lib().kvq_decode_step_host(q_host.data_ptr(), k_new_host.data_ptr(), v_new_host.data_ptr(),
+                                    ctypes.byref(kc), ctypes.byref(vc), seq_lens.data_ptr(), Hq,
+                                    float(softmax_scale), out_host.data_ptr(), out_dtype,
+                                    staging.data_ptr(), staging.numel(),
+                                    workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                    status.data_ptr() if status is not None else None, _stream_ptr(stream))
+    _check(st, "kvq_decode_step_host")
+    return out_host
+
+
+class DecodeStepHost:
+    """A decode_step_host call with its host buffers, staging, workspace and stream bound once,
+    for serving loops that run it every token: ``run(k, v)`` enqueues one step on the caches
+    given (their C views are cached) with little Python work per call."""
+
+    def __init__(self, q_host, k_new_host, v_new_host, seq_lens, out_host, softmax_scale: float = 0.0,
+                 out_dtype: int = OUT_F32, staging=None, workspace=None, status=None, stream=None,
+                 Hkv: Optional[int] = None, device="cuda"):
+        B, Hq, D = q_host.shape
+        Hkv = int(k_new_host.shape[1]) if Hkv is None else Hkv
+        self.staging = staging if staging is not None else decode_step_staging(B, Hq, Hkv, D, out_dtype, device)
+        self.workspace = workspace if workspace is not None else decode_workspace(B, Hq, Hkv, D, device)
+        self._keep = (q_host, k_new_host, v_new_host, seq_lens, out_host, status, stream)
+        self._head = (q_host.data_ptr(), k_new_host.data_ptr(), v_new_host.data_ptr())
+        self._tail = (seq_lens.data_ptr(), Hq, float(softmax_scale), out_host.data_ptr(), out_dtype,
+                      self.staging.data_ptr(), self.staging.numel(), self.workspace.data_ptr(),
+                      self.workspace.numel() * self.workspace.element_size(),
+                      status.data_ptr() if status is not None else None, _stream_ptr(stream))
+        self._fn = lib().kvq_decode_step_host
+
+    def run(self, k: QuantCache, v: QuantCache):
+        st = self._fn(*self._head, ctypes.byref(k.c_struct()), ctypes.byref(v.c_struct()), *self._tail)
+        if st != KVQ_OK:
+            raise KvqError(st, "kvq_decode_step_host")
 
 
 def prefill_attention(q, k, v, k_cache: QuantCache, v_cache: QuantCache, softmax_scale: float = 0.0,

@@ -198,6 +198,64 @@ KVQ_API kvq_status kvq_decode_attention_noalloc(const void* q, const kvq_cache* 
                                                 void* out, int32_t out_dtype,
                                                 int32_t* dev_status, void* stream);
 
+/*
+ * kvq_decode_step -- one step of a decode loop over the quantised cache (the
+ * decode phase of P4 §1.3: each new token's K/V is quantised on write, then
+ * the new query attends the cache with dequantisation inside the read).
+ *
+ * Appends the new token of every (sequence b, KV head) to both caches at
+ * position seq_lens[b] - 1, quantised exactly as kvq_quantize writes it, then
+ * computes kvq_decode_attention over positions 0 .. seq_lens[b] - 1.
+ *
+ * k_new, v_new: device bf16 [B][Hkv][D], contiguous, 16-byte aligned.
+ * seq_lens: device int32 [B], each length INCLUDING the new token.  A length
+ *           outside [1, Tcap] reports KVQ_ERR_INVALID_ARG in dev_status and
+ *           that sequence appends nothing (decode then treats the length as
+ *           kvq_decode_attention does).
+ * q, k, v, Hq, softmax_scale, out, out_dtype, workspace, dev_status, stream:
+ *           as kvq_decode_attention; the workspace is required.
+ * Two launches on `stream`: the append kernel (K and V together) and the
+ * decode kernel, whose prologue overlaps the append kernel's end
+ * (programmatic dependent launch); the decode waits for the append before
+ * reading memory.  All arguments are checked before the first launch.
+ */
+KVQ_API kvq_status kvq_decode_step(const void* q, const void* k_new, const void* v_new,
+                                   const kvq_cache* k, const kvq_cache* v, const int32_t* seq_lens,
+                                   int32_t Hq, float softmax_scale, void* out, int32_t out_dtype,
+                                   void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                   void* stream);
+
+/*
+ * Device staging bytes kvq_decode_step_host needs: q, k_new, v_new and the
+ * output, each rounded up to 256 bytes.  0 on invalid shape.
+ */
+KVQ_API size_t kvq_decode_step_staging_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t out_dtype);
+
+/*
+ * kvq_decode_step_host -- kvq_decode_step with the step's inputs and output in
+ * HOST memory: q_host bf16 [B][Hq][D], k_new_host / v_new_host bf16
+ * [B][Hkv][D], out_host [B][Hq][D] of out_dtype, all 16-byte aligned.
+ * When all four host buffers are pinned (page-locked, so mapped into the
+ * GPU's address space) the call makes no copy calls: the append launch reads
+ * the new K/V rows in place over the host link and stages q in `staging`,
+ * and the decode launch writes the output straight into out_host.  Otherwise
+ * it enqueues three host-to-device copies into `staging`, the two launches of
+ * kvq_decode_step and a device-to-host copy of the output (with pageable
+ * memory the copies may block the host).  Either way everything goes to
+ * `stream` and the call returns once it is enqueued; out_host holds the
+ * result after the caller synchronises the stream, and the host inputs and
+ * `staging` must stay untouched until then.
+ * staging: device scratch of >= kvq_decode_step_staging_bytes(B, Hq, Hkv, D,
+ * out_dtype) bytes, 256-byte aligned.  The caches, seq_lens, workspace and
+ * dev_status are device memory as in kvq_decode_step.
+ */
+KVQ_API kvq_status kvq_decode_step_host(const void* q_host, const void* k_new_host, const void* v_new_host,
+                                        const kvq_cache* k, const kvq_cache* v, const int32_t* seq_lens,
+                                        int32_t Hq, float softmax_scale, void* out_host, int32_t out_dtype,
+                                        void* staging, size_t staging_bytes,
+                                        void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                        void* stream);
+
 /* Static, human-readable name of a status code. */
 KVQ_API const char* kvq_status_str(kvq_status status);
 

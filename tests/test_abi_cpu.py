@@ -109,3 +109,46 @@ def test_prefill_validation_without_launch(L):
     k4, _ = _cache([8, 4], Tcap=256)
     v4, _ = _cache([8, 4], Tcap=256)
     assert L.kvq_prefill_attention(a, a, a, 1, 4, 2, 256, 128, 1, 0.0, None, 128, P(k4), P(v4), a, 0, None, None) == 2
+
+
+def test_decode_step_validation_without_launch(L):
+    k, hk = _cache([8, 8])
+    v, hv = _cache([8, 8])
+    P = ctypes.byref
+    q, kn, vn, lens, out, ws = 0x4000, 0x9000, 0xA000, 0x5000, 0x6000, 0x7000
+    args = lambda **o: [o.get("q", q), o.get("kn", kn), o.get("vn", vn), P(k), P(o.get("v", v)), lens,
+                        o.get("Hq", 8), 0.0, out, o.get("dt", 0), ws, 1 << 20, None, None]
+    assert L.kvq_decode_step(*args(kn=None)) == 1
+    assert L.kvq_decode_step(*args(vn=vn + 4)) == 1          # misaligned new row
+    assert L.kvq_decode_step(*args(q=None)) == 1
+    assert L.kvq_decode_step(*args(Hq=7)) == 1
+    assert L.kvq_decode_step(*args(Hq=32)) == 2              # 16 query heads per KV head
+    assert L.kvq_decode_step(*args(dt=5)) == 1
+    v2, hv2 = _cache([8, 4])
+    assert L.kvq_decode_step(*args(v=v2)) == 1               # bit-widths differ
+
+
+def test_decode_step_staging_bytes(L):
+    r = lambda x: (x + 255) // 256 * 256
+    for B, Hq, Hkv, D, dt in [(8, 32, 8, 128, 0), (8, 32, 8, 128, 1), (3, 4, 4, 64, 0), (1, 1, 1, 64, 1)]:
+        q, kv = B * Hq * D * 2, B * Hkv * D * 2
+        o = B * Hq * D * (4 if dt == 0 else 2)
+        assert L.kvq_decode_step_staging_bytes(B, Hq, Hkv, D, dt) == r(q) + 2 * r(kv) + r(o)
+    assert L.kvq_decode_step_staging_bytes(1, 3, 2, 128, 0) == 0
+    assert L.kvq_decode_step_staging_bytes(1, 4, 2, 96, 0) == 0
+    assert L.kvq_decode_step_staging_bytes(1, 4, 2, 128, 7) == 0
+
+
+def test_decode_step_host_validation_without_launch(L):
+    k, hk = _cache([8, 8])
+    v, hv = _cache([8, 8])
+    P = ctypes.byref
+    h, lens, st, ws = 0x10000, 0x5000, 0x20000, 0x7000
+    need = L.kvq_decode_step_staging_bytes(1, 8, 2, 128, 0)
+    call = lambda stg, n, qh=h, dt=0: L.kvq_decode_step_host(qh, h, h, P(k), P(v), lens, 8, 0.0, h, dt, stg, n,
+                                                             ws, 1 << 20, None, None)
+    assert call(st, need, qh=None) == 1
+    assert call(None, need) == 1
+    assert call(st, need - 1) == 1                            # staging too small
+    assert call(st + 16, need) == 1                           # staging not 256-byte aligned
+    assert call(st, need, dt=3) == 1

@@ -1,0 +1,227 @@
+"""GPU parity of kvq_decode_step / kvq_decode_step_host (append the new token's
+K/V, then attend) against the oracle.
+
+The cache is first filled from a copy of the inputs whose new-token rows
+(position len_b - 1) hold different values; the step must overwrite exactly
+those rows.  Afterwards every live cache row must equal the oracle's
+quantisation of the true inputs bit for bit, and the output must satisfy
+|o - ref| <= 2e-3 + 2e-3 |ref| against the fp64 oracle over the dequantised
+cache.
+"""
+import numpy as np
+import pytest
+
+from oracle import kvq_oracle as O
+import kvq_workloads as W
+from tests import kvq_testutil as U
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from attention_group_quantized_gb300 import kvq
+    kvq.lib()
+
+
+def _kvq():
+    from attention_group_quantized_gb300 import kvq
+    return kvq
+
+
+def _stale_new_rows(x: np.ndarray, lens, seed: int) -> np.ndarray:
+    """Copy of x with the row at len_b - 1 of every (b, head) replaced by other values."""
+    y = x.copy()
+    rng = np.random.default_rng(seed)
+    for b, L in enumerate(lens):
+        if 1 <= L <= x.shape[2]:
+            f = (rng.standard_normal((x.shape[1], x.shape[3])) * 3.0).astype(np.float32)
+            y[:, :, L - 1][b] = (f.view(np.uint32) >> 16).astype(np.uint16)
+    return y
+
+
+def _prepared(inp: W.DecodeInputs, seed: int):
+    """Caches filled from inputs whose new-token rows are stale; the new rows as device tensors."""
+    kvq = _kvq()
+    kc = kvq.empty_cache(inp.head_bits, inp.B, inp.Tcap, inp.D)
+    vc = kvq.empty_cache(inp.head_bits, inp.B, inp.Tcap, inp.D)
+    for c in (kc, vc):
+        c.codes.fill_(0xA5)
+        c.sz.fill_(-1)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lens = [int(x) for x in inp.seq_lens]
+    kvq.quantize(U.to_dev_bf16(_stale_new_rows(inp.k, lens, seed)), kc, 0, status)
+    kvq.quantize(U.to_dev_bf16(_stale_new_rows(inp.v, lens, seed + 1)), vc, 0, status)
+    pos = [min(max(L - 1, 0), inp.Tcap - 1) for L in lens]
+    k_new = np.stack([inp.k[b, :, pos[b]] for b in range(inp.B)])   # [B][Hkv][D]
+    v_new = np.stack([inp.v[b, :, pos[b]] for b in range(inp.B)])
+    return kc, vc, status, k_new, v_new
+
+
+def _check(inp: W.DecodeInputs, kc, vc, out, out_dtype):
+    lens = inp.seq_lens
+    deq = []
+    for cache, x in ((kc, inp.k), (vc, inp.v)):
+        planes, scale, zero = U.read_cache(cache, inp.Tcap)
+        o_planes, o_scale, o_zero, d = U.oracle_quantize(x, inp.head_bits)
+        for b, L in enumerate(lens):
+            for h in range(inp.Hkv):
+                assert np.array_equal(planes[h][b, :L], o_planes[h][b, :L]), (b, h)
+            assert np.array_equal(scale[b, :, :L].view(np.uint16), o_scale[b, :, :L].view(np.uint16)), b
+            assert np.array_equal(zero[b, :, :L].view(np.uint16), o_zero[b, :, :L].view(np.uint16)), b
+        deq.append(d)
+    ref = O.decode_attention(inp.q, deq[0], deq[1], lens, inp.softmax_scale)
+    return U.assert_close(out, ref, inp.name, out_bf16=out_dtype == 1)
+
+
+STEP_CASES = [
+    # name, seed, B, Hq, Hkv, D, Tcap, lens, bits, out_dtype
+    ("step_int8_ragged", 31, 3, 8, 2, 128, 640, [640, 65, 1], "8", 0),
+    ("step_mixed_bf16", 32, 2, 16, 4, 128, 512, [300, 512], "mixed", 1),
+    ("step_d64_int4", 33, 4, 8, 4, 64, 256, [2, 64, 129, 256], "4", 0),
+]
+
+
+@pytest.mark.parametrize("case", STEP_CASES, ids=[c[0] for c in STEP_CASES])
+def test_decode_step_parity(case):
+    name, seed, B, Hq, Hkv, D, Tcap, lens, bits, out_dtype = case
+    kvq = _kvq()
+    inp = W.make_decode(name, seed, B, Hq, Hkv, D, Tcap, lens=lens, bits=bits,
+                        outliers_per_head=2, outlier_head_mult=8.0)
+    kc, vc, status, k_new, v_new = _prepared(inp, seed)
+    sl = torch.from_numpy(inp.seq_lens).cuda()
+    out = kvq.decode_step(U.to_dev_bf16(inp.q), U.to_dev_bf16(k_new), U.to_dev_bf16(v_new), kc, vc, sl,
+                          inp.softmax_scale, out_dtype=out_dtype, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    _check(inp, kc, vc, out.float().cpu().numpy(), out_dtype)
+
+
+@pytest.mark.parametrize("out_dtype,pinned", [(0, True), (1, True), (0, False), (1, False)],
+                         ids=["f32_pinned", "bf16_pinned", "f32_pageable", "bf16_pageable"])
+def test_decode_step_host_parity(out_dtype, pinned):
+    """Pinned buffers take the in-place path (no copy calls), pageable ones the staged copies."""
+    kvq = _kvq()
+    inp = W.make_decode("step_host", 34, 3, 8, 2, 128, 384, lens=[384, 200, 7], bits="mixed",
+                        outliers_per_head=2, outlier_head_mult=8.0)
+    kc, vc, status, k_new, v_new = _prepared(inp, 34)
+    host = (lambda t: t.pin_memory()) if pinned else (lambda t: t.clone())
+    pin = lambda a: host(torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16))
+    h_q, h_k, h_v = pin(inp.q), pin(k_new), pin(v_new)
+    h_out = host(torch.full((inp.B, inp.Hq, inp.D), 7.0, dtype=torch.float32 if out_dtype == 0 else torch.bfloat16))
+    sl = torch.from_numpy(inp.seq_lens).cuda()
+    kvq.decode_step_host(h_q, h_k, h_v, kc, vc, sl, h_out, inp.softmax_scale, out_dtype=out_dtype, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    _check(inp, kc, vc, h_out.float().numpy(), out_dtype)
+
+
+def test_decode_step_consecutive_steps():
+    """Five steps in a row, each appending one token per sequence: every step
+    must see the tokens the earlier steps appended."""
+    kvq = _kvq()
+    T_final = [70, 129, 5]
+    inp = W.make_decode("step_seq", 35, 3, 8, 2, 128, 192, lens=T_final, bits="8",
+                        outliers_per_head=2, outlier_head_mult=8.0)
+    B, Hq, Hkv, D = inp.B, inp.Hq, inp.Hkv, inp.D
+    kc = kvq.empty_cache(inp.head_bits, B, inp.Tcap, D)
+    vc = kvq.empty_cache(inp.head_bits, B, inp.Tcap, D)
+    for c in (kc, vc):
+        c.codes.fill_(0xA5)
+        c.sz.fill_(-1)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    n_steps = 5
+    start = [L - n_steps for L in T_final]
+    pre_k, pre_v = inp.k.copy(), inp.v.copy()
+    for b, L0 in enumerate(start):
+        pre_k[b, :, L0:] = 0
+        pre_v[b, :, L0:] = 0
+    kvq.quantize(U.to_dev_bf16(pre_k), kc, 0, status)
+    kvq.quantize(U.to_dev_bf16(pre_v), vc, 0, status)
+    ws = kvq.decode_workspace(B, Hq, Hkv, D, "cuda")
+    rng = np.random.default_rng(36)
+    deq_k = U.oracle_quantize(inp.k, inp.head_bits)[3]
+    deq_v = U.oracle_quantize(inp.v, inp.head_bits)[3]
+    for s in range(n_steps):
+        lens = np.array([L0 + s + 1 for L0 in start], dtype=np.int32)
+        k_new = np.stack([inp.k[b, :, lens[b] - 1] for b in range(B)])
+        v_new = np.stack([inp.v[b, :, lens[b] - 1] for b in range(B)])
+        q = W._draw_bf16(rng, (B, Hq, D))
+        out = kvq.decode_step(U.to_dev_bf16(q), U.to_dev_bf16(k_new), U.to_dev_bf16(v_new), kc, vc,
+                              torch.from_numpy(lens).cuda(), inp.softmax_scale, workspace=ws, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        ref = O.decode_attention(q, deq_k, deq_v, lens, inp.softmax_scale)
+        U.assert_close(out.cpu().numpy(), ref, f"step {s}")
+    _check(W.DecodeInputs(inp.name, q, inp.k, inp.v, np.array(T_final, np.int32), inp.head_bits,
+                          inp.softmax_scale, Hq, Hkv, D, inp.Tcap), kc, vc, out.cpu().numpy(), 0)
+
+
+def test_decode_step_reports_invalid_length_and_appends_the_rest():
+    kvq = _kvq()
+    inp = W.make_decode("step_bad_len", 37, 3, 4, 1, 128, 128, lens=[128, 40, 0], bits="8")
+    kc, vc, status, k_new, v_new = _prepared(inp, 37)
+    codes_before = kc.codes.clone()
+    sl = torch.tensor([128, 40, 0], dtype=torch.int32, device="cuda")
+    out = kvq.decode_step(U.to_dev_bf16(inp.q), U.to_dev_bf16(k_new), U.to_dev_bf16(v_new), kc, vc, sl,
+                          inp.softmax_scale, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1          # sequence 2 has no position for its new token
+    got = out.cpu().numpy()
+    assert np.all(got[2] == 0.0)            # length 0: zero output row
+    # sequences 0 and 1 were appended and attended normally
+    sub = W.DecodeInputs(inp.name, inp.q[:2], inp.k[:2], inp.v[:2], inp.seq_lens[:2], inp.head_bits,
+                         inp.softmax_scale, inp.Hq, inp.Hkv, inp.D, inp.Tcap)
+    planes, _, _ = U.read_cache(kc, inp.Tcap)
+    o_planes = U.oracle_quantize(inp.k, inp.head_bits)[0]
+    for b, L in ((0, 128), (1, 40)):
+        assert np.array_equal(planes[0][b, :L], o_planes[0][b, :L]), b
+    deq_k = U.oracle_quantize(sub.k, sub.head_bits)[3]
+    deq_v = U.oracle_quantize(sub.v, sub.head_bits)[3]
+    ref = O.decode_attention(sub.q, deq_k, deq_v, sub.seq_lens, sub.softmax_scale)
+    U.assert_close(got[:2], ref, "valid sequences")
+    # sequence 2 wrote nothing anywhere in its plane
+    R = inp.D
+    b2 = kc.codes[2 * inp.Tcap * R:3 * inp.Tcap * R]
+    assert torch.equal(b2, codes_before[2 * inp.Tcap * R:3 * inp.Tcap * R])
+
+
+def test_decode_step_rejects_missing_workspace_without_appending():
+    kvq = _kvq()
+    inp = W.make_decode("step_ws", 38, 1, 4, 1, 128, 128, lens=[100], bits="8")
+    kc, vc, status, k_new, v_new = _prepared(inp, 38)
+    before = kc.codes.clone()
+    ws = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.decode_step(U.to_dev_bf16(inp.q), U.to_dev_bf16(k_new), U.to_dev_bf16(v_new), kc, vc,
+                        torch.from_numpy(inp.seq_lens).cuda(), 0.0, workspace=ws)
+    assert e.value.status == 4
+    torch.cuda.synchronize()
+    assert torch.equal(kc.codes, before)
+
+
+def test_decode_step_host_prepared_call_matches_the_function():
+    """The bound-once call object gives the same bytes as the plain function."""
+    kvq = _kvq()
+    inp = W.make_decode("step_prepared", 39, 2, 8, 2, 128, 256, lens=[256, 90], bits="8",
+                        outliers_per_head=2, outlier_head_mult=8.0)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+    outs = []
+    for use_obj in (False, True):
+        kc, vc, status, k_new, v_new = _prepared(inp, 39)
+        h_q, h_k, h_v = pin(inp.q), pin(k_new), pin(v_new)
+        h_out = torch.zeros((inp.B, inp.Hq, inp.D), dtype=torch.float32).pin_memory()
+        sl = torch.from_numpy(inp.seq_lens).cuda()
+        if use_obj:
+            kvq.DecodeStepHost(h_q, h_k, h_v, sl, h_out, inp.softmax_scale, status=status).run(kc, vc)
+        else:
+            kvq.decode_step_host(h_q, h_k, h_v, kc, vc, sl, h_out, inp.softmax_scale, status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        _check(inp, kc, vc, h_out.numpy(), 0)
+        outs.append(h_out.numpy().copy())
+    assert np.array_equal(outs[0], outs[1])
