@@ -88,6 +88,11 @@ constexpr int kStages = KVQ_DECODE_STAGES;
 #endif
 constexpr int kWarm = KVQ_DECODE_WARM;
 constexpr int kMaxRep = 8;      // query heads per KV head
+// tiles per CTA warmed into L2 before the dependency wait (tunable at build time)
+#ifndef KVQ_DECODE_L2_WARM
+#define KVQ_DECODE_L2_WARM 4
+#endif
+constexpr int kL2Warm = KVQ_DECODE_L2_WARM;
 
 struct DParams {
   CUtensorMap tm_k8, tm_k4, tm_v8, tm_v4;
@@ -588,6 +593,50 @@ __device__ __forceinline__ void consume_tiles(const uint32_t (&st_s)[NT], const 
   }
 }
 
+// Before the dependency wait (one warp): prefetch into L2 the first kL2Warm
+// tiles of this CTA's range, so that the copies issued after the wait find
+// them there while the previous kernel's last CTAs still run.  The lengths
+// read here may be stale -- the previous kernel may still be writing them --
+// but they only choose which lines to prefetch (clamped into the cache), and
+// an L2 prefetch returns nothing to the program, so no result depends on
+// them.  Batches of more than 32 sequences skip the warm-up.
+template <int D>
+__device__ __forceinline__ void warm_l2(const DParams& p, int lane) {
+  constexpr int G = D / 32;
+  if (kL2Warm <= 0 || p.B > 32) return;
+  int len = lane < p.B ? p.seq_lens[lane] : 0;
+  len = min(max(len, 0), p.Tcap);
+  const int n = (len + kTile - 1) / kTile;
+  int incl = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  const int64_t N = static_cast<int64_t>(p.Hkv) * total;
+  const int C = N < p.num_ctas ? static_cast<int>(N) : p.num_ctas;
+  if (N == 0 || static_cast<int>(blockIdx.x) >= C) return;
+  const int64_t f0 = N * blockIdx.x / C, f1 = N * (blockIdx.x + 1) / C;
+  const int64_t f = f0 + lane;   // this lane's tile
+  // its sequence: the number of sequences ending at or before f
+  int b = 0;
+  for (int s = 0; s < p.B; ++s) b += static_cast<int64_t>(p.Hkv) * __shfl_sync(0xffffffffu, incl, s) <= f ? 1 : 0;
+  const int bs = min(b, p.B - 1);
+  const int nb = __shfl_sync(0xffffffffu, n, bs);
+  const int eb = __shfl_sync(0xffffffffu, incl, bs) - nb;
+  if (lane >= kL2Warm || f >= f1 || b >= p.B || nb == 0) return;
+  const int64_t off = f - static_cast<int64_t>(p.Hkv) * eb;
+  const int kvh = static_cast<int>(off / nb), i = static_cast<int>(off % nb);
+  const int bits = p.bits[kvh];
+  const int32_t row0 = (p.plane[kvh] * p.B + bs) * p.Tcap + i * kTile;
+  const int64_t szoff = (static_cast<int64_t>(kvh) * p.B + bs) * p.Tcap + static_cast<int64_t>(i) * kTile;
+  prefetch_l2_tile_2d(bits == 8 ? &p.tm_k8 : &p.tm_k4, 0, row0);
+  prefetch_l2_tile_2d(bits == 8 ? &p.tm_v8 : &p.tm_v4, 0, row0);
+  prefetch_l2_bulk(p.k_sz + szoff * G, Smem<D>::kSzBytes);
+  prefetch_l2_bulk(p.v_sz + szoff * G, Smem<D>::kSzBytes);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_kernel(const __grid_constant__ DParams p) {
   using L = Smem<D>;
@@ -625,9 +674,11 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
     prefetch_tmap(&p.tm_k4);
     prefetch_tmap(&p.tm_v4);
   }
+  if (w == kWarps) warm_l2<D>(p, lane);
   // With programmatic dependent launch this kernel may start while the
   // previous kernel in the stream is finishing: wait for it (and its memory)
-  // before the first global access, then let the next one start early.
+  // before the first global access whose data is used, then let the next one
+  // start early.
   grid_dependency_wait();
   grid_launch_dependents();
   for (int b = tid; b < B; b += blockDim.x) {
