@@ -90,7 +90,7 @@ constexpr int kWarm = KVQ_DECODE_WARM;
 constexpr int kMaxRep = 8;      // query heads per KV head
 // tiles per CTA warmed into L2 before the dependency wait (tunable at build time)
 #ifndef KVQ_DECODE_L2_WARM
-#define KVQ_DECODE_L2_WARM 4
+#define KVQ_DECODE_L2_WARM 5
 #endif
 constexpr int kL2Warm = KVQ_DECODE_L2_WARM;
 
@@ -464,16 +464,14 @@ __device__ __forceinline__ void segment_end(const DParams& p, const EpiBuf<D>* e
   if (epi_empty != nullptr || !whole) sync();   // the group's reads of eb / stores are done
   if (epi_empty != nullptr && tid == 0) mbar_arrive(epi_empty);   // the consumers may refill the buffer
   if (whole) return;
-  // publish the piece and count the arrivals: after the group barrier, the
-  // leader's fence orders every member's partial stores (fences are
-  // cumulative) before its atomic; the last arriver's second fence orders the
-  // other pieces before the group's reads below
+  // publish the piece and count the arrivals with one acquire-release
+  // atomic: after the group barrier its release orders every member's partial
+  // stores (release is cumulative) before the count, and for the last
+  // arriver its acquire orders the other pieces' stores, released by their
+  // own arrivals, before the group's reads below
   if (tid == 0) {
     const int np = c1 - c0 + 1;   // every split CTA owns at least one tile
-    __threadfence();
-    const int last = (atomicAdd(&p.ws_cnt[seg], 1) + 1 == np) ? 1 : 0;
-    if (last) __threadfence();
-    *flag = last;
+    *flag = (atom_add_acq_rel_gpu(p.ws_cnt + seg, 1) + 1 == np) ? 1 : 0;
   }
   sync();
   if (*flag != 1) return;

@@ -87,6 +87,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase, int32_t
   return true;
 }
 
+// atomicAdd with release and acquire semantics at GPU scope: the memory
+// operations before it (including those of other threads ordered before it by
+// a barrier) become visible to whoever reads its result, and the operations
+// after it see everything the earlier adders released.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // ---------------------------------------------------------------------------
 // programmatic dependent launch: no-ops unless the kernel was launched with
 // the programmatic stream serialization attribute
