@@ -184,7 +184,8 @@ def run_reference(args, rank):
     print(json.dumps(line))
 
 
-def time_decode(torch, kvq, inp, dev, l2, steps, warmup, dist=None, keep=False, busy_s=0.0, sampler=None):
+def time_decode(torch, kvq, inp, dev, l2, steps, warmup, dist=None, keep=False, busy_s=0.0, sampler=None,
+                use_graph=True):
     """Back-to-back decode steps over cache copies larger than 3x L2 together.
 
     Returns the total device time of `steps` steps (max over ranks) and the
@@ -228,13 +229,32 @@ def time_decode(torch, kvq, inp, dev, l2, steps, warmup, dist=None, keep=False, 
         for i in range(200):
             step(i)
         torch.cuda.synchronize()
+    # the K timed steps as one CUDA graph (launches captured with their
+    # programmatic-dependency edges), so host launch jitter stays out of the
+    # device time; replayed once untimed first (graph upload)
+    graph = None
+    if use_graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for i in range(steps):
+                    step(i)
+            graph.replay()
+            torch.cuda.synchronize()
+        except Exception as e:   # capture unsupported here: time the eager loop
+            print(f"bench: CUDA graph capture failed ({e}); timing eager launches", file=sys.stderr)
+            graph = None
+            torch.cuda.synchronize()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for i in range(steps):
-        step(i)
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(steps):
+            step(i)
     t1.record(stream)
     torch.cuda.synchronize()
     if dist:
@@ -248,7 +268,8 @@ def time_decode(torch, kvq, inp, dev, l2, steps, warmup, dist=None, keep=False, 
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         t_total = float(tt.item())
     assert int(status.item()) == 0, f"device status {int(status.item())}"
-    res = {"t_total": t_total, "bytes": nbytes, "n_copies": n_copies, "clk": clk}
+    res = {"t_total": t_total, "bytes": nbytes, "n_copies": n_copies, "clk": clk,
+           "timing": "one CUDA graph of the K steps, event-timed" if graph is not None else "eager launches, event-timed"}
     if keep:
         res.update(caches=caches, q=q, sl=sl, ws=ws)
     return res
@@ -359,6 +380,7 @@ def main():
     d = time_decode(torch, kvq, inp, dev, l2, args.steps, args.warmup, dist, keep=True, busy_s=args.busy_seconds,
                     sampler=lambda: ClockSampler(local))
     clk = d["clk"]
+    timing = d["timing"]
     caches, n_copies, q, sl, ws = d["caches"], d["n_copies"], d["q"], d["sl"], d["ws"]
     bytes_per_step = d["bytes"]
     t_total = d["t_total"]
@@ -437,7 +459,8 @@ def main():
                        "bits": [int(b) for b in inp.head_bits],
                        "l2": f"inputs larger than L2: {n_copies} cache copies ({n_copies * bytes_per_step / 1e6:.0f} MB) "
                              "visited in turn, steps back to back",
-                       "per_rank": "each rank decodes its own batch (independent sequences)"},
+                       "per_rank": "each rank decodes its own batch (independent sequences)",
+                       "timing": timing},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                          "kernel": "decode_split_kernel (one launch per step, merge fused)",
