@@ -3,18 +3,43 @@
 // channels per the hook of §3.2).
 //
 // HBM-bound: every input byte is read once and every code/scale byte written
-// once.  Each thread takes 8 consecutive channels (one 16-byte load), four
-// threads form a group of 32 and agree on its range with two shuffles; codes
-// are written as 8 bytes (INT8) or 4 bytes (INT4) per thread, so a warp
-// stores whole contiguous rows.  All arithmetic is IEEE fp32 with explicit
-// rounding intrinsics so the result is bit-identical to the specification.
+// once.  One thread quantises one group of 32 channels on its own: four
+// 16-byte loads, the group's range, one IEEE division for the scale and one
+// correctly rounded reciprocal, then each quotient as x times the reciprocal
+// (exact division only where that product is within 2^-13 of a
+// half-integer, see rne_quotient_fast), and one 32-byte (INT8) or 16-byte
+// (INT4) store of codes; a warp's stores cover whole contiguous rows.  The
+// result is bit-identical to the specification's IEEE fp32 arithmetic.
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
 namespace kvq {
 namespace {
 
+// Division of 32-bit unsigned numerators by a divisor fixed for the launch
+// (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994, the round-up multiplier of their Figure 4.1):
+// with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+//   q = (t + ((n - t) >> 1)) >> (l - 1),  t = mulhi(m, n),   for d >= 2.
+struct FastDiv {
+  uint32_t d, m, l;
+  static FastDiv make(uint32_t d) {
+    FastDiv f;
+    f.d = d;
+    f.l = 0;
+    while ((uint64_t(1) << f.l) < d) ++f.l;
+    f.m = d <= 1 ? 0u : static_cast<uint32_t>(((uint64_t(1) << 32) * ((uint64_t(1) << f.l) - d)) / d + 1);
+    return f;
+  }
+  __device__ __forceinline__ uint32_t div(uint32_t n) const {
+    if (d <= 1) return n;
+    const uint32_t t = __umulhi(m, n);
+    return (t + ((n - t) >> 1)) >> (l - 1);
+  }
+};
+
 struct QParams {
+  FastDiv div_nt, div_hkv;   // row -> (b, h, t): row = (b * Hkv + h) * nt + t
   const uint16_t* x;
   int64_t sx_b, sx_h, sx_t;
   uint8_t* codes;
@@ -28,95 +53,135 @@ struct QParams {
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
 
-// Quantise one row of D channels: this thread holds channels 8*sub .. 8*sub+7
-// (x8, raw bf16), the four threads of a group exchange their range by
-// shuffles (all 32 lanes take part; `store` false skips the writes), and the
-// codes and the group's scale/zero word go to `crow` / `szrow`.
-template <int D>
-__device__ __forceinline__ void quantize_row(const uint4 raw, int sub, int bits, bool store, uint8_t* crow,
-                                             uint32_t* szrow, int32_t* status) {
-  float x[8];
-  x[0] = bf16_bits_to_float(raw.x & 0xFFFFu); x[1] = bf16_bits_to_float(raw.x >> 16);
-  x[2] = bf16_bits_to_float(raw.y & 0xFFFFu); x[3] = bf16_bits_to_float(raw.y >> 16);
-  x[4] = bf16_bits_to_float(raw.z & 0xFFFFu); x[5] = bf16_bits_to_float(raw.z >> 16);
-  x[6] = bf16_bits_to_float(raw.w & 0xFFFFu); x[7] = bf16_bits_to_float(raw.w >> 16);
+// rne(fl(x / s)) -- the IEEE fp32 quotient rounded to the nearest integer,
+// ties to even -- as a float, for |x / s| <= 512 (the quantiser's quotients
+// are within [-qmax, qmax]).  t = fl(x * fl(1/s)) is within 2^-14 of x / s
+// (two roundings of relative size 2^-24 at magnitudes below 2^9) and
+// fl(x / s) within 2^-16 of it, so when t lies more than 2^-13 from every
+// half-integer both round to the same integer.  `near` is set otherwise (and
+// for a NaN quotient); the caller then takes the exact division.
+__device__ __forceinline__ float rne_quotient_fast(float x, float rcp, bool& near) {
+  const float t = __fmul_rn(x, rcp);
+  const float r = rintf(t);
+  near |= !(fabsf(t - r) <= 0.5f - 0x1p-13f);
+  return r;
+}
 
-  bool finite = true;
-  float mn = x[0], mx = x[0];
+// Value i (0..31) of a group held as 16 words of raw bf16 pairs.
+__device__ __forceinline__ float group_value(const uint32_t (&w)[16], int i) {
+  return bf16_bits_to_float((i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu));
+}
+
+// Codes of a group packed for the store: 8-bit, four codes per word (8
+// words); 4-bit, eight codes per word (4 words).  r(i) gives the rounded
+// quotient of value i; codes are clamp(r + zero, 0, qmax).
+template <class R>
+__device__ __forceinline__ void pack_codes(uint32_t (&packed)[8], int bits, float zf, float qf, R r) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    finite &= isfinite(x[i]);
-    mn = fminf(mn, x[i]);
-    mx = fmaxf(mx, x[i]);
+  for (int k = 0; k < 8; ++k) packed[k] = 0u;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint32_t c = static_cast<uint32_t>(fminf(fmaxf(r(i) + zf, 0.0f), qf));
+    if (bits == 8) packed[i >> 2] |= c << (8 * (i & 3));
+    else packed[i >> 3] |= c << (4 * (i & 7));
   }
-  // the four threads of a group share its range
-  mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
-  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-  mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 2));
-  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+}
 
+// Quantise one group of 32 channels (this thread alone): w holds the 32 bf16
+// values as loaded by load_group (64 bytes, 16-byte aligned source), the
+// codes go to cdst (32 bytes for 8-bit, 16 for 4-bit) and the fp16
+// (scale, zero) word to *szw.  The values stay packed as loaded and are
+// widened where used, which keeps the thread's registers few.  Non-finite input:
+// an infinity makes the range, hence the scale, infinite; a NaN is dropped by
+// the min/max but gives a NaN quotient (seen on the exact path) or, in an
+// otherwise all-zero group, is tested directly.
+__device__ __forceinline__ void load_group(uint32_t (&w)[16], const uint16_t* src) {
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    const uint4 raw = reinterpret_cast<const uint4*>(src)[v];
+    w[4 * v] = raw.x; w[4 * v + 1] = raw.y; w[4 * v + 2] = raw.z; w[4 * v + 3] = raw.w;
+  }
+}
+
+__device__ __forceinline__ void quantize_group(const uint32_t (&w)[16], int bits, uint8_t* cdst, uint32_t* szw,
+                                               int32_t* status) {
+  float mn = group_value(w, 0), mx = mn;
+#pragma unroll
+  for (int i = 1; i < 32; ++i) {
+    const float x = group_value(w, i);
+    mn = fminf(mn, x);
+    mx = fmaxf(mx, x);
+  }
   const int qmax = (1 << bits) - 1;
+  const float qf = static_cast<float>(qmax);
   const float lo = fminf(0.0f, mn);
   const float hi = fmaxf(0.0f, mx);
   const float range = __fsub_rn(hi, lo);
 
   __half scale_h = __ushort_as_half(0x3C00);  // 1.0
   int zero = 0;
-  int code[8];
+  uint32_t packed[8];
+  bool bad = false;
   if (range == 0.0f) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) code[i] = 0;
-  } else {
-    scale_h = __float2half_ru(__fdiv_rn(range, static_cast<float>(qmax)));
-    const float sf = __half2float(scale_h);
-    finite &= isfinite(sf);
-    zero = min(max(__float2int_rn(__fdiv_rn(-lo, sf)), 0), qmax);
+    for (int i = 0; i < 32; ++i) {
+      const float x = group_value(w, i);
+      bad |= x != x;
+    }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) code[i] = min(max(__float2int_rn(__fdiv_rn(x[i], sf)) + zero, 0), qmax);
-  }
-  if (!store) return;
-  if (!finite) report(status, KVQ_ERR_NONFINITE);
-
-  if (bits == 8) {
-    uint2 w;
-    w.x = code[0] | (code[1] << 8) | (code[2] << 16) | (code[3] << 24);
-    w.y = code[4] | (code[5] << 8) | (code[6] << 16) | (code[7] << 24);
-    *reinterpret_cast<uint2*>(crow + sub * 8) = w;
+    for (int k = 0; k < 8; ++k) packed[k] = 0u;
   } else {
-    const uint32_t w = code[0] | (code[1] << 4) | (code[2] << 8) | (code[3] << 12) | (code[4] << 16) |
-                       (code[5] << 20) | (code[6] << 24) | (code[7] << 28);
-    *reinterpret_cast<uint32_t*>(crow + sub * 4) = w;
+    scale_h = __float2half_ru(__fdiv_rn(range, qf));
+    const float sf = __half2float(scale_h);
+    bad = !isfinite(sf);
+    const float rcp = __frcp_rn(sf);
+    bool near = false;
+    float zf = fminf(fmaxf(rne_quotient_fast(-lo, rcp, near), 0.0f), qf);
+    pack_codes(packed, bits, zf, qf, [&](int i) { return rne_quotient_fast(group_value(w, i), rcp, near); });
+    if (near) {   // rare: some quotient is within 2^-13 of a half-integer (or NaN): exact division
+      zf = fminf(fmaxf(rintf(__fdiv_rn(-lo, sf)), 0.0f), qf);
+      pack_codes(packed, bits, zf, qf, [&](int i) {
+        const float q = __fdiv_rn(group_value(w, i), sf);
+        bad |= q != q;
+        return rintf(q);
+      });
+    }
+    zero = static_cast<int>(zf);
   }
-  if ((sub & 3) == 0) {
-    const uint32_t zh = __half_as_ushort(__int2half_rn(zero));
-    szrow[sub / 4] = __half_as_ushort(scale_h) | (zh << 16);
-  }
+  if (bad) report(status, KVQ_ERR_NONFINITE);
+  uint4* dst = reinterpret_cast<uint4*>(cdst);
+  dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  if (bits == 8) dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  *szw = __half_as_ushort(scale_h) | (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(zero))) << 16);
 }
 
+// resident blocks of 256 threads per SM the register budget is sized for (tunable at build time)
+#ifndef KVQ_QUANT_MIN_BLOCKS
+#define KVQ_QUANT_MIN_BLOCKS 5
+#endif
+
+// One thread per (row, group): row = (b * Hkv + h) * nt + t.  (A persistent
+// loop that issued the next group's loads before this group's arithmetic
+// measured slower: the extra registers cost more occupancy than it gained.)
 template <int D>
-__global__ void __launch_bounds__(256) quantize_kernel(const __grid_constant__ QParams p) {
-  constexpr int TPR = D / 8;        // threads per row
-  constexpr int RPW = 32 / TPR;     // rows per warp
+__global__ void __launch_bounds__(256, KVQ_QUANT_MIN_BLOCKS) quantize_kernel(const __grid_constant__ QParams p) {
   constexpr int G = D / 32;
-  const int lane = threadIdx.x & 31;
-  const int sub = lane % TPR;
-  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-
-  for (int64_t base = warp * RPW; base < p.rows; base += nwarps * RPW) {
-    const int64_t row = base + lane / TPR;
-    const bool live = row < p.rows;
-    const int64_t r = live ? row : base;  // dead lanes shadow a live row (no stores)
-    const int t = static_cast<int>(r % p.nt);
-    const int64_t bh = r / p.nt;
-    const int h = static_cast<int>(bh % p.Hkv);
-    const int b = static_cast<int>(bh / p.Hkv);
-
-    const uint4 raw = *reinterpret_cast<const uint4*>(p.x + b * p.sx_b + h * p.sx_h + t * p.sx_t + sub * 8);
+  const int64_t n = p.rows * G;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint32_t r = static_cast<uint32_t>(i / G);
+    const int g = static_cast<int>(i % G);
+    const uint32_t bh = p.div_nt.div(r);
+    const int t = static_cast<int>(r - bh * p.div_nt.d);
+    const uint32_t bq = p.div_hkv.div(bh);
+    const int h = static_cast<int>(bh - bq * p.div_hkv.d);
+    const int b = static_cast<int>(bq);
     const int bits = p.bits[h];
     const int64_t pos = static_cast<int64_t>(b) * p.Tcap + p.t0 + t;
-    quantize_row<D>(raw, sub, bits, live, p.codes + p.plane_off[h] + pos * (D * bits / 8),
-                    p.sz + (static_cast<int64_t>(h) * p.B * p.Tcap + pos) * G, p.status);
+    uint32_t w[16];
+    load_group(w, p.x + b * p.sx_b + h * p.sx_h + t * p.sx_t + g * 32);
+    quantize_group(w, bits, p.codes + p.plane_off[h] + pos * (D * bits / 8) + g * (32 * bits / 8),
+                   p.sz + (static_cast<int64_t>(h) * p.B * p.Tcap + pos) * G + g, p.status);
   }
 }
 
@@ -138,36 +203,34 @@ struct AParams {
 
 template <int D>
 __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AParams p) {
-  constexpr int TPR = D / 8;
-  constexpr int RPW = 32 / TPR;
   constexpr int G = D / 32;
   // the decode launched after this kernel may begin its prologue now; it
   // waits for this grid's completion before reading memory
   grid_launch_dependents();
-  const int lane = threadIdx.x & 31;
-  const int sub = lane % TPR;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.q_vec;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     p.q_dst[i] = p.q_src[i];
-  const int64_t rows = 2 * static_cast<int64_t>(p.B) * p.Hkv;
-  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t base = warp * RPW; base < rows; base += nwarps * RPW) {
-    const int64_t row = base + lane / TPR;
-    const bool live = row < rows;
-    const int64_t r = live ? row : base;
-    const int job = static_cast<int>(r / (static_cast<int64_t>(p.B) * p.Hkv));
-    const int64_t bh = r % (static_cast<int64_t>(p.B) * p.Hkv);
+  const int64_t bhn = static_cast<int64_t>(p.B) * p.Hkv;
+  const int64_t n = 2 * bhn * G;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / G;                 // [k rows | v rows] of [b][h]
+    const int g = static_cast<int>(i % G);
+    const int job = static_cast<int>(r / bhn);
+    const int64_t bh = r % bhn;
     const int h = static_cast<int>(bh % p.Hkv);
     const int b = static_cast<int>(bh / p.Hkv);
     const int len = p.seq_lens[b];
-    const bool in_range = len >= 1 && len <= p.Tcap;
-    if (live && !in_range && sub == 0 && job == 0 && h == 0) report(p.status, KVQ_ERR_INVALID_ARG);
-    const uint4 raw = *reinterpret_cast<const uint4*>(p.x[job] + bh * D + sub * 8);
+    if (len < 1 || len > p.Tcap) {
+      if (job == 0 && h == 0 && g == 0) report(p.status, KVQ_ERR_INVALID_ARG);
+      continue;
+    }
     const int bits = p.bits[h];
-    const int64_t pos = static_cast<int64_t>(b) * p.Tcap + (in_range ? len - 1 : 0);
-    quantize_row<D>(raw, sub, bits, live && in_range, p.codes[job] + p.plane_off[h] + pos * (D * bits / 8),
-                    p.sz[job] + (static_cast<int64_t>(h) * p.B * p.Tcap + pos) * G, p.status);
+    const int64_t pos = static_cast<int64_t>(b) * p.Tcap + len - 1;
+    uint32_t w[16];
+    load_group(w, p.x[job] + bh * D + g * 32);
+    quantize_group(w, bits, p.codes[job] + p.plane_off[h] + pos * (D * bits / 8) + g * (32 * bits / 8),
+                   p.sz[job] + (static_cast<int64_t>(h) * p.B * p.Tcap + pos) * G + g, p.status);
   }
 }
 
@@ -180,14 +243,16 @@ cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t stream) {
   p.codes = a.codes; p.sz = a.sz; p.status = a.status;
   p.B = a.B; p.Hkv = a.Hkv; p.Tcap = a.Tcap; p.t0 = a.t0; p.nt = a.nt;
   p.rows = static_cast<int64_t>(a.B) * a.Hkv * a.nt;
+  if (p.rows >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // rows are indexed in 32 bits
+  p.div_nt = FastDiv::make(static_cast<uint32_t>(a.nt));
+  p.div_hkv = FastDiv::make(static_cast<uint32_t>(a.Hkv));
   for (int h = 0; h < KVQ_MAX_HKV; ++h) {
     p.plane_off[h] = a.layout.plane_off[h];
     p.bits[h] = a.layout.bits[h];
   }
   if (p.rows == 0) return cudaSuccess;
-  const int rows_per_block = 256 / (a.D / 8) * 1;  // threads / threads-per-row
-  int64_t blocks = (p.rows + rows_per_block - 1) / rows_per_block;
-  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
+  int64_t blocks = (p.rows * (a.D / 32) + 255) / 256;   // one thread per (row, group)
+  const int64_t cap = int64_t(1) << 30;                   // grid-stride beyond that
   if (blocks > cap) blocks = cap;
   if (a.D == 128) {
     quantize_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
@@ -213,8 +278,7 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
     p.bits[h] = a.layout.bits[h];
   }
   const int64_t rows = 2 * static_cast<int64_t>(a.B) * a.Hkv;
-  const int rows_per_block = 256 / (a.D / 8);
-  int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
+  int64_t blocks = (rows * (a.D / 32) + 255) / 256;   // one thread per (row, group)
   const int64_t qblocks = (p.q_vec + 255) / 256;   // one 16-byte vector per thread
   if (qblocks > blocks) blocks = qblocks;
   const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;

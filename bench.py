@@ -291,6 +291,36 @@ def bench_extra_decodes(torch, kvq, W, peaks, dev, steps, warmup):
     return res
 
 
+def bench_quantize(torch, kvq, inp, peaks, steps, warmup, dev):
+    """kvq_quantize on the decode workload's K tensor ([B][Hkv][T][D] bf16 -> codes + scale/zero words):
+    HBM bytes = bf16 read + codes and words written, two input copies visited in turn (each larger
+    than L2), calls back to back between CUDA events."""
+    import numpy as np
+    B, Hkv, T, D = inp.B, inp.Hkv, inp.Tcap, inp.D
+    x0 = torch.from_numpy(np.ascontiguousarray(inp.k).view(np.int16)).view(torch.bfloat16).to(dev)
+    xs = [x0, x0.clone()]
+    cache = kvq.empty_cache(inp.head_bits, B, T, D, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    rd = x0.numel() * 2
+    wr = sum(B * T * D * int(b) // 8 for b in inp.head_bits) + B * Hkv * T * (D // 32) * 4
+    for i in range(warmup):
+        kvq.quantize(xs[i % 2], cache, 0, status)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        kvq.quantize(xs[i % 2], cache, 0, status)
+    e1.record()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    t = e0.elapsed_time(e1) / 1e3 / steps
+    gbs = (rd + wr) / t / 1e9
+    return {"workload": f"quantize {inp.name} K ({B}x{Hkv}x{T}x{D} bf16)", "value": gbs, "unit": "GB/s",
+            "us_per_call": t * 1e6, "bytes_per_call": int(rd + wr), "read_bytes": int(rd), "write_bytes": int(wr),
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "peak_src": peaks["hbm_src"]}}
+
+
 def bench_prefill(torch, kvq, W, peaks, steps, warmup, dev):
     """Causal prefill workload (quantise K/V + tile-masked attention): TFLOP/s."""
     import numpy as np
@@ -434,6 +464,9 @@ def main():
 
     del caches, d
     torch.cuda.empty_cache()
+    quant = None
+    if rank == 0:
+        quant = bench_quantize(torch, kvq, inp, peaks, max(5, min(args.steps, 20)), 3, dev)
     prefill = None
     if not args.no_prefill and rank == 0:
         prefill = bench_prefill(torch, kvq, W, peaks, max(3, min(args.steps, 10)), 3, dev)
@@ -469,6 +502,7 @@ def main():
             "cpu_baseline": cpu,
             "clocks": clk.summary(),
             "gpu_launches": args.steps,
+            "quantize": quant,
             "prefill": prefill,
             "other_decode_workloads": extras,
         }

@@ -145,15 +145,68 @@ def test_quantize_special_groups_bit_exact():
         assert np.array_equal(zero.view(np.uint16), o_zero.view(np.uint16))
 
 
-def test_quantize_reports_nonfinite():
+def _near_tie_rows(bits: int, n_rows: int = 64, seed: int = 9):
+    """bf16 rows [n][128] whose groups hold quotients x / s exactly on a
+    half-integer (scale 1/16 from a range of 15.9375 (8-bit) or 0.9375
+    (4-bit)) and, from a seeded search, within 2^-13 of one: the cases where
+    a reciprocal-based quotient could round differently from the IEEE
+    division."""
+    qmax = 2 ** bits - 1
+    hi, lo = (8.0, -7.9375) if bits == 8 else (0.5, -0.4375)
+    rows = []
+    ties = np.array([(2 * k + 1) / 32.0 for k in range(-16, 16)], np.float32)
+    ties = ties[(ties <= hi) & (ties >= lo)]
+    g = np.concatenate([[hi, lo], ties, np.zeros(32)])[:32].astype(np.float32)
+    rows.append(np.tile(g, 4))
+    rng = np.random.default_rng(seed)
+    found = []
+    while len(found) < 8 * (n_rows - 1):
+        cand = W.bf16_bits((rng.standard_normal((256, 32)) * rng.uniform(0.1, 50.0)).astype(np.float32))
+        xf = O.bf16_to_f32(cand)
+        _, sc, _ = O.quantize_groups(cand, bits)
+        q = xf / sc.astype(np.float32)                  # IEEE fp32 quotients
+        d = np.abs(q - np.floor(q) - np.float32(0.5))
+        hit = (d <= np.float32(2.0 ** -13)).any(axis=-1)
+        found.extend(xf[hit])
+    rows.extend(np.stack(found[: 4 * (n_rows - 1)]).reshape(n_rows - 1, 128))
+    return W.bf16_bits(np.stack(rows).astype(np.float32))
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_quantize_near_tie_quotients_bit_exact(bits):
+    """Quotients on or next to a half-integer take the kernel's exact-division
+    path; codes must still equal the oracle's bit for bit."""
     kvq = _kvq()
-    x = np.zeros((1, 1, 1, 128), np.float32)
-    x[0, 0, 0, 5] = np.inf
-    c = kvq.empty_cache(np.array([8], np.int8), 1, 64, 128)
+    x = _near_tie_rows(bits)[None, None]            # [1][1][n][128]
+    n = x.shape[2]
+    c = kvq.empty_cache(np.array([bits], np.int8), 1, ((n + 63) // 64) * 64, 128)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    kvq.quantize(U.to_dev_bf16(W.bf16_bits(x)), c, 0, status)
+    kvq.quantize(U.to_dev_bf16(x), c, 0, status)
     torch.cuda.synchronize()
-    assert int(status.item()) == 6
+    assert int(status.item()) == 0
+    planes, scale, zero = U.read_cache(c, n)
+    o_planes, o_scale, o_zero, _ = U.oracle_quantize(x, [bits])
+    assert np.array_equal(planes[0], o_planes[0])
+    assert np.array_equal(scale.view(np.uint16), o_scale.view(np.uint16))
+    assert np.array_equal(zero.view(np.uint16), o_zero.view(np.uint16))
+
+
+@pytest.mark.parametrize("bad,where", [(np.inf, "inf"), (-np.inf, "-inf"), (np.nan, "nan in a live group"),
+                                       (np.nan, "nan in an all-zero group")],
+                         ids=["inf", "neg_inf", "nan_live", "nan_zero_group"])
+def test_quantize_reports_nonfinite(bad, where):
+    kvq = _kvq()
+    rng = np.random.default_rng(5)
+    x = np.zeros((1, 1, 2, 128), np.float32)
+    if where != "nan in an all-zero group":
+        x[0, 0, :] = rng.standard_normal((2, 128))
+    x[0, 0, 1, 37] = bad
+    for bits in (8, 4):
+        c = kvq.empty_cache(np.array([bits], np.int8), 1, 64, 128)
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        kvq.quantize(U.to_dev_bf16(W.bf16_bits(x)), c, 0, status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 6, (where, bits)
 
 
 def test_decode_reports_length_beyond_capacity():
