@@ -5,9 +5,10 @@
 // HBM-bound: every input byte is read once and every code/scale byte written
 // once.  One thread quantises one group of 32 channels on its own: four
 // 16-byte loads, the group's range, one IEEE division for the scale and one
-// correctly rounded reciprocal, then each quotient as x times the reciprocal
-// (exact division only where that product is within 2^-13 of a
-// half-integer, see rne_quotient_fast), and one 32-byte (INT8) or 16-byte
+// correctly rounded reciprocal, then each code from x times the reciprocal,
+// rounded by a 1.5 * 2^23 addend on the FMA pipe rather than the conversion
+// unit (exact division only where that product is within 2^-13 of a
+// half-integer, see code_fast), and one 32-byte (INT8) or 16-byte
 // (INT4) store of codes; a warp's stores cover whole contiguous rows.  The
 // result is bit-identical to the specification's IEEE fp32 arithmetic.
 #include "kvq_device.cuh"
@@ -53,18 +54,28 @@ struct QParams {
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
 
-// rne(fl(x / s)) -- the IEEE fp32 quotient rounded to the nearest integer,
-// ties to even -- as a float, for |x / s| <= 512 (the quantiser's quotients
-// are within [-qmax, qmax]).  t = fl(x * fl(1/s)) is within 2^-14 of x / s
-// (two roundings of relative size 2^-24 at magnitudes below 2^9) and
-// fl(x / s) within 2^-16 of it, so when t lies more than 2^-13 from every
-// half-integer both round to the same integer.  `near` is set otherwise (and
-// for a NaN quotient); the caller then takes the exact division.
-__device__ __forceinline__ float rne_quotient_fast(float x, float rcp, bool& near) {
+// 1.5 * 2^23: adding it to a float of magnitude below 2^22 rounds that value
+// to the nearest integer (ties to even) -- floats in [2^23, 2^24) are spaced
+// 1 apart -- and leaves the integer in the low mantissa bits.
+constexpr float kRoundAdd = 12582912.0f;
+constexpr int kRoundAddBits = 0x4B400000;
+
+// code = clamp(rne(fl(x / s)) + z, 0, qmax) on the fast path, with
+// C = z + 1.5 * 2^23 (z an integer, exact):
+//   t = fl(x * fl(1/s)) is within 2^-14 of x / s (two roundings of relative
+//   size 2^-24 at magnitudes below 2^9) and fl(x / s) within 2^-16 of it;
+//   m = fl(t + C) = C + rne(t + z), the code before clamping in m's low bits;
+//   e = (m - C) - t, exactly the rounding error of t + z.
+// When |e| is more than 2^-13 below 1/2, t + z and fl(x / s) + z lie on the
+// same side of every half-integer, so rne(t + z) = rne(fl(x / s)) + z.
+// Otherwise (and for a NaN quotient) `near` is set and the caller redoes the
+// group with the exact division.
+__device__ __forceinline__ int code_fast(float x, float rcp, float C, int qmax, bool& near) {
   const float t = __fmul_rn(x, rcp);
-  const float r = rintf(t);
-  near |= !(fabsf(t - r) <= 0.5f - 0x1p-13f);
-  return r;
+  const float m = __fadd_rn(t, C);
+  const float e = __fsub_rn(__fsub_rn(m, C), t);
+  near |= !(fabsf(e) <= 0.5f - 0x1p-13f);
+  return min(max(__float_as_int(m) - kRoundAddBits, 0), qmax);
 }
 
 // Value i (0..31) of a group held as 16 words of raw bf16 pairs.
@@ -73,15 +84,14 @@ __device__ __forceinline__ float group_value(const uint32_t (&w)[16], int i) {
 }
 
 // Codes of a group packed for the store: 8-bit, four codes per word (8
-// words); 4-bit, eight codes per word (4 words).  r(i) gives the rounded
-// quotient of value i; codes are clamp(r + zero, 0, qmax).
-template <class R>
-__device__ __forceinline__ void pack_codes(uint32_t (&packed)[8], int bits, float zf, float qf, R r) {
+// words); 4-bit, eight codes per word (4 words).  code(i) gives value i's code.
+template <class F>
+__device__ __forceinline__ void pack_codes(uint32_t (&packed)[8], int bits, F code) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) packed[k] = 0u;
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    const uint32_t c = static_cast<uint32_t>(fminf(fmaxf(r(i) + zf, 0.0f), qf));
+    const uint32_t c = static_cast<uint32_t>(code(i));
     if (bits == 8) packed[i >> 2] |= c << (8 * (i & 3));
     else packed[i >> 3] |= c << (4 * (i & 7));
   }
@@ -105,13 +115,16 @@ __device__ __forceinline__ void load_group(uint32_t (&w)[16], const uint16_t* sr
 
 __device__ __forceinline__ void quantize_group(const uint32_t (&w)[16], int bits, uint8_t* cdst, uint32_t* szw,
                                                int32_t* status) {
-  float mn = group_value(w, 0), mx = mn;
+  // min and max over the 32 values in bf16 pairs (exact), then the two lanes
+  __nv_bfloat162 mn2 = *reinterpret_cast<const __nv_bfloat162*>(&w[0]), mx2 = mn2;
 #pragma unroll
-  for (int i = 1; i < 32; ++i) {
-    const float x = group_value(w, i);
-    mn = fminf(mn, x);
-    mx = fmaxf(mx, x);
+  for (int k = 1; k < 16; ++k) {
+    const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+    mn2 = __hmin2(mn2, v);
+    mx2 = __hmax2(mx2, v);
   }
+  const float mn = fminf(__low2float(mn2), __high2float(mn2));
+  const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
   const int qmax = (1 << bits) - 1;
   const float qf = static_cast<float>(qmax);
   const float lo = fminf(0.0f, mn);
@@ -135,18 +148,19 @@ __device__ __forceinline__ void quantize_group(const uint32_t (&w)[16], int bits
     const float sf = __half2float(scale_h);
     bad = !isfinite(sf);
     const float rcp = __frcp_rn(sf);
+    // zero point: one exact quotient per group
+    const float zf = fminf(fmaxf(rintf(__fdiv_rn(-lo, sf)), 0.0f), qf);
+    zero = static_cast<int>(zf);
+    const float C = zf + kRoundAdd;   // exact
     bool near = false;
-    float zf = fminf(fmaxf(rne_quotient_fast(-lo, rcp, near), 0.0f), qf);
-    pack_codes(packed, bits, zf, qf, [&](int i) { return rne_quotient_fast(group_value(w, i), rcp, near); });
+    pack_codes(packed, bits, [&](int i) { return code_fast(group_value(w, i), rcp, C, qmax, near); });
     if (near) {   // rare: some quotient is within 2^-13 of a half-integer (or NaN): exact division
-      zf = fminf(fmaxf(rintf(__fdiv_rn(-lo, sf)), 0.0f), qf);
-      pack_codes(packed, bits, zf, qf, [&](int i) {
+      pack_codes(packed, bits, [&](int i) {
         const float q = __fdiv_rn(group_value(w, i), sf);
         bad |= q != q;
-        return rintf(q);
+        return static_cast<int>(fminf(fmaxf(rintf(q) + zf, 0.0f), qf));
       });
     }
-    zero = static_cast<int>(zf);
   }
   if (bad) report(status, KVQ_ERR_NONFINITE);
   uint4* dst = reinterpret_cast<uint4*>(cdst);
