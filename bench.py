@@ -146,6 +146,20 @@ def _oracle_subprocess(workload: str, seconds: float):
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
+def max_over_ranks(torch, dist, value: float, device) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    if not dist:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_step: int, world: int, steps: int, t_max: float) -> float:
+    """Whole-job GB/s: every rank moves bytes_per_step per step (weak scaling)."""
+    return bytes_per_step * world * steps / t_max / 1e9
+
+
 def decode_bytes(inp) -> int:
     D = inp.D
     tot = 0
@@ -262,11 +276,7 @@ def time_decode(torch, kvq, inp, dev, l2, steps, warmup, dist=None, keep=False, 
     torch.cuda.synchronize()
     if clk:
         clk.__exit__(None, None, None)
-    t_total = t0.elapsed_time(t1) / 1e3
-    if dist:
-        tt = torch.tensor([t_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_total = float(tt.item())
+    t_total = max_over_ranks(torch, dist, t0.elapsed_time(t1) / 1e3, dev)
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     res = {"t_total": t_total, "bytes": nbytes, "n_copies": n_copies, "clk": clk,
            "timing": "one CUDA graph of the K steps, event-timed" if graph is not None else "eager launches, event-timed"}
@@ -414,7 +424,7 @@ def main():
     caches, n_copies, q, sl, ws = d["caches"], d["n_copies"], d["q"], d["sl"], d["ws"]
     bytes_per_step = d["bytes"]
     t_total = d["t_total"]
-    value = bytes_per_step * world * args.steps / t_total / 1e9
+    value = job_gbs(bytes_per_step, world, args.steps, t_total)
     avg = t_total / args.steps
     achieved = bytes_per_step / avg / 1e9
     stream = torch.cuda.current_stream()
@@ -449,12 +459,8 @@ def main():
             e1.record(stream)
             e1.synchronize()          # the step's result is read back before the next step
             et.append(e0.elapsed_time(e1) / 1e3)
-        te = sum(et)
-        if dist:
-            tt = torch.tensor([te], dtype=torch.float64, device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            te = float(tt.item())
-        e2e = {"value": bytes_per_step * world * args.steps / te / 1e9, "unit": "GB/s",
+        te = max_over_ranks(torch, dist, sum(et), dev)
+        e2e = {"value": job_gbs(bytes_per_step, world, args.steps, te), "unit": "GB/s",
                "h2d_bytes_per_step": int(h_q.numel() * 2 + h_k.numel() * 2 + h_v.numel() * 2),
                "d2h_bytes_per_step": int(h_out.numel() * 2),
                "ms_per_step": te / args.steps * 1e3,
