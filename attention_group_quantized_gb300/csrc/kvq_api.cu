@@ -151,15 +151,26 @@ static bool same_cache_shape(const kvq_cache& a, const kvq_cache& b) {
   return true;
 }
 
-kvq_status kvq_decode_attention(const void* q, const kvq_cache* k, const kvq_cache* v, const int32_t* seq_lens,
-                                int32_t Hq, float softmax_scale, void* out, int32_t out_dtype, void* workspace,
-                                size_t workspace_bytes, int32_t* dev_status, void* stream) {
+}  // extern "C"
+
+// A block table's checks: the caches are page pools of 64-token pages.
+static bool table_ok(const kvq_block_table* t, const kvq_cache& pool) {
+  return t != nullptr && t->pages != nullptr && (reinterpret_cast<uintptr_t>(t->pages) & 3u) == 0 && t->B > 0 &&
+         t->max_pages > 0 && pool.Tcap == KVQ_TILE_TOKENS &&
+         static_cast<int64_t>(t->max_pages) * KVQ_TILE_TOKENS < (int64_t(1) << 31);
+}
+
+// Decode over contiguous caches (table == nullptr) or page pools.
+static kvq_status decode_impl(const void* q, const kvq_cache* k, const kvq_cache* v, const kvq_block_table* table,
+                              const int32_t* seq_lens, int32_t Hq, float softmax_scale, void* out, int32_t out_dtype,
+                              void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
   if (q == nullptr || k == nullptr || v == nullptr || seq_lens == nullptr || out == nullptr)
     return KVQ_ERR_INVALID_ARG;
   if (k->codes == nullptr || k->sz == nullptr || v->codes == nullptr || v->sz == nullptr) return KVQ_ERR_INVALID_ARG;
   if (k->D > 0 && k->D != 64 && k->D != 128) return KVQ_ERR_UNSUPPORTED;
   DecodeArgs a;
   if (!resolve_layout(*k, &a.layout) || !same_cache_shape(*k, *v)) return KVQ_ERR_INVALID_ARG;
+  if (table != nullptr && !table_ok(table, *k)) return KVQ_ERR_INVALID_ARG;
   if (Hq <= 0 || Hq % k->Hkv) return KVQ_ERR_INVALID_ARG;
   if (Hq / k->Hkv > 8) return KVQ_ERR_UNSUPPORTED;
   if (out_dtype != KVQ_OUT_F32 && out_dtype != KVQ_OUT_BF16) return KVQ_ERR_INVALID_ARG;
@@ -180,7 +191,55 @@ kvq_status kvq_decode_attention(const void* q, const kvq_cache* k, const kvq_cac
   a.ws = workspace;
   a.ws_bytes = workspace_bytes;
   a.status = dev_status;
+  if (table != nullptr) {
+    a.bt = table->pages;
+    a.bt_B = table->B;
+    a.bt_max_pages = table->max_pages;
+  }
   return launch_decode(a, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" {
+
+kvq_status kvq_decode_attention(const void* q, const kvq_cache* k, const kvq_cache* v, const int32_t* seq_lens,
+                                int32_t Hq, float softmax_scale, void* out, int32_t out_dtype, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return decode_impl(q, k, v, nullptr, seq_lens, Hq, softmax_scale, out, out_dtype, workspace, workspace_bytes,
+                     dev_status, stream);
+}
+
+kvq_status kvq_decode_attention_paged(const void* q, const kvq_cache* k_pool, const kvq_cache* v_pool,
+                                      const kvq_block_table* table, const int32_t* seq_lens, int32_t Hq,
+                                      float softmax_scale, void* out, int32_t out_dtype, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (table == nullptr) return KVQ_ERR_INVALID_ARG;
+  return decode_impl(q, k_pool, v_pool, table, seq_lens, Hq, softmax_scale, out, out_dtype, workspace,
+                     workspace_bytes, dev_status, stream);
+}
+
+kvq_status kvq_quantize_paged(const void* x, int64_t sx_b, int64_t sx_h, int64_t sx_t, int32_t t0, int32_t nt,
+                              const kvq_cache* pool, const kvq_block_table* table, int32_t* dev_status,
+                              void* stream) {
+  if (pool == nullptr || x == nullptr || pool->codes == nullptr || pool->sz == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (pool->D != 64 && pool->D != 128 && pool->D > 0) return KVQ_ERR_UNSUPPORTED;
+  QuantizeArgs a;
+  if (!resolve_layout(*pool, &a.layout) || !table_ok(table, *pool)) return KVQ_ERR_INVALID_ARG;
+  if (t0 < 0 || nt < 0 || static_cast<int64_t>(t0) + nt > static_cast<int64_t>(table->max_pages) * KVQ_TILE_TOKENS)
+    return KVQ_ERR_INVALID_ARG;
+  if (sx_b < 0 || sx_h < 0 || sx_t < 0) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(x) || (sx_b % 8) || (sx_h % 8) || (sx_t % 8)) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(pool->codes) || !aligned16(pool->sz)) return KVQ_ERR_INVALID_ARG;
+  if (nt == 0) return KVQ_OK;
+  a.x = static_cast<const uint16_t*>(x);
+  a.sx_b = sx_b; a.sx_h = sx_h; a.sx_t = sx_t;
+  a.t0 = t0; a.nt = nt;
+  a.codes = pool->codes; a.sz = pool->sz;
+  a.B = pool->B; a.Hkv = pool->Hkv; a.Tcap = pool->Tcap; a.D = pool->D;
+  a.status = dev_status;
+  a.bt = table->pages;
+  a.bt_B = table->B;
+  a.bt_max_pages = table->max_pages;
+  return launch_quantize(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
 }  // extern "C"
@@ -189,9 +248,9 @@ kvq_status kvq_decode_attention(const void* q, const kvq_cache* k, const kvq_cac
 // from q_src (any device-visible memory) to q, the decode's query buffer.
 static kvq_status decode_step_impl(const void* q, const void* q_src, size_t q_bytes, const void* k_new,
                                    const void* v_new, const kvq_cache* k, const kvq_cache* v,
-                                   const int32_t* seq_lens, int32_t Hq, float softmax_scale, void* out,
-                                   int32_t out_dtype, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                                   void* stream) {
+                                   const kvq_block_table* table, const int32_t* seq_lens, int32_t Hq,
+                                   float softmax_scale, void* out, int32_t out_dtype, void* workspace,
+                                   size_t workspace_bytes, int32_t* dev_status, void* stream) {
   if (k_new == nullptr || v_new == nullptr) return KVQ_ERR_INVALID_ARG;
   if (!aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_INVALID_ARG;
   // every check of the decode call first, so that nothing is appended unless both launches are valid
@@ -201,6 +260,7 @@ static kvq_status decode_step_impl(const void* q, const void* q_src, size_t q_by
   if (k->D > 0 && k->D != 64 && k->D != 128) return KVQ_ERR_UNSUPPORTED;
   AppendArgs a;
   if (!resolve_layout(*k, &a.layout) || !same_cache_shape(*k, *v)) return KVQ_ERR_INVALID_ARG;
+  if (table != nullptr && !table_ok(table, *k)) return KVQ_ERR_INVALID_ARG;
   if (Hq <= 0 || Hq % k->Hkv) return KVQ_ERR_INVALID_ARG;
   if (Hq / k->Hkv > 8) return KVQ_ERR_UNSUPPORTED;
   if (out_dtype != KVQ_OUT_F32 && out_dtype != KVQ_OUT_BF16) return KVQ_ERR_INVALID_ARG;
@@ -208,8 +268,9 @@ static kvq_status decode_step_impl(const void* q, const void* q_src, size_t q_by
       !aligned16(out) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
     return KVQ_ERR_INVALID_ARG;
   if (static_cast<int64_t>(k->Hkv) * k->B * k->Tcap >= (int64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
-  if (k->B > 4096) return KVQ_ERR_UNSUPPORTED;   // the decode kernel's shared memory holds up to 4096 lengths
-  const size_t need = kvq_decode_workspace_bytes(k->B, Hq, k->Hkv, k->D);
+  const int nseq = table != nullptr ? table->B : k->B;
+  if (nseq > 4096) return KVQ_ERR_UNSUPPORTED;   // the decode kernel's shared memory holds up to 4096 lengths
+  const size_t need = kvq_decode_workspace_bytes(nseq, Hq, k->Hkv, k->D);
   if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)) return KVQ_ERR_WORKSPACE;
   if (q_src != nullptr && (!aligned16(q_src) || (q_bytes & 15u))) return KVQ_ERR_INVALID_ARG;
   a.q_src = q_src;
@@ -222,9 +283,14 @@ static kvq_status decode_step_impl(const void* q, const void* q_src, size_t q_by
   a.seq_lens = seq_lens;
   a.B = k->B; a.Hkv = k->Hkv; a.Tcap = k->Tcap; a.D = k->D;
   a.status = dev_status;
+  if (table != nullptr) {
+    a.bt = table->pages;
+    a.bt_B = table->B;
+    a.bt_max_pages = table->max_pages;
+  }
   if (launch_append(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
-  return kvq_decode_attention(q, k, v, seq_lens, Hq, softmax_scale, out, out_dtype, workspace, workspace_bytes,
-                              dev_status, stream);
+  return decode_impl(q, k, v, table, seq_lens, Hq, softmax_scale, out, out_dtype, workspace, workspace_bytes,
+                     dev_status, stream);
 }
 
 extern "C" {
@@ -233,8 +299,17 @@ kvq_status kvq_decode_step(const void* q, const void* k_new, const void* v_new, 
                            const kvq_cache* v, const int32_t* seq_lens, int32_t Hq, float softmax_scale, void* out,
                            int32_t out_dtype, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                            void* stream) {
-  return decode_step_impl(q, nullptr, 0, k_new, v_new, k, v, seq_lens, Hq, softmax_scale, out, out_dtype, workspace,
-                          workspace_bytes, dev_status, stream);
+  return decode_step_impl(q, nullptr, 0, k_new, v_new, k, v, nullptr, seq_lens, Hq, softmax_scale, out, out_dtype,
+                          workspace, workspace_bytes, dev_status, stream);
+}
+
+kvq_status kvq_decode_step_paged(const void* q, const void* k_new, const void* v_new, const kvq_cache* k_pool,
+                                 const kvq_cache* v_pool, const kvq_block_table* table, const int32_t* seq_lens,
+                                 int32_t Hq, float softmax_scale, void* out, int32_t out_dtype, void* workspace,
+                                 size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (table == nullptr) return KVQ_ERR_INVALID_ARG;
+  return decode_step_impl(q, nullptr, 0, k_new, v_new, k_pool, v_pool, table, seq_lens, Hq, softmax_scale, out,
+                          out_dtype, workspace, workspace_bytes, dev_status, stream);
 }
 
 static size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -286,15 +361,15 @@ kvq_status kvq_decode_step_host(const void* q_host, const void* k_new_host, cons
   void* p_v = p_k ? pinned_device_view(v_new_host) : nullptr;
   void* p_o = p_v ? pinned_device_view(out_host) : nullptr;
   if (p_o != nullptr && aligned16(p_q) && aligned16(p_k) && aligned16(p_v) && aligned16(p_o))
-    return decode_step_impl(d_q, p_q, qb, p_k, p_v, k, v, seq_lens, Hq, softmax_scale, p_o, out_dtype, workspace,
-                            workspace_bytes, dev_status, stream);
+    return decode_step_impl(d_q, p_q, qb, p_k, p_v, k, v, nullptr, seq_lens, Hq, softmax_scale, p_o, out_dtype,
+                            workspace, workspace_bytes, dev_status, stream);
   // pageable memory: asynchronous copies through the staging buffer
   if (cudaMemcpyAsync(d_q, q_host, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(d_k, k_new_host, kvb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(d_v, v_new_host, kvb, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return KVQ_ERR_CUDA;
-  const kvq_status r = decode_step_impl(d_q, nullptr, 0, d_k, d_v, k, v, seq_lens, Hq, softmax_scale, d_o, out_dtype,
-                                        workspace, workspace_bytes, dev_status, stream);
+  const kvq_status r = decode_step_impl(d_q, nullptr, 0, d_k, d_v, k, v, nullptr, seq_lens, Hq, softmax_scale, d_o,
+                                        out_dtype, workspace, workspace_bytes, dev_status, stream);
   if (r != KVQ_OK) return r;
   return cudaMemcpyAsync(out_host, d_o, ob, cudaMemcpyDeviceToHost, s) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

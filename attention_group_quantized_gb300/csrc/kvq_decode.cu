@@ -106,7 +106,12 @@ struct DParams {
   void* out;
   int32_t* status;
   int32_t out_dtype;
-  int32_t B, Hq, Hkv, Tcap, rep, num_ctas;
+  int32_t B, Hq, Hkv, Tcap, rep, num_ctas;   // B sequences, Tcap tokens each at most
+  // where a tile lives: without a block table, sequence b's tile i is row
+  // (plane * pB + b) * pT + 64 i of the code planes (pB = B, pT = Tcap); with
+  // one, it is page bt[b * bt_stride + i] of a pool of pB pages of pT = 64
+  const int32_t* bt;
+  int32_t bt_stride, pB, pT;
   float scale_log2;
   int32_t plane[KVQ_MAX_HKV];
   int8_t bits[KVQ_MAX_HKV];
@@ -627,8 +632,13 @@ __device__ __forceinline__ void warm_l2(const DParams& p, int lane) {
   const int64_t off = f - static_cast<int64_t>(p.Hkv) * eb;
   const int kvh = static_cast<int>(off / nb), i = static_cast<int>(off % nb);
   const int bits = p.bits[kvh];
-  const int32_t row0 = (p.plane[kvh] * p.B + bs) * p.Tcap + i * kTile;
-  const int64_t szoff = (static_cast<int64_t>(kvh) * p.B + bs) * p.Tcap + static_cast<int64_t>(i) * kTile;
+  int pb = bs, pt = i * kTile;
+  if (p.bt != nullptr) {   // (a stale or bad page id only misdirects this prefetch)
+    pb = min(max(p.bt[static_cast<int64_t>(bs) * p.bt_stride + i], 0), p.pB - 1);
+    pt = 0;
+  }
+  const int32_t row0 = (p.plane[kvh] * p.pB + pb) * p.pT + pt;
+  const int64_t szoff = (static_cast<int64_t>(kvh) * p.pB + pb) * p.pT + pt;
   prefetch_l2_tile_2d(bits == 8 ? &p.tm_k8 : &p.tm_k4, 0, row0);
   prefetch_l2_tile_2d(bits == 8 ? &p.tm_v8 : &p.tm_v4, 0, row0);
   prefetch_l2_bulk(p.k_sz + szoff * G, Smem<D>::kSzBytes);
@@ -730,6 +740,18 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
       if (lane != 0) return;
       const uint64_t pol = l2_evict_first_policy();   // the cache is streamed once per call
       Cursor pc = locate(f0, pre, B, Hkv);
+      // paged caches: the page ids are loaded kStages tiles ahead of their
+      // copies (a ring of registers), so the lookups overlap the stage waits
+      Cursor pa = pc;
+      int pg[kStages];
+#pragma unroll
+      for (int j = 0; j < kStages; ++j) {
+        pg[j] = 0;
+        if (p.bt != nullptr && j < ntiles) {
+          pg[j] = p.bt[static_cast<int64_t>(pa.b) * p.bt_stride + pa.i];
+          advance(pa, pre, B, Hkv);
+        }
+      }
       for (int k = 0; k < ntiles; ++k) {
         const int slot = k % kStages;
         if (k >= kStages && !mbar_wait(&empty[slot], ((k / kStages) - 1) & 1, p.status)) return;
@@ -738,9 +760,24 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
         uint8_t* st = smem + slot * L::kStageBytes;
         const int bits = p.bits[pc.kvh];
         const int R = D * bits / 8;
-        const int32_t row0 = (p.plane[pc.kvh] * B + pc.b) * p.Tcap + pc.i * kTile;
-        const int64_t szoff =
-            (static_cast<int64_t>(pc.kvh) * B + pc.b) * p.Tcap + static_cast<int64_t>(pc.i) * kTile;
+        int pb = pc.b, pt = pc.i * kTile;
+        if (p.bt != nullptr) {
+          pb = pg[0];
+#pragma unroll
+          for (int j = 0; j + 1 < kStages; ++j) pg[j] = pg[j + 1];
+          pg[kStages - 1] = 0;
+          if (k + kStages < ntiles) {
+            pg[kStages - 1] = p.bt[static_cast<int64_t>(pa.b) * p.bt_stride + pa.i];
+            advance(pa, pre, B, Hkv);
+          }
+          if (pb < 0 || pb >= p.pB) {   // a page outside the pool: report, read page 0 instead
+            report(p.status, KVQ_ERR_INVALID_ARG);
+            pb = 0;
+          }
+          pt = 0;
+        }
+        const int32_t row0 = (p.plane[pc.kvh] * p.pB + pb) * p.pT + pt;
+        const int64_t szoff = (static_cast<int64_t>(pc.kvh) * p.pB + pb) * p.pT + pt;
         uint64_t* bar = &full[slot];
         const bool first = pc.i == 0 || k == 0;
         const uint32_t qbytes = first ? static_cast<uint32_t>(p.rep * D * 2) : 0u;
@@ -1028,7 +1065,11 @@ size_t decode_workspace_bytes(int B, int Hq, int Hkv, int D, int num_ctas) {
 kvq_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const kvq_cache& K = *a.k;
   const kvq_cache& Vc = *a.v;
-  const int D = K.D, B = K.B, Hkv = K.Hkv, Tcap = K.Tcap;
+  // K.B x K.Tcap is the storage (a page pool when a block table is given);
+  // B x Tcap the sequences and their capacity
+  const int D = K.D, Hkv = K.Hkv;
+  const int B = a.bt != nullptr ? a.bt_B : K.B;
+  const int Tcap = a.bt != nullptr ? a.bt_max_pages * kTile : K.Tcap;
   if (B > 4096) return KVQ_ERR_UNSUPPORTED;  // dynamic shared memory was sized for B <= 4096
   if (!(D == 128 ? regs_ok<128>() : regs_ok<64>())) return KVQ_ERR_UNSUPPORTED;
   const int C = decode_num_ctas(D);
@@ -1038,8 +1079,8 @@ kvq_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   DParams p;
   memset(&p, 0, sizeof(p));
   const HeadLayout& hl = a.layout;
-  const uint64_t rows8 = static_cast<uint64_t>(hl.n8) * B * Tcap;
-  const uint64_t rows4 = static_cast<uint64_t>(hl.n4) * B * Tcap;
+  const uint64_t rows8 = static_cast<uint64_t>(hl.n8) * K.B * K.Tcap;
+  const uint64_t rows4 = static_cast<uint64_t>(hl.n4) * K.B * K.Tcap;
   auto enc = [&](CUtensorMap* m, const uint8_t* base, int bits, uint64_t rows) -> bool {
     if (rows == 0) return true;
     const uint32_t R = static_cast<uint32_t>(D * bits / 8);
@@ -1067,6 +1108,10 @@ kvq_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.status = a.status;
   p.out_dtype = a.out_dtype;
   p.B = B; p.Hq = a.Hq; p.Hkv = Hkv; p.Tcap = Tcap; p.rep = rep; p.num_ctas = C;
+  p.bt = a.bt;
+  p.bt_stride = a.bt_max_pages;
+  p.pB = K.B;
+  p.pT = K.Tcap;
   const float scale = a.softmax_scale > 0.0f ? a.softmax_scale : 1.0f / sqrtf(static_cast<float>(D));
   p.scale_log2 = scale * 1.4426950408889634f;
   for (int h = 0; h < KVQ_MAX_HKV; ++h) {

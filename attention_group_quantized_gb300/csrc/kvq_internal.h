@@ -30,6 +30,10 @@ struct QuantizeArgs {
   int32_t B, Hkv, Tcap, D;
   int32_t* status;
   HeadLayout layout;
+  // optional block table: the cache is a page pool (B = pages, Tcap = 64) and
+  // x's rows are indexed by sequence bt_B x positions
+  const int32_t* bt = nullptr;
+  int32_t bt_B = 0, bt_max_pages = 0;
 };
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t stream);
 
@@ -49,6 +53,8 @@ struct AppendArgs {
   int32_t B, Hkv, Tcap, D;
   int32_t* status;
   HeadLayout layout;                // shared by K and V
+  const int32_t* bt = nullptr;      // optional block table, as in QuantizeArgs
+  int32_t bt_B = 0, bt_max_pages = 0;
 };
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 
@@ -65,6 +71,9 @@ struct DecodeArgs {
   void* ws;
   size_t ws_bytes;
   int32_t* status;
+  // optional block table: the caches are page pools (B = pages, Tcap = 64)
+  const int32_t* bt = nullptr;
+  int32_t bt_B = 0, bt_max_pages = 0;
 };
 // Number of persistent split CTAs on the current device for head dim D.
 int decode_num_ctas(int D);

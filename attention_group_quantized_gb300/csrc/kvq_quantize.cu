@@ -41,6 +41,10 @@ struct FastDiv {
 
 struct QParams {
   FastDiv div_nt, div_hkv;   // row -> (b, h, t): row = (b * Hkv + h) * nt + t
+  // optional block table: the cache is a pool of B pages of Tcap = 64 tokens
+  // and sequence b's token t sits in page bt[b * bt_stride + t / 64]
+  const int32_t* bt;
+  int32_t bt_stride;
   const uint16_t* x;
   int64_t sx_b, sx_h, sx_t;
   uint8_t* codes;
@@ -191,7 +195,16 @@ __global__ void __launch_bounds__(256, KVQ_QUANT_MIN_BLOCKS) quantize_kernel(con
     const int h = static_cast<int>(bh - bq * p.div_hkv.d);
     const int b = static_cast<int>(bq);
     const int bits = p.bits[h];
-    const int64_t pos = static_cast<int64_t>(b) * p.Tcap + p.t0 + t;
+    int64_t pos = static_cast<int64_t>(b) * p.Tcap + p.t0 + t;
+    if (p.bt != nullptr) {
+      const int tl = p.t0 + t;
+      const int page = p.bt[static_cast<int64_t>(b) * p.bt_stride + tl / 64];
+      if (page < 0 || page >= p.B) {   // a page outside the pool: report, write nothing
+        if (g == 0) report(p.status, KVQ_ERR_INVALID_ARG);
+        continue;
+      }
+      pos = static_cast<int64_t>(page) * 64 + tl % 64;
+    }
     uint32_t w[16];
     load_group(w, p.x + b * p.sx_b + h * p.sx_h + t * p.sx_t + g * 32);
     quantize_group(w, bits, p.codes + p.plane_off[h] + pos * (D * bits / 8) + g * (32 * bits / 8),
@@ -202,6 +215,8 @@ __global__ void __launch_bounds__(256, KVQ_QUANT_MIN_BLOCKS) quantize_kernel(con
 // Append: the new token of every (sequence b, KV head h) of K and of V, rows
 // [k rows | v rows] of [b][h], written at cache position seq_lens[b] - 1.
 struct AParams {
+  const int32_t* bt;        // optional block table (the caches are page pools), as in QParams
+  int32_t bt_stride;
   const uint4* q_src;       // optional: q vectors to stage for the decode (host memory read in place)
   uint4* q_dst;
   int64_t q_vec;            // 16-byte vectors to copy
@@ -210,7 +225,8 @@ struct AParams {
   uint32_t* sz[2];
   const int32_t* seq_lens;
   int32_t* status;
-  int32_t B, Hkv, Tcap;
+  int32_t B, Hkv, Tcap;     // storage: B sequences (or pages) of Tcap tokens
+  int32_t nseq, cap;        // sequences and their capacity in tokens
   int64_t plane_off[KVQ_MAX_HKV];
   int8_t bits[KVQ_MAX_HKV];
 };
@@ -224,7 +240,7 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ APa
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.q_vec;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     p.q_dst[i] = p.q_src[i];
-  const int64_t bhn = static_cast<int64_t>(p.B) * p.Hkv;
+  const int64_t bhn = static_cast<int64_t>(p.nseq) * p.Hkv;
   const int64_t n = 2 * bhn * G;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -235,12 +251,20 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ APa
     const int h = static_cast<int>(bh % p.Hkv);
     const int b = static_cast<int>(bh / p.Hkv);
     const int len = p.seq_lens[b];
-    if (len < 1 || len > p.Tcap) {
+    if (len < 1 || len > p.cap) {
       if (job == 0 && h == 0 && g == 0) report(p.status, KVQ_ERR_INVALID_ARG);
       continue;
     }
     const int bits = p.bits[h];
-    const int64_t pos = static_cast<int64_t>(b) * p.Tcap + len - 1;
+    int64_t pos = static_cast<int64_t>(b) * p.Tcap + len - 1;
+    if (p.bt != nullptr) {
+      const int page = p.bt[static_cast<int64_t>(b) * p.bt_stride + (len - 1) / 64];
+      if (page < 0 || page >= p.B) {
+        if (job == 0 && h == 0 && g == 0) report(p.status, KVQ_ERR_INVALID_ARG);
+        continue;
+      }
+      pos = static_cast<int64_t>(page) * 64 + (len - 1) % 64;
+    }
     uint32_t w[16];
     load_group(w, p.x[job] + bh * D + g * 32);
     quantize_group(w, bits, p.codes[job] + p.plane_off[h] + pos * (D * bits / 8) + g * (32 * bits / 8),
@@ -256,7 +280,9 @@ cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t stream) {
   p.sx_b = a.sx_b; p.sx_h = a.sx_h; p.sx_t = a.sx_t;
   p.codes = a.codes; p.sz = a.sz; p.status = a.status;
   p.B = a.B; p.Hkv = a.Hkv; p.Tcap = a.Tcap; p.t0 = a.t0; p.nt = a.nt;
-  p.rows = static_cast<int64_t>(a.B) * a.Hkv * a.nt;
+  p.bt = a.bt;
+  p.bt_stride = a.bt_max_pages;
+  p.rows = static_cast<int64_t>(a.bt != nullptr ? a.bt_B : a.B) * a.Hkv * a.nt;
   if (p.rows >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // rows are indexed in 32 bits
   p.div_nt = FastDiv::make(static_cast<uint32_t>(a.nt));
   p.div_hkv = FastDiv::make(static_cast<uint32_t>(a.Hkv));
@@ -287,11 +313,15 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
   p.seq_lens = a.seq_lens;
   p.status = a.status;
   p.B = a.B; p.Hkv = a.Hkv; p.Tcap = a.Tcap;
+  p.bt = a.bt;
+  p.bt_stride = a.bt_max_pages;
+  p.nseq = a.bt != nullptr ? a.bt_B : a.B;
+  p.cap = a.bt != nullptr ? a.bt_max_pages * 64 : a.Tcap;
   for (int h = 0; h < KVQ_MAX_HKV; ++h) {
     p.plane_off[h] = a.layout.plane_off[h];
     p.bits[h] = a.layout.bits[h];
   }
-  const int64_t rows = 2 * static_cast<int64_t>(a.B) * a.Hkv;
+  const int64_t rows = 2 * static_cast<int64_t>(p.nseq) * a.Hkv;
   int64_t blocks = (rows * (a.D / 32) + 255) / 256;   // one thread per (row, group)
   const int64_t qblocks = (p.q_vec + 255) / 256;   // one 16-byte vector per thread
   if (qblocks > blocks) blocks = qblocks;

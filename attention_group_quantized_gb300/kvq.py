@@ -28,7 +28,12 @@ TILE_TOKENS = 64
 EXPORTS = ("kvq_cache_codes_bytes", "kvq_cache_sz_bytes", "kvq_cache_head_offset", "kvq_quantize",
            "kvq_decode_workspace_bytes", "kvq_decode_attention", "kvq_prefill_attention",
            "kvq_decode_attention_noalloc", "kvq_decode_step", "kvq_decode_step_staging_bytes",
-           "kvq_decode_step_host", "kvq_status_str")
+           "kvq_decode_step_host", "kvq_quantize_paged", "kvq_decode_attention_paged", "kvq_decode_step_paged",
+           "kvq_status_str")
+
+
+class CBlockTable(ctypes.Structure):
+    _fields_ = [("pages", ctypes.c_void_p), ("B", ctypes.c_int32), ("max_pages", ctypes.c_int32)]
 
 
 class KvqError(RuntimeError):
@@ -74,6 +79,13 @@ def lib() -> ctypes.CDLL:
         L.kvq_decode_step_staging_bytes.restype = SZ
         L.kvq_decode_step_host.argtypes = [P, P, P, CP, CP, P, I32, F32, P, I32, P, SZ, P, SZ, P, P]
         L.kvq_decode_step_host.restype = I32
+        BT = ctypes.POINTER(CBlockTable)
+        L.kvq_quantize_paged.argtypes = [P, I64, I64, I64, I32, I32, CP, BT, P, P]
+        L.kvq_quantize_paged.restype = I32
+        L.kvq_decode_attention_paged.argtypes = [P, CP, CP, BT, P, I32, F32, P, I32, P, SZ, P, P]
+        L.kvq_decode_attention_paged.restype = I32
+        L.kvq_decode_step_paged.argtypes = [P, P, P, CP, CP, BT, P, I32, F32, P, I32, P, SZ, P, P]
+        L.kvq_decode_step_paged.restype = I32
         L.kvq_status_str.argtypes = [I32]; L.kvq_status_str.restype = ctypes.c_char_p
         _LIB = L
     return _LIB
@@ -276,6 +288,72 @@ class DecodeStepHost:
         st = self._fn(*self._head, ctypes.byref(k.c_struct()), ctypes.byref(v.c_struct()), *self._tail)
         if st != KVQ_OK:
             raise KvqError(st, "kvq_decode_step_host")
+
+
+PAGE_TOKENS = 64
+
+
+def empty_page_pool(head_bits: Sequence[int], n_pages: int, D: int, device="cuda") -> QuantCache:
+    """A page pool: a cache of n_pages pages of 64 tokens (B = n_pages, Tcap = 64)."""
+    return empty_cache(head_bits, n_pages, PAGE_TOKENS, D, device=device)
+
+
+def _table(block_table) -> CBlockTable:
+    """block_table: device int32 [B][max_pages] of page ids."""
+    assert block_table.dtype.itemsize == 4 and block_table.dim() == 2 and block_table.is_contiguous()
+    return CBlockTable(block_table.data_ptr(), int(block_table.shape[0]), int(block_table.shape[1]))
+
+
+def quantize_paged(x, pool: QuantCache, block_table, t0: int = 0, status=None, stream=None):
+    """Quantise bf16 x[B][Hkv][T][D] (strided, channels contiguous) into positions t0.. of the
+    sequences of block_table, stored in the page pool."""
+    assert x.dtype.itemsize == 2 and x.stride(-1) == 1
+    cs, bt = pool.c_struct(), _table(block_table)
+    st = lib().kvq_quantize_paged(x.data_ptr(), x.stride(0), x.stride(1), x.stride(2), t0, x.shape[2],
+                                  ctypes.byref(cs), ctypes.byref(bt),
+                                  status.data_ptr() if status is not None else None, _stream_ptr(stream))
+    _check(st, "kvq_quantize_paged")
+
+
+def decode_attention_paged(q, k_pool: QuantCache, v_pool: QuantCache, block_table, seq_lens,
+                           softmax_scale: float = 0.0, out=None, out_dtype: int = OUT_F32, workspace=None,
+                           status=None, stream=None):
+    """Decode attention over page pools through a block table; returns out [B][Hq][D]."""
+    import torch
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32 if out_dtype == OUT_F32 else torch.bfloat16,
+                          device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, k_pool.Hkv, D, q.device)
+    kc, vc, bt = k_pool.c_struct(), v_pool.c_struct(), _table(block_table)
+    st = lib().kvq_decode_attention_paged(q.data_ptr(), ctypes.byref(kc), ctypes.byref(vc), ctypes.byref(bt),
+                                          seq_lens.data_ptr(), Hq, float(softmax_scale), out.data_ptr(), out_dtype,
+                                          workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                          status.data_ptr() if status is not None else None, _stream_ptr(stream))
+    _check(st, "kvq_decode_attention_paged")
+    return out
+
+
+def decode_step_paged(q, k_new, v_new, k_pool: QuantCache, v_pool: QuantCache, block_table, seq_lens,
+                      softmax_scale: float = 0.0, out=None, out_dtype: int = OUT_F32, workspace=None, status=None,
+                      stream=None):
+    """decode_step over page pools: append at position seq_lens[b] - 1 through the block table, then attend."""
+    import torch
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32 if out_dtype == OUT_F32 else torch.bfloat16,
+                          device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, k_pool.Hkv, D, q.device)
+    kc, vc, bt = k_pool.c_struct(), v_pool.c_struct(), _table(block_table)
+    st = lib().kvq_decode_step_paged(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), ctypes.byref(kc),
+                                     ctypes.byref(vc), ctypes.byref(bt), seq_lens.data_ptr(), Hq,
+                                     float(softmax_scale), out.data_ptr(), out_dtype,
+                                     workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                     status.data_ptr() if status is not None else None, _stream_ptr(stream))
+    _check(st, "kvq_decode_step_paged")
+    return out
 
 
 def prefill_attention(q, k, v, k_cache: QuantCache, v_cache: QuantCache, softmax_scale: float = 0.0,

@@ -256,6 +256,62 @@ KVQ_API kvq_status kvq_decode_step_host(const void* q_host, const void* k_new_ho
                                         void* workspace, size_t workspace_bytes, int32_t* dev_status,
                                         void* stream);
 
+/*
+ * Paged caches: the block-table layout of the serving systems the pages
+ * compare against (PagedAttention with an INT8 cache), here for the
+ * group-quantised cache.  A page POOL is a kvq_cache whose B counts pages and
+ * whose Tcap is KVQ_TILE_TOKENS (64): page p holds 64 consecutive tokens of
+ * one sequence, in every head's code plane and in the scale/zero words, in
+ * exactly the kvq_cache layout.  A block table maps sequence b's token t to
+ * page pages[b * max_pages + t / 64], slot t % 64.  Pages are the caller's to
+ * allocate; two sequences may share a page only while no call writes it.
+ */
+typedef struct kvq_block_table {
+  const int32_t* pages;   /* device int32 [B][max_pages], 4-byte aligned */
+  int32_t B;              /* sequences */
+  int32_t max_pages;      /* pages per sequence: capacity max_pages * 64 tokens */
+} kvq_block_table;
+
+/*
+ * kvq_quantize into a page pool: x's rows are (sequence b < table->B, KV
+ * head, position t0 + t) with the strides of kvq_quantize, and each row is
+ * written to its page and slot, quantised exactly as kvq_quantize does.
+ * t0 + nt <= max_pages * 64.  A page id outside [0, pool->B) reports
+ * KVQ_ERR_INVALID_ARG in dev_status and that row is not written.
+ */
+KVQ_API kvq_status kvq_quantize_paged(const void* x, int64_t sx_b, int64_t sx_h, int64_t sx_t,
+                                      int32_t t0, int32_t nt, const kvq_cache* pool,
+                                      const kvq_block_table* table, int32_t* dev_status, void* stream);
+
+/*
+ * kvq_decode_attention over page pools: q [table->B][Hq][D]; sequence b
+ * attends its tokens 0 .. seq_lens[b] - 1 through the block table
+ * (seq_lens[b] <= max_pages * 64, else KVQ_ERR_INVALID_ARG in dev_status and
+ * the length is clamped).  A page id outside the pool reports
+ * KVQ_ERR_INVALID_ARG and that tile reads page 0 instead.  The workspace is
+ * kvq_decode_workspace_bytes(table->B, Hq, Hkv, D).  Other arguments as
+ * kvq_decode_attention.
+ */
+KVQ_API kvq_status kvq_decode_attention_paged(const void* q, const kvq_cache* k_pool, const kvq_cache* v_pool,
+                                              const kvq_block_table* table, const int32_t* seq_lens,
+                                              int32_t Hq, float softmax_scale, void* out, int32_t out_dtype,
+                                              void* workspace, size_t workspace_bytes,
+                                              int32_t* dev_status, void* stream);
+
+/*
+ * kvq_decode_step over page pools: the new token of sequence b goes to page
+ * pages[b * max_pages + (seq_lens[b] - 1) / 64], slot (seq_lens[b] - 1) % 64,
+ * then kvq_decode_attention_paged.  A length outside [1, max_pages * 64] or a
+ * page id outside the pool reports KVQ_ERR_INVALID_ARG and that sequence
+ * appends nothing.
+ */
+KVQ_API kvq_status kvq_decode_step_paged(const void* q, const void* k_new, const void* v_new,
+                                         const kvq_cache* k_pool, const kvq_cache* v_pool,
+                                         const kvq_block_table* table, const int32_t* seq_lens,
+                                         int32_t Hq, float softmax_scale, void* out, int32_t out_dtype,
+                                         void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                         void* stream);
+
 /* Static, human-readable name of a status code. */
 KVQ_API const char* kvq_status_str(kvq_status status);
 
