@@ -199,11 +199,13 @@ def run_reference(args, rank):
 
 
 def time_decode(torch, kvq, inp, dev, l2, steps, warmup, dist=None, keep=False, busy_s=0.0, sampler=None,
-                use_graph=True):
+                use_graph=True, paged=False):
     """Back-to-back decode steps over cache copies larger than 3x L2 together.
 
-    Returns the total device time of `steps` steps (max over ranks) and the
-    algorithmic bytes per step; with keep=True also the device buffers.
+    With paged=True each copy is a pair of page pools addressed through a
+    shuffled block table (kvq_decode_attention_paged).  Returns the total
+    device time of `steps` steps (max over ranks) and the algorithmic bytes
+    per step; with keep=True also the device buffers.
     """
     import numpy as np
     B, Hq, Hkv, D, Tcap = inp.B, inp.Hq, inp.Hkv, inp.D, inp.Tcap
@@ -212,11 +214,23 @@ def time_decode(torch, kvq, inp, dev, l2, steps, warmup, dist=None, keep=False, 
     n_copies = max(2, -(-3 * l2 // max(nbytes, 1)))
     kd, vd = todev(inp.k), todev(inp.v)
     caches = []
-    for _ in range(n_copies):
-        kc = kvq.empty_cache(inp.head_bits, B, Tcap, D, device=dev)
-        vc = kvq.empty_cache(inp.head_bits, B, Tcap, D, device=dev)
-        kvq.quantize(kd, kc)
-        kvq.quantize(vd, vc)
+    tables = []
+    for c in range(n_copies):
+        if paged:
+            max_pages = Tcap // 64
+            n_pages = B * max_pages
+            perm = np.random.default_rng(100 + c).permutation(n_pages).astype(np.int32)
+            bt = torch.from_numpy(perm.reshape(B, max_pages)).to(dev)
+            kc = kvq.empty_page_pool(inp.head_bits, n_pages, D, device=dev)
+            vc = kvq.empty_page_pool(inp.head_bits, n_pages, D, device=dev)
+            kvq.quantize_paged(kd, kc, bt)
+            kvq.quantize_paged(vd, vc, bt)
+            tables.append(bt)
+        else:
+            kc = kvq.empty_cache(inp.head_bits, B, Tcap, D, device=dev)
+            vc = kvq.empty_cache(inp.head_bits, B, Tcap, D, device=dev)
+            kvq.quantize(kd, kc)
+            kvq.quantize(vd, vc)
         caches.append((kc, vc))
     del kd, vd
     q = todev(inp.q)
@@ -228,7 +242,11 @@ def time_decode(torch, kvq, inp, dev, l2, steps, warmup, dist=None, keep=False, 
 
     def step(i):
         kc_i, vc_i = caches[i % n_copies]
-        kvq.decode_attention(q, kc_i, vc_i, sl, inp.softmax_scale, out=out, workspace=ws, status=status)
+        if paged:
+            kvq.decode_attention_paged(q, kc_i, vc_i, tables[i % n_copies], sl, inp.softmax_scale, out=out,
+                                       workspace=ws, status=status)
+        else:
+            kvq.decode_attention(q, kc_i, vc_i, sl, inp.softmax_scale, out=out, workspace=ws, status=status)
 
     for i in range(warmup):
         step(i)
@@ -289,12 +307,14 @@ def bench_extra_decodes(torch, kvq, W, peaks, dev, steps, warmup):
     """The other decode workloads, measured the same way (context for the main line)."""
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     res = {}
-    for name in ("decode_long_ragged", "decode_mixed", "decode_tiny"):
+    for name, paged in (("decode_long_ragged", False), ("decode_mixed", False), ("decode_tiny", False),
+                        ("decode_gqa", True)):
         inp = W.NAMED[name]()
-        d = time_decode(torch, kvq, inp, dev, l2, steps, warmup)
+        d = time_decode(torch, kvq, inp, dev, l2, steps, warmup, paged=paged)
         avg = d["t_total"] / steps
         gbs = d["bytes"] / avg / 1e9
-        res[inp.name] = {"GB/s": round(gbs, 1), "us_per_step": round(avg * 1e6, 2),
+        key = inp.name + ("_paged_shuffled_block_table" if paged else "")
+        res[key] = {"GB/s": round(gbs, 1), "us_per_step": round(avg * 1e6, 2),
                          "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4), "bytes_per_step": d["bytes"]}
         del d
         torch.cuda.empty_cache()
