@@ -603,7 +603,7 @@ __device__ __forceinline__ void consume_tiles(const uint32_t (&st_s)[NT], const 
 // but they only choose which lines to prefetch (clamped into the cache), and
 // an L2 prefetch returns nothing to the program, so no result depends on
 // them.  Batches of more than 32 sequences skip the warm-up.
-template <int D>
+template <int D, bool PAGED>
 __device__ __forceinline__ void warm_l2(const DParams& p, int lane) {
   constexpr int G = D / 32;
   if (kL2Warm <= 0 || p.B > 32) return;
@@ -633,7 +633,7 @@ __device__ __forceinline__ void warm_l2(const DParams& p, int lane) {
   const int kvh = static_cast<int>(off / nb), i = static_cast<int>(off % nb);
   const int bits = p.bits[kvh];
   int pb = bs, pt = i * kTile;
-  if (p.bt != nullptr) {   // (a stale or bad page id only misdirects this prefetch)
+  if constexpr (PAGED) {   // (a stale or bad page id only misdirects this prefetch)
     pb = min(max(p.bt[static_cast<int64_t>(bs) * p.bt_stride + i], 0), p.pB - 1);
     pt = 0;
   }
@@ -645,7 +645,9 @@ __device__ __forceinline__ void warm_l2(const DParams& p, int lane) {
   prefetch_l2_bulk(p.v_sz + szoff * G, Smem<D>::kSzBytes);
 }
 
-template <int D>
+// PAGED: the tiles are pages of a pool found through p.bt (a separate
+// instantiation, so the contiguous kernel carries none of it)
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_kernel(const __grid_constant__ DParams p) {
   using L = Smem<D>;
   constexpr int G = D / 32;
@@ -682,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
     prefetch_tmap(&p.tm_k4);
     prefetch_tmap(&p.tm_v4);
   }
-  if (w == kWarps) warm_l2<D>(p, lane);
+  if (w == kWarps) warm_l2<D, PAGED>(p, lane);
   // With programmatic dependent launch this kernel may start while the
   // previous kernel in the stream is finishing: wait for it (and its memory)
   // before the first global access whose data is used, then let the next one
@@ -747,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
 #pragma unroll
       for (int j = 0; j < kStages; ++j) {
         pg[j] = 0;
-        if (p.bt != nullptr && j < ntiles) {
+        if (PAGED && j < ntiles) {
           pg[j] = p.bt[static_cast<int64_t>(pa.b) * p.bt_stride + pa.i];
           advance(pa, pre, B, Hkv);
         }
@@ -761,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
         const int bits = p.bits[pc.kvh];
         const int R = D * bits / 8;
         int pb = pc.b, pt = pc.i * kTile;
-        if (p.bt != nullptr) {
+        if constexpr (PAGED) {
           pb = pg[0];
 #pragma unroll
           for (int j = 0; j + 1 < kStages; ++j) pg[j] = pg[j + 1];
@@ -996,7 +998,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
   }
 }
 
-template <int D>
+template <int D, bool PAGED>
 int ctas_per_sm() {
   static int cached[64] = {0};
   int dev = 0;
@@ -1004,9 +1006,9 @@ int ctas_per_sm() {
   if (cached[dev] == 0) {
     int n = 0;
     const size_t sm = Smem<D>::bytes(64);
-    cudaFuncSetAttribute(decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(decode_split_kernel<D, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(Smem<D>::bytes(4096)));
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<D>, kThreads, sm) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<D, PAGED>, kThreads, sm) != cudaSuccess ||
         n < 1)
       n = 1;
     cached[dev] = n;
@@ -1016,12 +1018,12 @@ int ctas_per_sm() {
 
 // The register split inside the kernel assumes 128 registers per thread at
 // launch; any other count would make the consumers' setmaxnreg wait forever.
-template <int D>
+template <int D, bool PAGED>
 bool regs_ok() {
   static int cached = -1;
   if (cached < 0) {
     cudaFuncAttributes fa;
-    cached = (cudaFuncGetAttributes(&fa, decode_split_kernel<D>) == cudaSuccess && fa.numRegs == 128) ? 1 : 0;
+    cached = (cudaFuncGetAttributes(&fa, decode_split_kernel<D, PAGED>) == cudaSuccess && fa.numRegs == 128) ? 1 : 0;
   }
   return cached == 1;
 }
@@ -1029,7 +1031,7 @@ bool regs_ok() {
 // Launched with programmatic stream serialization: the kernel's CTAs may be
 // scheduled while the previous kernel of the stream drains; the kernel waits
 // for it (griddepcontrol.wait) before its first global memory access.
-template <int D>
+template <int D, bool PAGED>
 cudaError_t launch_split(const DParams& p, int C, int B, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(C));
@@ -1041,13 +1043,14 @@ cudaError_t launch_split(const DParams& p, int C, int B, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_split_kernel<D>, p);
+  return cudaLaunchKernelEx(&cfg, decode_split_kernel<D, PAGED>, p);
 }
 
 }  // namespace
 
 int decode_num_ctas(int D) {
-  const int per = D == 128 ? ctas_per_sm<128>() : ctas_per_sm<64>();
+  // the paged instantiations have the same resources (checked by regs_ok)
+  const int per = D == 128 ? ctas_per_sm<128, false>() : ctas_per_sm<64, false>();
   return device_sm_count() * per;
 }
 
@@ -1071,7 +1074,10 @@ kvq_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const int B = a.bt != nullptr ? a.bt_B : K.B;
   const int Tcap = a.bt != nullptr ? a.bt_max_pages * kTile : K.Tcap;
   if (B > 4096) return KVQ_ERR_UNSUPPORTED;  // dynamic shared memory was sized for B <= 4096
-  if (!(D == 128 ? regs_ok<128>() : regs_ok<64>())) return KVQ_ERR_UNSUPPORTED;
+  const bool paged = a.bt != nullptr;
+  const bool regs = D == 128 ? (paged ? regs_ok<128, true>() : regs_ok<128, false>())
+                             : (paged ? regs_ok<64, true>() : regs_ok<64, false>());
+  if (!regs) return KVQ_ERR_UNSUPPORTED;
   const int C = decode_num_ctas(D);
   const size_t need = decode_workspace_bytes(B, a.Hq, Hkv, D, C);
   if (a.ws == nullptr || a.ws_bytes < need) return KVQ_ERR_WORKSPACE;
@@ -1118,7 +1124,9 @@ kvq_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.plane[h] = hl.plane_idx[h];
     p.bits[h] = hl.bits[h];
   }
-  const cudaError_t e = D == 128 ? launch_split<128>(p, C, B, stream) : launch_split<64>(p, C, B, stream);
+  if (paged) (void)(D == 128 ? ctas_per_sm<128, true>() : ctas_per_sm<64, true>());   // sets its smem limit
+  const cudaError_t e = D == 128 ? (paged ? launch_split<128, true>(p, C, B, stream) : launch_split<128, false>(p, C, B, stream))
+                                 : (paged ? launch_split<64, true>(p, C, B, stream) : launch_split<64, false>(p, C, B, stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

@@ -181,7 +181,9 @@ __device__ __forceinline__ void quantize_group(const uint32_t (&w)[16], int bits
 // One thread per (row, group): row = (b * Hkv + h) * nt + t.  (A persistent
 // loop that issued the next group's loads before this group's arithmetic
 // measured slower: the extra registers cost more occupancy than it gained.)
-template <int D>
+// PAGED: the cache is a page pool addressed through p.bt (a separate
+// instantiation, so the contiguous kernel carries none of it).
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(256, KVQ_QUANT_MIN_BLOCKS) quantize_kernel(const __grid_constant__ QParams p) {
   constexpr int G = D / 32;
   const int64_t n = p.rows * G;
@@ -196,7 +198,7 @@ __global__ void __launch_bounds__(256, KVQ_QUANT_MIN_BLOCKS) quantize_kernel(con
     const int b = static_cast<int>(bq);
     const int bits = p.bits[h];
     int64_t pos = static_cast<int64_t>(b) * p.Tcap + p.t0 + t;
-    if (p.bt != nullptr) {
+    if constexpr (PAGED) {
       const int tl = p.t0 + t;
       const int page = p.bt[static_cast<int64_t>(b) * p.bt_stride + tl / 64];
       if (page < 0 || page >= p.B) {   // a page outside the pool: report, write nothing
@@ -231,7 +233,7 @@ struct AParams {
   int8_t bits[KVQ_MAX_HKV];
 };
 
-template <int D>
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ AParams p) {
   constexpr int G = D / 32;
   // the decode launched after this kernel may begin its prologue now; it
@@ -257,7 +259,7 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ APa
     }
     const int bits = p.bits[h];
     int64_t pos = static_cast<int64_t>(b) * p.Tcap + len - 1;
-    if (p.bt != nullptr) {
+    if constexpr (PAGED) {
       const int page = p.bt[static_cast<int64_t>(b) * p.bt_stride + (len - 1) / 64];
       if (page < 0 || page >= p.B) {
         if (job == 0 && h == 0 && g == 0) report(p.status, KVQ_ERR_INVALID_ARG);
@@ -294,10 +296,13 @@ cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t stream) {
   int64_t blocks = (p.rows * (a.D / 32) + 255) / 256;   // one thread per (row, group)
   const int64_t cap = int64_t(1) << 30;                   // grid-stride beyond that
   if (blocks > cap) blocks = cap;
+  const unsigned g = static_cast<unsigned>(blocks);
   if (a.D == 128) {
-    quantize_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+    if (p.bt != nullptr) quantize_kernel<128, true><<<g, 256, 0, stream>>>(p);
+    else quantize_kernel<128, false><<<g, 256, 0, stream>>>(p);
   } else {
-    quantize_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+    if (p.bt != nullptr) quantize_kernel<64, true><<<g, 256, 0, stream>>>(p);
+    else quantize_kernel<64, false><<<g, 256, 0, stream>>>(p);
   }
   return cudaGetLastError();
 }
@@ -327,10 +332,13 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
   if (qblocks > blocks) blocks = qblocks;
   const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
   if (blocks > cap) blocks = cap;
+  const unsigned g = static_cast<unsigned>(blocks);
   if (a.D == 128) {
-    append_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+    if (p.bt != nullptr) append_kernel<128, true><<<g, 256, 0, stream>>>(p);
+    else append_kernel<128, false><<<g, 256, 0, stream>>>(p);
   } else {
-    append_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+    if (p.bt != nullptr) append_kernel<64, true><<<g, 256, 0, stream>>>(p);
+    else append_kernel<64, false><<<g, 256, 0, stream>>>(p);
   }
   return cudaGetLastError();
 }
