@@ -374,6 +374,15 @@ kvq_status kvq_decode_step_host(const void* q_host, const void* k_new_host, cons
   return cudaMemcpyAsync(out_host, d_o, ob, cudaMemcpyDeviceToHost, s) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
+kvq_status kvq_build_tile_mask(uint8_t* mask, int32_t nT, int32_t skip_num, int32_t skip_den, uint64_t seed,
+                               void* stream) {
+  if (mask == nullptr || nT < 1 || nT > 16384 || skip_den < 1 || skip_num < 0 || skip_num > skip_den)
+    return KVQ_ERR_INVALID_ARG;
+  return launch_tile_mask(mask, nT, skip_num, skip_den, seed, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? KVQ_OK
+             : KVQ_ERR_CUDA;
+}
+
 kvq_status kvq_prefill_attention(const void* q, const void* k, const void* v, int32_t B, int32_t Hq, int32_t Hkv,
                                  int32_t S, int32_t D, int32_t causal, float softmax_scale,
                                  const uint8_t* tile_mask, int32_t tile, const kvq_cache* k_cache,

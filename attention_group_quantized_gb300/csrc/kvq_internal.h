@@ -96,6 +96,8 @@ struct PrefillArgs {
 };
 kvq_status launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 
+cudaError_t launch_tile_mask(uint8_t* mask, int nT, int num, int den, uint64_t seed, cudaStream_t stream);
+
 // cuTensorMapEncodeTiled, resolved from the driver at first use (no link to
 // libcuda, so the library loads on machines without a GPU driver).
 CUresult encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,

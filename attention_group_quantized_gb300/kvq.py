@@ -29,7 +29,7 @@ EXPORTS = ("kvq_cache_codes_bytes", "kvq_cache_sz_bytes", "kvq_cache_head_offset
            "kvq_decode_workspace_bytes", "kvq_decode_attention", "kvq_prefill_attention",
            "kvq_decode_attention_noalloc", "kvq_decode_step", "kvq_decode_step_staging_bytes",
            "kvq_decode_step_host", "kvq_quantize_paged", "kvq_decode_attention_paged", "kvq_decode_step_paged",
-           "kvq_status_str")
+           "kvq_build_tile_mask", "kvq_status_str")
 
 
 class CBlockTable(ctypes.Structure):
@@ -86,6 +86,8 @@ def lib() -> ctypes.CDLL:
         L.kvq_decode_attention_paged.restype = I32
         L.kvq_decode_step_paged.argtypes = [P, P, P, CP, CP, BT, P, I32, F32, P, I32, P, SZ, P, P]
         L.kvq_decode_step_paged.restype = I32
+        L.kvq_build_tile_mask.argtypes = [P, I32, I32, I32, ctypes.c_uint64, P]
+        L.kvq_build_tile_mask.restype = I32
         L.kvq_status_str.argtypes = [I32]; L.kvq_status_str.restype = ctypes.c_char_p
         _LIB = L
     return _LIB
@@ -353,6 +355,18 @@ def decode_step_paged(q, k_new, v_new, k_pool: QuantCache, v_pool: QuantCache, b
                                      workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                      status.data_ptr() if status is not None else None, _stream_ptr(stream))
     _check(st, "kvq_decode_step_paged")
+    return out
+
+
+def build_tile_mask(nT: int, skip_num: int, skip_den: int, seed: int, device="cuda", out=None, stream=None):
+    """A prefill tile mask uint8 [nT][nT] built on the GPU: per query tile, floor((qt-1)*num/den) of the
+    key tiles in [1, qt) skipped (smallest SplitMix64 keys); tile 0 and the diagonal kept."""
+    import torch
+    if out is None:
+        out = torch.empty((nT, nT), dtype=torch.uint8, device=device)
+    st = lib().kvq_build_tile_mask(out.data_ptr(), nT, skip_num, skip_den, int(seed) & 0xFFFFFFFFFFFFFFFF,
+                                   _stream_ptr(stream))
+    _check(st, "kvq_build_tile_mask")
     return out
 
 

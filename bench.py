@@ -382,8 +382,20 @@ def bench_prefill(torch, kvq, W, peaks, steps, warmup, dev):
         times.append(e0.elapsed_time(e1) / 1e3)
     t = statistics.mean(times)
     tf = flops / t / 1e12
+    # the device-side tile-mask builder for this prefill's grid (25 % of the candidate tiles per row)
+    for _ in range(3):
+        kvq.build_tile_mask(n_t, 1, 4, 4, device=dev)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(10):
+        kvq.build_tile_mask(n_t, 1, 4, 4, device=dev)
+    e1.record()
+    torch.cuda.synchronize()
+    mask_us = e0.elapsed_time(e1) * 1e3 / 10
     return {"workload": inp.name, "value": tf, "unit": "TFLOP/s", "ms_per_step": t * 1e3,
             "algorithmic_flop": flops,
+            "tile_mask_build_us": {"nT": n_t, "skip": "1/4 per row", "us": mask_us},
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": tf / peaks["bf16_tflops"], "peak_src": peaks["bf16_src"],
                          "note": "time includes the two quantise launches of the same call"}}

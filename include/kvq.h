@@ -174,6 +174,24 @@ KVQ_API kvq_status kvq_prefill_attention(const void* q, const void* k, const voi
                                  int32_t* dev_status, void* stream);
 
 /*
+ * kvq_build_tile_mask -- a block-sparse tile mask for kvq_prefill_attention
+ * (P4 §2.3: tiles judged unnecessary are skipped, the skipped share capped so
+ * that no query block is starved), built on the GPU.
+ *
+ * mask: device uint8 [nT][nT], written whole.  For query tile qt the
+ *   candidates are key tiles kt in [1, qt); the row skips
+ *   floor(max(qt - 1, 0) * skip_num / skip_den) of them (0 <= skip_num <=
+ *   skip_den; integer arithmetic, so each row's cap is exact): those with the
+ *   smallest keys SplitMix64(seed, qt * nT + kt + 1) -- output number
+ *   qt * nT + kt + 1 of the SplitMix64 generator (Steele, Lea and Flood,
+ *   2014) seeded with `seed` -- ties to the smaller kt.  Entries are 1 for kept
+ *   tiles, key tile 0 and the diagonal, 0 for skipped tiles and above the
+ *   diagonal.  1 <= nT <= 16384.  One launch on `stream`.
+ */
+KVQ_API kvq_status kvq_build_tile_mask(uint8_t* mask, int32_t nT, int32_t skip_num, int32_t skip_den,
+                                       uint64_t seed, void* stream);
+
+/*
  * kvq_decode_attention_noalloc -- kvq_decode_attention for callers that may
  * not allocate device memory (for example code running inside another
  * framework's memory pool, or a plugin whose host forbids cudaMalloc at call

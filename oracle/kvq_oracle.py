@@ -20,6 +20,10 @@ page's title and the section on it):
 * [P1] 《一只"兔子"如何搅动大模型推理赛道的底层逻辑》 (m.xxqk.cn) §3.1:
   Attention(Q, K, V) = softmax(Q K^T / sqrt(d_k)) V.
 
+* [P4] §2.3 also caps the skipped share so that no block is starved: the
+  tile-mask builder below skips, per query tile, a fixed fraction of its
+  candidate key tiles and always keeps key tile 0 and the diagonal.
+
 Readings taken where the pages are silent (each listed in the design notes):
 
 * Quantiser form (P4 §2.4 says only "scale factor and zero point per group"):
@@ -287,3 +291,44 @@ def lse_merge(parts) -> np.ndarray:
     w = np.exp(lses - M)
     o = sum(wi * p[0] for wi, p in zip(w, parts))
     return o / np.sum(w)
+
+
+# ---------------------------------------------------------------------------
+# Tile-mask builder (P4 §2.3: whole tiles are skipped, the skipped share is
+# capped so no block is starved).  Reading: per query tile qt, of the key
+# tiles kt in [1, qt) skip floor(n * num / den) (n = max(qt - 1, 0)), those
+# with the smallest SplitMix64 keys, ties to the smaller kt; keep tile 0 and
+# the diagonal; zero above the diagonal.
+# ---------------------------------------------------------------------------
+
+_SM64_GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_SM64_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_SM64_M2 = np.uint64(0x94D049BB133111EB)
+
+
+def splitmix64(seed: int, n: np.ndarray) -> np.ndarray:
+    """Output number n (1-based) of SplitMix64 seeded with `seed` (Steele, Lea
+    and Flood, "Fast splittable pseudorandom number generators", 2014): the
+    state after n steps is seed + n * gamma (mod 2^64), mixed by the
+    generator's finaliser."""
+    n = np.asarray(n, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = np.uint64(seed) + n * _SM64_GAMMA
+        z = (z ^ (z >> np.uint64(30))) * _SM64_M1
+        z = (z ^ (z >> np.uint64(27))) * _SM64_M2
+    return z ^ (z >> np.uint64(31))
+
+
+def build_tile_mask(nT: int, skip_num: int, skip_den: int, seed: int) -> np.ndarray:
+    """uint8 [nT][nT]: 1 = key tile kept for that query tile."""
+    mask = np.zeros((nT, nT), dtype=np.uint8)
+    for qt in range(nT):
+        mask[qt, :qt + 1] = 1
+        cand = np.arange(1, qt, dtype=np.int64)
+        k = (len(cand) * skip_num) // skip_den
+        if k == 0:
+            continue
+        keys = splitmix64(seed, qt * nT + cand + 1)
+        order = np.argsort(keys, kind="stable")     # equal keys keep the smaller kt first
+        mask[qt, cand[order[:k]]] = 0
+    return mask
