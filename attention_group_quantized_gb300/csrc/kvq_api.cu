@@ -391,7 +391,7 @@ kvq_status kvq_prefill_attention(const void* q, const void* k, const void* v, in
   if (q == nullptr || k == nullptr || v == nullptr || k_cache == nullptr || v_cache == nullptr || out == nullptr)
     return KVQ_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || Hq % Hkv) return KVQ_ERR_INVALID_ARG;
-  if (causal != 1 || tile != 128 || D != 128 || S % 128) return KVQ_ERR_UNSUPPORTED;
+  if ((causal != 0 && causal != 1) || tile != 128 || D != 128 || S % 128) return KVQ_ERR_UNSUPPORTED;
   if (out_dtype != KVQ_OUT_F32 && out_dtype != KVQ_OUT_BF16) return KVQ_ERR_INVALID_ARG;
   PrefillArgs a;
   if (!resolve_layout(*k_cache, &a.layout) || !same_cache_shape(*k_cache, *v_cache)) return KVQ_ERR_INVALID_ARG;
@@ -415,6 +415,7 @@ kvq_status kvq_prefill_attention(const void* q, const void* k, const void* v, in
   a.out = out;
   a.out_dtype = out_dtype;
   a.status = dev_status;
+  a.causal = causal;
   return launch_prefill(a, st);
 }
 

@@ -93,6 +93,7 @@ struct PrefillArgs {
   void* out;
   int32_t out_dtype;
   int32_t* status;
+  int32_t causal = 1;
 };
 kvq_status launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 

@@ -1,4 +1,4 @@
-// kvq_prefill.cu -- causal prefill attention over the group-quantised KV cache
+// kvq_prefill.cu -- prefill attention (causal or not) over the group-quantised KV cache
 // on the 5th-generation tensor cores (tcgen05, accumulators in TMEM).
 //
 // Method (《分块稀疏注意力与KV Cache量化：长文本推理显存优化实践》): the score matrix is
@@ -7,7 +7,9 @@
 // by the normaliser (§2.2); whole key tiles may be skipped by a block-sparse
 // mask (§1.3, §2.3); K and V are read as group-quantised codes and dequantised
 // on the fly (§1.3, §2.4).  The attention itself is softmax(Q K^T / sqrt(d)) V
-// (《一只"兔子"如何搅动大模型推理赛道的底层逻辑》 §3.1) with the causal rule.
+// (《一只"兔子"如何搅动大模型推理赛道的底层逻辑》 §3.1), with the causal rule or, for
+// non-causal prefill, over every key of the sequence (then the mask may skip
+// any off-diagonal tile; query tiles all carry nT key tiles).
 //
 // One CTA (512 threads, one per SM) computes one 128-row query tile for two
 // query heads that share a KV head, so every dequantised K/V tile feeds two
@@ -22,7 +24,7 @@
 //               the 128-byte-swizzled layout the tensor core reads (2 stages);
 //   warps 8-11  softmax of head 0, warps 12-15 softmax of head 1: one thread
 //               per query row reads its S row from TMEM, applies the causal
-//               rule on the diagonal tile, updates (max, sum) in the log2
+//               rule on the diagonal tile (causal only), updates (max, sum) in the log2
 //               domain, writes P (fp16) back over S, and at the end scales O by
 //               1 / sum and stores it.
 // TMEM (512 columns): S_0 [0,128) O_0 [128,256) S_1 [256,384) O_1 [384,512).
@@ -53,6 +55,7 @@ struct PParams {
   int32_t* status;
   int32_t out_dtype;
   int32_t B, Hq, Hkv, S, Tcap, rep, pairs, nT;
+  int32_t causal;                 // 1: keys j <= i; 0: every key of the sequence
   float scale_log2;
 };
 
@@ -125,8 +128,12 @@ __device__ __forceinline__ void store_dequant(uint8_t* dst, const CodeRegs& r, i
   }
 }
 
+// key tiles [0, kt_end) of query tile qt can take part
+__device__ __forceinline__ int key_tile_end(const PParams& p, int qt) { return p.causal ? qt + 1 : p.nT; }
+
 __device__ __forceinline__ int next_kept(const PParams& p, int qt, int kt) {
-  while (kt <= qt && !tile_kept(p, qt, kt)) ++kt;
+  const int end = key_tile_end(p, qt);
+  while (kt < end && !tile_kept(p, qt, kt)) ++kt;
   return kt;
 }
 
@@ -176,8 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   // 32 x (80 + 192 + 120 + 120) = 16384, its whole register file.
 
   // number of kept key tiles (identical in every role)
+  const int kt_end = key_tile_end(p, qt);
   int n_kept = 0;
-  for (int kt = 0; kt <= qt; ++kt) n_kept += tile_kept(p, qt, kt) ? 1 : 0;
+  for (int kt = 0; kt < kt_end; ++kt) n_kept += tile_kept(p, qt, kt) ? 1 : 0;
 
   if (warp < 4) {
   tc::reg_dealloc<80>();
@@ -286,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     // next part's codes are already on their way from L2 / HBM
     CodeRegs ra, rb;
     int kt = next_kept(p, qt, 0);
-    if (kt <= qt) load_codes(ra, kcodes + static_cast<size_t>(kt) * kT * kD, ksz + kt * kT * 4, wt);
-    for (int j = 0; kt <= qt; ++j) {
+    if (kt < kt_end) load_codes(ra, kcodes + static_cast<size_t>(kt) * kT * kD, ksz + kt * kT * 4, wt);
+    for (int j = 0; kt < kt_end; ++j) {
       const int st = j & 1;
       const int kt_next = next_kept(p, qt, kt + 1);
       load_codes(rb, vcodes + static_cast<size_t>(kt) * kT * kD, vsz + kt * kT * 4, wt);
@@ -296,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[B_KFULL0 + st]);
-      if (kt_next <= qt)
+      if (kt_next < kt_end)
         load_codes(ra, kcodes + static_cast<size_t>(kt_next) * kT * kD, ksz + kt_next * kT * 4, wt);
       store_dequant(smem + kOff_V + st * kQBytes, rb, wt);
       fence_proxy_async_smem();
@@ -320,9 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   float m_run = -INFINITY, l_run = 0.0f;
   bool ok = true;
   int j = 0;
-  for (int kt = 0; kt <= qt && ok; ++kt) {
+  for (int kt = 0; kt < kt_end && ok; ++kt) {
     if (!tile_kept(p, qt, kt)) continue;
-    const bool diag = kt == qt;
+    const bool diag = p.causal && kt == qt;   // the element-wise causal rule
     ok = mbar_wait(&bar[B_SFULL0 + h], j & 1, p.status);
     tc::fence_after_sync();
     // pass 1: row max (the causal rule only applies on the diagonal tile)
@@ -457,6 +465,7 @@ kvq_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.rep = a.Hq / a.Hkv;
   p.pairs = (p.rep + 1) / 2;
   p.nT = a.S / kT;
+  p.causal = a.causal;
   const float scale = a.softmax_scale > 0.0f ? a.softmax_scale : 1.0f / sqrtf(static_cast<float>(kD));
   p.scale_log2 = scale * 1.4426950408889634f;
   if (g_regs_ok < 0) {

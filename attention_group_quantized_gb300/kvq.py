@@ -371,8 +371,9 @@ def build_tile_mask(nT: int, skip_num: int, skip_den: int, seed: int, device="cu
 
 
 def prefill_attention(q, k, v, k_cache: QuantCache, v_cache: QuantCache, softmax_scale: float = 0.0,
-                      tile_mask=None, out=None, out_dtype: int = OUT_F32, status=None, stream=None):
-    """Causal prefill: q bf16 [B][Hq][S][D], k/v bf16 [B][Hkv][S][D]; fills the caches, returns out."""
+                      tile_mask=None, out=None, out_dtype: int = OUT_F32, status=None, stream=None,
+                      causal: bool = True):
+    """Prefill (causal by default): q bf16 [B][Hq][S][D], k/v bf16 [B][Hkv][S][D]; fills the caches, returns out."""
     import torch
     B, Hq, S, D = q.shape
     Hkv = k.shape[1]
@@ -380,8 +381,8 @@ def prefill_attention(q, k, v, k_cache: QuantCache, v_cache: QuantCache, softmax
         out = torch.empty((B, Hq, S, D), dtype=torch.float32 if out_dtype == OUT_F32 else torch.bfloat16,
                           device=q.device)
     kc, vc = k_cache.c_struct(), v_cache.c_struct()
-    st = lib().kvq_prefill_attention(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, Hq, Hkv, S, D, 1,
-                                     float(softmax_scale),
+    st = lib().kvq_prefill_attention(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, Hq, Hkv, S, D,
+                                     1 if causal else 0, float(softmax_scale),
                                      tile_mask.data_ptr() if tile_mask is not None else None, 128,
                                      ctypes.byref(kc), ctypes.byref(vc), out.data_ptr(), out_dtype,
                                      status.data_ptr() if status is not None else None, _stream_ptr(stream))

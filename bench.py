@@ -16,7 +16,7 @@ Also reported: ``e2e`` (the same metric through the C ABI with the step's
 new inputs copied from pinned host memory and the output read back every
 step), ``roofline`` for the split kernel, the CPU oracle timed on a bounded
 sample (``cpu_baseline``), clocks sampled during the timed region, and the
-causal prefill workload's TFLOP/s when the prefill kernel is available.
+causal and non-causal prefill workloads' TFLOP/s when the prefill kernel is available.
 """
 from __future__ import annotations
 
@@ -351,37 +351,51 @@ def bench_quantize(torch, kvq, inp, peaks, steps, warmup, dev):
                          "frac": gbs / peaks["hbm_gbs"], "peak_src": peaks["hbm_src"]}}
 
 
-def bench_prefill(torch, kvq, W, peaks, steps, warmup, dev):
-    """Causal prefill workload (quantise K/V + tile-masked attention): TFLOP/s."""
+def bench_prefill(torch, kvq, W, peaks, steps, warmup, dev, causal=True):
+    """Prefill workload (quantise K/V + attention): TFLOP/s.  Causal: the
+    tile-masked causal workload; non-causal: the same shapes, every key visible,
+    no mask."""
     import numpy as np
-    inp = W.prefill_causal()
+    inp = W.prefill_causal() if causal else W.prefill_noncausal()
     B, Hq, Hkv, S, D = inp.B, inp.Hq, inp.Hkv, inp.S, inp.D
     todev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
     q, k, v = todev(inp.q), todev(inp.k), todev(inp.v)
-    mask = torch.from_numpy(inp.tile_mask).to(dev)
+    mask = torch.from_numpy(inp.tile_mask).to(dev) if inp.tile_mask is not None else None
+    run = lambda: kvq.prefill_attention(q, k, v, kc, vc, inp.softmax_scale, mask, out=out, out_dtype=kvq.OUT_BF16,
+                                        causal=causal)
     kc = kvq.empty_cache(inp.head_bits, B, S, D, device=dev)
     vc = kvq.empty_cache(inp.head_bits, B, S, D, device=dev)
     out = torch.empty((B, Hq, S, D), dtype=torch.bfloat16, device=dev)
     try:
-        kvq.prefill_attention(q, k, v, kc, vc, inp.softmax_scale, mask, out=out, out_dtype=kvq.OUT_BF16)
+        run()
     except kvq.KvqError as e:
         return {"unavailable": str(e)}
     n_t = S // 128
-    kept = int(np.tril(inp.tile_mask, -1).sum())
-    flops = 4.0 * D * Hq * B * (kept * 128 * 128 + n_t * 128 * 129 / 2)
+    if causal:
+        kept = int(np.tril(inp.tile_mask, -1).sum())
+        flops = 4.0 * D * Hq * B * (kept * 128 * 128 + n_t * 128 * 129 / 2)
+    else:
+        flops = 4.0 * D * Hq * B * S * S
     for _ in range(warmup):
-        kvq.prefill_attention(q, k, v, kc, vc, inp.softmax_scale, mask, out=out, out_dtype=kvq.OUT_BF16)
+        run()
     torch.cuda.synchronize()
     times = []
     for _ in range(steps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        kvq.prefill_attention(q, k, v, kc, vc, inp.softmax_scale, mask, out=out, out_dtype=kvq.OUT_BF16)
+        run()
         e1.record()
         torch.cuda.synchronize()
         times.append(e0.elapsed_time(e1) / 1e3)
     t = statistics.mean(times)
     tf = flops / t / 1e12
+    res = {"workload": inp.name, "value": tf, "unit": "TFLOP/s", "ms_per_step": t * 1e3,
+           "algorithmic_flop": flops,
+           "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                        "frac": tf / peaks["bf16_tflops"], "peak_src": peaks["bf16_src"],
+                        "note": "time includes the two quantise launches of the same call"}}
+    if not causal:
+        return res
     # the device-side tile-mask builder for this prefill's grid (25 % of the candidate tiles per row)
     for _ in range(3):
         kvq.build_tile_mask(n_t, 1, 4, 4, device=dev)
@@ -393,12 +407,8 @@ def bench_prefill(torch, kvq, W, peaks, steps, warmup, dev):
     e1.record()
     torch.cuda.synchronize()
     mask_us = e0.elapsed_time(e1) * 1e3 / 10
-    return {"workload": inp.name, "value": tf, "unit": "TFLOP/s", "ms_per_step": t * 1e3,
-            "algorithmic_flop": flops,
-            "tile_mask_build_us": {"nT": n_t, "skip": "1/4 per row", "us": mask_us},
-            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                         "frac": tf / peaks["bf16_tflops"], "peak_src": peaks["bf16_src"],
-                         "note": "time includes the two quantise launches of the same call"}}
+    res["tile_mask_build_us"] = {"nT": n_t, "skip": "1/4 per row", "us": mask_us}
+    return res
 
 
 def main():
@@ -414,7 +424,7 @@ def main():
     ap.add_argument("--busy-seconds", type=float, default=1.0,
                     help="untimed sustained decode steps before the timed ones, under the clock sampler")
     ap.add_argument("--only-prefill", action="store_true",
-                    help="run only the causal prefill workload and print its JSON object")
+                    help="run only the prefill workloads (causal, non-causal) and print their JSON object")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -441,7 +451,9 @@ def main():
     peaks = _peaks()
     if args.only_prefill:
         if rank == 0:
-            print(json.dumps(bench_prefill(torch, kvq, W, peaks, args.steps, args.warmup, dev)))
+            res = bench_prefill(torch, kvq, W, peaks, args.steps, args.warmup, dev)
+            res["non_causal"] = bench_prefill(torch, kvq, W, peaks, args.steps, args.warmup, dev, causal=False)
+            print(json.dumps(res))
         if dist:
             dist.destroy_process_group()
         return
@@ -508,6 +520,7 @@ def main():
     prefill = None
     if not args.no_prefill and rank == 0:
         prefill = bench_prefill(torch, kvq, W, peaks, max(3, min(args.steps, 10)), 3, dev)
+        prefill["non_causal"] = bench_prefill(torch, kvq, W, peaks, 3, 3, dev, causal=False)
     extras = None
     if not args.no_extras and rank == 0:
         extras = bench_extra_decodes(torch, kvq, W, peaks, dev, args.steps, args.warmup)

@@ -146,23 +146,26 @@ KVQ_API kvq_status kvq_decode_attention(const void* q, const kvq_cache* k, const
                                 int32_t* dev_status, void* stream);
 
 /*
- * kvq_prefill_attention -- causal prefill over a group-quantised KV cache.
+ * kvq_prefill_attention -- prefill (causal or not) over a group-quantised KV cache.
  *
  * Quantises K and V into k_cache / v_cache (positions 0 .. S-1, exactly as
  * kvq_quantize), then computes, per query head h and query position i,
  *   O[i] = softmax_j(scale * Q[i] . K_hat[j]) V_hat[j]
- * over keys j <= i (P1 §3.1 with the causal rule), where K_hat, V_hat are the
- * dequantised cache rows, tile by tile with an online softmax (P4 §2.2).
- * With a tile mask (P4 §1.3, §2.3: skipped blocks are not computed), key tile
- * kt < query tile qt takes part only if tile_mask[qt * nT + kt] != 0, where
- * nT = S / tile; the keys of a skipped tile are left out of the softmax.
- * Diagonal tiles are always computed with the element-wise causal rule.
+ * over keys j <= i when causal == 1 (P1 §3.1 with the causal rule), over all
+ * keys j < S when causal == 0, where K_hat, V_hat are the dequantised cache
+ * rows, tile by tile with an online softmax (P4 §2.2).
+ * With a tile mask (P4 §1.3, §2.3: skipped blocks are not computed), an
+ * off-diagonal key tile kt of query tile qt takes part only if
+ * tile_mask[qt * nT + kt] != 0, where nT = S / tile; the keys of a skipped
+ * tile are left out of the softmax.  Causal prefill reads only kt < qt of the
+ * mask; non-causal reads every off-diagonal entry.  Diagonal tiles are always
+ * computed (element-wise causal rule when causal == 1, whole when 0).
  *
  * q:    device bf16 [B][Hq][S][D]; k, v: device bf16 [B][Hkv][S][D];
  *       contiguous, 16-byte aligned.
- * causal must be 1; tile must be 128; S a multiple of 128; D == 128;
+ * causal 0 or 1; tile must be 128; S a multiple of 128; D == 128;
  * Hq % Hkv == 0; caches 8-bit for every head, Tcap >= S.
- * tile_mask: device uint8 [nT][nT] or NULL (dense causal).
+ * tile_mask: device uint8 [nT][nT] or NULL (every tile kept).
  * out:  device [B][Hq][S][D], fp32 or bf16.
  */
 KVQ_API kvq_status kvq_prefill_attention(const void* q, const void* k, const void* v,

@@ -220,6 +220,12 @@ def decode_long_ragged() -> DecodeInputs:
                        lens="uniform", len_range=(32768, 131072), bits="4")
 
 
+def prefill_noncausal() -> PrefillInputs:
+    """Prefill non-causal: the causal workload's shapes (B1, 32/8 heads, D128, S32768, INT8 KV), no tile mask."""
+    return make_prefill("prefill_noncausal_b1_h32kv8_d128_s32768_dense", 3, 1, 32, 8, 128, 32768,
+                        mask_seed=None)
+
+
 def prefill_causal() -> PrefillInputs:
     """Prefill causal: B1, 32/8 heads, D128, S32768, INT8 KV, 25% of below-diagonal tiles skipped."""
     return make_prefill("prefill_causal_b1_h32kv8_d128_s32768_skip25", 3, 1, 32, 8, 128, 32768,

@@ -36,10 +36,11 @@ Readings taken where the pages are silent (each listed in the design notes):
 * INT4 packing: two codes per byte, even channel in the low nibble.
 * Dequantisation: x_hat = (code - zero) * scale, evaluated exactly in float64.
 * Decode: the single query of sequence b attends keys 0 .. len_b-1.
-* Prefill: causal (key j visible to query i iff j <= i); a tile-mask entry 0
-  at (query tile, key tile) below the diagonal removes those keys from the
-  softmax entirely, as if their scores were -inf; diagonal tiles are always
-  computed with the element-wise causal rule.
+* Prefill: causal (key j visible to query i iff j <= i) or non-causal (every
+  key of the sequence visible); a tile-mask entry 0 at an off-diagonal
+  (query tile, key tile) removes those keys from the softmax entirely, as if
+  their scores were -inf; diagonal tiles are always computed (with the
+  element-wise causal rule when causal).
 * GQA: query head h reads KV head h // (Hq / Hkv).
 
 Parity pins for every function live in tests/test_oracle_pins.py.
@@ -200,15 +201,15 @@ def decode_attention(q_bits: np.ndarray, k_hat: np.ndarray, v_hat: np.ndarray,
 
 
 def prefill_allowed(rows: np.ndarray, n_keys: int, tile_mask: np.ndarray | None,
-                    tile: int = 128) -> np.ndarray:
+                    tile: int = 128, causal: bool = True) -> np.ndarray:
     """Visibility of keys 0..n_keys-1 to the given query rows.
 
-    Key j is visible to query i iff j <= i and, for key tiles strictly below
-    the query's own tile, tile_mask[i // tile][j // tile] == 1.
+    Key j is visible to query i iff (j <= i, when causal) and, for key tiles
+    other than the query's own tile, tile_mask[i // tile][j // tile] == 1.
     """
     i = np.asarray(rows)[:, None]
     j = np.arange(n_keys)[None, :]
-    ok = j <= i
+    ok = j <= i if causal else np.ones((i.shape[0], n_keys), dtype=bool)
     if tile_mask is not None:
         qt = i // tile
         kt = j // tile
@@ -220,19 +221,20 @@ def prefill_allowed(rows: np.ndarray, n_keys: int, tile_mask: np.ndarray | None,
 
 def prefill_rows(q_bits: np.ndarray, k_hat: np.ndarray, v_hat: np.ndarray, b: int, h: int,
                  rows: np.ndarray, tile_mask: np.ndarray | None, softmax_scale: float,
-                 tile: int = 128) -> np.ndarray:
-    """Causal (tile-masked) attention output for selected query rows of one head.
+                 tile: int = 128, causal: bool = True) -> np.ndarray:
+    """(Tile-masked) attention output for selected query rows of one head.
 
-    q_bits: bf16 [B][Hq][S][D]; k_hat, v_hat: float64 [B][Hkv][S][D].
+    q_bits: bf16 [B][Hq][S][D]; k_hat, v_hat: float64 [B][Hkv][S][D].  Causal
+    rows see keys up to their own position, non-causal rows all S keys.
     Returns float64 [len(rows)][D].
     """
     Hq = q_bits.shape[1]
     Hkv = k_hat.shape[1]
     kv = h // (Hq // Hkv)
     rows = np.asarray(rows)
-    n_keys = int(rows.max()) + 1
+    n_keys = int(rows.max()) + 1 if causal else q_bits.shape[2]
     q = bf16_to_f32(q_bits[b, h, rows]).astype(np.float64)
-    allowed = prefill_allowed(rows, n_keys, tile_mask, tile)
+    allowed = prefill_allowed(rows, n_keys, tile_mask, tile, causal)
     return attention(q, k_hat[b, kv, :n_keys], v_hat[b, kv, :n_keys], softmax_scale, allowed)
 
 

@@ -101,7 +101,7 @@ def test_prefill_validation_without_launch(L):
     v, hv = _cache([8, 8], Tcap=256)
     P = ctypes.byref
     a = 0x8000
-    assert L.kvq_prefill_attention(a, a, a, 1, 4, 2, 256, 128, 0, 0.0, None, 128, P(k), P(v), a, 0, None, None) == 2
+    assert L.kvq_prefill_attention(a, a, a, 1, 4, 2, 256, 128, 2, 0.0, None, 128, P(k), P(v), a, 0, None, None) == 2
     assert L.kvq_prefill_attention(a, a, a, 1, 4, 2, 256, 128, 1, 0.0, None, 64, P(k), P(v), a, 0, None, None) == 2
     assert L.kvq_prefill_attention(a, a, a, 1, 4, 2, 200, 128, 1, 0.0, None, 128, P(k), P(v), a, 0, None, None) == 2
     assert L.kvq_prefill_attention(a, a, a, 1, 4, 2, 512, 128, 1, 0.0, None, 128, P(k), P(v), a, 0, None, None) == 1

@@ -313,6 +313,34 @@ def test_prefill_mask_semantics_brute_force():
     assert np.allclose(O.prefill_rows(q, k, v, 0, 0, np.array([0]), mask, 0.8, tile)[0], v[0, 0, 0])
 
 
+def test_prefill_non_causal_mask_semantics_brute_force():
+    """Non-causal + tile mask (entries above and below the diagonal) with tile 2
+    on 7 tokens, against key deletion in scalar Python."""
+    rng = np.random.default_rng(16)
+    S, D, tile = 7, 4, 2
+    q = _bf16_of(rng.standard_normal((1, 3, S, D)))
+    k = rng.standard_normal((1, 1, S, D)); v = rng.standard_normal((1, 1, S, D))
+    mask = np.ones((4, 4), np.uint8); mask[0, 3] = 0; mask[1, 0] = 0; mask[1, 2] = 0; mask[3, 1] = 0
+    mask[2, 2] = 0                                   # a diagonal entry is ignored: the tile is always kept
+    rows = np.arange(S)
+    qf = O.bf16_to_f32(q).astype(np.float64)
+    for h in range(3):
+        got = O.prefill_rows(q, k, v, 0, h, rows, mask, 0.8, tile, causal=False)
+        for i in range(S):
+            keys = [j for j in range(S) if j // tile == i // tile or mask[i // tile, j // tile]]
+            want = _brute_attention([qf[0, h, i].tolist()], k[0, 0, keys].tolist(), v[0, 0, keys].tolist(), 0.8)
+            assert np.allclose(got[i], want[0], rtol=1e-12, atol=1e-13)
+    # the last row, non-causal with no mask, is plain attention over all keys; row 0 too
+    for r in (0, S - 1):
+        want = _brute_attention([qf[0, 0, r].tolist()], k[0, 0].tolist(), v[0, 0].tolist(), 0.8)
+        got = O.prefill_rows(q, k, v, 0, 0, np.array([r]), None, 0.8, tile, causal=False)
+        assert np.allclose(got[0], want[0], rtol=1e-12, atol=1e-13)
+    # causal and non-causal agree on the last row when the mask keeps every tile
+    a = O.prefill_rows(q, k, v, 0, 1, np.array([S - 1]), None, 0.8, tile, causal=True)
+    b = O.prefill_rows(q, k, v, 0, 1, np.array([S - 1]), None, 0.8, tile, causal=False)
+    assert np.array_equal(a, b)
+
+
 def test_prefill_all_ones_mask_equals_dense_causal():
     rng = np.random.default_rng(7)
     S, D = 300, 16
