@@ -1,9 +1,13 @@
 // kvq_api.cu -- the C ABI of libkvq: argument validation, cache layout,
 // tensor-map encoding and dispatch to the kernels.  Nothing here allocates
 // device memory or synchronises; every launch goes to the caller's stream.
+#include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <cudaTypedefs.h>
 #include <mutex>
+#include <numeric>
+#include <vector>
 
 #include "kvq_internal.h"
 
@@ -381,6 +385,54 @@ kvq_status kvq_build_tile_mask(uint8_t* mask, int32_t nT, int32_t skip_num, int3
   return launch_tile_mask(mask, nT, skip_num, skip_den, seed, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? KVQ_OK
              : KVQ_ERR_CUDA;
+}
+
+size_t kvq_head_error_stats_workspace_bytes(int32_t H) {
+  return H <= 0 ? 0 : static_cast<size_t>(H) * kHeadStatsMaxChunks * 2 * sizeof(double);
+}
+
+kvq_status kvq_head_error_stats(const void* x, int32_t B, int32_t H, int32_t T, int32_t D, const int32_t* seq_lens,
+                                const float* weights, int32_t bits, double* stats, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (x == nullptr || stats == nullptr || B <= 0 || H <= 0 || H > 65535 || T <= 0) return KVQ_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(B) * T >= (int64_t(1) << 31)) return KVQ_ERR_INVALID_ARG;   // rows in 32 bits
+  if (bits != 4 && bits != 8) return KVQ_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return KVQ_ERR_UNSUPPORTED;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(stats) & 7u) != 0 ||
+      (weights != nullptr && (reinterpret_cast<uintptr_t>(weights) & 3u) != 0))
+    return KVQ_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < kvq_head_error_stats_workspace_bytes(H) || !aligned16(workspace))
+    return KVQ_ERR_WORKSPACE;
+  HeadStatsArgs a;
+  a.x = static_cast<const uint16_t*>(x);
+  a.w = weights;
+  a.lens = seq_lens;
+  a.B = B; a.H = H; a.T = T; a.D = D; a.bits = bits;
+  a.part = static_cast<double*>(workspace);
+  a.stats = stats;
+  a.status = dev_status;
+  return launch_head_stats(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+kvq_status kvq_allocate_head_bits(const double* k_stats, const double* v_stats, int32_t H, int32_t n_high,
+                                  int32_t low_bits, int8_t* head_bits, double* score) {
+  if (k_stats == nullptr || v_stats == nullptr || head_bits == nullptr || H <= 0 || n_high < 0 || n_high > H)
+    return KVQ_ERR_INVALID_ARG;
+  if (low_bits != 4 && low_bits != 8) return KVQ_ERR_INVALID_ARG;
+  std::vector<double> sc(static_cast<size_t>(H));
+  for (int32_t h = 0; h < H; ++h) {
+    const double* k = k_stats + 2 * h;
+    const double* v = v_stats + 2 * h;
+    sc[h] = (k[1] != 0.0 ? k[0] / k[1] : 0.0) + (v[1] != 0.0 ? v[0] / v[1] : 0.0);
+    if (!std::isfinite(sc[h])) return KVQ_ERR_NONFINITE;
+  }
+  std::vector<int32_t> order(static_cast<size_t>(H));
+  std::iota(order.begin(), order.end(), 0);
+  // largest score first; a stable sort keeps equal scores in head order
+  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return sc[a] > sc[b]; });
+  for (int32_t i = 0; i < H; ++i) head_bits[order[i]] = static_cast<int8_t>(i < n_high ? 8 : low_bits);
+  if (score != nullptr) std::copy(sc.begin(), sc.end(), score);
+  return KVQ_OK;
 }
 
 kvq_status kvq_prefill_attention(const void* q, const void* k, const void* v, int32_t B, int32_t Hq, int32_t Hkv,

@@ -99,6 +99,20 @@ kvq_status launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 
 cudaError_t launch_tile_mask(uint8_t* mask, int nT, int num, int den, uint64_t seed, cudaStream_t stream);
 
+// per-KV-head quantisation-error statistics (two launches: chunk partials, fixed-order sum)
+constexpr int kHeadStatsMaxChunks = 256;
+struct HeadStatsArgs {
+  const uint16_t* x;        // bf16 [B][H][T][D]
+  const float* w;           // [B][H][T] or null
+  const int32_t* lens;      // [B] or null
+  int32_t B, H, T, D, bits;
+  double* part;             // [H][kHeadStatsMaxChunks][2] scratch
+  double* stats;            // [H][2]
+  int32_t* status;
+};
+int head_stats_chunks(int B, int H, int T, int D);
+cudaError_t launch_head_stats(const HeadStatsArgs& a, cudaStream_t stream);
+
 // cuTensorMapEncodeTiled, resolved from the driver at first use (no link to
 // libcuda, so the library loads on machines without a GPU driver).
 CUresult encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base,

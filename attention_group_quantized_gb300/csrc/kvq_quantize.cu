@@ -7,8 +7,8 @@
 // 16-byte loads, the group's range, one IEEE division for the scale and one
 // correctly rounded reciprocal, then each code from x times the reciprocal,
 // rounded by a 1.5 * 2^23 addend on the FMA pipe rather than the conversion
-// unit (exact division only where that product is within 2^-13 of a
-// half-integer, see code_fast), and one 32-byte (INT8) or 16-byte
+// unit (where that product is within 2^-13 of a half-integer, an exact
+// remainder decides instead, see code_near), and one 32-byte (INT8) or 16-byte
 // (INT4) store of codes; a warp's stores cover whole contiguous rows.  The
 // result is bit-identical to the specification's IEEE fp32 arithmetic.
 #include "kvq_device.cuh"
@@ -73,7 +73,7 @@ constexpr int kRoundAddBits = 0x4B400000;
 // When |e| is more than 2^-13 below 1/2, t + z and fl(x / s) + z lie on the
 // same side of every half-integer, so rne(t + z) = rne(fl(x / s)) + z.
 // Otherwise (and for a NaN quotient) `near` is set and the caller redoes the
-// group with the exact division.
+// group's codes with code_checked.
 __device__ __forceinline__ int code_fast(float x, float rcp, float C, int qmax, bool& near) {
   const float t = __fmul_rn(x, rcp);
   const float m = __fadd_rn(t, C);
@@ -117,8 +117,19 @@ __device__ __forceinline__ void load_group(uint32_t (&w)[16], const uint16_t* sr
   }
 }
 
-__device__ __forceinline__ void quantize_group(const uint32_t (&w)[16], int bits, uint8_t* cdst, uint32_t* szw,
-                                               int32_t* status) {
+// A group's parameters: the range widened to contain 0, the fp16 scale
+// s = round-up(range / qmax), the zero point z = clamp(rne(-lo / s), 0, qmax)
+// (one exact quotient per group), and the fast path's constants.
+struct GroupParams {
+  __half scale_h;   // 1 when the range is 0
+  float mn, mx;     // the group's min and max (before widening)
+  float sf, rcp, zf, C;
+  int qmax;
+  bool flat;        // range 0 (all zeros, or NaN among zeros): every code 0
+  bool bad;         // non-finite scale
+};
+
+__device__ __forceinline__ GroupParams group_params(const uint32_t (&w)[16], int bits) {
   // min and max over the 32 values in bf16 pairs (exact), then the two lanes
   __nv_bfloat162 mn2 = *reinterpret_cast<const __nv_bfloat162*>(&w[0]), mx2 = mn2;
 #pragma unroll
@@ -129,48 +140,188 @@ __device__ __forceinline__ void quantize_group(const uint32_t (&w)[16], int bits
   }
   const float mn = fminf(__low2float(mn2), __high2float(mn2));
   const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
-  const int qmax = (1 << bits) - 1;
-  const float qf = static_cast<float>(qmax);
+  GroupParams g;
+  g.mn = mn;
+  g.mx = mx;
+  g.qmax = (1 << bits) - 1;
+  const float qf = static_cast<float>(g.qmax);
   const float lo = fminf(0.0f, mn);
   const float hi = fmaxf(0.0f, mx);
   const float range = __fsub_rn(hi, lo);
+  g.flat = range == 0.0f;
+  g.scale_h = __ushort_as_half(0x3C00);  // 1.0
+  g.sf = 1.0f; g.rcp = 1.0f; g.zf = 0.0f; g.C = kRoundAdd;
+  g.bad = false;
+  if (!g.flat) {
+    g.scale_h = __float2half_ru(__fdiv_rn(range, qf));
+    g.sf = __half2float(g.scale_h);
+    g.bad = !isfinite(g.sf);
+    g.rcp = __frcp_rn(g.sf);
+    g.zf = fminf(fmaxf(rintf(__fdiv_rn(-lo, g.sf)), 0.0f), qf);
+    g.C = g.zf + kRoundAdd;   // exact
+  }
+  return g;
+}
 
-  __half scale_h = __ushort_as_half(0x3C00);  // 1.0
-  int zero = 0;
-  uint32_t packed[8];
-  bool bad = false;
-  if (range == 0.0f) {
+// The code by the exact IEEE division (the fallback of code_fast).
+__device__ __forceinline__ int code_exact(float x, const GroupParams& g, bool& bad) {
+  const float q = __fdiv_rn(x, g.sf);
+  bad |= q != q;
+  return static_cast<int>(fminf(fmaxf(rintf(q) + g.zf, 0.0f), static_cast<float>(g.qmax)));
+}
+
+// The code of a value whose fast-path quotient t = fl(x * 1/s) lies within
+// 2^-13 of a half-integer h, without a division.  With u = rne(t) and
+// e = u - t, h = u - copysign(1/2, e).  The specification's quotient
+// fl(x / s) equals h when |x / s - h| < ulp(h) / 2 (x has 8 significant bits
+// and s 11, so x / s never sits on that boundary), and otherwise lies on the
+// same side of h as x / s, within 1/2 of it.  Both tests read the remainder
+// r = x - h * s, which is exact in fp32 (h * s has at most 20 significant
+// bits and |r| is far below |x|).  rne(fl(x / s)) is then the even neighbour
+// of h on equality, else the neighbour on r's side.  (Checked against the
+// IEEE quotient for every finite bf16 x, fp16 scales from 2^-24 to 2^8 and
+// several zero points.)
+__device__ __forceinline__ int code_near(float x, float t, float u, const GroupParams& g) {
+  const float e = __fsub_rn(u, t);
+  const float h = __fsub_rn(u, copysignf(0.5f, e));
+  const float r = __fmaf_rn(-h, g.sf, x);
+  const float half_ulp = __int_as_float((__float_as_int(h) & 0x7F800000) - (24 << 23));
+  const float lo = __fsub_rn(h, 0.5f), hi = __fadd_rn(h, 0.5f);
+  float q;
+  if (fabsf(r) < __fmul_rn(half_ulp, g.sf)) q = (__float2int_rn(lo) & 1) == 0 ? lo : hi;
+  else q = r > 0.0f ? hi : lo;
+  return min(max(__float2int_rn(q) + static_cast<int>(g.zf), 0), g.qmax);
+}
+
+// The code of one value: the fast path where it is decided, code_near next
+// to a half-integer, code_exact for a NaN quotient.
+__device__ __forceinline__ int code_checked(float x, const GroupParams& g, bool& bad) {
+  const float t = __fmul_rn(x, g.rcp);
+  const float m = __fadd_rn(t, g.C);
+  const float u = __fsub_rn(m, g.C);
+  if (fabsf(__fsub_rn(u, t)) <= 0.5f - 0x1p-13f) return min(max(__float_as_int(m) - kRoundAddBits, 0), g.qmax);
+  if (t != t) return code_exact(x, g, bad);
+  return code_near(x, t, u, g);
+}
+
+// The rare path of a group, a quarter at a time: the 8 values of quarter v
+// are re-read from `src` (an L1 hit) and passed to f(i, x) with i their index
+// in the group.  The loop stays rolled so the group's registers are not all
+// live at once.
+template <class F>
+__device__ __forceinline__ void for_each_quarter(const uint16_t* src, F f) {
+#pragma unroll 1
+  for (int v = 0; v < 4; ++v) {
+    const uint4 raw = reinterpret_cast<const uint4*>(src)[v];
+    const uint32_t q4[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float x = group_value(w, i);
-      bad |= x != x;
-    }
+    for (int j = 0; j < 8; ++j)
+      f(v, j, bf16_bits_to_float((j & 1) ? (q4[j >> 1] >> 16) : (q4[j >> 1] & 0xFFFFu)));
+  }
+}
+
+__device__ __forceinline__ bool group_has_nan(const uint32_t (&w)[16]) {
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float x = group_value(w, i);
+    bad |= x != x;
+  }
+  return bad;
+}
+
+// src: the group's 32 bf16 values in global memory (what w was loaded from).
+__device__ __forceinline__ void quantize_group(const uint32_t (&w)[16], const uint16_t* src, int bits,
+                                               uint8_t* cdst, uint32_t* szw, int32_t* status) {
+  const GroupParams gp = group_params(w, bits);
+  uint32_t packed[8];
+  bool bad = gp.bad;
+  bool near = false;
+  if (gp.flat) {
+    bad = group_has_nan(w);
 #pragma unroll
     for (int k = 0; k < 8; ++k) packed[k] = 0u;
   } else {
-    scale_h = __float2half_ru(__fdiv_rn(range, qf));
-    const float sf = __half2float(scale_h);
-    bad = !isfinite(sf);
-    const float rcp = __frcp_rn(sf);
-    // zero point: one exact quotient per group
-    const float zf = fminf(fmaxf(rintf(__fdiv_rn(-lo, sf)), 0.0f), qf);
-    zero = static_cast<int>(zf);
-    const float C = zf + kRoundAdd;   // exact
-    bool near = false;
-    pack_codes(packed, bits, [&](int i) { return code_fast(group_value(w, i), rcp, C, qmax, near); });
-    if (near) {   // rare: some quotient is within 2^-13 of a half-integer (or NaN): exact division
-      pack_codes(packed, bits, [&](int i) {
-        const float q = __fdiv_rn(group_value(w, i), sf);
-        bad |= q != q;
-        return static_cast<int>(fminf(fmaxf(rintf(q) + zf, 0.0f), qf));
-      });
-    }
+    pack_codes(packed, bits, [&](int i) { return code_fast(group_value(w, i), gp.rcp, gp.C, gp.qmax, near); });
+  }
+  if (!near) {
+    uint4* dst = reinterpret_cast<uint4*>(cdst);
+    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    if (bits == 8) dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+  } else {   // rare: some quotient is within 2^-13 of a half-integer (or NaN); 8 codes per store
+    uint32_t c8[2] = {0u, 0u};
+    for_each_quarter(src, [&](int v, int j, float x) {
+      const uint32_t c = static_cast<uint32_t>(code_checked(x, gp, bad));
+      if (bits == 8) c8[j >> 2] |= c << (8 * (j & 3));
+      else c8[0] |= c << (4 * j);
+      if (j == 7) {
+        if (bits == 8) reinterpret_cast<uint2*>(cdst)[v] = make_uint2(c8[0], c8[1]);
+        else reinterpret_cast<uint32_t*>(cdst)[v] = c8[0];
+        c8[0] = 0u;
+        c8[1] = 0u;
+      }
+    });
   }
   if (bad) report(status, KVQ_ERR_NONFINITE);
-  uint4* dst = reinterpret_cast<uint4*>(cdst);
-  dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-  if (bits == 8) dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-  *szw = __half_as_ushort(scale_h) | (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(zero))) << 16);
+  *szw = __half_as_ushort(gp.scale_h) |
+         (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(static_cast<int>(gp.zf)))) << 16);
+}
+
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// Squared quantisation error of one group, sum_i (x_i - x_hat_i)^2 with
+// x_hat = (code - z) * s the value the cache would hold at `bits` bits, and
+// its squared norm sum_i x_i^2, two values per instruction (paired fp32).
+// The code is rne(fl(x / s)) + z, and for bf16 x and fp16 s that is
+// rne(x / s) + z exactly: fl(x / s) equals a half-integer h only when x / s
+// does (a nonzero x - h * s is a multiple of 2^(e_x - 20), far above the
+// half-ulp band around h), and otherwise lies on the same side of every
+// half-integer as x / s.  The fast quotient t = fl(x * 1/s) is within 2^-14 of
+// x / s, so u = rne(t) (through the 1.5 * 2^23 addend, as in code_fast) is at
+// most one step from rne(x / s); d = x - u * s is exact (u * s has at most 19
+// significant bits, |d| <= s with s >= |x| / 255), and the error of the
+// nearest code is min(|d|, s - |d|) (s - |d| is exact by Sterbenz where it is
+// the smaller; at a tie both neighbours give s / 2).  This holds while no
+// code is clamped; u is monotone in x, so the group's min and max tell.  A
+// clamped group, or one with a NaN, is redone value by value with
+// code_checked.  Each square-and-add rounds once.
+__device__ __forceinline__ float2 group_sq_error(const uint32_t (&w)[16], const uint16_t* src, int bits, bool& bad) {
+  const GroupParams gp = group_params(w, bits);
+  bad |= gp.bad;
+  if (gp.flat) {   // every value 0 (x_hat = 0): no error; a NaN among zeros is reported
+    bad |= group_has_nan(w);
+    return make_float2(0.0f, 0.0f);
+  }
+  const float2 rcp2 = make_float2(gp.rcp, gp.rcp), c2 = make_float2(gp.C, gp.C);
+  const float2 nc2 = make_float2(-gp.C, -gp.C), ns2 = make_float2(-gp.sf, -gp.sf);
+  float2 err2 = make_float2(0.0f, 0.0f), nrm2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const float2 x2 = bf16x2_to_float2(w[k]);
+    nrm2 = __ffma2_rn(x2, x2, nrm2);
+    const float2 u2 = __fadd2_rn(__fadd2_rn(__fmul2_rn(x2, rcp2), c2), nc2);
+    const float2 d2 = __ffma2_rn(u2, ns2, x2);         // x - u * s, exact
+    const float ax = fabsf(d2.x), ay = fabsf(d2.y);
+    const float2 m2 = make_float2(fminf(ax, __fsub_rn(gp.sf, ax)), fminf(ay, __fsub_rn(gp.sf, ay)));
+    err2 = __ffma2_rn(m2, m2, err2);
+  }
+  float err = __fadd_rn(err2.x, err2.y);
+  const float nrm = __fadd_rn(nrm2.x, nrm2.y);
+  const float qf = static_cast<float>(gp.qmax);
+  const float umn = __fsub_rn(__fadd_rn(__fmul_rn(gp.mn, gp.rcp), gp.C), gp.C);
+  const float umx = __fsub_rn(__fadd_rn(__fmul_rn(gp.mx, gp.rcp), gp.C), gp.C);
+  // a NaN value makes the error sum NaN
+  if (err != err || umn < -gp.zf || umx > qf - gp.zf) {
+    const int zero = static_cast<int>(gp.zf);
+    err = 0.0f;
+    for_each_quarter(src, [&](int, int, float x) {
+      const float d = __fsub_rn(x, __fmul_rn(static_cast<float>(code_checked(x, gp, bad) - zero), gp.sf));
+      err = __fmaf_rn(d, d, err);
+    });
+  }
+  return make_float2(err, nrm);
 }
 
 // resident blocks of 256 threads per SM the register budget is sized for (tunable at build time)
@@ -208,8 +359,9 @@ __global__ void __launch_bounds__(256, KVQ_QUANT_MIN_BLOCKS) quantize_kernel(con
       pos = static_cast<int64_t>(page) * 64 + tl % 64;
     }
     uint32_t w[16];
-    load_group(w, p.x + b * p.sx_b + h * p.sx_h + t * p.sx_t + g * 32);
-    quantize_group(w, bits, p.codes + p.plane_off[h] + pos * (D * bits / 8) + g * (32 * bits / 8),
+    const uint16_t* src = p.x + b * p.sx_b + h * p.sx_h + t * p.sx_t + g * 32;
+    load_group(w, src);
+    quantize_group(w, src, bits, p.codes + p.plane_off[h] + pos * (D * bits / 8) + g * (32 * bits / 8),
                    p.sz + (static_cast<int64_t>(h) * p.B * p.Tcap + pos) * G + g, p.status);
   }
 }
@@ -268,13 +420,127 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ APa
       pos = static_cast<int64_t>(page) * 64 + (len - 1) % 64;
     }
     uint32_t w[16];
-    load_group(w, p.x[job] + bh * D + g * 32);
-    quantize_group(w, bits, p.codes[job] + p.plane_off[h] + pos * (D * bits / 8) + g * (32 * bits / 8),
+    const uint16_t* src = p.x[job] + bh * D + g * 32;
+    load_group(w, src);
+    quantize_group(w, src, bits, p.codes[job] + p.plane_off[h] + pos * (D * bits / 8) + g * (32 * bits / 8),
                    p.sz[job] + (static_cast<int64_t>(h) * p.B * p.Tcap + pos) * G + g, p.status);
   }
 }
 
+// Per-head error statistics: grid (chunks, H); block (c, h) takes groups
+// c * 256 + tid, then every chunks * 256, of head h's B * T * G groups
+// (row r = b * T + t, group g), and writes its (error, norm) sums in fp64 to
+// part[h][c]; head_stats_reduce adds the chunks in a fixed order, so the
+// result does not depend on scheduling.
+struct SParams {
+  FastDiv div_t;            // r -> (b, t)
+  const uint16_t* x;        // bf16 [B][H][T][D]
+  const float* w;           // [B][H][T] or null (1)
+  const int32_t* lens;      // [B] or null (T)
+  double* part;             // [H][chunks][2]
+  int32_t* status;
+  int32_t B, H, T, bits, chunks;
+};
+
+constexpr int kStatThreads = 256;
+constexpr int kStatBlocksPerSM = 4;   // resident blocks the register budget is sized for
+
+template <int D>
+__global__ void __launch_bounds__(kStatThreads, kStatBlocksPerSM) head_stats_kernel(const __grid_constant__ SParams p) {
+  constexpr int G = D / 32;
+  const int h = blockIdx.y;
+  const int64_t n = static_cast<int64_t>(p.B) * p.T * G;
+  // (error, norm) summed in fp32 with Kahan's compensation (sum - comp is the
+  // running total), widened to fp64 once for the block's reduction
+  float2 sum = make_float2(0.0f, 0.0f), comp = make_float2(0.0f, 0.0f);
+  const float2 m1 = make_float2(-1.0f, -1.0f);
+  bool bad = false;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kStatThreads + threadIdx.x; i < n;
+       i += static_cast<int64_t>(p.chunks) * kStatThreads) {
+    const uint32_t r = static_cast<uint32_t>(i / G);
+    const int g = static_cast<int>(i % G);
+    const uint32_t b = p.div_t.div(r);
+    const int t = static_cast<int>(r - b * p.div_t.d);
+    if (p.lens != nullptr && t >= p.lens[b]) continue;
+    const int64_t row = (static_cast<int64_t>(b) * p.H + h) * p.T + t;
+    uint32_t v[16];
+    const uint16_t* src = p.x + row * D + g * 32;
+    load_group(v, src);
+    float2 e = group_sq_error(v, src, p.bits, bad);
+    if (p.w != nullptr) {
+      const float wt = p.w[row];
+      e = __fmul2_rn(e, make_float2(wt, wt));
+    }
+    const float2 y = __ffma2_rn(comp, m1, e);           // e - comp
+    const float2 nsum = __fadd2_rn(sum, y);
+    comp = __ffma2_rn(y, m1, __ffma2_rn(sum, m1, nsum));   // (nsum - sum) - y
+    sum = nsum;
+  }
+  if (bad) report(p.status, KVQ_ERR_NONFINITE);
+  double err = static_cast<double>(sum.x) - static_cast<double>(comp.x);
+  double nrm = static_cast<double>(sum.y) - static_cast<double>(comp.y);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    err += __shfl_down_sync(0xffffffffu, err, o);
+    nrm += __shfl_down_sync(0xffffffffu, nrm, o);
+  }
+  __shared__ double red[kStatThreads / 32][2];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) { red[warp][0] = err; red[warp][1] = nrm; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double e = 0.0, m = 0.0;
+    for (int k = 0; k < kStatThreads / 32; ++k) { e += red[k][0]; m += red[k][1]; }
+    double* out = p.part + (static_cast<int64_t>(h) * p.chunks + blockIdx.x) * 2;
+    out[0] = e;
+    out[1] = m;
+  }
+}
+
+// One warp per head: stats[h] = the sum of part[h][0 .. chunks) in a fixed order.
+__global__ void __launch_bounds__(32) head_stats_reduce(const double* part, int chunks, double* stats) {
+  const int h = blockIdx.x, lane = threadIdx.x;
+  double e = 0.0, m = 0.0;
+  for (int c = lane; c < chunks; c += 32) {
+    e += part[(static_cast<int64_t>(h) * chunks + c) * 2];
+    m += part[(static_cast<int64_t>(h) * chunks + c) * 2 + 1];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    e += __shfl_xor_sync(0xffffffffu, e, o);
+    m += __shfl_xor_sync(0xffffffffu, m, o);
+  }
+  if (lane == 0) {
+    stats[2 * h] = e;
+    stats[2 * h + 1] = m;
+  }
+}
+
 }  // namespace
+
+int head_stats_chunks(int B, int H, int T, int D) {
+  const int64_t groups = static_cast<int64_t>(B) * T * (D / 32);
+  // one resident wave over all heads
+  int64_t c = (static_cast<int64_t>(device_sm_count()) * kStatBlocksPerSM + H - 1) / H;
+  const int64_t need = (groups + kStatThreads - 1) / kStatThreads;
+  if (c > need) c = need;
+  if (c > kHeadStatsMaxChunks) c = kHeadStatsMaxChunks;
+  return c < 1 ? 1 : static_cast<int>(c);
+}
+
+cudaError_t launch_head_stats(const HeadStatsArgs& a, cudaStream_t stream) {
+  SParams p;
+  p.div_t = FastDiv::make(static_cast<uint32_t>(a.T));
+  p.x = a.x; p.w = a.w; p.lens = a.lens;
+  p.part = a.part; p.status = a.status;
+  p.B = a.B; p.H = a.H; p.T = a.T; p.bits = a.bits;
+  p.chunks = head_stats_chunks(a.B, a.H, a.T, a.D);
+  const dim3 grid(static_cast<unsigned>(p.chunks), static_cast<unsigned>(a.H));
+  if (a.D == 128) head_stats_kernel<128><<<grid, kStatThreads, 0, stream>>>(p);
+  else head_stats_kernel<64><<<grid, kStatThreads, 0, stream>>>(p);
+  head_stats_reduce<<<static_cast<unsigned>(a.H), 32, 0, stream>>>(a.part, p.chunks, a.stats);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t stream) {
   QParams p;

@@ -29,7 +29,8 @@ EXPORTS = ("kvq_cache_codes_bytes", "kvq_cache_sz_bytes", "kvq_cache_head_offset
            "kvq_decode_workspace_bytes", "kvq_decode_attention", "kvq_prefill_attention",
            "kvq_decode_attention_noalloc", "kvq_decode_step", "kvq_decode_step_staging_bytes",
            "kvq_decode_step_host", "kvq_quantize_paged", "kvq_decode_attention_paged", "kvq_decode_step_paged",
-           "kvq_build_tile_mask", "kvq_status_str")
+           "kvq_build_tile_mask", "kvq_head_error_stats_workspace_bytes", "kvq_head_error_stats",
+           "kvq_allocate_head_bits", "kvq_status_str")
 
 
 class CBlockTable(ctypes.Structure):
@@ -88,6 +89,12 @@ def lib() -> ctypes.CDLL:
         L.kvq_decode_step_paged.restype = I32
         L.kvq_build_tile_mask.argtypes = [P, I32, I32, I32, ctypes.c_uint64, P]
         L.kvq_build_tile_mask.restype = I32
+        L.kvq_head_error_stats_workspace_bytes.argtypes = [I32]
+        L.kvq_head_error_stats_workspace_bytes.restype = SZ
+        L.kvq_head_error_stats.argtypes = [P, I32, I32, I32, I32, P, P, I32, P, P, SZ, P, P]
+        L.kvq_head_error_stats.restype = I32
+        L.kvq_allocate_head_bits.argtypes = [P, P, I32, I32, I32, P, P]
+        L.kvq_allocate_head_bits.restype = I32
         L.kvq_status_str.argtypes = [I32]; L.kvq_status_str.restype = ctypes.c_char_p
         _LIB = L
     return _LIB
@@ -368,6 +375,46 @@ def build_tile_mask(nT: int, skip_num: int, skip_den: int, seed: int, device="cu
                                    _stream_ptr(stream))
     _check(st, "kvq_build_tile_mask")
     return out
+
+
+def head_error_stats_workspace(H: int, device="cuda"):
+    import torch
+    n = lib().kvq_head_error_stats_workspace_bytes(H)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def head_error_stats(x, bits: int = 4, seq_lens=None, weights=None, workspace=None, out=None, status=None,
+                     stream=None):
+    """Per-head (weighted squared quantisation error, weighted squared norm) of bf16 x [B][H][T][D] at `bits`
+    bits: a device float64 tensor [H][2].  seq_lens: device int32 [B]; weights: device float32 [B][H][T]."""
+    import torch
+    B, H, T, D = x.shape
+    if workspace is None:
+        workspace = head_error_stats_workspace(H, x.device)
+    if out is None:
+        out = torch.empty((H, 2), dtype=torch.float64, device=x.device)
+    st = lib().kvq_head_error_stats(x.data_ptr(), B, H, T, D,
+                                    seq_lens.data_ptr() if seq_lens is not None else None,
+                                    weights.data_ptr() if weights is not None else None, bits,
+                                    out.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                    status.data_ptr() if status is not None else None, _stream_ptr(stream))
+    _check(st, "kvq_head_error_stats")
+    return out
+
+
+def allocate_head_bits(k_stats, v_stats, n_high: int, low_bits: int = 4):
+    """(head_bits int8 [H], score float64 [H]) from K and V statistics (kvq_head_error_stats results, on the
+    device or the host): 8 bits for the n_high most sensitive heads, low_bits for the others."""
+    import numpy as np
+    ks = np.ascontiguousarray(k_stats.cpu().numpy() if hasattr(k_stats, "cpu") else k_stats, dtype=np.float64)
+    vs = np.ascontiguousarray(v_stats.cpu().numpy() if hasattr(v_stats, "cpu") else v_stats, dtype=np.float64)
+    H = ks.shape[0]
+    bits = np.empty(H, dtype=np.int8)
+    score = np.empty(H, dtype=np.float64)
+    st = lib().kvq_allocate_head_bits(ks.ctypes.data, vs.ctypes.data, H, n_high, low_bits, bits.ctypes.data,
+                                      score.ctypes.data)
+    _check(st, "kvq_allocate_head_bits")
+    return bits, score
 
 
 def prefill_attention(q, k, v, k_cache: QuantCache, v_cache: QuantCache, softmax_scale: float = 0.0,

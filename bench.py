@@ -351,6 +351,48 @@ def bench_quantize(torch, kvq, inp, peaks, steps, warmup, dev):
                          "frac": gbs / peaks["hbm_gbs"], "peak_src": peaks["hbm_src"]}}
 
 
+def bench_head_bits(torch, kvq, W, peaks, steps, warmup, dev):
+    """Per-head bit allocation on the head_bits workload (decode_gqa's K/V shape, weighted): one step =
+    kvq_head_error_stats of K and of V (two launches each, the device-side part) back to back between CUDA
+    events; K and V are visited in turn, together larger than L2.  HBM bytes = the bf16 rows + the float
+    weights read by each call.  The host allocation (a sort of H scores) is timed apart, after the
+    statistics are copied back."""
+    import numpy as np
+    inp = W.head_bits_kv()
+    B, H, T, D = inp.k.shape
+    todev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    k, v = todev(inp.k), todev(inp.v)
+    w = torch.from_numpy(inp.weights).to(dev)
+    ws = kvq.head_error_stats_workspace(H, dev)
+    ks = torch.empty((H, 2), dtype=torch.float64, device=dev)
+    vs = torch.empty((H, 2), dtype=torch.float64, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    step = lambda: (kvq.head_error_stats(k, 4, weights=w, workspace=ws, out=ks, status=status),
+                    kvq.head_error_stats(v, 4, weights=w, workspace=ws, out=vs, status=status))
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    t = e0.elapsed_time(e1) / 1e3 / steps / 2            # per call (one tensor)
+    per_call = k.numel() * 2 + w.numel() * 4
+    gbs = per_call / t / 1e9
+    t0 = time.perf_counter()
+    bits, _ = kvq.allocate_head_bits(ks, vs, len(inp.outlier_heads))
+    alloc_us = (time.perf_counter() - t0) * 1e6
+    return {"workload": inp.name, "value": gbs, "unit": "GB/s", "us_per_call": t * 1e6,
+            "bytes_per_call": int(per_call), "host_allocation_us": alloc_us,
+            "chosen_8bit_heads": [int(h) for h in np.flatnonzero(bits == 8)],
+            "outlier_heads": [int(h) for h in inp.outlier_heads],
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "peak_src": peaks["hbm_src"]}}
+
+
 def bench_prefill(torch, kvq, W, peaks, steps, warmup, dev, causal=True):
     """Prefill workload (quantise K/V + attention): TFLOP/s.  Causal: the
     tile-masked causal workload; non-causal: the same shapes, every key visible,
@@ -425,6 +467,8 @@ def main():
                     help="untimed sustained decode steps before the timed ones, under the clock sampler")
     ap.add_argument("--only-prefill", action="store_true",
                     help="run only the prefill workloads (causal, non-causal) and print their JSON object")
+    ap.add_argument("--only-head-bits", action="store_true",
+                    help="run only the per-head bit allocation workload and print its JSON object")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -449,6 +493,12 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     kvq.lib()   # fail loudly if the library is missing
     peaks = _peaks()
+    if args.only_head_bits:
+        if rank == 0:
+            print(json.dumps(bench_head_bits(torch, kvq, W, peaks, args.steps, args.warmup, dev)))
+        if dist:
+            dist.destroy_process_group()
+        return
     if args.only_prefill:
         if rank == 0:
             res = bench_prefill(torch, kvq, W, peaks, args.steps, args.warmup, dev)
@@ -517,6 +567,9 @@ def main():
     quant = None
     if rank == 0:
         quant = bench_quantize(torch, kvq, inp, peaks, max(5, min(args.steps, 20)), 3, dev)
+    head_bits = None
+    if rank == 0:
+        head_bits = bench_head_bits(torch, kvq, W, peaks, max(5, min(args.steps, 20)), 3, dev)
     prefill = None
     if not args.no_prefill and rank == 0:
         prefill = bench_prefill(torch, kvq, W, peaks, max(3, min(args.steps, 10)), 3, dev)
@@ -555,6 +608,7 @@ def main():
             "gpu_launches": args.steps,
             "quantize": quant,
             "prefill": prefill,
+            "head_bits": head_bits,
             "other_decode_workloads": extras,
         }
         print(json.dumps(line))

@@ -177,6 +177,52 @@ KVQ_API kvq_status kvq_prefill_attention(const void* q, const void* k, const voi
                                  int32_t* dev_status, void* stream);
 
 /*
+ * kvq_head_error_stats -- per-head quantisation-error statistics, the input
+ * of a sensitivity-driven per-head bit allocation (P4 §2.4: every attention
+ * head gets a sensitivity score; sensitive heads are stored at the higher
+ * bit-width, the rest at the lower one).
+ *
+ * For each head h, with x_hat the dequantised value that kvq_quantize would
+ * store at `bits` bits (the same codes, bit for bit):
+ *   stats[h][0] = sum_{b, t < len_b} w[b][h][t] * sum_d (x - x_hat)^2
+ *   stats[h][1] = sum_{b, t < len_b} w[b][h][t] * sum_d x^2
+ * x:        device bf16 [B][H][T][D], contiguous, 16-byte aligned; D 64 or 128.
+ * seq_lens: device int32 [B] or NULL (every sequence T tokens); tokens
+ *           t >= len_b are left out.
+ * weights:  device float [B][H][T] or NULL (1): a per-token attention mass,
+ *           expected >= 0.
+ * bits:     4 or 8.
+ * stats:    device double [H][2], written whole.
+ * workspace: device, at least kvq_head_error_stats_workspace_bytes(H) bytes,
+ *           16-byte aligned, else KVQ_ERR_WORKSPACE.
+ * The sums are fp32 within a 32-channel group and fp64 beyond it, in an order
+ * fixed by the sizes and the device (the same result on every call).
+ * Non-finite input reports KVQ_ERR_NONFINITE in dev_status.  Two launches.
+ */
+KVQ_API size_t kvq_head_error_stats_workspace_bytes(int32_t H);
+KVQ_API kvq_status kvq_head_error_stats(const void* x, int32_t B, int32_t H, int32_t T, int32_t D,
+                                const int32_t* seq_lens, const float* weights, int32_t bits,
+                                double* stats, void* workspace, size_t workspace_bytes,
+                                int32_t* dev_status, void* stream);
+
+/*
+ * kvq_allocate_head_bits -- per-head bit-widths from K and V error statistics
+ * (host function; P4 §2.4, and P4 §3.4: keeping more heads at high precision
+ * trades compression, about 4x down to 2.5x, for accuracy).
+ *
+ * score[h] = k_stats[h][0] / k_stats[h][1] + v_stats[h][0] / v_stats[h][1]
+ * (a term with a zero norm counts 0): the relative error of the head's K and
+ * V at the low bit-width.  The n_high heads with the largest scores get 8
+ * bits, ties going to the smaller head index; the others get low_bits.
+ * k_stats, v_stats: host double [H][2] (kvq_head_error_stats, copied back);
+ * head_bits: host int8 [H], written; score: host double [H] or NULL.
+ * 0 <= n_high <= H; low_bits 4 or 8.  A non-finite score returns
+ * KVQ_ERR_NONFINITE and writes nothing.
+ */
+KVQ_API kvq_status kvq_allocate_head_bits(const double* k_stats, const double* v_stats, int32_t H,
+                                  int32_t n_high, int32_t low_bits, int8_t* head_bits, double* score);
+
+/*
  * kvq_build_tile_mask -- a block-sparse tile mask for kvq_prefill_attention
  * (P4 §2.3: tiles judged unnecessary are skipped, the skipped share capped so
  * that no query block is starved), built on the GPU.

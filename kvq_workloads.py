@@ -238,6 +238,51 @@ def decode_mixed() -> DecodeInputs:
                        bits="mixed", outliers_per_head=2, outlier_head_mult=8.0)
 
 
+@dataclass
+class SensitivityInputs:
+    """K and V rows [B][H][T][D] (bf16 bits) whose per-head statistics choose the bit-widths."""
+    name: str
+    k: np.ndarray
+    v: np.ndarray
+    seq_lens: np.ndarray                  # int32 [B]
+    weights: Optional[np.ndarray]         # float32 [B][H][T] attention mass per token, or None
+    outlier_heads: np.ndarray             # heads whose K carries outlier channels
+    H: int
+    D: int
+    T: int
+
+
+def make_sensitivity(name: str, seed: int, B: int, H: int, D: int, T: int, outlier_heads,
+                     n_outlier_ch: int = 4, outlier_mult: float = 10.0, lens="full",
+                     weights: bool = True) -> SensitivityInputs:
+    """Heads listed in ``outlier_heads`` get ``n_outlier_ch`` K channels scaled by
+    ``outlier_mult`` (channels drawn per head); the other heads are plain N(0,1).
+    Draw order: outlier channels, K, V (each [B][H][T][D] in C order), then the
+    weights, float32 exponential(1) per token ([B][H][T]); lengths "full" or an
+    explicit list (tokens past a sequence's length are zero)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    seq_lens = (np.full(B, T, dtype=np.int32) if isinstance(lens, str)
+                else np.asarray(lens, dtype=np.int32))
+    kscale = np.ones((H, D), dtype=np.float32)
+    for h in outlier_heads:
+        ch = rng.choice(D, n_outlier_ch, replace=False)
+        kscale[h, ch] *= np.float32(outlier_mult)
+    k = _draw_bf16(rng, (B, H, T, D), kscale)
+    v = _draw_bf16(rng, (B, H, T, D))
+    w = rng.exponential(1.0, size=(B, H, T)).astype(np.float32) if weights else None
+    for b in range(B):
+        k[b, :, seq_lens[b]:] = 0
+        v[b, :, seq_lens[b]:] = 0
+    return SensitivityInputs(name, k, v, seq_lens, w, np.asarray(sorted(outlier_heads), dtype=np.int32),
+                             H, D, T)
+
+
+def head_bits_kv() -> SensitivityInputs:
+    """Per-head bit allocation input: decode_gqa's K/V shape (B8, 8 KV heads, D128, 8192 tokens);
+    heads 1, 4, 6 carry 4 K outlier channels x10; exponential(1) attention-mass weights."""
+    return make_sensitivity("head_bits_b8_h8_d128_t8192_outliers3", 5, 8, 8, 128, 8192, [1, 4, 6])
+
+
 NAMED = {
     "decode_tiny": decode_tiny,
     "decode_gqa": decode_gqa,

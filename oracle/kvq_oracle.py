@@ -334,3 +334,61 @@ def build_tile_mask(nT: int, skip_num: int, skip_den: int, seed: int) -> np.ndar
         order = np.argsort(keys, kind="stable")     # equal keys keep the smaller kt first
         mask[qt, cand[order[:k]]] = 0
     return mask
+
+
+# ---------------------------------------------------------------------------
+# Per-head sensitivity and bit allocation (P4 §2.4: every attention head gets
+# a sensitivity score, sensitive heads are stored at the higher bit-width and
+# the rest at the lower one; P4 §3.4: keeping more heads at high precision
+# lowers the compression from about 4x to 2.5x).  The pages give no formula.
+# Reading: a head's sensitivity is the relative error its cached K and V
+# would carry at the low bit-width, each token weighted by a caller-given
+# attention mass w (1 when absent):
+#   e_h = sum_{b, t < len_b} w[b,h,t] * sum_d (x - x_hat)^2,
+#   n_h = sum_{b, t < len_b} w[b,h,t] * sum_d x^2,
+#   score_h = e_h(K) / n_h(K) + e_h(V) / n_h(V)   (a 0 / 0 term counts 0);
+# the n_high heads with the largest scores (ties to the smaller head index)
+# get 8 bits, the others the low bit-width.
+# ---------------------------------------------------------------------------
+
+def head_error_stats(x_bits: np.ndarray, bits: int, seq_lens=None, weights=None) -> np.ndarray:
+    """float64 [H][2]: (weighted squared quantisation error, weighted squared norm) per head.
+
+    x_bits: bf16 patterns [B][H][T][D]; seq_lens: [B] (tokens t >= len_b are
+    left out; None = all T); weights: [B][H][T] float32 (None = 1).
+    x_hat is the dequantised value the cache would hold at `bits` bits.
+    """
+    x_bits = np.asarray(x_bits)
+    B, H, T, D = x_bits.shape
+    c, sc, z = quantize_groups(x_bits, bits)
+    x_hat = dequantize(c, sc, z)                       # float64, exact
+    xf = bf16_to_f32(x_bits).astype(np.float64)
+    err_tok = np.sum((xf - x_hat) ** 2, axis=-1)       # [B][H][T]
+    nrm_tok = np.sum(xf * xf, axis=-1)
+    w = np.ones((B, H, T)) if weights is None else np.asarray(weights, dtype=np.float32).astype(np.float64)
+    live = np.ones((B, T), dtype=bool)
+    if seq_lens is not None:
+        live = np.arange(T)[None, :] < np.asarray(seq_lens)[:, None]
+    w = np.where(live[:, None, :], w, 0.0)
+    out = np.zeros((H, 2))
+    out[:, 0] = np.sum(w * err_tok, axis=(0, 2))
+    out[:, 1] = np.sum(w * nrm_tok, axis=(0, 2))
+    return out
+
+
+def head_sensitivity(k_stats: np.ndarray, v_stats: np.ndarray) -> np.ndarray:
+    """score_h = relative low-bit error of K plus that of V (0 / 0 counts 0)."""
+    def rel(st):
+        st = np.asarray(st, dtype=np.float64)
+        return np.divide(st[:, 0], st[:, 1], out=np.zeros(st.shape[0]), where=st[:, 1] != 0)
+    return rel(k_stats) + rel(v_stats)
+
+
+def allocate_head_bits(score: np.ndarray, n_high: int, low_bits: int = 4) -> np.ndarray:
+    """int8 [H]: 8 bits for the n_high largest scores (ties to the smaller index), low_bits elsewhere."""
+    score = np.asarray(score, dtype=np.float64)
+    order = sorted(range(len(score)), key=lambda h: (-score[h], h))
+    bits = np.full(len(score), low_bits, dtype=np.int8)
+    bits[order[:n_high]] = 8
+    return bits
+
