@@ -1,16 +1,18 @@
 // kvq_quantize.cu -- quantise-on-write of bf16 K/V rows into the group-quantised
 // cache (《分块稀疏注意力与KV Cache量化：长文本推理显存优化实践》 §2.4, group of 32
-// channels per the hook of §3.2).
+// channels per the hook of §3.2), and per-head quantisation-error statistics
+// for the per-head bit allocation of the same section.
 //
 // HBM-bound: every input byte is read once and every code/scale byte written
 // once.  One thread quantises one group of 32 channels on its own: four
-// 16-byte loads, the group's range, one IEEE division for the scale and one
-// correctly rounded reciprocal, then each code from x times the reciprocal,
-// rounded by a 1.5 * 2^23 addend on the FMA pipe rather than the conversion
-// unit (where that product is within 2^-13 of a half-integer, an exact
-// remainder decides instead, see code_near), and one 32-byte (INT8) or 16-byte
-// (INT4) store of codes; a warp's stores cover whole contiguous rows.  The
-// result is bit-identical to the specification's IEEE fp32 arithmetic.
+// 16-byte loads, the group's range, one IEEE division for the scale, then
+// each code from x times an approximate reciprocal of the scale, rounded by a
+// 1.5 * 2^23 addend inside the same FMA, two values per instruction (paired
+// fp32).  The exact remainder x - u * s tells whether that rounding is the
+// specification's (see rne_div); the rare quarter-groups where it might not
+// be are redone value by value.  One 32-byte (INT8) or 16-byte (INT4) store
+// of codes per group; a warp's stores cover whole contiguous rows.  The result
+// is bit-identical to the specification's IEEE fp32 arithmetic.
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
@@ -56,59 +58,47 @@ struct QParams {
   int8_t bits[KVQ_MAX_HKV];
 };
 
-__device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
-
 // 1.5 * 2^23: adding it to a float of magnitude below 2^22 rounds that value
 // to the nearest integer (ties to even) -- floats in [2^23, 2^24) are spaced
 // 1 apart -- and leaves the integer in the low mantissa bits.
 constexpr float kRoundAdd = 12582912.0f;
 constexpr int kRoundAddBits = 0x4B400000;
 
-// code = clamp(rne(fl(x / s)) + z, 0, qmax) on the fast path, with
-// C = z + 1.5 * 2^23 (z an integer, exact):
-//   t = fl(x * fl(1/s)) is within 2^-14 of x / s (two roundings of relative
-//   size 2^-24 at magnitudes below 2^9) and fl(x / s) within 2^-16 of it;
-//   m = fl(t + C) = C + rne(t + z), the code before clamping in m's low bits;
-//   e = (m - C) - t, exactly the rounding error of t + z.
-// When |e| is more than 2^-13 below 1/2, t + z and fl(x / s) + z lie on the
-// same side of every half-integer, so rne(t + z) = rne(fl(x / s)) + z.
-// Otherwise (and for a NaN quotient) `near` is set and the caller redoes the
-// group's codes with code_checked.
-__device__ __forceinline__ int code_fast(float x, float rcp, float C, int qmax, bool& near) {
-  const float t = __fmul_rn(x, rcp);
-  const float m = __fadd_rn(t, C);
-  const float e = __fsub_rn(__fsub_rn(m, C), t);
-  near |= !(fabsf(e) <= 0.5f - 0x1p-13f);
-  return min(max(__float_as_int(m) - kRoundAddBits, 0), qmax);
+__device__ __forceinline__ float rcp_approx(float s) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+  return r;
 }
 
-// Value i (0..31) of a group held as 16 words of raw bf16 pairs.
-__device__ __forceinline__ float group_value(const uint32_t (&w)[16], int i) {
-  return bf16_bits_to_float((i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu));
+// rne(a / s), ties to even, for a bf16 value a and an fp16 scale s with
+// |a / s| <= 256, given any r within 2^-21 (relative) of 1/s:
+//   u = rne(a * r) is at most one step from rne(a / s);
+//   d = a - u * s is exact in fp32 (u * s has at most 20 significant bits and
+//     |d| <= 1.5 s while s >= |a| / 256, so d fits in 24 bits);
+//   u moves one step towards a / s when |d| > s / 2, or when |d| = s / 2
+//     (a / s is a half-integer) and u is odd.
+// For such a and s this is also rne(fl(a / s)), the IEEE fp32 quotient
+// rounded: fl(a / s) equals a half-integer h only when a / s does (a nonzero
+// a - h * s is a multiple of 2^(e_a - 20), while fl(a / s) = h needs
+// |a - h * s| < s * ulp(h) / 2, about 2^(e_a - 23)), and otherwise stays on
+// the same side of every half-integer as a / s.  (Checked against the IEEE
+// quotient for every finite bf16 a and fp16 scales from 2^-24 to 2^8.)
+__device__ __forceinline__ float rne_div(float a, float s, float r) {
+  float u = __fsub_rn(__fmaf_rn(a, r, kRoundAdd), kRoundAdd);
+  const float d = __fmaf_rn(-u, s, a);
+  const float ad = fabsf(d), hs = 0.5f * s;
+  if (ad > hs || (ad == hs && (static_cast<int>(u) & 1) != 0)) u = __fadd_rn(u, copysignf(1.0f, d));
+  return u;
 }
 
-// Codes of a group packed for the store: 8-bit, four codes per word (8
-// words); 4-bit, eight codes per word (4 words).  code(i) gives value i's code.
-template <class F>
-__device__ __forceinline__ void pack_codes(uint32_t (&packed)[8], int bits, F code) {
-#pragma unroll
-  for (int k = 0; k < 8; ++k) packed[k] = 0u;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const uint32_t c = static_cast<uint32_t>(code(i));
-    if (bits == 8) packed[i >> 2] |= c << (8 * (i & 3));
-    else packed[i >> 3] |= c << (4 * (i & 7));
-  }
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
-// Quantise one group of 32 channels (this thread alone): w holds the 32 bf16
-// values as loaded by load_group (64 bytes, 16-byte aligned source), the
-// codes go to cdst (32 bytes for 8-bit, 16 for 4-bit) and the fp16
-// (scale, zero) word to *szw.  The values stay packed as loaded and are
-// widened where used, which keeps the thread's registers few.  Non-finite input:
-// an infinity makes the range, hence the scale, infinite; a NaN is dropped by
-// the min/max but gives a NaN quotient (seen on the exact path) or, in an
-// otherwise all-zero group, is tested directly.
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+// Load one group of 32 bf16 values (64 bytes, 16-byte aligned source) as 16
+// words of raw bf16 pairs; they stay packed and are widened where used.
 __device__ __forceinline__ void load_group(uint32_t (&w)[16], const uint16_t* src) {
 #pragma unroll
   for (int v = 0; v < 4; ++v) {
@@ -118,12 +108,15 @@ __device__ __forceinline__ void load_group(uint32_t (&w)[16], const uint16_t* sr
 }
 
 // A group's parameters: the range widened to contain 0, the fp16 scale
-// s = round-up(range / qmax), the zero point z = clamp(rne(-lo / s), 0, qmax)
-// (one exact quotient per group), and the fast path's constants.
+// s = round-up(range / qmax) (one IEEE division), the zero point
+// z = clamp(rne(-lo / s), 0, qmax) (rne_div), and the fast path's constants.
+// Non-finite input: an infinity makes the range, hence the scale, infinite; a
+// NaN is dropped by the min/max but shows in the fast path's remainders (or,
+// in an otherwise all-zero group, in group_has_nan).
 struct GroupParams {
   __half scale_h;   // 1 when the range is 0
   float mn, mx;     // the group's min and max (before widening)
-  float sf, rcp, zf, C;
+  float sf, rcp, zf, C;   // scale, approximate 1/scale, zero point, zero + 1.5 * 2^23
   int qmax;
   bool flat;        // range 0 (all zeros, or NaN among zeros): every code 0
   bool bad;         // non-finite scale
@@ -138,15 +131,13 @@ __device__ __forceinline__ GroupParams group_params(const uint32_t (&w)[16], int
     mn2 = __hmin2(mn2, v);
     mx2 = __hmax2(mx2, v);
   }
-  const float mn = fminf(__low2float(mn2), __high2float(mn2));
-  const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
   GroupParams g;
-  g.mn = mn;
-  g.mx = mx;
+  g.mn = fminf(__low2float(mn2), __high2float(mn2));
+  g.mx = fmaxf(__low2float(mx2), __high2float(mx2));
   g.qmax = (1 << bits) - 1;
   const float qf = static_cast<float>(g.qmax);
-  const float lo = fminf(0.0f, mn);
-  const float hi = fmaxf(0.0f, mx);
+  const float lo = fminf(0.0f, g.mn);
+  const float hi = fmaxf(0.0f, g.mx);
   const float range = __fsub_rn(hi, lo);
   g.flat = range == 0.0f;
   g.scale_h = __ushort_as_half(0x3C00);  // 1.0
@@ -156,137 +147,139 @@ __device__ __forceinline__ GroupParams group_params(const uint32_t (&w)[16], int
     g.scale_h = __float2half_ru(__fdiv_rn(range, qf));
     g.sf = __half2float(g.scale_h);
     g.bad = !isfinite(g.sf);
-    g.rcp = __frcp_rn(g.sf);
-    g.zf = fminf(fmaxf(rintf(__fdiv_rn(-lo, g.sf)), 0.0f), qf);
+    g.rcp = rcp_approx(g.sf);
+    g.zf = fminf(fmaxf(rne_div(-lo, g.sf, g.rcp), 0.0f), qf);
     g.C = g.zf + kRoundAdd;   // exact
   }
   return g;
 }
 
-// The code by the exact IEEE division (the fallback of code_fast).
-__device__ __forceinline__ int code_exact(float x, const GroupParams& g, bool& bad) {
-  const float q = __fdiv_rn(x, g.sf);
-  bad |= q != q;
-  return static_cast<int>(fminf(fmaxf(rintf(q) + g.zf, 0.0f), static_cast<float>(g.qmax)));
+// Whether some code of the group is clamped: rne(mx / s) + z > qmax or
+// rne(mn / s) + z < 0, decided exactly from the remainders against the
+// half-integers k + 1/2 (k = qmax - z) and -z - 1/2 (exact as in rne_div), a
+// remainder of 0 being a tie that rounds to the even side.  Codes are
+// monotone in x, so no other value is clamped when these two are not.
+__device__ __forceinline__ bool group_clamps(const GroupParams& g) {
+  const float k = static_cast<float>(g.qmax) - g.zf;
+  const float rt = __fmaf_rn(-(k + 0.5f), g.sf, g.mx);
+  const float rb = __fmaf_rn(g.zf + 0.5f, g.sf, g.mn);
+  return rt > 0.0f || (rt == 0.0f && (static_cast<int>(k) & 1) != 0) ||
+         rb < 0.0f || (rb == 0.0f && (static_cast<int>(g.zf) & 1) != 0);
 }
 
-// The code of a value whose fast-path quotient t = fl(x * 1/s) lies within
-// 2^-13 of a half-integer h, without a division.  With u = rne(t) and
-// e = u - t, h = u - copysign(1/2, e).  The specification's quotient
-// fl(x / s) equals h when |x / s - h| < ulp(h) / 2 (x has 8 significant bits
-// and s 11, so x / s never sits on that boundary), and otherwise lies on the
-// same side of h as x / s, within 1/2 of it.  Both tests read the remainder
-// r = x - h * s, which is exact in fp32 (h * s has at most 20 significant
-// bits and |r| is far below |x|).  rne(fl(x / s)) is then the even neighbour
-// of h on equality, else the neighbour on r's side.  (Checked against the
-// IEEE quotient for every finite bf16 x, fp16 scales from 2^-24 to 2^8 and
-// several zero points.)
-__device__ __forceinline__ int code_near(float x, float t, float u, const GroupParams& g) {
-  const float e = __fsub_rn(u, t);
-  const float h = __fsub_rn(u, copysignf(0.5f, e));
-  const float r = __fmaf_rn(-h, g.sf, x);
-  const float half_ulp = __int_as_float((__float_as_int(h) & 0x7F800000) - (24 << 23));
-  const float lo = __fsub_rn(h, 0.5f), hi = __fadd_rn(h, 0.5f);
-  float q;
-  if (fabsf(r) < __fmul_rn(half_ulp, g.sf)) q = (__float2int_rn(lo) & 1) == 0 ? lo : hi;
-  else q = r > 0.0f ? hi : lo;
-  return min(max(__float2int_rn(q) + static_cast<int>(g.zf), 0), g.qmax);
-}
-
-// The code of one value: the fast path where it is decided, code_near next
-// to a half-integer, code_exact for a NaN quotient.
-__device__ __forceinline__ int code_checked(float x, const GroupParams& g, bool& bad) {
-  const float t = __fmul_rn(x, g.rcp);
-  const float m = __fadd_rn(t, g.C);
-  const float u = __fsub_rn(m, g.C);
-  if (fabsf(__fsub_rn(u, t)) <= 0.5f - 0x1p-13f) return min(max(__float_as_int(m) - kRoundAddBits, 0), g.qmax);
-  if (t != t) return code_exact(x, g, bad);
-  return code_near(x, t, u, g);
-}
-
-// The rare path of a group, a quarter at a time: the 8 values of quarter v
-// are re-read from `src` (an L1 hit) and passed to f(i, x) with i their index
-// in the group.  The loop stays rolled so the group's registers are not all
-// live at once.
-template <class F>
-__device__ __forceinline__ void for_each_quarter(const uint16_t* src, F f) {
-#pragma unroll 1
-  for (int v = 0; v < 4; ++v) {
-    const uint4 raw = reinterpret_cast<const uint4*>(src)[v];
-    const uint32_t q4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      f(v, j, bf16_bits_to_float((j & 1) ? (q4[j >> 1] >> 16) : (q4[j >> 1] & 0xFFFFu)));
-  }
+// The specification's code of one value (a NaN gives code 0, as the
+// specification's clamp of a NaN quotient does).
+__device__ __forceinline__ int code_exact(float x, const GroupParams& g) {
+  return static_cast<int>(fminf(fmaxf(__fadd_rn(rne_div(x, g.sf, g.rcp), g.zf), 0.0f), static_cast<float>(g.qmax)));
 }
 
 __device__ __forceinline__ bool group_has_nan(const uint32_t (&w)[16]) {
   bool bad = false;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float x = group_value(w, i);
-    bad |= x != x;
+  for (int k = 0; k < 16; ++k) {
+    const float2 x2 = bf16x2_to_float2(w[k]);
+    bad |= (x2.x != x2.x) || (x2.y != x2.y);
   }
   return bad;
 }
 
-// src: the group's 32 bf16 values in global memory (what w was loaded from).
+// Quarter v (values 8v .. 8v+7) of a group re-read from `src` (an L1 hit),
+// passed to f(j, x) with j = 0..7.  Used by the rare paths, which run a
+// quarter at a time in a rolled loop so the group's registers are not all
+// live at once.
+template <class F>
+__device__ __forceinline__ void quarter_values(const uint16_t* src, int v, F f) {
+  const uint4 raw = reinterpret_cast<const uint4*>(src)[v];
+  const uint32_t q4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) f(j, bf16_bits_to_float((j & 1) ? (q4[j >> 1] >> 16) : (q4[j >> 1] & 0xFFFFu)));
+}
+
+// Quantise one group of 32 channels (this thread alone): w holds the 32 bf16
+// values as loaded by load_group from src; the codes go to cdst (32 bytes for
+// 8-bit, 16 for 4-bit) and the fp16 (scale, zero) word to *szw.
+// Fast path, per pair of values: m = fl(x * r + C) holds rne(x * r) + z in its
+// low mantissa bits, u = m - C = rne(x * r), d = x - u * s exact; the code is
+// the specification's wherever |d| < s / 2 (then u is the integer nearest
+// x / s) and no code is clamped (group_clamps).  A quarter with some |d| at
+// least s / 2 (a tie, or u one step off), or a NaN (the sum of the d's), or a
+// clamped group, is redone with code_exact and stored 8 codes at a time.
 __device__ __forceinline__ void quantize_group(const uint32_t (&w)[16], const uint16_t* src, int bits,
                                                uint8_t* cdst, uint32_t* szw, int32_t* status) {
   const GroupParams gp = group_params(w, bits);
-  uint32_t packed[8];
   bool bad = gp.bad;
-  bool near = false;
-  if (gp.flat) {
-    bad = group_has_nan(w);
+  uint32_t packed[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) packed[k] = 0u;
+  for (int k = 0; k < 8; ++k) packed[k] = 0u;
+  unsigned redo = 0;   // quarters to redo, one bit each
+  if (gp.flat) {
+    bad |= group_has_nan(w);
   } else {
-    pack_codes(packed, bits, [&](int i) { return code_fast(group_value(w, i), gp.rcp, gp.C, gp.qmax, near); });
+    const float2 r2 = make_float2(gp.rcp, gp.rcp), c2 = make_float2(gp.C, gp.C);
+    const float2 nc2 = make_float2(-gp.C, -gp.C), ns2 = make_float2(-gp.sf, -gp.sf);
+    float2 dsum = make_float2(0.0f, 0.0f);
+    const float hs = 0.5f * gp.sf;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      float dmax = 0.0f;
+#pragma unroll
+      for (int k = 4 * v; k < 4 * v + 4; ++k) {
+        const float2 x2 = bf16x2_to_float2(w[k]);
+        const float2 m2 = __ffma2_rn(x2, r2, c2);
+        const float2 d2 = __ffma2_rn(__fadd2_rn(m2, nc2), ns2, x2);
+        dsum = __fadd2_rn(dsum, d2);
+        dmax = fmaxf(dmax, fmaxf(fabsf(d2.x), fabsf(d2.y)));
+        const uint32_t c0 = static_cast<uint32_t>(__float_as_int(m2.x) - kRoundAddBits);
+        const uint32_t c1 = static_cast<uint32_t>(__float_as_int(m2.y) - kRoundAddBits);
+        const int i = 2 * k;
+        if (bits == 8) packed[i >> 2] |= (c0 | (c1 << 8)) << (8 * (i & 3));
+        else packed[i >> 3] |= (c0 | (c1 << 4)) << (4 * (i & 7));
+      }
+      redo |= (dmax < hs ? 0u : 1u) << v;
+    }
+    const float dtot = __fadd_rn(dsum.x, dsum.y);
+    if (dtot != dtot || group_clamps(gp)) redo = 0xFu;
   }
-  if (!near) {
+  if (redo == 0u) {
     uint4* dst = reinterpret_cast<uint4*>(cdst);
     dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
     if (bits == 8) dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-  } else {   // rare: some quotient is within 2^-13 of a half-integer (or NaN); 8 codes per store
-    uint32_t c8[2] = {0u, 0u};
-    for_each_quarter(src, [&](int v, int j, float x) {
-      const uint32_t c = static_cast<uint32_t>(code_checked(x, gp, bad));
-      if (bits == 8) c8[j >> 2] |= c << (8 * (j & 3));
-      else c8[0] |= c << (4 * j);
-      if (j == 7) {
-        if (bits == 8) reinterpret_cast<uint2*>(cdst)[v] = make_uint2(c8[0], c8[1]);
-        else reinterpret_cast<uint32_t*>(cdst)[v] = c8[0];
+  } else {   // rare: whole group stored quarter by quarter, the flagged quarters recomputed
+#pragma unroll 1
+    for (int v = 0; v < 4; ++v) {
+      uint32_t c8[2];
+      if ((redo >> v) & 1u) {
         c8[0] = 0u;
         c8[1] = 0u;
+        quarter_values(src, v, [&](int j, float x) {
+          bad |= x != x;
+          const uint32_t c = static_cast<uint32_t>(code_exact(x, gp));
+          if (bits == 8) c8[j >> 2] |= c << (8 * (j & 3));
+          else c8[0] |= c << (4 * j);
+        });
+      } else if (bits == 8) {
+        c8[0] = v == 0 ? packed[0] : v == 1 ? packed[2] : v == 2 ? packed[4] : packed[6];
+        c8[1] = v == 0 ? packed[1] : v == 1 ? packed[3] : v == 2 ? packed[5] : packed[7];
+      } else {
+        c8[0] = v == 0 ? packed[0] : v == 1 ? packed[1] : v == 2 ? packed[2] : packed[3];
+        c8[1] = 0u;
       }
-    });
+      if (bits == 8) reinterpret_cast<uint2*>(cdst)[v] = make_uint2(c8[0], c8[1]);
+      else reinterpret_cast<uint32_t*>(cdst)[v] = c8[0];
+    }
   }
   if (bad) report(status, KVQ_ERR_NONFINITE);
   *szw = __half_as_ushort(gp.scale_h) |
          (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(static_cast<int>(gp.zf)))) << 16);
 }
 
-__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
-  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-}
-
 // Squared quantisation error of one group, sum_i (x_i - x_hat_i)^2 with
 // x_hat = (code - z) * s the value the cache would hold at `bits` bits, and
-// its squared norm sum_i x_i^2, two values per instruction (paired fp32).
-// The code is rne(fl(x / s)) + z, and for bf16 x and fp16 s that is
-// rne(x / s) + z exactly: fl(x / s) equals a half-integer h only when x / s
-// does (a nonzero x - h * s is a multiple of 2^(e_x - 20), far above the
-// half-ulp band around h), and otherwise lies on the same side of every
-// half-integer as x / s.  The fast quotient t = fl(x * 1/s) is within 2^-14 of
-// x / s, so u = rne(t) (through the 1.5 * 2^23 addend, as in code_fast) is at
-// most one step from rne(x / s); d = x - u * s is exact (u * s has at most 19
-// significant bits, |d| <= s with s >= |x| / 255), and the error of the
-// nearest code is min(|d|, s - |d|) (s - |d| is exact by Sterbenz where it is
-// the smaller; at a tie both neighbours give s / 2).  This holds while no
-// code is clamped; u is monotone in x, so the group's min and max tell.  A
-// clamped group, or one with a NaN, is redone value by value with
-// code_checked.  Each square-and-add rounds once.
+// its squared norm sum_i x_i^2, two values per instruction.  With u and d as
+// in quantize_group, x - x_hat = d wherever |d| <= s / 2 and no code is
+// clamped (at a tie, |d| = s / 2, either neighbour gives the same error).  A
+// quarter with some |d| > s / 2, or a NaN, or a clamped group, is redone with
+// code_exact.  Each square-and-add rounds once.
 __device__ __forceinline__ float2 group_sq_error(const uint32_t (&w)[16], const uint16_t* src, int bits, bool& bad) {
   const GroupParams gp = group_params(w, bits);
   bad |= gp.bad;
@@ -294,34 +287,44 @@ __device__ __forceinline__ float2 group_sq_error(const uint32_t (&w)[16], const 
     bad |= group_has_nan(w);
     return make_float2(0.0f, 0.0f);
   }
-  const float2 rcp2 = make_float2(gp.rcp, gp.rcp), c2 = make_float2(gp.C, gp.C);
+  const float2 r2 = make_float2(gp.rcp, gp.rcp), c2 = make_float2(gp.C, gp.C);
   const float2 nc2 = make_float2(-gp.C, -gp.C), ns2 = make_float2(-gp.sf, -gp.sf);
-  float2 err2 = make_float2(0.0f, 0.0f), nrm2 = make_float2(0.0f, 0.0f);
+  const float hs = 0.5f * gp.sf;
+  float2 nrm2 = make_float2(0.0f, 0.0f);
+  float errq[4];
+  unsigned redo = 0;
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const float2 x2 = bf16x2_to_float2(w[k]);
-    nrm2 = __ffma2_rn(x2, x2, nrm2);
-    const float2 u2 = __fadd2_rn(__fadd2_rn(__fmul2_rn(x2, rcp2), c2), nc2);
-    const float2 d2 = __ffma2_rn(u2, ns2, x2);         // x - u * s, exact
-    const float ax = fabsf(d2.x), ay = fabsf(d2.y);
-    const float2 m2 = make_float2(fminf(ax, __fsub_rn(gp.sf, ax)), fminf(ay, __fsub_rn(gp.sf, ay)));
-    err2 = __ffma2_rn(m2, m2, err2);
+  for (int v = 0; v < 4; ++v) {
+    float2 err2 = make_float2(0.0f, 0.0f);
+    float dmax = 0.0f;
+#pragma unroll
+    for (int k = 4 * v; k < 4 * v + 4; ++k) {
+      const float2 x2 = bf16x2_to_float2(w[k]);
+      nrm2 = __ffma2_rn(x2, x2, nrm2);
+      const float2 d2 = __ffma2_rn(__fadd2_rn(__ffma2_rn(x2, r2, c2), nc2), ns2, x2);
+      dmax = fmaxf(dmax, fmaxf(fabsf(d2.x), fabsf(d2.y)));
+      err2 = __ffma2_rn(d2, d2, err2);
+    }
+    errq[v] = __fadd_rn(err2.x, err2.y);
+    redo |= (dmax <= hs && errq[v] == errq[v] ? 0u : 1u) << v;   // a NaN makes the sum NaN
   }
-  float err = __fadd_rn(err2.x, err2.y);
-  const float nrm = __fadd_rn(nrm2.x, nrm2.y);
-  const float qf = static_cast<float>(gp.qmax);
-  const float umn = __fsub_rn(__fadd_rn(__fmul_rn(gp.mn, gp.rcp), gp.C), gp.C);
-  const float umx = __fsub_rn(__fadd_rn(__fmul_rn(gp.mx, gp.rcp), gp.C), gp.C);
-  // a NaN value makes the error sum NaN
-  if (err != err || umn < -gp.zf || umx > qf - gp.zf) {
+  if (group_clamps(gp)) redo = 0xFu;
+  if (redo != 0u) {
     const int zero = static_cast<int>(gp.zf);
-    err = 0.0f;
-    for_each_quarter(src, [&](int, int, float x) {
-      const float d = __fsub_rn(x, __fmul_rn(static_cast<float>(code_checked(x, gp, bad) - zero), gp.sf));
-      err = __fmaf_rn(d, d, err);
-    });
+#pragma unroll 1
+    for (int v = 0; v < 4; ++v) {
+      if (!((redo >> v) & 1u)) continue;
+      float e = 0.0f;
+      quarter_values(src, v, [&](int, float x) {
+        bad |= x != x;
+        const float d = __fmaf_rn(-static_cast<float>(code_exact(x, gp) - zero), gp.sf, x);
+        e = __fmaf_rn(d, d, e);
+      });
+      errq[v] = e;
+    }
   }
-  return make_float2(err, nrm);
+  return make_float2(__fadd_rn(__fadd_rn(errq[0], errq[1]), __fadd_rn(errq[2], errq[3])),
+                     __fadd_rn(nrm2.x, nrm2.y));
 }
 
 // resident blocks of 256 threads per SM the register budget is sized for (tunable at build time)
@@ -443,7 +446,10 @@ struct SParams {
 };
 
 constexpr int kStatThreads = 256;
-constexpr int kStatBlocksPerSM = 4;   // resident blocks the register budget is sized for
+// Resident blocks the register budget is sized for.  Measured alternatives
+// (3, 5 or 6 blocks; two groups per iteration; a register prefetch of the
+// next group) were no faster.
+constexpr int kStatBlocksPerSM = 4;
 
 template <int D>
 __global__ void __launch_bounds__(kStatThreads, kStatBlocksPerSM) head_stats_kernel(const __grid_constant__ SParams p) {
@@ -455,6 +461,13 @@ __global__ void __launch_bounds__(kStatThreads, kStatBlocksPerSM) head_stats_ker
   float2 sum = make_float2(0.0f, 0.0f), comp = make_float2(0.0f, 0.0f);
   const float2 m1 = make_float2(-1.0f, -1.0f);
   bool bad = false;
+  auto accumulate = [&](float2 e, float wt) {
+    e = __fmul2_rn(e, make_float2(wt, wt));
+    const float2 y = __ffma2_rn(comp, m1, e);              // e - comp
+    const float2 nsum = __fadd2_rn(sum, y);
+    comp = __ffma2_rn(y, m1, __ffma2_rn(sum, m1, nsum));   // (nsum - sum) - y
+    sum = nsum;
+  };
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * kStatThreads + threadIdx.x; i < n;
        i += static_cast<int64_t>(p.chunks) * kStatThreads) {
     const uint32_t r = static_cast<uint32_t>(i / G);
@@ -466,31 +479,25 @@ __global__ void __launch_bounds__(kStatThreads, kStatBlocksPerSM) head_stats_ker
     uint32_t v[16];
     const uint16_t* src = p.x + row * D + g * 32;
     load_group(v, src);
-    float2 e = group_sq_error(v, src, p.bits, bad);
-    if (p.w != nullptr) {
-      const float wt = p.w[row];
-      e = __fmul2_rn(e, make_float2(wt, wt));
-    }
-    const float2 y = __ffma2_rn(comp, m1, e);           // e - comp
-    const float2 nsum = __fadd2_rn(sum, y);
-    comp = __ffma2_rn(y, m1, __ffma2_rn(sum, m1, nsum));   // (nsum - sum) - y
-    sum = nsum;
+    accumulate(group_sq_error(v, src, p.bits, bad), p.w != nullptr ? p.w[row] : 1.0f);
   }
   if (bad) report(p.status, KVQ_ERR_NONFINITE);
-  double err = static_cast<double>(sum.x) - static_cast<double>(comp.x);
-  double nrm = static_cast<double>(sum.y) - static_cast<double>(comp.y);
+  // the block's sum in fp32 (a tree of depth 8 over compensated per-thread
+  // totals: a few units of 2^-24 relative), then fp64 across blocks (the fp64
+  // pipe is narrow, so it is kept out of the per-thread tail)
+  float2 tot = __ffma2_rn(comp, m1, sum);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    err += __shfl_down_sync(0xffffffffu, err, o);
-    nrm += __shfl_down_sync(0xffffffffu, nrm, o);
+    tot.x = __fadd_rn(tot.x, __shfl_down_sync(0xffffffffu, tot.x, o));
+    tot.y = __fadd_rn(tot.y, __shfl_down_sync(0xffffffffu, tot.y, o));
   }
-  __shared__ double red[kStatThreads / 32][2];
+  __shared__ float2 red[kStatThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) { red[warp][0] = err; red[warp][1] = nrm; }
+  if (lane == 0) red[warp] = tot;
   __syncthreads();
   if (threadIdx.x == 0) {
     double e = 0.0, m = 0.0;
-    for (int k = 0; k < kStatThreads / 32; ++k) { e += red[k][0]; m += red[k][1]; }
+    for (int k = 0; k < kStatThreads / 32; ++k) { e += static_cast<double>(red[k].x); m += static_cast<double>(red[k].y); }
     double* out = p.part + (static_cast<int64_t>(h) * p.chunks + blockIdx.x) * 2;
     out[0] = e;
     out[1] = m;
