@@ -121,8 +121,11 @@ const char* kvq_status_str(kvq_status s) {
   return "unknown status";
 }
 
-kvq_status kvq_quantize(const void* x, int64_t sx_b, int64_t sx_h, int64_t sx_t, int32_t t0, int32_t nt,
-                        const kvq_cache* dst, int32_t* dev_status, void* stream) {
+}  // extern "C"
+
+// kvq_quantize, optionally skipping the rows at positions >= lens[b]
+static kvq_status quantize_impl(const void* x, int64_t sx_b, int64_t sx_h, int64_t sx_t, int32_t t0, int32_t nt,
+                                const kvq_cache* dst, const int32_t* lens, int32_t* dev_status, void* stream) {
   if (dst == nullptr || x == nullptr || dst->codes == nullptr || dst->sz == nullptr) return KVQ_ERR_INVALID_ARG;
   if (dst->D != 64 && dst->D != 128 && dst->D > 0) return KVQ_ERR_UNSUPPORTED;
   QuantizeArgs a;
@@ -139,7 +142,15 @@ kvq_status kvq_quantize(const void* x, int64_t sx_b, int64_t sx_h, int64_t sx_t,
   a.codes = dst->codes; a.sz = dst->sz;
   a.B = dst->B; a.Hkv = dst->Hkv; a.Tcap = dst->Tcap; a.D = dst->D;
   a.status = dev_status;
+  a.lens = lens;
   return launch_quantize(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+extern "C" {
+
+kvq_status kvq_quantize(const void* x, int64_t sx_b, int64_t sx_h, int64_t sx_t, int32_t t0, int32_t nt,
+                        const kvq_cache* dst, int32_t* dev_status, void* stream) {
+  return quantize_impl(x, sx_b, sx_h, sx_t, t0, nt, dst, nullptr, dev_status, stream);
 }
 
 size_t kvq_decode_workspace_bytes(int32_t B, int32_t Hq, int32_t Hkv, int32_t D) {
@@ -435,11 +446,13 @@ kvq_status kvq_allocate_head_bits(const double* k_stats, const double* v_stats, 
   return KVQ_OK;
 }
 
-kvq_status kvq_prefill_attention(const void* q, const void* k, const void* v, int32_t B, int32_t Hq, int32_t Hkv,
-                                 int32_t S, int32_t D, int32_t causal, float softmax_scale,
-                                 const uint8_t* tile_mask, int32_t tile, const kvq_cache* k_cache,
-                                 const kvq_cache* v_cache, void* out, int32_t out_dtype, int32_t* dev_status,
-                                 void* stream) {
+}  // extern "C"
+
+static kvq_status prefill_impl(const void* q, const void* k, const void* v, int32_t B, int32_t Hq, int32_t Hkv,
+                               int32_t S, int32_t D, const int32_t* seq_lens, int32_t causal, float softmax_scale,
+                               const uint8_t* tile_mask, int32_t tile, const kvq_cache* k_cache,
+                               const kvq_cache* v_cache, void* out, int32_t out_dtype, int32_t* dev_status,
+                               void* stream) {
   if (q == nullptr || k == nullptr || v == nullptr || k_cache == nullptr || v_cache == nullptr || out == nullptr)
     return KVQ_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || Hq % Hkv) return KVQ_ERR_INVALID_ARG;
@@ -454,9 +467,9 @@ kvq_status kvq_prefill_attention(const void* q, const void* k, const void* v, in
     return KVQ_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t sx_t = D, sx_h = static_cast<int64_t>(S) * D, sx_b = sx_h * Hkv;
-  kvq_status s = kvq_quantize(k, sx_b, sx_h, sx_t, 0, S, k_cache, dev_status, stream);
+  kvq_status s = quantize_impl(k, sx_b, sx_h, sx_t, 0, S, k_cache, seq_lens, dev_status, stream);
   if (s != KVQ_OK) return s;
-  s = kvq_quantize(v, sx_b, sx_h, sx_t, 0, S, v_cache, dev_status, stream);
+  s = quantize_impl(v, sx_b, sx_h, sx_t, 0, S, v_cache, seq_lens, dev_status, stream);
   if (s != KVQ_OK) return s;
   a.q = static_cast<const uint16_t*>(q);
   a.k = k_cache;
@@ -468,7 +481,29 @@ kvq_status kvq_prefill_attention(const void* q, const void* k, const void* v, in
   a.out_dtype = out_dtype;
   a.status = dev_status;
   a.causal = causal;
+  a.lens = seq_lens;
   return launch_prefill(a, st);
+}
+
+extern "C" {
+
+kvq_status kvq_prefill_attention(const void* q, const void* k, const void* v, int32_t B, int32_t Hq, int32_t Hkv,
+                                 int32_t S, int32_t D, int32_t causal, float softmax_scale,
+                                 const uint8_t* tile_mask, int32_t tile, const kvq_cache* k_cache,
+                                 const kvq_cache* v_cache, void* out, int32_t out_dtype, int32_t* dev_status,
+                                 void* stream) {
+  return prefill_impl(q, k, v, B, Hq, Hkv, S, D, nullptr, causal, softmax_scale, tile_mask, tile, k_cache, v_cache,
+                      out, out_dtype, dev_status, stream);
+}
+
+kvq_status kvq_prefill_attention_varlen(const void* q, const void* k, const void* v, int32_t B, int32_t Hq,
+                                        int32_t Hkv, int32_t S, int32_t D, const int32_t* seq_lens, int32_t causal,
+                                        float softmax_scale, const uint8_t* tile_mask, int32_t tile,
+                                        const kvq_cache* k_cache, const kvq_cache* v_cache, void* out,
+                                        int32_t out_dtype, int32_t* dev_status, void* stream) {
+  if (seq_lens == nullptr) return KVQ_ERR_INVALID_ARG;
+  return prefill_impl(q, k, v, B, Hq, Hkv, S, D, seq_lens, causal, softmax_scale, tile_mask, tile, k_cache, v_cache,
+                      out, out_dtype, dev_status, stream);
 }
 
 }  // extern "C"

@@ -34,6 +34,9 @@ struct QuantizeArgs {
   // x's rows are indexed by sequence bt_B x positions
   const int32_t* bt = nullptr;
   int32_t bt_B = 0, bt_max_pages = 0;
+  // optional per-sequence lengths: rows at positions t0 + t >= lens[b] are
+  // skipped (contiguous caches only)
+  const int32_t* lens = nullptr;
 };
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t stream);
 
@@ -94,6 +97,7 @@ struct PrefillArgs {
   int32_t out_dtype;
   int32_t* status;
   int32_t causal = 1;
+  const int32_t* lens = nullptr;   // device [B] sequence lengths or null
 };
 kvq_status launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 

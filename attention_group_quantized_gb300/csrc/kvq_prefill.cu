@@ -56,6 +56,7 @@ struct PParams {
   int32_t out_dtype;
   int32_t B, Hq, Hkv, S, Tcap, rep, pairs, nT;
   int32_t causal;                 // 1: keys j <= i; 0: every key of the sequence
+  const int32_t* lens;            // [B] sequence lengths (<= S) or null (every sequence S long)
   float scale_log2;
 };
 
@@ -128,13 +129,26 @@ __device__ __forceinline__ void store_dequant(uint8_t* dst, const CodeRegs& r, i
   }
 }
 
-// key tiles [0, kt_end) of query tile qt can take part
-__device__ __forceinline__ int key_tile_end(const PParams& p, int qt) { return p.causal ? qt + 1 : p.nT; }
+// key tiles [0, kt_end) of query tile qt can take part (L: the sequence's length)
+__device__ __forceinline__ int key_tile_end(const PParams& p, int qt, int L) {
+  return p.causal ? qt + 1 : (L + kT - 1) / kT;
+}
 
-__device__ __forceinline__ int next_kept(const PParams& p, int qt, int kt) {
-  const int end = key_tile_end(p, qt);
+__device__ __forceinline__ int next_kept(const PParams& p, int qt, int kt, int end) {
   while (kt < end && !tile_kept(p, qt, kt)) ++kt;
   return kt;
+}
+
+// Zeros in the output rows of this work item (a query tile past its sequence's end).
+__device__ __forceinline__ void zero_out_tile(const PParams& p, int b, int h0, int nh, int qt) {
+  const size_t row0 = (static_cast<size_t>(b) * p.Hq + h0) * p.S + static_cast<size_t>(qt) * kT;
+  const int vec_per_row = kD * (p.out_dtype == KVQ_OUT_F32 ? 4 : 2) / 16;
+  for (int h = 0; h < nh; ++h) {
+    uint4* base = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) +
+                                           (row0 + static_cast<size_t>(h) * p.S) * kD *
+                                               (p.out_dtype == KVQ_OUT_F32 ? 4 : 2));
+    for (int i = threadIdx.x; i < kT * vec_per_row; i += kThreads) base[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PParams p) {
@@ -153,6 +167,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const int b = rem / p.Hkv;
   const int h0 = kvh * p.rep + 2 * pair;
   const int nh = (2 * pair + 1 < p.rep) ? 2 : 1;
+  // the sequence's length: a query tile wholly past it writes zeros and ends
+  // here, before any barrier or TMEM is set up (the decision is the CTA's own)
+  int L = p.S;
+  if (p.lens != nullptr) {
+    L = p.lens[b];
+    if (L < 0 || L > p.S) {
+      if (threadIdx.x == 0 && qt == 0) report(p.status, KVQ_ERR_INVALID_ARG);
+      L = min(max(L, 0), p.S);
+    }
+  }
+  if (qt * kT >= L) {
+    zero_out_tile(p, b, h0, nh, qt);
+    return;
+  }
+  const int q_valid = min(kT, L - qt * kT);   // query rows of this tile inside the sequence
 
   if (threadIdx.x == 0) {
     mbar_init(&bar[B_QFULL], 1);
@@ -183,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   // 32 x (80 + 192 + 120 + 120) = 16384, its whole register file.
 
   // number of kept key tiles (identical in every role)
-  const int kt_end = key_tile_end(p, qt);
+  const int kt_end = key_tile_end(p, qt, L);
   int n_kept = 0;
   for (int kt = 0; kt < kt_end; ++kt) n_kept += tile_kept(p, qt, kt) ? 1 : 0;
 
@@ -270,6 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     bool finite = true;
     for (int i = wt; i < nh * kQBytes / 16; i += 128) {
       uint4* ptr = reinterpret_cast<uint4*>(smem + kOff_Q) + i;
+      if (q_valid < kT && ((i & 1023) >> 3) >= q_valid) {   // row past the sequence's end
+        *ptr = make_uint4(0u, 0u, 0u, 0u);
+        continue;
+      }
       uint4 v = *ptr;
       uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -291,13 +324,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     const uint32_t* ksz = p.ksz + plane * 4;
     const uint32_t* vsz = p.vsz + plane * 4;
     // two register sets: while one part (K or V of a tile) is converted, the
-    // next part's codes are already on their way from L2 / HBM
+    // next part's codes are already on their way from L2 / HBM.  Positions
+    // past a shorter sequence's end within its last tile read as zeros: the
+    // quantiser cleared them (codes and scale/zero words 0), so a masked score
+    // (P = 0) never meets a non-finite V_hat in the P.V product.
     CodeRegs ra, rb;
-    int kt = next_kept(p, qt, 0);
+    int kt = next_kept(p, qt, 0, kt_end);
     if (kt < kt_end) load_codes(ra, kcodes + static_cast<size_t>(kt) * kT * kD, ksz + kt * kT * 4, wt);
     for (int j = 0; kt < kt_end; ++j) {
       const int st = j & 1;
-      const int kt_next = next_kept(p, qt, kt + 1);
+      const int kt_next = next_kept(p, qt, kt + 1, kt_end);
       load_codes(rb, vcodes + static_cast<size_t>(kt) * kT * kD, vsz + kt * kT * 4, wt);
       if (j >= 2 && !mbar_wait(&bar[B_KVEMPTY0 + st], ((j >> 1) - 1) & 1, p.status)) return;
       store_dequant(smem + kOff_K + st * kQBytes, ra, wt);
@@ -330,22 +366,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   int j = 0;
   for (int kt = 0; kt < kt_end && ok; ++kt) {
     if (!tile_kept(p, qt, kt)) continue;
-    const bool diag = p.causal && kt == qt;   // the element-wise causal rule
+    // columns past `lim` are masked: the element-wise causal rule on the
+    // diagonal tile, the sequence's end on the last key tile of non-causal
+    // prefill (causal rows inside the sequence never reach past it)
+    bool masked = p.causal && kt == qt;
+    int lim = r;
+    if (!p.causal) {
+      const int climit = min(kT, L - kt * kT);
+      masked = climit < kT;
+      lim = climit - 1;
+    }
     ok = mbar_wait(&bar[B_SFULL0 + h], j & 1, p.status);
     tc::fence_after_sync();
-    // pass 1: row max (the causal rule only applies on the diagonal tile)
+    // pass 1: row max
     float mx = -INFINITY;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t v[32];
       tc::ld_32x32b_x32(s_addr + c * 32, v);
       tc::wait_ld();
-      if (!diag) {
+      if (!masked) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(v[i]));
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx = (c * 32 + i > r) ? mx : fmaxf(mx, __uint_as_float(v[i]));
+        for (int i = 0; i < 32; ++i) mx = (c * 32 + i > lim) ? mx : fmaxf(mx, __uint_as_float(v[i]));
       }
     }
     const float m_tile = mx * sl2;
@@ -364,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       uint32_t pk[16];
       tc::ld_32x32b_x32(s_addr + c * 32, v);
       tc::wait_ld();
-      if (!diag) {
+      if (!masked) {
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           const float p0 = fast_exp2(fmaf(__uint_as_float(v[i]), sl2, -m_use));
@@ -375,8 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       } else {
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float p0 = (c * 32 + i > r) ? 0.0f : fast_exp2(fmaf(__uint_as_float(v[i]), sl2, -m_use));
-          const float p1 = (c * 32 + i + 1 > r) ? 0.0f : fast_exp2(fmaf(__uint_as_float(v[i + 1]), sl2, -m_use));
+          const float p0 = (c * 32 + i > lim) ? 0.0f : fast_exp2(fmaf(__uint_as_float(v[i]), sl2, -m_use));
+          const float p1 = (c * 32 + i + 1 > lim) ? 0.0f : fast_exp2(fmaf(__uint_as_float(v[i + 1]), sl2, -m_use));
           psum += p0 + p1;
           pk[i / 2] = pack_half2(p0, p1);
         }
@@ -407,7 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   // epilogue: O / l
   if (ok && n_kept > 0) ok = mbar_wait(&bar[B_ORDY0 + h], (n_kept - 1) & 1, p.status);
   tc::fence_after_sync();
-  const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;
+  // rows past the sequence's end are written as zeros
+  const float inv = (l_run > 0.0f && r < q_valid) ? 1.0f / l_run : 0.0f;
   const size_t orow = (static_cast<size_t>(b) * p.Hq + h0 + h) * p.S + static_cast<size_t>(qt) * kT + r;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
@@ -466,6 +512,7 @@ kvq_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.pairs = (p.rep + 1) / 2;
   p.nT = a.S / kT;
   p.causal = a.causal;
+  p.lens = a.lens;
   const float scale = a.softmax_scale > 0.0f ? a.softmax_scale : 1.0f / sqrtf(static_cast<float>(kD));
   p.scale_log2 = scale * 1.4426950408889634f;
   if (g_regs_ok < 0) {

@@ -47,6 +47,7 @@ struct QParams {
   // and sequence b's token t sits in page bt[b * bt_stride + t / 64]
   const int32_t* bt;
   int32_t bt_stride;
+  const int32_t* lens;      // optional per-sequence lengths (contiguous caches only)
   const uint16_t* x;
   int64_t sx_b, sx_h, sx_t;
   uint8_t* codes;
@@ -335,9 +336,12 @@ __device__ __forceinline__ float2 group_sq_error(const uint32_t (&w)[16], const 
 // One thread per (row, group): row = (b * Hkv + h) * nt + t.  (A persistent
 // loop that issued the next group's loads before this group's arithmetic
 // measured slower: the extra registers cost more occupancy than it gained.)
-// PAGED: the cache is a page pool addressed through p.bt (a separate
-// instantiation, so the contiguous kernel carries none of it).
-template <int D, bool PAGED>
+// PAGED: the cache is a page pool addressed through p.bt; LENS: rows at
+// positions t0 + t >= p.lens[b] are not quantised, and those before the end
+// of that length's 128-token tile are cleared (codes and scale/zero word 0,
+// which dequantise to exact zeros for the prefill's last tile); separate
+// instantiations, so the plain kernel carries none of it.
+template <int D, bool PAGED, bool LENS>
 __global__ void __launch_bounds__(256, KVQ_QUANT_MIN_BLOCKS) quantize_kernel(const __grid_constant__ QParams p) {
   constexpr int G = D / 32;
   const int64_t n = p.rows * G;
@@ -352,6 +356,18 @@ __global__ void __launch_bounds__(256, KVQ_QUANT_MIN_BLOCKS) quantize_kernel(con
     const int b = static_cast<int>(bq);
     const int bits = p.bits[h];
     int64_t pos = static_cast<int64_t>(b) * p.Tcap + p.t0 + t;
+    if constexpr (LENS) {
+      const int len = min(max(p.lens[b], 0), p.Tcap);
+      if (p.t0 + t >= len) {
+        if (p.t0 + t < ((len + 127) & ~127)) {
+          uint4* dst = reinterpret_cast<uint4*>(p.codes + p.plane_off[h] + pos * (D * bits / 8) + g * (32 * bits / 8));
+          dst[0] = make_uint4(0u, 0u, 0u, 0u);
+          if (bits == 8) dst[1] = make_uint4(0u, 0u, 0u, 0u);
+          p.sz[(static_cast<int64_t>(h) * p.B * p.Tcap + pos) * G + g] = 0u;
+        }
+        continue;
+      }
+    }
     if constexpr (PAGED) {
       const int tl = p.t0 + t;
       const int page = p.bt[static_cast<int64_t>(b) * p.bt_stride + tl / 64];
@@ -557,6 +573,8 @@ cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t stream) {
   p.B = a.B; p.Hkv = a.Hkv; p.Tcap = a.Tcap; p.t0 = a.t0; p.nt = a.nt;
   p.bt = a.bt;
   p.bt_stride = a.bt_max_pages;
+  p.lens = a.lens;
+  if (p.lens != nullptr && p.bt != nullptr) return cudaErrorInvalidValue;
   p.rows = static_cast<int64_t>(a.bt != nullptr ? a.bt_B : a.B) * a.Hkv * a.nt;
   if (p.rows >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // rows are indexed in 32 bits
   p.div_nt = FastDiv::make(static_cast<uint32_t>(a.nt));
@@ -571,11 +589,13 @@ cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t stream) {
   if (blocks > cap) blocks = cap;
   const unsigned g = static_cast<unsigned>(blocks);
   if (a.D == 128) {
-    if (p.bt != nullptr) quantize_kernel<128, true><<<g, 256, 0, stream>>>(p);
-    else quantize_kernel<128, false><<<g, 256, 0, stream>>>(p);
+    if (p.bt != nullptr) quantize_kernel<128, true, false><<<g, 256, 0, stream>>>(p);
+    else if (p.lens != nullptr) quantize_kernel<128, false, true><<<g, 256, 0, stream>>>(p);
+    else quantize_kernel<128, false, false><<<g, 256, 0, stream>>>(p);
   } else {
-    if (p.bt != nullptr) quantize_kernel<64, true><<<g, 256, 0, stream>>>(p);
-    else quantize_kernel<64, false><<<g, 256, 0, stream>>>(p);
+    if (p.bt != nullptr) quantize_kernel<64, true, false><<<g, 256, 0, stream>>>(p);
+    else if (p.lens != nullptr) quantize_kernel<64, false, true><<<g, 256, 0, stream>>>(p);
+    else quantize_kernel<64, false, false><<<g, 256, 0, stream>>>(p);
   }
   return cudaGetLastError();
 }

@@ -29,7 +29,7 @@ EXPORTS = ("kvq_cache_codes_bytes", "kvq_cache_sz_bytes", "kvq_cache_head_offset
            "kvq_decode_workspace_bytes", "kvq_decode_attention", "kvq_prefill_attention",
            "kvq_decode_attention_noalloc", "kvq_decode_step", "kvq_decode_step_staging_bytes",
            "kvq_decode_step_host", "kvq_quantize_paged", "kvq_decode_attention_paged", "kvq_decode_step_paged",
-           "kvq_build_tile_mask", "kvq_head_error_stats_workspace_bytes", "kvq_head_error_stats",
+           "kvq_build_tile_mask", "kvq_prefill_attention_varlen", "kvq_head_error_stats_workspace_bytes", "kvq_head_error_stats",
            "kvq_allocate_head_bits", "kvq_status_str")
 
 
@@ -72,6 +72,9 @@ def lib() -> ctypes.CDLL:
         L.kvq_prefill_attention.argtypes = [P, P, P, I32, I32, I32, I32, I32, I32, F32, P, I32, CP, CP, P, I32,
                                             P, P]
         L.kvq_prefill_attention.restype = I32
+        L.kvq_prefill_attention_varlen.argtypes = [P, P, P, I32, I32, I32, I32, I32, P, I32, F32, P, I32, CP, CP,
+                                                   P, I32, P, P]
+        L.kvq_prefill_attention_varlen.restype = I32
         L.kvq_decode_attention_noalloc.argtypes = [P, CP, CP, P, I32, F32, P, I32, P, P]
         L.kvq_decode_attention_noalloc.restype = I32
         L.kvq_decode_step.argtypes = [P, P, P, CP, CP, P, I32, F32, P, I32, P, SZ, P, P]
@@ -419,8 +422,9 @@ def allocate_head_bits(k_stats, v_stats, n_high: int, low_bits: int = 4):
 
 def prefill_attention(q, k, v, k_cache: QuantCache, v_cache: QuantCache, softmax_scale: float = 0.0,
                       tile_mask=None, out=None, out_dtype: int = OUT_F32, status=None, stream=None,
-                      causal: bool = True):
-    """Prefill (causal by default): q bf16 [B][Hq][S][D], k/v bf16 [B][Hkv][S][D]; fills the caches, returns out."""
+                      causal: bool = True, seq_lens=None):
+    """Prefill (causal by default): q bf16 [B][Hq][S][D], k/v bf16 [B][Hkv][S][D]; fills the caches, returns out.
+    seq_lens (device int32 [B]): per-sequence lengths within the padded S (kvq_prefill_attention_varlen)."""
     import torch
     B, Hq, S, D = q.shape
     Hkv = k.shape[1]
@@ -428,10 +432,18 @@ def prefill_attention(q, k, v, k_cache: QuantCache, v_cache: QuantCache, softmax
         out = torch.empty((B, Hq, S, D), dtype=torch.float32 if out_dtype == OUT_F32 else torch.bfloat16,
                           device=q.device)
     kc, vc = k_cache.c_struct(), v_cache.c_struct()
-    st = lib().kvq_prefill_attention(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, Hq, Hkv, S, D,
-                                     1 if causal else 0, float(softmax_scale),
-                                     tile_mask.data_ptr() if tile_mask is not None else None, 128,
-                                     ctypes.byref(kc), ctypes.byref(vc), out.data_ptr(), out_dtype,
-                                     status.data_ptr() if status is not None else None, _stream_ptr(stream))
-    _check(st, "kvq_prefill_attention")
+    mask_p = tile_mask.data_ptr() if tile_mask is not None else None
+    status_p = status.data_ptr() if status is not None else None
+    if seq_lens is None:
+        st = lib().kvq_prefill_attention(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, Hq, Hkv, S, D,
+                                         1 if causal else 0, float(softmax_scale), mask_p, 128,
+                                         ctypes.byref(kc), ctypes.byref(vc), out.data_ptr(), out_dtype,
+                                         status_p, _stream_ptr(stream))
+        _check(st, "kvq_prefill_attention")
+    else:
+        st = lib().kvq_prefill_attention_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, Hq, Hkv, S, D,
+                                                seq_lens.data_ptr(), 1 if causal else 0, float(softmax_scale),
+                                                mask_p, 128, ctypes.byref(kc), ctypes.byref(vc), out.data_ptr(),
+                                                out_dtype, status_p, _stream_ptr(stream))
+        _check(st, "kvq_prefill_attention_varlen")
     return out

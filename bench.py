@@ -393,6 +393,39 @@ def bench_head_bits(torch, kvq, W, peaks, steps, warmup, dev):
                          "frac": gbs / peaks["hbm_gbs"], "peak_src": peaks["hbm_src"]}}
 
 
+def bench_prefill_varlen(torch, kvq, W, peaks, steps, warmup, dev):
+    """Causal prefill of 4 sequences of different lengths padded to one S (kvq_prefill_attention_varlen):
+    TFLOP/s of the work the lengths ask for, 4 * D * Hq * sum_b L_b (L_b + 1) / 2."""
+    import numpy as np
+    inp, lens = W.prefill_varlen()
+    B, Hq, Hkv, S, D = inp.B, inp.Hq, inp.Hkv, inp.S, inp.D
+    todev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    q, k, v = todev(inp.q), todev(inp.k), todev(inp.v)
+    sl = torch.from_numpy(lens).to(dev)
+    kc = kvq.empty_cache(inp.head_bits, B, S, D, device=dev)
+    vc = kvq.empty_cache(inp.head_bits, B, S, D, device=dev)
+    out = torch.empty((B, Hq, S, D), dtype=torch.bfloat16, device=dev)
+    run = lambda: kvq.prefill_attention(q, k, v, kc, vc, inp.softmax_scale, None, out=out, out_dtype=kvq.OUT_BF16,
+                                        seq_lens=sl)
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / steps
+    flops = 4.0 * D * Hq * float(sum(int(L) * (int(L) + 1) / 2 for L in lens))
+    tf = flops / t / 1e12
+    return {"workload": inp.name, "lengths": [int(L) for L in lens], "value": tf, "unit": "TFLOP/s",
+            "ms_per_step": t * 1e3, "algorithmic_flop": flops,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["bf16_tflops"], "peak_src": peaks["bf16_src"],
+                         "note": "time includes the two quantise launches; causal work only (no padding)"}}
+
+
 def bench_prefill(torch, kvq, W, peaks, steps, warmup, dev, causal=True):
     """Prefill workload (quantise K/V + attention): TFLOP/s.  Causal: the
     tile-masked causal workload; non-causal: the same shapes, every key visible,
@@ -503,6 +536,7 @@ def main():
         if rank == 0:
             res = bench_prefill(torch, kvq, W, peaks, args.steps, args.warmup, dev)
             res["non_causal"] = bench_prefill(torch, kvq, W, peaks, args.steps, args.warmup, dev, causal=False)
+            res["varlen"] = bench_prefill_varlen(torch, kvq, W, peaks, args.steps, args.warmup, dev)
             print(json.dumps(res))
         if dist:
             dist.destroy_process_group()
@@ -574,6 +608,7 @@ def main():
     if not args.no_prefill and rank == 0:
         prefill = bench_prefill(torch, kvq, W, peaks, max(3, min(args.steps, 10)), 3, dev)
         prefill["non_causal"] = bench_prefill(torch, kvq, W, peaks, 3, 3, dev, causal=False)
+        prefill["varlen"] = bench_prefill_varlen(torch, kvq, W, peaks, 5, 3, dev)
     extras = None
     if not args.no_extras and rank == 0:
         extras = bench_extra_decodes(torch, kvq, W, peaks, dev, args.steps, args.warmup)

@@ -223,6 +223,32 @@ KVQ_API kvq_status kvq_allocate_head_bits(const double* k_stats, const double* v
                                   int32_t n_high, int32_t low_bits, int8_t* head_bits, double* score);
 
 /*
+ * kvq_prefill_attention_varlen -- kvq_prefill_attention over a batch of
+ * sequences of different lengths, padded to S.
+ *
+ * seq_lens: device int32 [B], sequence b's length L_b (0 <= L_b <= S; a value
+ *   outside that range reports KVQ_ERR_INVALID_ARG in dev_status and is
+ *   clamped).  Rows i < L_b of q, k, v hold the sequence; rows L_b .. S-1 are
+ *   padding and are never read into the result (they may hold anything,
+ *   non-finite values included).
+ * Cache positions 0 .. L_b-1 get the codes kvq_quantize would write;
+ * positions from L_b to the end of its 128-token tile are cleared (codes and
+ * scale/zero words 0); positions past that keep their contents.  Output rows
+ * i < L_b are the attention of query i over keys j <= i (causal == 1) or
+ * j < L_b (causal == 0), with the tile mask as in kvq_prefill_attention;
+ * rows L_b .. S-1 of out are written as zeros.  Query tiles wholly past L_b
+ * cost one store of zeros.  Other arguments, layouts and errors as in
+ * kvq_prefill_attention.
+ */
+KVQ_API kvq_status kvq_prefill_attention_varlen(const void* q, const void* k, const void* v,
+                                        int32_t B, int32_t Hq, int32_t Hkv, int32_t S, int32_t D,
+                                        const int32_t* seq_lens, int32_t causal, float softmax_scale,
+                                        const uint8_t* tile_mask, int32_t tile,
+                                        const kvq_cache* k_cache, const kvq_cache* v_cache,
+                                        void* out, int32_t out_dtype,
+                                        int32_t* dev_status, void* stream);
+
+/*
  * kvq_build_tile_mask -- a block-sparse tile mask for kvq_prefill_attention
  * (P4 §2.3: tiles judged unnecessary are skipped, the skipped share capped so
  * that no query block is starved), built on the GPU.

@@ -226,6 +226,15 @@ def prefill_noncausal() -> PrefillInputs:
                         mask_seed=None)
 
 
+def prefill_varlen():
+    """Prefill varlen: B4 sequences padded to S8192, 32/8 heads, D128, INT8 KV, causal, no mask; lengths
+    U[2048, 8192] from their own generator (seed 7), so the padded draws match make_prefill's recipe.
+    Returns (inputs, lengths int32 [B])."""
+    inp = make_prefill("prefill_varlen_b4_h32kv8_d128_s8192_len2k-8k", 6, 4, 32, 8, 128, 8192, mask_seed=None)
+    lens = np.random.Generator(np.random.PCG64(7)).integers(2048, 8192, size=4, endpoint=True).astype(np.int32)
+    return inp, lens
+
+
 def prefill_causal() -> PrefillInputs:
     """Prefill causal: B1, 32/8 heads, D128, S32768, INT8 KV, 25% of below-diagonal tiles skipped."""
     return make_prefill("prefill_causal_b1_h32kv8_d128_s32768_skip25", 3, 1, 32, 8, 128, 32768,

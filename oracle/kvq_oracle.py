@@ -221,18 +221,21 @@ def prefill_allowed(rows: np.ndarray, n_keys: int, tile_mask: np.ndarray | None,
 
 def prefill_rows(q_bits: np.ndarray, k_hat: np.ndarray, v_hat: np.ndarray, b: int, h: int,
                  rows: np.ndarray, tile_mask: np.ndarray | None, softmax_scale: float,
-                 tile: int = 128, causal: bool = True) -> np.ndarray:
+                 tile: int = 128, causal: bool = True, seq_len: int | None = None) -> np.ndarray:
     """(Tile-masked) attention output for selected query rows of one head.
 
-    q_bits: bf16 [B][Hq][S][D]; k_hat, v_hat: float64 [B][Hkv][S][D].  Causal
-    rows see keys up to their own position, non-causal rows all S keys.
-    Returns float64 [len(rows)][D].
+    q_bits: bf16 [B][Hq][S][D]; k_hat, v_hat: float64 [B][Hkv][S][D].  The
+    sequence is seq_len long (S when None; the rows must lie inside it).
+    Causal rows see keys up to their own position, non-causal rows all
+    seq_len keys.  Returns float64 [len(rows)][D].
     """
     Hq = q_bits.shape[1]
     Hkv = k_hat.shape[1]
     kv = h // (Hq // Hkv)
     rows = np.asarray(rows)
-    n_keys = int(rows.max()) + 1 if causal else q_bits.shape[2]
+    L = q_bits.shape[2] if seq_len is None else int(seq_len)
+    assert rows.max() < L, "query rows must lie inside the sequence"
+    n_keys = int(rows.max()) + 1 if causal else L
     q = bf16_to_f32(q_bits[b, h, rows]).astype(np.float64)
     allowed = prefill_allowed(rows, n_keys, tile_mask, tile, causal)
     return attention(q, k_hat[b, kv, :n_keys], v_hat[b, kv, :n_keys], softmax_scale, allowed)

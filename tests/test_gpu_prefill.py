@@ -165,3 +165,115 @@ def test_prefill_non_causal_medium_sampled_rows():
             ref = O.prefill_rows(inp.q[:, h:h + 1], kd, vd, 0, 0, rows, inp.tile_mask, inp.softmax_scale,
                                  causal=False)
             U.assert_close(got[0, h, rows], ref, f"non-causal prefill h={h}")
+
+
+# ---------------------------------------------------------------- varlen
+
+NAN_BF16 = 0x7FC0
+
+
+def _run_varlen(inp, lens, causal, out_dtype=0):
+    """Padding rows of q, k, v hold NaN and the caches hold a NaN-scale sentinel, so any padding value that
+    reached a valid row, or any cache slot that was written past a sequence's end, shows."""
+    from attention_group_quantized_gb300 import kvq
+    B, Hq, Hkv, S, D = inp.B, inp.Hq, inp.Hkv, inp.S, inp.D
+    q, k, v = inp.q.copy(), inp.k.copy(), inp.v.copy()
+    for b, L in enumerate(lens):
+        q[b, :, L:] = NAN_BF16
+        k[b, :, L:] = NAN_BF16
+        v[b, :, L:] = NAN_BF16
+    kc = kvq.empty_cache(np.full(Hkv, 8, np.int8), B, S, D)
+    vc = kvq.empty_cache(np.full(Hkv, 8, np.int8), B, S, D)
+    for c in (kc, vc):
+        c.codes.fill_(0xA5)
+        c.sz.fill_(-1)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mask = torch.from_numpy(inp.tile_mask).cuda() if inp.tile_mask is not None else None
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out = kvq.prefill_attention(U.to_dev_bf16(q), U.to_dev_bf16(k), U.to_dev_bf16(v), kc, vc, inp.softmax_scale,
+                                mask, out_dtype=out_dtype, status=status, causal=causal, seq_lens=sl)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), kc, vc, int(status.item())
+
+
+def _check_varlen(inp, lens, causal, got, kc, out_bf16=False):
+    S, Hkv = inp.S, inp.Hkv
+    planes, scale, zero = U.read_cache(kc, S)
+    for b, L in enumerate(lens):
+        L = min(max(L, 0), S)
+        assert np.all(got[b, :, L:] == 0), f"padding rows of sequence {b} are not zero"
+        if L > 0:
+            kd = _oracle_deq(inp.k[b:b + 1, :, :L])
+            vd = _oracle_deq(inp.v[b:b + 1, :, :L])
+            for h in range(inp.Hq):
+                ref = O.prefill_rows(inp.q[b:b + 1, :, :L], kd, vd, 0, h, np.arange(L), inp.tile_mask,
+                                     inp.softmax_scale, causal=causal)
+                U.assert_close(got[b, h, :L], ref, f"{inp.name} b={b} h={h}", out_bf16)
+            o_planes, o_scale, o_zero, _ = U.oracle_quantize(inp.k[b:b + 1, :, :L], [8] * Hkv)
+            for h in range(Hkv):
+                assert np.array_equal(planes[h][b, :L], o_planes[h][0]), (b, h)
+            assert np.array_equal(scale[b, :, :L].view(np.uint16), o_scale[0].view(np.uint16))
+            assert np.array_equal(zero[b, :, :L].view(np.uint16), o_zero[0].view(np.uint16))
+        # cache positions past the sequence: cleared to the end of its 128-token tile, untouched after
+        E = (L + 127) // 128 * 128
+        for h in range(Hkv):
+            assert np.all(planes[h][b, L:E] == 0), (b, h)
+            assert np.all(planes[h][b, E:] == 0xA5), (b, h)
+        assert np.all(scale[b, :, L:E].view(np.uint16) == 0) and np.all(zero[b, :, L:E].view(np.uint16) == 0)
+        assert np.all(scale[b, :, E:].view(np.uint16) == 0xFFFF)
+
+
+VARLEN = [
+    # name, seed, B, Hq, Hkv, S, lens, causal, mask ("causal" seed / "full" seed / None)
+    ("vl_causal", 71, 3, 4, 2, 512, [512, 300, 1], True, None),
+    ("vl_causal_masked", 72, 2, 8, 2, 640, [640, 129], True, ("causal", 5)),
+    ("vl_noncausal", 73, 3, 4, 1, 384, [384, 200, 127], False, None),
+    ("vl_noncausal_masked", 74, 2, 6, 2, 512, [511, 256], False, ("full", 6)),
+    ("vl_empty_and_one_tile", 75, 2, 2, 1, 256, [0, 128], True, None),
+]
+
+
+@pytest.mark.parametrize("case", VARLEN, ids=[c[0] for c in VARLEN])
+def test_prefill_varlen_parity(case):
+    name, seed, B, Hq, Hkv, S, lens, causal, mk = case
+    inp = W.make_prefill(name, seed, B, Hq, Hkv, 128, S, mask_seed=None)
+    if mk is not None:
+        kind, mseed = mk
+        inp.tile_mask = (W.make_tile_mask(mseed, S // 128) if kind == "causal" else _full_mask(S // 128, mseed))
+    got, kc, vc, status = _run_varlen(inp, lens, causal)
+    assert status == 0
+    _check_varlen(inp, lens, causal, got, kc)
+
+
+def test_prefill_varlen_bf16_out():
+    inp = W.make_prefill("vl_bf16", 76, 2, 4, 2, 128, 384, mask_seed=None)
+    got, kc, vc, status = _run_varlen(inp, [383, 130], True, out_dtype=1)
+    assert status == 0
+    _check_varlen(inp, [383, 130], True, got, kc, out_bf16=True)
+
+
+def test_prefill_varlen_full_lengths_equal_the_plain_call():
+    inp = W.make_prefill("vl_same", 77, 2, 4, 2, 128, 256, mask_seed=3)
+    plain, _, _ = _run(inp)
+    got, _, _, status = _run_varlen(inp, [256, 256], True)
+    assert status == 0
+    assert np.array_equal(plain, got)
+
+
+def test_prefill_varlen_length_out_of_range_is_reported_and_clamped():
+    inp = W.make_prefill("vl_bad", 78, 2, 2, 1, 128, 256, mask_seed=None)
+    from attention_group_quantized_gb300 import kvq
+    kc = kvq.empty_cache(np.full(1, 8, np.int8), 2, 256, 128)
+    vc = kvq.empty_cache(np.full(1, 8, np.int8), 2, 256, 128)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sl = torch.tensor([300, -5], dtype=torch.int32, device="cuda")
+    out = kvq.prefill_attention(U.to_dev_bf16(inp.q), U.to_dev_bf16(inp.k), U.to_dev_bf16(inp.v), kc, vc,
+                                inp.softmax_scale, None, status=status, seq_lens=sl)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+    got = out.cpu().numpy()
+    assert np.all(got[1] == 0)                      # -5 -> 0: nothing
+    kd, vd = _oracle_deq(inp.k[:1]), _oracle_deq(inp.v[:1])
+    for h in range(2):                              # 300 -> 256: the whole sequence
+        ref = O.prefill_rows(inp.q[:1], kd, vd, 0, h, np.arange(256), None, inp.softmax_scale)
+        U.assert_close(got[0, h], ref, f"clamped h={h}")
