@@ -111,6 +111,23 @@ def test_prefill_validation_without_launch(L):
     assert L.kvq_prefill_attention(a, a, a, 1, 4, 2, 256, 128, 1, 0.0, None, 128, P(k4), P(v4), a, 0, None, None) == 2
 
 
+def test_prefill_varlen_validation_without_launch(L):
+    """The varlen entry point checks what the plain one checks, plus its lengths pointer, before any launch."""
+    k, hk = _cache([8, 8], Tcap=256)
+    v, hv = _cache([8, 8], Tcap=256)
+    P = ctypes.byref
+    a, lens = 0x8000, 0x9000
+    call = lambda **o: L.kvq_prefill_attention_varlen(
+        a, a, a, 1, o.get("Hq", 4), 2, o.get("S", 256), 128, o.get("lens", lens), o.get("causal", 1), 0.0, None,
+        o.get("tile", 128), P(k), P(v), a, 0, None, None)
+    assert call(lens=None) == 1
+    assert call(causal=2) == 2
+    assert call(tile=64) == 2
+    assert call(S=200) == 2
+    assert call(S=512) == 1          # longer than the caches
+    assert call(Hq=3) == 1
+
+
 def test_decode_step_validation_without_launch(L):
     k, hk = _cache([8, 8])
     v, hv = _cache([8, 8])
