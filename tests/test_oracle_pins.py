@@ -341,6 +341,25 @@ def test_prefill_non_causal_mask_semantics_brute_force():
     assert np.array_equal(a, b)
 
 
+def test_prefill_seq_len_equals_truncated_inputs():
+    """A sequence of length L inside a padded S: the same as the oracle on inputs cut to L (both modes, with a
+    mask), and padding keys never matter (they are overwritten with large values here)."""
+    rng = np.random.default_rng(17)
+    S, L, D, tile = 12, 7, 4, 4
+    q = _bf16_of(rng.standard_normal((1, 2, S, D)))
+    k = rng.standard_normal((1, 1, S, D)); v = rng.standard_normal((1, 1, S, D))
+    k[:, :, L:] = 1e6; v[:, :, L:] = -1e6
+    mask = np.ones((3, 3), np.uint8); mask[1, 0] = 0; mask[0, 1] = 0
+    rows = np.arange(L)
+    for causal in (True, False):
+        for h in range(2):
+            a = O.prefill_rows(q, k, v, 0, h, rows, mask, 0.5, tile, causal=causal, seq_len=L)
+            b = O.prefill_rows(q[:, :, :L], k[:, :, :L], v[:, :, :L], 0, h, rows, mask, 0.5, tile, causal=causal)
+            assert np.array_equal(a, b)
+    with pytest.raises(AssertionError):
+        O.prefill_rows(q, k, v, 0, 0, np.array([L]), None, 0.5, tile, seq_len=L)
+
+
 def test_prefill_all_ones_mask_equals_dense_causal():
     rng = np.random.default_rng(7)
     S, D = 300, 16
