@@ -457,6 +457,8 @@ static kvq_status prefill_impl(const void* q, const void* k, const void* v, int3
     return KVQ_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || Hq % Hkv) return KVQ_ERR_INVALID_ARG;
   if ((causal != 0 && causal != 1) || tile != 128 || D != 128 || S % 128) return KVQ_ERR_UNSUPPORTED;
+  // the kernel indexes a tile mask [nT][nT] with 32-bit integers
+  if (tile_mask != nullptr && static_cast<int64_t>(S / 128) * (S / 128) >= (int64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
   if (out_dtype != KVQ_OUT_F32 && out_dtype != KVQ_OUT_BF16) return KVQ_ERR_INVALID_ARG;
   PrefillArgs a;
   if (!resolve_layout(*k_cache, &a.layout) || !same_cache_shape(*k_cache, *v_cache)) return KVQ_ERR_INVALID_ARG;

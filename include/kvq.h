@@ -165,7 +165,9 @@ KVQ_API kvq_status kvq_decode_attention(const void* q, const kvq_cache* k, const
  *       contiguous, 16-byte aligned.
  * causal 0 or 1; tile must be 128; S a multiple of 128; D == 128;
  * Hq % Hkv == 0; caches 8-bit for every head, Tcap >= S.
- * tile_mask: device uint8 [nT][nT] or NULL (every tile kept).
+ * tile_mask: device uint8 [nT][nT] or NULL (every tile kept); with a mask,
+ *       nT * nT must stay below 2^31 (S up to 5,931,520), else
+ *       KVQ_ERR_UNSUPPORTED.
  * out:  device [B][Hq][S][D], fp32 or bf16.
  */
 KVQ_API kvq_status kvq_prefill_attention(const void* q, const void* k, const void* v,

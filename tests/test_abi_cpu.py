@@ -128,6 +128,18 @@ def test_prefill_varlen_validation_without_launch(L):
     assert call(Hq=3) == 1
 
 
+def test_prefill_rejects_a_mask_too_large_to_index(L):
+    """nT * nT >= 2^31 with a mask: unsupported before any other check needs the caches."""
+    k, hk = _cache([8, 8], Tcap=128)
+    v, hv = _cache([8, 8], Tcap=128)
+    P = ctypes.byref
+    a = 0x8000
+    S = 46341 * 128                    # nT = 46341, nT^2 > 2^31
+    assert L.kvq_prefill_attention(a, a, a, 1, 4, 2, S, 128, 1, 0.0, a, 128, P(k), P(v), a, 0, None, None) == 2
+    # the same length without a mask gets as far as the cache-shape check
+    assert L.kvq_prefill_attention(a, a, a, 1, 4, 2, S, 128, 1, 0.0, None, 128, P(k), P(v), a, 0, None, None) == 1
+
+
 def test_decode_step_validation_without_launch(L):
     k, hk = _cache([8, 8])
     v, hv = _cache([8, 8])
