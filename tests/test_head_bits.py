@@ -301,3 +301,49 @@ def test_stats_full_size_workload():
     assert np.allclose(vs, o_vs, rtol=1e-5)
     bits, _ = kvq.allocate_head_bits(ks, vs, len(inp.outlier_heads))
     assert list(np.flatnonzero(bits == 8)) == list(inp.outlier_heads)
+
+
+# ------------------------------------------------------------ properties (CPU)
+
+def test_allocation_is_equivariant_and_nested():
+    """Permuting the heads permutes the bit-widths (distinct scores); raising n_high only adds 8-bit heads."""
+    rng = np.random.default_rng(21)
+    for H in (2, 5, 16, 64):
+        sc = rng.random(H)
+        perm = rng.permutation(H)
+        for n_high in range(H + 1):
+            bits = O.allocate_head_bits(sc, n_high)
+            assert np.array_equal(O.allocate_head_bits(sc[perm], n_high), bits[perm])
+            assert int(np.sum(bits == 8)) == n_high
+            if n_high > 0:
+                prev = O.allocate_head_bits(sc, n_high - 1)
+                assert np.all((prev == 8) <= (bits == 8))          # nested: the set only grows
+        # the chosen heads are exactly the n_high largest scores
+        n = H // 2
+        chosen = set(np.flatnonzero(O.allocate_head_bits(sc, n) == 8))
+        assert chosen == set(np.argsort(-sc)[:n])
+
+
+def test_statistics_add_over_sequences_and_ignore_token_order():
+    rng = np.random.default_rng(22)
+    B, H, T, D = 3, 2, 9, 64
+    x = (rng.standard_normal((B, H, T, D)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    w = rng.exponential(1.0, (B, H, T)).astype(np.float32)
+    whole = O.head_error_stats(x, 4, weights=w)
+    parts = sum(O.head_error_stats(x[b:b + 1], 4, weights=w[b:b + 1]) for b in range(B))
+    assert np.allclose(whole, parts, rtol=1e-14)
+    perm = rng.permutation(T)
+    assert np.allclose(O.head_error_stats(x[:, :, perm], 4, weights=w[:, :, perm]), whole, rtol=1e-14)
+
+
+def test_host_allocator_is_equivariant(L):
+    rng = np.random.default_rng(23)
+    H = 24
+    ks = np.stack([rng.random(H), rng.random(H) + 0.5], 1)
+    vs = np.stack([rng.random(H), rng.random(H) + 0.5], 1)
+    perm = rng.permutation(H)
+    for n_high in (0, 5, 12, 24):
+        st, bits, score = _alloc(L, ks, vs, n_high)
+        st2, bits2, score2 = _alloc(L, ks[perm], vs[perm], n_high)
+        assert st == st2 == 0
+        assert np.array_equal(bits2, bits[perm]) and np.array_equal(score2, score[perm])
