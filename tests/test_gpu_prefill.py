@@ -230,6 +230,8 @@ VARLEN = [
     ("vl_noncausal", 73, 3, 4, 1, 384, [384, 200, 127], False, None),
     ("vl_noncausal_masked", 74, 2, 6, 2, 512, [511, 256], False, ("full", 6)),
     ("vl_empty_and_one_tile", 75, 2, 2, 1, 256, [0, 128], True, None),
+    ("vl_tile_edges_causal", 79, 5, 4, 2, 1024, [1024, 1023, 897, 128, 0], True, ("causal", 8)),
+    ("vl_tile_edges_noncausal", 80, 5, 4, 2, 1024, [1, 1023, 897, 129, 1024], False, ("full", 9)),
 ]
 
 
