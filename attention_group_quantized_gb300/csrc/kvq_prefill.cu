@@ -31,6 +31,8 @@
 // The running max is only moved (and O rescaled) when it grows by more than
 // 2^8, so P stays <= 256 and rescales are rare; the final division uses the
 // sum accumulated against the same max, which keeps the result exact.
+#include <mutex>
+
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 #include "kvq_tc.cuh"
@@ -486,8 +488,29 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   if (lane == 0) mbar_arrive(&bar[B_DONE]);
 }
 
-bool g_attr_set = false;
-int g_regs_ok = -1;   // the register split above assumes 128 registers per thread at launch
+// Per device, set once under a lock: the kernel's large dynamic shared memory
+// limit, and whether it was built with the 128 registers per thread that the
+// register split above assumes.  1 = ready, -1 = not usable, 0 = not yet set.
+std::mutex g_prep_mu;
+int g_prep[64] = {};
+
+int prepare_prefill_on_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  std::lock_guard<std::mutex> lock(g_prep_mu);
+  if (g_prep[dev] == 0) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, prefill_kernel) != cudaSuccess || fa.numRegs != 128) {
+      g_prep[dev] = -2;   // unsupported build
+    } else if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+               cudaSuccess) {
+      return -1;          // a CUDA error; try again on the next call
+    } else {
+      g_prep[dev] = 1;
+    }
+  }
+  return g_prep[dev];
+}
 
 }  // namespace
 
@@ -515,16 +538,9 @@ kvq_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.lens = a.lens;
   const float scale = a.softmax_scale > 0.0f ? a.softmax_scale : 1.0f / sqrtf(static_cast<float>(kD));
   p.scale_log2 = scale * 1.4426950408889634f;
-  if (g_regs_ok < 0) {
-    cudaFuncAttributes fa;
-    g_regs_ok = (cudaFuncGetAttributes(&fa, prefill_kernel) == cudaSuccess && fa.numRegs == 128) ? 1 : 0;
-  }
-  if (g_regs_ok != 1) return KVQ_ERR_UNSUPPORTED;
-  if (!g_attr_set) {
-    if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
-      return KVQ_ERR_CUDA;
-    g_attr_set = true;
-  }
+  const int prep = prepare_prefill_on_current_device();
+  if (prep == -2) return KVQ_ERR_UNSUPPORTED;
+  if (prep != 1) return KVQ_ERR_CUDA;
   const int64_t items = static_cast<int64_t>(p.nT) * a.B * a.Hkv * p.pairs;
   if (items >= (int64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
   prefill_kernel<<<static_cast<unsigned>(items), kThreads, kSmemBytes, stream>>>(p);

@@ -35,6 +35,8 @@ if ROOT not in sys.path:
 
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+# the one metric string both arms print, so their lines can be paired
+METRIC = "quant-KV decode attn HBM GB/s (% of peak); prefill attn TFLOP/s (% of peak)"
 
 
 def _peaks():
@@ -137,13 +139,22 @@ def _traffic_from_profile(kernel_src: str, workload: str):
         return None
 
 
-def _oracle_subprocess(workload: str, seconds: float):
+def _oracle_subprocess(workload: str, seconds: float, procs: int = 1):
+    """The CPU oracle timed on a bounded sample, in a child process (BLAS one
+    thread per process; procs = 0 runs one worker process per host core)."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, "-m", "oracle.timing", "--workload", workload, "--seconds", str(seconds)],
-                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    r = subprocess.run([sys.executable, "-m", "oracle.timing", "--workload", workload, "--seconds", str(seconds),
+                        "--procs", str(procs)],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
     if r.returncode != 0:
         return {"error": r.stderr.strip().splitlines()[-1:] or ["failed"]}
     return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def _cpu_entry(r: dict) -> dict:
+    if "error" in r:
+        return r
+    return {"value": r["value"], "unit": r["unit"], "cores": r["cores"], "kind": "oracle", "sample": r["sample"]}
 
 
 def max_over_ranks(torch, dist, value: float, device) -> float:
@@ -170,31 +181,47 @@ def decode_bytes(inp) -> int:
 
 
 def run_reference(args, rank):
-    """Reference arm: the CPU oracle, as it stands, on a bounded sample (rank 0 only)."""
+    """Reference arm: the CPU oracle, as it stands, on the host cores (rank 0
+    only).  A step is a bounded sample of the decode workload, run by one
+    worker process per host core; the prefill workload's oracle is timed once
+    beside it on one core."""
     if rank != 0:
         return
     import kvq_workloads as W
+    from oracle import timing as OT
     name = W.NAMED[args.workload]().name
-    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    per_step = getattr(args, "step_seconds", None) or max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    procs = os.cpu_count() or 1
+    try:
+        timer = OT.ParallelDecodeTimer(args.workload, procs)
+    except Exception as e:   # no process pool on this host
+        print(json.dumps({"impl": "reference", "unavailable": f"oracle worker pool failed: {e}"}))
+        return
     vals = []
     last = None
-    for i in range(args.warmup + args.steps):
-        r = _oracle_subprocess(args.workload, per_step)
-        if "error" in r:
-            print(json.dumps({"impl": "reference", "unavailable": f"oracle run failed: {r['error']}"}))
-            return
-        if i >= args.warmup:
-            vals.append(r["value"])
-        last = r
+    try:
+        for i in range(args.warmup + args.steps):
+            r = timer.step(per_step)
+            if i >= args.warmup:
+                vals.append(r["value"])
+            last = r
+    finally:
+        timer.close()
     v = statistics.mean(vals)
-    line = {"impl": "reference", "metric": "quant-KV decode attn HBM GB/s", "value": v, "unit": "GB/s",
+    pre = _oracle_subprocess("prefill_causal", 10.0)
+    prefill = None
+    if "error" not in pre:
+        prefill = {"workload": W.NAMED["prefill_causal"]().name, "value": pre["value"], "unit": pre["unit"],
+                   "cpu_baseline": _cpu_entry(pre)}
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic (seeded, kvq_workloads)",
             "config": {"workload": name},
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": last["cores"], "kind": "oracle",
                              "sample": last["sample"]},
-            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "prefill": prefill}
     print(json.dumps(line))
 
 
@@ -615,15 +642,16 @@ def main():
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
-        cpu = _oracle_subprocess(args.workload, 15.0)
-        if "error" not in cpu:
-            cpu = {"value": cpu["value"], "unit": cpu["unit"], "cores": cpu["cores"], "kind": "oracle",
-                   "sample": cpu["sample"]}
+        # every host core (one oracle process each), and one core alone
+        cpu = _cpu_entry(_oracle_subprocess(args.workload, 15.0, procs=0))
+        cpu["single_core"] = _cpu_entry(_oracle_subprocess(args.workload, 10.0))
+        if prefill is not None and "unavailable" not in prefill:
+            prefill["cpu_baseline"] = _cpu_entry(_oracle_subprocess("prefill_causal", 10.0))
 
     if rank == 0:
         traffic = _traffic_from_profile("kvq_decode.cu", args.workload)
         line = {
-            "metric": "quant-KV decode attn HBM GB/s (% of peak); prefill attn TFLOP/s (% of peak)",
+            "metric": METRIC,
             "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": avg * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "u8/u4 codes, f16 mma, f32 accumulate", "data": "synthetic (seeded, kvq_workloads)",

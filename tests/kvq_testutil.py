@@ -55,7 +55,9 @@ def oracle_quantize(kbits: np.ndarray, head_bits) -> tuple:
 
 def assert_close(got: np.ndarray, ref: np.ndarray, what: str = "", out_bf16: bool = False):
     """|got - ref| <= 2e-3 + 2e-3 |ref|; a bf16 output may also differ by its own
-    rounding, at most half a bf16 ulp = 2^-8 |ref| (8 significant bits)."""
+    rounding, at most half a bf16 ulp = 2^-8 |ref| (8 significant bits).
+
+    Returns the largest err / bound over the elements (1.0 = at the tolerance)."""
     got = np.asarray(got, dtype=np.float64)
     err = np.abs(got - ref)
     bound = TOL_ABS + (TOL_REL + (2.0 ** -8 if out_bf16 else 0.0)) * np.abs(ref)
@@ -64,4 +66,31 @@ def assert_close(got: np.ndarray, ref: np.ndarray, what: str = "", out_bf16: boo
         i = np.unravel_index(np.argmax(err - bound), err.shape)
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance; worst at {i}: "
                              f"got {got[i]!r} ref {ref[i]!r} err {err[i]:.3e} bound {bound[i]:.3e}")
-    return float(err.max()) if err.size else 0.0
+    return float((err / bound).max()) if err.size else 0.0
+
+
+class Margin:
+    """Worst err / bound ratio over several assert_close calls of one case.
+
+    ``report()`` prints it and, when the environment names a file in
+    KVQ_MARGIN_LOG, appends one JSON line there, so a test run can record how
+    far each workload stays inside the tolerance."""
+
+    def __init__(self, name: str):
+        self.name = name
+        self.worst = 0.0
+        self.n = 0
+
+    def add(self, ratio: float, count: int = 1):
+        self.worst = max(self.worst, ratio)
+        self.n += count
+
+    def report(self):
+        import json
+        import os
+        line = {"case": self.name, "worst_err_over_bound": self.worst, "rows": self.n}
+        print(f"parity margin {self.name}: worst err/bound {self.worst:.4f} over {self.n} rows")
+        path = os.environ.get("KVQ_MARGIN_LOG")
+        if path:
+            with open(path, "a") as f:
+                f.write(json.dumps(line) + "\n")

@@ -4,8 +4,8 @@ The call quantises K and V into the caches (bit-exact against the oracle)
 and computes causal or non-causal, tile-masked attention over the
 dequantised cache;
 outputs must satisfy |o - ref| <= 2e-3 + 2e-3 |ref| against the fp64 oracle.
-Small cases are compared on every row; the full-size workload on sampled
-rows of every query head.
+Small cases are compared on every row; the full-size workload on two rows
+of every query tile of every query head.
 """
 import numpy as np
 import pytest
@@ -49,10 +49,12 @@ def _oracle_deq(x):
 def _check_all_rows(inp, got, out_bf16=False, causal=True):
     kd, vd = _oracle_deq(inp.k), _oracle_deq(inp.v)
     rows = np.arange(inp.S)
+    margin = U.Margin(inp.name + ("" if causal else " non-causal"))
     for b in range(inp.B):
         for h in range(inp.Hq):
             ref = O.prefill_rows(inp.q, kd, vd, b, h, rows, inp.tile_mask, inp.softmax_scale, causal=causal)
-            U.assert_close(got[b, h], ref, f"{inp.name} b={b} h={h}", out_bf16)
+            margin.add(U.assert_close(got[b, h], ref, f"{inp.name} b={b} h={h}", out_bf16), len(rows))
+    margin.report()
 
 
 CASES = [
@@ -94,19 +96,29 @@ def test_prefill_bf16_output_and_larger_capacity():
     _check_all_rows(inp, got, out_bf16=True)
 
 
-def test_prefill_full_size_sampled_rows():
+def test_prefill_full_size_rows_of_every_query_tile():
+    """prefill_causal at full size: per query head, two rows of every one of
+    the 256 query tiles -- a tile edge (first row of even tiles, last row of
+    odd ones, so rows 128k - 1 and 128k both occur) and a seeded random row --
+    plus the sequence's last row, against the oracle."""
     inp = W.prefill_causal()
     got, _, _ = _run(inp)
     rng = np.random.default_rng(0)
     rep = inp.Hq // inp.Hkv
+    n_t = inp.S // 128
+    margin = U.Margin(inp.name)
     for kv in range(inp.Hkv):
         kd = _oracle_deq(inp.k[:, kv:kv + 1])
         vd = _oracle_deq(inp.v[:, kv:kv + 1])
         for h in range(kv * rep, (kv + 1) * rep):
-            rows = np.sort(np.concatenate([rng.integers(0, inp.S, 6), [0, 127, 128, inp.S - 1]]))
+            qt = np.arange(n_t)
+            edge = 128 * qt + np.where(qt % 2 == 0, 0, 127)
+            rows = np.unique(np.concatenate([edge, 128 * qt + rng.integers(0, 128, n_t), [inp.S - 1]]))
             sub_q = inp.q[:, h:h + 1]
-            ref = O.prefill_rows(sub_q, kd, vd, 0, 0, rows, inp.tile_mask, inp.softmax_scale)
-            U.assert_close(got[0, h, rows], ref, f"full prefill h={h}")
+            for part in np.array_split(rows, 4):
+                ref = O.prefill_rows(sub_q, kd, vd, 0, 0, part, inp.tile_mask, inp.softmax_scale)
+                margin.add(U.assert_close(got[0, h, part], ref, f"full prefill h={h}"), len(part))
+    margin.report()
 
 
 def _full_mask(n_t: int, seed: int, keep: float = 0.7) -> np.ndarray:

@@ -69,3 +69,29 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
 
     b.run_reference(Args(), 1)    # any rank but 0 returns without work or output
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line_pairs_with_the_main_arm(capsys, monkeypatch):
+    """The reference arm prints the main arm's metric, unit and direction (so
+    the two lines can be paired), its oracle run on a pool of worker
+    processes, and a prefill sub-object."""
+    import json
+    b = _bench()
+    monkeypatch.setattr(b.os, "cpu_count", lambda: 2)
+    monkeypatch.setattr(b, "_oracle_subprocess", lambda w, s, procs=1: {
+        "value": 1e-6, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": "stub"})
+
+    class Args:
+        workload = "decode_tiny"
+        steps = 2
+        warmup = 0
+        gpus = 1
+        step_seconds = 0.2
+
+    b.run_reference(Args(), 0)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["metric"] == b.METRIC
+    assert line["unit"] == "GB/s" and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["cores"] == 2 and line["value"] > 0
+    assert line["prefill"]["unit"] == "TFLOP/s"

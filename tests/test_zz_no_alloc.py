@@ -3,8 +3,8 @@
 kvq_decode_attention_noalloc uses a fixed scratch array inside the library
 instead of a caller workspace.  Through the C ABI, two calls in a row must
 give the same outputs as kvq_decode_attention (within the parity tolerance of
-the other tests), and a shape too large for the built-in scratch must be
-refused without a launch.  This file is collected last on purpose.
+the other tests) and match the oracle directly, and a shape too large for the
+built-in scratch must be refused without a launch.  This file is collected last on purpose.
 """
 import ctypes
 
@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 
 import kvq_workloads as W
+from oracle import kvq_oracle as O
 from tests import kvq_testutil as U
 
 pytestmark = pytest.mark.gpu
@@ -53,12 +54,18 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(kvq):
         sl = torch.from_numpy(inp.seq_lens).cuda()
         status = torch.zeros(1, dtype=torch.int32, device="cuda")
         ref = kvq.decode_attention(q, kc, vc, sl, inp.softmax_scale, status=status)
+        # the oracle over its own dequantised cache, for a direct check as well
+        _, _, _, kd = U.oracle_quantize(inp.k, inp.head_bits)
+        _, _, _, vd = U.oracle_quantize(inp.v, inp.head_bits)
+        oracle = O.decode_attention(inp.q, kd, vd, inp.seq_lens, inp.softmax_scale)
         for call in range(2):
             out = torch.full((inp.B, inp.Hq, inp.D), float("nan"), dtype=torch.float32, device="cuda")
             assert _noalloc(kvq, q, kc, vc, sl, inp.softmax_scale, out, status) == 0
             torch.cuda.synchronize()
             assert int(status.item()) == 0
-            U.assert_close(out.cpu().numpy(), ref.cpu().numpy().astype(np.float64), f"{inp.name} call {call}")
+            got = out.cpu().numpy()
+            U.assert_close(got, ref.cpu().numpy().astype(np.float64), f"{inp.name} call {call}")
+            U.assert_close(got, oracle, f"{inp.name} call {call} vs oracle")
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch(kvq):
