@@ -85,6 +85,25 @@ static int64_t codes_bytes(const kvq_cache& c) {
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// A caller's policy (or the defaults) checked and resolved.
+static bool resolve_policy(const kvq_policy* in, Policy* out) {
+  *out = Policy{};
+  if (in == nullptr) return true;
+  // the ring depth is even: the decode's two table warps take even and odd
+  // tiles, and with an even depth every slot's fills all go to one of them,
+  // which then waits on each of that slot's phases in turn
+  if ((in->decode_ring_tiles != 2 && in->decode_ring_tiles != 4) || in->decode_l2_warm_tiles < 0 ||
+      in->decode_l2_warm_tiles > 16 || in->decode_l2_ahead_tiles < 0 || in->decode_l2_ahead_tiles > 16 ||
+      in->wait_limit_us < 1 || in->wait_limit_us > 60000000u)
+    return false;
+  out->ring = in->decode_ring_tiles;
+  out->l2_warm = in->decode_l2_warm_tiles;
+  out->l2_ahead = in->decode_l2_ahead_tiles;
+  out->wait_ns = static_cast<uint64_t>(in->wait_limit_us) * 1000u;
+  out->issue_limit = in->test_issue_limit < 0 ? -1 : in->test_issue_limit;
+  return true;
+}
+
 }  // namespace kvq
 
 using namespace kvq;
@@ -106,6 +125,16 @@ int64_t kvq_cache_head_offset(const kvq_cache* cache, int32_t h) {
   HeadLayout hl;
   if (!resolve_layout(*cache, &hl) || h < 0 || h >= cache->Hkv) return -1;
   return hl.plane_off[h];
+}
+
+void kvq_policy_default(kvq_policy* policy) {
+  if (policy == nullptr) return;
+  const Policy d{};
+  policy->decode_ring_tiles = d.ring;
+  policy->decode_l2_warm_tiles = d.l2_warm;
+  policy->decode_l2_ahead_tiles = d.l2_ahead;
+  policy->wait_limit_us = static_cast<uint32_t>(d.wait_ns / 1000u);
+  policy->test_issue_limit = d.issue_limit;
 }
 
 const char* kvq_status_str(kvq_status s) {
@@ -178,7 +207,8 @@ static bool table_ok(const kvq_block_table* t, const kvq_cache& pool) {
 // Decode over contiguous caches (table == nullptr) or page pools.
 static kvq_status decode_impl(const void* q, const kvq_cache* k, const kvq_cache* v, const kvq_block_table* table,
                               const int32_t* seq_lens, int32_t Hq, float softmax_scale, void* out, int32_t out_dtype,
-                              void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+                              void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream,
+                              const kvq_policy* policy = nullptr) {
   if (q == nullptr || k == nullptr || v == nullptr || seq_lens == nullptr || out == nullptr)
     return KVQ_ERR_INVALID_ARG;
   if (k->codes == nullptr || k->sz == nullptr || v->codes == nullptr || v->sz == nullptr) return KVQ_ERR_INVALID_ARG;
@@ -206,6 +236,7 @@ static kvq_status decode_impl(const void* q, const kvq_cache* k, const kvq_cache
   a.ws = workspace;
   a.ws_bytes = workspace_bytes;
   a.status = dev_status;
+  if (!resolve_policy(policy, &a.pol)) return KVQ_ERR_INVALID_ARG;
   if (table != nullptr) {
     a.bt = table->pages;
     a.bt_B = table->B;
@@ -221,6 +252,14 @@ kvq_status kvq_decode_attention(const void* q, const kvq_cache* k, const kvq_cac
                                 size_t workspace_bytes, int32_t* dev_status, void* stream) {
   return decode_impl(q, k, v, nullptr, seq_lens, Hq, softmax_scale, out, out_dtype, workspace, workspace_bytes,
                      dev_status, stream);
+}
+
+kvq_status kvq_decode_attention_ex(const void* q, const kvq_cache* k, const kvq_cache* v, const int32_t* seq_lens,
+                                   int32_t Hq, float softmax_scale, void* out, int32_t out_dtype, void* workspace,
+                                   size_t workspace_bytes, const kvq_policy* policy, int32_t* dev_status,
+                                   void* stream) {
+  return decode_impl(q, k, v, nullptr, seq_lens, Hq, softmax_scale, out, out_dtype, workspace, workspace_bytes,
+                     dev_status, stream, policy);
 }
 
 kvq_status kvq_decode_attention_paged(const void* q, const kvq_cache* k_pool, const kvq_cache* v_pool,
@@ -452,18 +491,18 @@ static kvq_status prefill_impl(const void* q, const void* k, const void* v, int3
                                int32_t S, int32_t D, const int32_t* seq_lens, int32_t causal, float softmax_scale,
                                const uint8_t* tile_mask, int32_t tile, const kvq_cache* k_cache,
                                const kvq_cache* v_cache, void* out, int32_t out_dtype, int32_t* dev_status,
-                               void* stream) {
+                               void* stream, const kvq_policy* policy = nullptr) {
   if (q == nullptr || k == nullptr || v == nullptr || k_cache == nullptr || v_cache == nullptr || out == nullptr)
     return KVQ_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || Hq % Hkv) return KVQ_ERR_INVALID_ARG;
-  if ((causal != 0 && causal != 1) || tile != 128 || D != 128 || S % 128) return KVQ_ERR_UNSUPPORTED;
+  if ((causal != 0 && causal != 1) || tile != 128 || (D != 64 && D != 128) || S % 128) return KVQ_ERR_UNSUPPORTED;
   // the kernel indexes a tile mask [nT][nT] with 32-bit integers
   if (tile_mask != nullptr && static_cast<int64_t>(S / 128) * (S / 128) >= (int64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
   if (out_dtype != KVQ_OUT_F32 && out_dtype != KVQ_OUT_BF16) return KVQ_ERR_INVALID_ARG;
   PrefillArgs a;
+  if (!resolve_policy(policy, &a.pol)) return KVQ_ERR_INVALID_ARG;
   if (!resolve_layout(*k_cache, &a.layout) || !same_cache_shape(*k_cache, *v_cache)) return KVQ_ERR_INVALID_ARG;
   if (k_cache->B != B || k_cache->Hkv != Hkv || k_cache->D != D || k_cache->Tcap < S) return KVQ_ERR_INVALID_ARG;
-  if (a.layout.n4 != 0) return KVQ_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(k_cache->codes) ||
       !aligned16(k_cache->sz) || !aligned16(v_cache->codes) || !aligned16(v_cache->sz))
     return KVQ_ERR_INVALID_ARG;
@@ -506,6 +545,15 @@ kvq_status kvq_prefill_attention_varlen(const void* q, const void* k, const void
   if (seq_lens == nullptr) return KVQ_ERR_INVALID_ARG;
   return prefill_impl(q, k, v, B, Hq, Hkv, S, D, seq_lens, causal, softmax_scale, tile_mask, tile, k_cache, v_cache,
                       out, out_dtype, dev_status, stream);
+}
+
+kvq_status kvq_prefill_attention_ex(const void* q, const void* k, const void* v, int32_t B, int32_t Hq, int32_t Hkv,
+                                    int32_t S, int32_t D, const int32_t* seq_lens, int32_t causal,
+                                    float softmax_scale, const uint8_t* tile_mask, int32_t tile,
+                                    const kvq_cache* k_cache, const kvq_cache* v_cache, void* out, int32_t out_dtype,
+                                    const kvq_policy* policy, int32_t* dev_status, void* stream) {
+  return prefill_impl(q, k, v, B, Hq, Hkv, S, D, seq_lens, causal, softmax_scale, tile_mask, tile, k_cache, v_cache,
+                      out, out_dtype, dev_status, stream, policy);
 }
 
 }  // extern "C"

@@ -82,17 +82,10 @@ static_assert(kWarps * (kConsumerRegs + kHelperRegs) == 2 * kWarps * 128, "regis
 #ifndef KVQ_DECODE_MIN_BLOCKS
 #define KVQ_DECODE_MIN_BLOCKS 2
 #endif
+// ring slots in shared memory; a call may keep fewer tiles in flight (its policy)
 constexpr int kStages = KVQ_DECODE_STAGES;
-#ifndef KVQ_DECODE_WARM
-#define KVQ_DECODE_WARM 4
-#endif
-constexpr int kWarm = KVQ_DECODE_WARM;
 constexpr int kMaxRep = 8;      // query heads per KV head
-// tiles per CTA warmed into L2 before the dependency wait (tunable at build time)
-#ifndef KVQ_DECODE_L2_WARM
-#define KVQ_DECODE_L2_WARM 5
-#endif
-constexpr int kL2Warm = KVQ_DECODE_L2_WARM;
+constexpr int kMaxL2Tiles = 16; // most tiles per CTA a policy may prefetch into L2 (warm-up or look-ahead)
 
 struct DParams {
   CUtensorMap tm_k8, tm_k4, tm_v8, tm_v4;
@@ -113,9 +106,25 @@ struct DParams {
   const int32_t* bt;
   int32_t bt_stride, pB, pT;
   float scale_log2;
+  // per-call policy: tiles kept in flight into shared memory (2 or kStages:
+  // an even depth, so that each ring slot is only ever filled with even or
+  // only with odd tiles and one table warp waits on all of its phases),
+  // tiles per CTA prefetched into L2 before the dependency wait and ahead of
+  // the ring while streaming (0 .. kMaxL2Tiles), the bounded-wait limit, and
+  // the test-only issue limit (tiles the copy issuer streams before it stops;
+  // negative = no limit)
+  int32_t ring, l2_warm, l2_ahead, issue_limit;
+  uint64_t wait_ns;
   int32_t plane[KVQ_MAX_HKV];
   int8_t bits[KVQ_MAX_HKV];
 };
+
+// Ring slot and phase parity of the k-th tile of a CTA's range in a ring of R slots.
+__device__ __forceinline__ void ring_pos(int k, int R, int& slot, uint32_t& parity) {
+  const int q = k / R;
+  slot = k - q * R;
+  parity = static_cast<uint32_t>(q & 1);
+}
 
 // Hand-off buffer from the consumer warps to the epilogue warp at a piece end.
 template <int D>
@@ -413,10 +422,11 @@ struct ConsumerSync {
   uint32_t* phase;
   bool* ok;
   int32_t* status;
+  uint64_t wait_ns;
   __device__ __forceinline__ void operator()() const {
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-    *ok = *ok && mbar_wait(bar, *phase & 1, status);
+    *ok = *ok && mbar_wait(bar, *phase & 1, status, wait_ns);
     ++*phase;
     __syncwarp();
   }
@@ -596,7 +606,7 @@ __device__ __forceinline__ void consume_tiles(const uint32_t (&st_s)[NT], const 
   }
 }
 
-// Before the dependency wait (one warp): prefetch into L2 the first kL2Warm
+// Before the dependency wait (one warp): prefetch into L2 the first p.l2_warm
 // tiles of this CTA's range, so that the copies issued after the wait find
 // them there while the previous kernel's last CTAs still run.  The lengths
 // read here may be stale -- the previous kernel may still be writing them --
@@ -606,7 +616,7 @@ __device__ __forceinline__ void consume_tiles(const uint32_t (&st_s)[NT], const 
 template <int D, bool PAGED>
 __device__ __forceinline__ void warm_l2(const DParams& p, int lane) {
   constexpr int G = D / 32;
-  if (kL2Warm <= 0 || p.B > 32) return;
+  if (p.l2_warm <= 0 || p.B > 32) return;
   int len = lane < p.B ? p.seq_lens[lane] : 0;
   len = min(max(len, 0), p.Tcap);
   const int n = (len + kTile - 1) / kTile;
@@ -628,7 +638,7 @@ __device__ __forceinline__ void warm_l2(const DParams& p, int lane) {
   const int bs = min(b, p.B - 1);
   const int nb = __shfl_sync(0xffffffffu, n, bs);
   const int eb = __shfl_sync(0xffffffffu, incl, bs) - nb;
-  if (lane >= kL2Warm || f >= f1 || b >= p.B || nb == 0) return;
+  if (lane >= p.l2_warm || f >= f1 || b >= p.B || nb == 0) return;
   const int64_t off = f - static_cast<int64_t>(p.Hkv) * eb;
   const int kvh = static_cast<int>(off / nb), i = static_cast<int>(off % nb);
   const int bits = p.bits[kvh];
@@ -738,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
   if (w >= kWarps) {
     tc::reg_dealloc<kHelperRegs>();
     if (w == kWarps) {
-      // ---------------- TMA issuer warp: lane 0 keeps kStages tiles in flight ----------------
+      // ---------------- TMA issuer warp: lane 0 keeps p.ring tiles in flight ----------------
       if (lane != 0) return;
       const uint64_t pol = l2_evict_first_policy();   // the cache is streamed once per call
       Cursor pc = locate(f0, pre, B, Hkv);
@@ -754,14 +764,40 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
           advance(pa, pre, B, Hkv);
         }
       }
+      // L2 look-ahead (policy): tiles k + 1 .. k + l2_ahead are requested
+      // into L2 before the ring has room for them, so more of the cache is on
+      // its way from HBM than the shared-memory ring holds
+      const int ahead = p.l2_ahead;
+      Cursor pf = pc;
+      int n_pf = 0;   // tiles of the range prefetched so far (tile 0 is copied at once)
+      auto prefetch_next = [&]() {
+        if (n_pf == 0) { advance(pf, pre, B, Hkv); n_pf = 1; }
+        if (n_pf >= ntiles) return;
+        const int bits_f = p.bits[pf.kvh];
+        int fb = pf.b, ft = pf.i * kTile;
+        if constexpr (PAGED) {   // a bad page id only misdirects this prefetch
+          fb = min(max(p.bt[static_cast<int64_t>(pf.b) * p.bt_stride + pf.i], 0), p.pB - 1);
+          ft = 0;
+        }
+        const int32_t frow = (p.plane[pf.kvh] * p.pB + fb) * p.pT + ft;
+        const int64_t fsz = (static_cast<int64_t>(pf.kvh) * p.pB + fb) * p.pT + ft;
+        prefetch_l2_tile_2d(bits_f == 8 ? &p.tm_k8 : &p.tm_k4, 0, frow);
+        prefetch_l2_tile_2d(bits_f == 8 ? &p.tm_v8 : &p.tm_v4, 0, frow);
+        prefetch_l2_bulk(p.k_sz + fsz * G, L::kSzBytes);
+        prefetch_l2_bulk(p.v_sz + fsz * G, L::kSzBytes);
+        advance(pf, pre, B, Hkv);
+        ++n_pf;
+      };
+      const int R = p.ring;
       for (int k = 0; k < ntiles; ++k) {
-        const int slot = k % kStages;
-        if (k >= kStages && !mbar_wait(&empty[slot], ((k / kStages) - 1) & 1, p.status)) return;
-        // start with kWarm tiles so the first one lands early, the rest once it has
-        if (k == kWarm && kWarm < kStages && !mbar_wait(&full[0], 0, p.status)) return;
+        if (p.issue_limit >= 0 && k >= p.issue_limit) return;   // test-only: stop streaming here
+        int slot;
+        uint32_t par;
+        ring_pos(k, R, slot, par);
+        if (k >= R && !mbar_wait(&empty[slot], par ^ 1u, p.status, p.wait_ns)) return;
         uint8_t* st = smem + slot * L::kStageBytes;
         const int bits = p.bits[pc.kvh];
-        const int R = D * bits / 8;
+        const int Rb = D * bits / 8;
         int pb = pc.b, pt = pc.i * kTile;
         if constexpr (PAGED) {
           pb = pg[0];
@@ -783,7 +819,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
         uint64_t* bar = &full[slot];
         const bool first = pc.i == 0 || k == 0;
         const uint32_t qbytes = first ? static_cast<uint32_t>(p.rep * D * 2) : 0u;
-        mbar_arrive_expect_tx(bar, 2 * kTile * R + 2 * L::kSzBytes + qbytes);
+        mbar_arrive_expect_tx(bar, 2 * kTile * Rb + 2 * L::kSzBytes + qbytes);
         if (first)
           bulk_g2s(st + L::kOffQ, p.q + (static_cast<int64_t>(pc.b) * p.Hq + pc.kvh * p.rep) * D, qbytes, bar);
         tma_2d_g2s_hint(st + L::kOffK, bits == 8 ? &p.tm_k8 : &p.tm_k4, 0, row0, bar, pol);
@@ -791,6 +827,8 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
         bulk_g2s_hint(st + L::kOffKsz, p.k_sz + szoff * G, L::kSzBytes, bar, pol);
         bulk_g2s_hint(st + L::kOffVsz, p.v_sz + szoff * G, L::kSzBytes, bar, pol);
         advance(pc, pre, B, Hkv);
+        // keep the look-ahead l2_ahead tiles past the newest copy
+        while (ahead > 0 && n_pf < ntiles && n_pf <= k + ahead) prefetch_next();
       }
       return;
     }
@@ -801,8 +839,10 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
       Cursor tc = locate(f0 + par, pre, B, Hkv);
       const float sl2 = p.scale_log2;
       for (int kk = par; kk < ntiles; kk += 2) {
-        const int slot = kk % kStages;
-        const bool okw = mbar_wait(&full[slot], (kk / kStages) & 1, p.status);
+        int slot;
+        uint32_t parity;
+        ring_pos(kk, p.ring, slot, parity);
+        const bool okw = mbar_wait(&full[slot], parity, p.status, p.wait_ns);
         if (!__all_sync(0xffffffffu, okw)) return;
         uint8_t* st = smem + slot * L::kStageBytes;
         const uint32_t* ksz = reinterpret_cast<const uint32_t*>(st + L::kOffKsz);
@@ -863,7 +903,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
       zero_empty_rows<D>(p, lens, lane);
       const int npieces = count_pieces(f0, ntiles, pre, B, Hkv);
       for (int e = 0; e + 1 < npieces; ++e) {
-        const bool okw = mbar_wait(epi_full, e & 1, p.status);
+        const bool okw = mbar_wait(epi_full, e & 1, p.status, p.wait_ns);
         if (!__all_sync(0xffffffffu, okw)) return;
         const int4 info = eb->info;
         segment_end<D, 8>(p, eb, &eb->flag[0], info.x, info.y, pre, N, C, lane, 32, WarpSync{}, epi_empty);
@@ -885,9 +925,12 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
   int n_end = 0;
   uint32_t gphase = 0;
 
+  const int R = p.ring;
   for (int k = 0; k < ntiles;) {
-    const int slot = k % kStages;
-    ok = ok && mbar_wait(&ready[slot], (k / kStages) & 1, p.status);
+    int slot, slot1 = 0;
+    uint32_t parity;
+    ring_pos(k, R, slot, parity);
+    ok = ok && mbar_wait(&ready[slot], parity, p.status, p.wait_ns);
     if (!ok) break;   // a timed-out wait ends this warp (status already set)
     const uint8_t* st0 = smem + slot * L::kStageBytes;
     const int4 meta = *reinterpret_cast<const int4*>(st0 + L::kOffMeta);
@@ -913,8 +956,9 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
     int fend, nt;
     if (!(meta.z & kFlagEnd)) {
       // the next tile belongs to the same piece: take both in one step
-      const int slot1 = (k + 1) % kStages;
-      ok = ok && mbar_wait(&ready[slot1], ((k + 1) / kStages) & 1, p.status);
+      uint32_t parity1;
+      ring_pos(k + 1, R, slot1, parity1);
+      ok = ok && mbar_wait(&ready[slot1], parity1, p.status, p.wait_ns);
       if (!ok) break;
       const uint8_t* st1 = smem + slot1 * L::kStageBytes;
       const int f1 = reinterpret_cast<const int4*>(st1 + L::kOffMeta)->z;
@@ -944,7 +988,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
         l_tot[0] += __shfl_xor_sync(0xffffffffu, l_tot[0], o);
         l_tot[1] += __shfl_xor_sync(0xffffffffu, l_tot[1], o);
       }
-      if (n_end > 0) ok = ok && mbar_wait(epi_empty, (n_end - 1) & 1, p.status);
+      if (n_end > 0) ok = ok && mbar_wait(epi_empty, (n_end - 1) & 1, p.status, p.wait_ns);
       if (!ok) break;
       if (g == 0) {
 #pragma unroll
@@ -984,7 +1028,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
       } else {
         // the last piece: the CTA has no more tiles, so the four consumer
         // warps finish it themselves
-        const ConsumerSync cs{gbar, &gphase, &ok, p.status};
+        const ConsumerSync cs{gbar, &gphase, &ok, p.status, p.wait_ns};
         cs();
         segment_end<D, 8>(p, eb, &eb->flag[1], cb, ckvh, pre, N, C, tid, kWarps * 32, cs, nullptr);
       }
@@ -992,7 +1036,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
     __syncwarp();
     if (lane == 0) {
       mbar_arrive(&empty[slot]);
-      if (nt == 2) mbar_arrive(&empty[(k + 1) % kStages]);
+      if (nt == 2) mbar_arrive(&empty[slot1]);
     }
     k += nt;
   }
@@ -1124,6 +1168,14 @@ kvq_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.plane[h] = hl.plane_idx[h];
     p.bits[h] = hl.bits[h];
   }
+  p.ring = a.pol.ring;
+  p.l2_warm = a.pol.l2_warm;
+  p.l2_ahead = a.pol.l2_ahead;
+  p.issue_limit = a.pol.issue_limit;
+  p.wait_ns = a.pol.wait_ns;
+  if ((p.ring != 2 && p.ring != kStages) || p.l2_warm < 0 || p.l2_warm > kMaxL2Tiles || p.l2_ahead < 0 ||
+      p.l2_ahead > kMaxL2Tiles || p.wait_ns == 0)
+    return KVQ_ERR_INVALID_ARG;
   if (paged) (void)(D == 128 ? ctas_per_sm<128, true>() : ctas_per_sm<64, true>());   // sets its smem limit
   const cudaError_t e = D == 128 ? (paged ? launch_split<128, true>(p, C, B, stream) : launch_split<128, false>(p, C, B, stream))
                                  : (paged ? launch_split<64, true>(p, C, B, stream) : launch_split<64, false>(p, C, B, stream));

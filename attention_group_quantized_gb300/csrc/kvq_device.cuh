@@ -27,8 +27,9 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Every spin in these kernels gives up after this long and reports a timeout.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// Every spin in these kernels gives up after a limit (a kernel parameter,
+// 2 s unless the caller's policy says otherwise) and reports a timeout.
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
 // ---------------------------------------------------------------------------
 // mbarrier (shared memory, CTA scope)
@@ -73,13 +74,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
 }
 
 // Bounded wait on an mbarrier phase.  Returns false (and reports
-// KVQ_ERR_TIMEOUT) if the phase did not complete within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase, int32_t* status) {
+// KVQ_ERR_TIMEOUT) if the phase did not complete within limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t phase, int32_t* status, uint64_t limit_ns) {
   if (mbar_try_wait(bar, phase)) return true;
   const uint64_t t0 = global_ns();
   uint32_t n = 0;
   while (!mbar_try_wait(bar, phase)) {
-    if ((++n & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) {
+    if ((++n & 255u) == 0 && global_ns() - t0 > limit_ns) {
       report(status, KVQ_ERR_TIMEOUT);
       return false;
     }

@@ -21,6 +21,15 @@ struct HeadLayout {
 
 bool resolve_layout(const kvq_cache& c, HeadLayout* out);
 
+// Resolved per-call policy (kvq_policy, or its defaults).
+struct Policy {
+  int32_t ring = 4;               // decode: tiles in flight into shared memory (2 .. 4)
+  int32_t l2_warm = 5;            // decode: tiles per CTA prefetched into L2 before the dependency wait
+  int32_t l2_ahead = 0;           // decode: tiles prefetched into L2 ahead of the ring while streaming
+  uint64_t wait_ns = 2000000000ull;   // every bounded wait
+  int32_t issue_limit = -1;       // test only: tiles (decode) / Q loads (prefill) issued before stopping
+};
+
 struct QuantizeArgs {
   const uint16_t* x;
   int64_t sx_b, sx_h, sx_t;
@@ -77,6 +86,7 @@ struct DecodeArgs {
   // optional block table: the caches are page pools (B = pages, Tcap = 64)
   const int32_t* bt = nullptr;
   int32_t bt_B = 0, bt_max_pages = 0;
+  Policy pol;
 };
 // Number of persistent split CTAs on the current device for head dim D.
 int decode_num_ctas(int D);
@@ -98,6 +108,7 @@ struct PrefillArgs {
   int32_t* status;
   int32_t causal = 1;
   const int32_t* lens = nullptr;   // device [B] sequence lengths or null
+  Policy pol;
 };
 kvq_status launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 

@@ -5,8 +5,9 @@
 // cut into 128x128 tiles and never materialised; each tile's softmax statistics
 // (running max, normaliser) are carried forward and a final correction divides
 // by the normaliser (§2.2); whole key tiles may be skipped by a block-sparse
-// mask (§1.3, §2.3); K and V are read as group-quantised codes and dequantised
-// on the fly (§1.3, §2.4).  The attention itself is softmax(Q K^T / sqrt(d)) V
+// mask (§1.3, §2.3); K and V are read as group-quantised codes -- 8 or 4 bits,
+// chosen per KV head (§2.4) -- and dequantised on the fly (§1.3, §2.4).  The
+// attention itself is softmax(Q K^T / sqrt(d)) V
 // (《一只"兔子"如何搅动大模型推理赛道的底层逻辑》 §3.1), with the causal rule or, for
 // non-causal prefill, over every key of the sequence (then the mask may skip
 // any off-diagonal tile; query tiles all carry nT key tiles).
@@ -14,23 +15,35 @@
 // One CTA (512 threads, one per SM) computes one 128-row query tile for two
 // query heads that share a KV head, so every dequantised K/V tile feeds two
 // heads' products:
-//   warp 0      allocates TMEM, loads the bf16 Q tiles by TMA, frees TMEM;
+//   warp 0      allocates TMEM, loads the bf16 Q tiles by TMA, then streams
+//               the K and V code tiles of the kept key tiles by bulk copies
+//               into a ring of 2 KB slots in shared memory (about two tile
+//               parts ahead of the dequant warpgroup), and frees TMEM last;
 //   warp 1      one thread issues every tcgen05.mma:
 //                 S_h = Q_h K^T (A, B from shared memory) and
 //                 O_h += P_h V   (P from TMEM, V from shared memory);
 //   warps 4-7   convert Q to fp16 in place, then per kept key tile read the
-//               INT8 codes and fp16 scale/zero words from global memory and
-//               write exact-rounded fp16 K_hat = (c - z) * s and V_hat tiles in
-//               the 128-byte-swizzled layout the tensor core reads (2 stages);
+//               codes from the ring (the fp16 scale/zero words by global
+//               loads a tile ahead) and write exact-rounded fp16
+//               K_hat = (c - z) * s and V_hat tiles in the 128-byte-swizzled
+//               layout the tensor core reads (2 stages); which row and chunk
+//               each lane takes is chosen per code format so that every
+//               8-lane phase of a 16-byte load or store covers all 32 banks;
 //   warps 8-11  softmax of head 0, warps 12-15 softmax of head 1: one thread
 //               per query row reads its S row from TMEM, applies the causal
-//               rule on the diagonal tile (causal only), updates (max, sum) in the log2
-//               domain, writes P (fp16) back over S, and at the end scales O by
-//               1 / sum and stores it.
-// TMEM (512 columns): S_0 [0,128) O_0 [128,256) S_1 [256,384) O_1 [384,512).
+//               rule on the diagonal tile (causal only), updates (max, sum) in
+//               the log2 domain with two-wide fp32 arithmetic, writes P (fp16)
+//               back over S, and at the end scales O by 1 / sum and stores it.
+// TMEM (512 columns): S_0 [0,128) O_0 [128,128+D) S_1 [256,384) O_1 [384,384+D).
 // The running max is only moved (and O rescaled) when it grows by more than
 // 2^8, so P stays <= 256 and rescales are rare; the final division uses the
 // sum accumulated against the same max, which keeps the result exact.
+//
+// 4-bit heads: a code byte holds channels 2i (low nibble) and 2i+1.  Within
+// each 8-channel block the fp16 tiles hold the channels in the order
+// 0,4,1,5,2,6,3,7 (what one shift and one mask per pair of values give); Q
+// gets the same order when it is converted, so Q.K is unchanged, and O's
+// columns come out in that order and are put back in the epilogue.
 #include <mutex>
 
 #include "kvq_device.cuh"
@@ -41,14 +54,15 @@ namespace kvq {
 namespace {
 
 constexpr int kT = 128;           // tile edge (query rows, keys)
-constexpr int kD = 128;           // head dim
 constexpr int kThreads = 512;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kSub = 2048;        // bytes of one code sub-chunk: 128 dequant threads x 16 B
+constexpr int kRing = 16;         // sub-chunk slots in the code ring (32 KB)
 
 struct PParams {
-  CUtensorMap tm_q;               // bf16 [B*Hq*S][128], box [64][128], 128B swizzle
-  const uint8_t* kcodes;          // plane base of the K cache (all heads 8-bit)
+  CUtensorMap tm_q;               // bf16 [B*Hq*S][D], box [64][128], 128B swizzle
+  const uint8_t* kcodes;          // code buffer of the K cache (every head's plane)
   const uint8_t* vcodes;
   const uint32_t* ksz;
   const uint32_t* vsz;
@@ -60,75 +74,90 @@ struct PParams {
   int32_t causal;                 // 1: keys j <= i; 0: every key of the sequence
   const int32_t* lens;            // [B] sequence lengths (<= S) or null (every sequence S long)
   float scale_log2;
+  uint64_t wait_ns;               // bounded-wait limit
+  int32_t issue_limit;            // test only: 0 withholds the query load (every first wait then runs out)
+  int64_t plane_off[KVQ_MAX_HKV]; // byte offset of each KV head's code plane
+  int8_t bits[KVQ_MAX_HKV];       // 8 or 4 per KV head
 };
 
-// shared memory layout (bytes from a 1024-aligned base)
-constexpr int kQBytes = kT * kD * 2;                 // one head, fp16: 32 KB (2 k-blocks of 16 KB)
-constexpr int kOff_Q = 0;                            // 2 heads
-constexpr int kOff_K = kOff_Q + 2 * kQBytes;         // 2 stages x 32 KB
-constexpr int kOff_V = kOff_K + 2 * kQBytes;         // 2 stages x 32 KB
-constexpr int kOff_Bar = kOff_V + 2 * kQBytes;
 // barriers
 enum {
   B_QFULL = 0, B_QREADY, B_KFULL0, B_KFULL1, B_VFULL0, B_VFULL1, B_KVEMPTY0, B_KVEMPTY1,
-  B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_ORDY0, B_ORDY1, B_DONE, B_COUNT
+  B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_ORDY0, B_ORDY1, B_MMADONE, B_EXIT,
+  B_RFULL,                        // kRing barriers: a code slot has landed
+  B_REMPTY = B_RFULL + kRing,     // kRing barriers: the four dequant warps have read a slot
+  B_COUNT = B_REMPTY + kRing
 };
-constexpr int kOff_Tmem = kOff_Bar + B_COUNT * 8;
-constexpr int kSmemBytes = kOff_Tmem + 16 + 1024;
+// Every warp but warp 0 arrives once on B_EXIT when it is done with shared
+// memory, TMEM and its asynchronous operations, on the normal path and after
+// a timed-out wait alike; warp 0 frees TMEM only after that.
+constexpr int kExitArrivals = kThreads / 32 - 1;
+
+// shared memory layout (bytes from a 1024-aligned base)
+template <int D>
+struct PLayout {
+  static constexpr int kQBytes = kT * D * 2;            // one head's fp16 tile: D/64 blocks of [128 rows][128 B]
+  static constexpr int kOffQ = 0;                       // 2 heads
+  static constexpr int kOffK = kOffQ + 2 * kQBytes;     // 2 stages
+  static constexpr int kOffV = kOffK + 2 * kQBytes;     // 2 stages
+  static constexpr int kOffRing = kOffV + 2 * kQBytes;  // kRing slots of kSub bytes
+  static constexpr int kOffBar = kOffRing + kRing * kSub;
+  static constexpr int kOffTmem = kOffBar + B_COUNT * 8;
+  static constexpr int kBytes = kOffTmem + 16 + 1024;
+};
+static_assert(PLayout<128>::kBytes <= 232448, "shared memory of the D = 128 prefill");
+
+// How the dequant warpgroup walks one code tile (the K or V part of a key
+// tile) of a (D, BITS) head.  Iteration `it` reads one 2 KB sub-chunk of the
+// ring (RPI token rows of R bytes), 16 bytes per thread; a 16-byte chunk
+// holds VPC channels (16 or 32) and becomes two or four 16-byte fp16 chunks
+// of the swizzled operand tile.
+template <int D, int BITS>
+struct DqFmt {
+  static constexpr int R = D * BITS / 8;     // code bytes per token row
+  static constexpr int RPI = kSub / R;       // rows per iteration
+  static constexpr int NI = kT / RPI;        // iterations (ring sub-chunks) per part
+  static constexpr int VPC = 128 / BITS;     // channels per chunk
+  static_assert(RPI * NI == kT, "whole sub-chunks per part");
+};
+
+// Row (within an iteration) and chunk of the 16 bytes thread t reads.  With
+// the 128-byte swizzle, chunk x of fp16 row r sits at bank group x ^ (r & 7),
+// and the D/64 blocks of a tile are 16 KB apart (the same banks).  Per
+// format, the eight lanes of each phase take:
+//   8-bit, D 128: one half (64 B) of row r and the other half of row r + 1:
+//                 the reads cover 128 distinct bytes of banks, and the stores
+//                 (two chunks per lane) go to even chunk indices in one row
+//                 and odd ones in the other;
+//   4-bit, D 128: rows r .. r+3 (r a multiple of 4), the first 32 bytes of rows
+//                 r, r+3 and the last 32 of rows r+1, r+2 (or the other way
+//                 round): again 128 distinct bytes of banks, and each store
+//                 phase writes the four swizzle rows of a quad, once in the
+//                 low and once in the high half of the chunk index;
+//   D 64:         two (8-bit) or four (4-bit) whole consecutive rows.
+template <int D, int BITS>
+__device__ __forceinline__ void dq_lane(int t, int& row, int& c) {
+  const int w = t >> 5, l = t & 31;
+  if constexpr (D == 128 && BITS == 8) {
+    const int sub = (l & 7) >> 2, ph = (l >> 3) & 1;
+    row = 4 * w + 2 * (l >> 4) + sub;
+    c = (l & 3) + 4 * (sub ^ ph);
+  } else if constexpr (D == 128 && BITS == 4) {
+    const int rr = (l & 7) >> 1, ph = (l >> 3) & 1;
+    const int hi = (rr ^ (rr >> 1)) & 1;     // rows 1, 2 of the quad take the other half
+    row = 8 * w + 4 * (l >> 4) + rr;
+    c = 2 * (hi ^ ph) + (l & 1);
+  } else if constexpr (BITS == 8) {          // D 64
+    row = t >> 2;
+    c = t & 3;
+  } else {
+    row = t >> 1;
+    c = t & 1;
+  }
+}
 
 __device__ __forceinline__ bool tile_kept(const PParams& p, int qt, int kt) {
   return kt == qt || p.tile_mask == nullptr || p.tile_mask[qt * p.nT + kt] != 0;
-}
-
-// One 128-token x 128-channel code tile (K or V) of the dequant warpgroup,
-// held in registers between its global loads and its conversion.  Thread wt
-// (0..127), iteration it (0..7): k-block kb = it & 1 (64 channels), row
-// 32 * (it >> 1) + 8 * (wt >> 5) + ((wt & 31) >> 2), 16 channels from
-// chunk c8 = 4 * kb + (wt & 3).  A quarter warp then stores two adjacent rows,
-// whose swizzled chunks never share banks.
-struct CodeRegs {
-  uint4 c[8];
-  uint32_t sz[8];
-};
-
-__device__ __forceinline__ int dq_row(int it, int wt) { return 32 * (it >> 1) + 8 * (wt >> 5) + ((wt & 31) >> 2); }
-__device__ __forceinline__ int dq_c8(int it, int wt) { return 4 * (it & 1) + (wt & 3); }
-
-__device__ __forceinline__ void load_codes(CodeRegs& r, const uint8_t* codes, const uint32_t* sz, int wt) {
-#pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const int row = dq_row(it, wt), c8 = dq_c8(it, wt);
-    r.c[it] = __ldg(reinterpret_cast<const uint4*>(codes + static_cast<size_t>(row) * kD + c8 * 16));
-    r.sz[it] = __ldg(sz + row * 4 + (c8 >> 1));
-  }
-}
-
-// fp16 K_hat / V_hat = (c - z) * s (exact difference, one rounding) into the
-// 128-byte-swizzled K-major operand layout: [2 k-blocks][128 rows][128 B].
-__device__ __forceinline__ void store_dequant(uint8_t* dst, const CodeRegs& r, int wt) {
-#pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const int row = dq_row(it, wt), c8 = dq_c8(it, wt);
-    const uint32_t word = r.sz[it];
-    const uint32_t zb = zero_biased2(word);
-    const uint32_t s2 = (word & 0xFFFFu) | (word << 16);
-    const __half2 sh = *reinterpret_cast<const __half2*>(&s2);
-    uint32_t o[8];
-    const uint32_t w[4] = {r.c[it].x, r.c[it].y, r.c[it].z, r.c[it].w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      uint32_t lo = hsub2_u32(bytes01_biased(w[i]), zb);
-      uint32_t hi = hsub2_u32(bytes23_biased(w[i]), zb);
-      __half2 x = __hmul2(*reinterpret_cast<__half2*>(&lo), sh);
-      __half2 y = __hmul2(*reinterpret_cast<__half2*>(&hi), sh);
-      o[2 * i] = *reinterpret_cast<uint32_t*>(&x);
-      o[2 * i + 1] = *reinterpret_cast<uint32_t*>(&y);
-    }
-    const int kb = c8 >> 2, ch2 = (c8 & 3) * 2, sw = row & 7;
-    uint8_t* rowp = dst + kb * (kT * 128) + row * 128;
-    *reinterpret_cast<uint4*>(rowp + ((ch2 ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-    *reinterpret_cast<uint4*>(rowp + (((ch2 + 1) ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
-  }
 }
 
 // key tiles [0, kt_end) of query tile qt can take part (L: the sequence's length)
@@ -141,23 +170,223 @@ __device__ __forceinline__ int next_kept(const PParams& p, int qt, int kt, int e
   return kt;
 }
 
+// two-wide fp32 arithmetic (one instruction for a pair of values)
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %4};\n\t"
+      "mov.b64 rc, {%5, %5};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n\t.reg .b64 ra, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rd, {%0, %1};\n\t"
+      "add.f32x2 rd, rd, ra;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// 16 bytes of shared memory at a shared-window address
+__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// One code chunk (16 bytes, channels ch0 ..) -> OC fp16 chunks of (c - z) * s
+// (exact difference, one rounding) in the 128-byte-swizzled K-major tile
+// [D/64 blocks][128 rows][128 B] at dst.
+template <int BITS>
+__device__ __forceinline__ void dequant_chunk(uint32_t dst, int row, int ch0, uint4 w, uint32_t word) {
+  constexpr int OC = BITS == 8 ? 2 : 4;
+  const uint32_t zb = zero_biased2(word);
+  const uint32_t s2 = (word & 0xFFFFu) | (word << 16);
+  const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+  uint32_t o[4 * OC];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (BITS == 8) {
+      // channels 4i .. 4i + 3 in order
+      o[2 * i] = hmul2_u32(hsub2_u32(bytes01_biased(wv[i]), zb), s2);
+      o[2 * i + 1] = hmul2_u32(hsub2_u32(bytes23_biased(wv[i]), zb), s2);
+    } else {
+      // channels 8i .. 8i + 7 in the order 0,4,1,5,2,6,3,7
+      o[4 * i + 0] = hmul2_u32(hsub2_u32(nib_biased(wv[i]), zb), s2);
+      o[4 * i + 1] = hmul2_u32(hsub2_u32(nib_biased(wv[i] >> 4), zb), s2);
+      o[4 * i + 2] = hmul2_u32(hsub2_u32(nib_biased(wv[i] >> 8), zb), s2);
+      o[4 * i + 3] = hmul2_u32(hsub2_u32(nib_biased(wv[i] >> 12), zb), s2);
+    }
+  }
+  const int kb = ch0 >> 6, cb = (ch0 & 63) >> 3, sw = row & 7;
+  const uint32_t rowp = dst + kb * (kT * 128) + row * 128;
+#pragma unroll
+  for (int i = 0; i < OC; ++i) sts128(rowp + (((cb + i) ^ sw) << 4), o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+}
+
+// Scale/zero words a thread needs for one part of key tile kt: one per iteration.
+template <int D, int BITS>
+__device__ __forceinline__ void load_part_words(uint32_t (&w)[DqFmt<D, BITS>::NI], const uint32_t* sz, int kt, int row,
+                                                int g) {
+  using F = DqFmt<D, BITS>;
+  constexpr int G = D / 32;
+#pragma unroll
+  for (int it = 0; it < F::NI; ++it) w[it] = __ldg(sz + static_cast<size_t>(kt * kT + F::RPI * it + row) * G + g);
+}
+
+// Dequantise one part (K or V) of a key tile from the code ring into an fp16
+// operand tile.  `seq` counts ring sub-chunks in the producer's order.
+// Returns false (warp-uniformly) if a ring wait ran out.
+template <int D, int BITS>
+__device__ __forceinline__ bool dequant_part(uint32_t dst, uint32_t ring, uint64_t* bar, int& seq,
+                                             const uint32_t (&words)[DqFmt<D, BITS>::NI], int row, int c, int lane,
+                                             const PParams& p) {
+  using F = DqFmt<D, BITS>;
+  const uint32_t roff = static_cast<uint32_t>(row * F::R + c * 16);
+#pragma unroll
+  for (int it = 0; it < F::NI; ++it) {
+    const int q = seq % kRing;
+    const uint32_t par = static_cast<uint32_t>((seq / kRing) & 1);
+    if (!__all_sync(0xffffffffu, mbar_wait(&bar[B_RFULL + q], par, p.status, p.wait_ns))) return false;
+    const uint4 w = lds128(ring + q * kSub + roff);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[B_REMPTY + q]);   // this warp's reads of the slot are done
+    dequant_chunk<BITS>(dst, F::RPI * it + row, c * F::VPC, w, words[it]);
+    ++seq;
+  }
+  return true;
+}
+
+// Dequant warpgroup after Q: every kept key tile's K and V parts into the
+// two-stage fp16 operand tiles.
+template <int D, int BITS>
+__device__ __forceinline__ void dequant_loop(const PParams& p, uint8_t* smem, uint64_t* bar, int b, int kvh, int qt,
+                                             int kt_end, int t, int lane) {
+  using L = PLayout<D>;
+  using F = DqFmt<D, BITS>;
+  int row, c;
+  dq_lane<D, BITS>(t, row, c);
+  const int g = c * F::VPC / 32;
+  const size_t szrow = (static_cast<size_t>(kvh) * p.B + b) * p.Tcap;
+  const uint32_t* ksz = p.ksz + szrow * (D / 32);
+  const uint32_t* vsz = p.vsz + szrow * (D / 32);
+  const uint32_t ring = smem_u32(smem + L::kOffRing);
+  const uint32_t kdst = smem_u32(smem + L::kOffK);
+  const uint32_t vdst = smem_u32(smem + L::kOffV);
+  // scale/zero words one key tile ahead: `cur` for this tile, `nxt` in flight
+  uint32_t kcur[F::NI], vcur[F::NI], knxt[F::NI], vnxt[F::NI];
+  int kt = next_kept(p, qt, 0, kt_end);
+  if (kt < kt_end) {
+    load_part_words<D, BITS>(knxt, ksz, kt, row, g);
+    load_part_words<D, BITS>(vnxt, vsz, kt, row, g);
+  }
+  int seq = 0;
+  for (int j = 0; kt < kt_end; ++j) {
+    const int st = j & 1;
+#pragma unroll
+    for (int it = 0; it < F::NI; ++it) {
+      kcur[it] = knxt[it];
+      vcur[it] = vnxt[it];
+    }
+    const int kt_next = next_kept(p, qt, kt + 1, kt_end);
+    if (kt_next < kt_end) {
+      load_part_words<D, BITS>(knxt, ksz, kt_next, row, g);
+      load_part_words<D, BITS>(vnxt, vsz, kt_next, row, g);
+    }
+    if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bar[B_KVEMPTY0 + st], ((j >> 1) - 1) & 1, p.status, p.wait_ns)))
+      return;
+    if (!dequant_part<D, BITS>(kdst + st * L::kQBytes, ring, bar, seq, kcur, row, c, lane, p)) return;
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[B_KFULL0 + st]);
+    if (!dequant_part<D, BITS>(vdst + st * L::kQBytes, ring, bar, seq, vcur, row, c, lane, p)) return;
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[B_VFULL0 + st]);
+    kt = kt_next;
+  }
+}
+
+// Warp 0's producer loop (one thread): the K and V code parts of every kept
+// key tile, in 2 KB sub-chunks, into the ring.  Returns the number of
+// sub-chunks issued (it stops early if a wait for a free slot runs out).
+template <int D>
+__device__ __forceinline__ int stream_codes(const PParams& p, uint8_t* smem, uint64_t* bar, const uint8_t* kplane,
+                                            const uint8_t* vplane, int R, int qt, int kt_end) {
+  using L = PLayout<D>;
+  const int part_bytes = kT * R;
+  const int nsub = part_bytes / kSub;
+  int seq = 0;
+  for (int kt = next_kept(p, qt, 0, kt_end); kt < kt_end; kt = next_kept(p, qt, kt + 1, kt_end)) {
+    for (int part = 0; part < 2; ++part) {
+      const uint8_t* src = (part ? vplane : kplane) + static_cast<size_t>(kt) * part_bytes;
+      for (int s = 0; s < nsub; ++s) {
+        const int q = seq % kRing;
+        const int round = seq / kRing;
+        if (round > 0 && !mbar_wait(&bar[B_REMPTY + q], static_cast<uint32_t>((round - 1) & 1), p.status, p.wait_ns))
+          return seq;
+        mbar_arrive_expect_tx(&bar[B_RFULL + q], kSub);
+        bulk_g2s(smem + L::kOffRing + q * kSub, src + s * kSub, kSub, &bar[B_RFULL + q]);
+        ++seq;
+      }
+    }
+  }
+  return seq;
+}
+
 // Zeros in the output rows of this work item (a query tile past its sequence's end).
+template <int D>
 __device__ __forceinline__ void zero_out_tile(const PParams& p, int b, int h0, int nh, int qt) {
   const size_t row0 = (static_cast<size_t>(b) * p.Hq + h0) * p.S + static_cast<size_t>(qt) * kT;
-  const int vec_per_row = kD * (p.out_dtype == KVQ_OUT_F32 ? 4 : 2) / 16;
+  const int esz = p.out_dtype == KVQ_OUT_F32 ? 4 : 2;
+  const int vec_per_row = D * esz / 16;
   for (int h = 0; h < nh; ++h) {
-    uint4* base = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) +
-                                           (row0 + static_cast<size_t>(h) * p.S) * kD *
-                                               (p.out_dtype == KVQ_OUT_F32 ? 4 : 2));
+    uint4* base =
+        reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + (row0 + static_cast<size_t>(h) * p.S) * D * esz);
     for (int i = threadIdx.x; i < kT * vec_per_row; i += kThreads) base[i] = make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
+// 32 output values of one row (TMEM columns 32c .. 32c+31, times inv) to global memory.
+__device__ __forceinline__ void store_row32(const PParams& p, size_t off, const float (&o)[32]) {
+  if (p.out_dtype == KVQ_OUT_F32) {
+    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + off);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + off);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __nv_bfloat162 t2 = __floats2bfloat162_rn(o[8 * i + 2 * e], o[8 * i + 2 * e + 1]);
+        w[e] = *reinterpret_cast<uint32_t*>(&t2);
+      }
+      dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PParams p) {
+  using L = PLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kOff_Bar);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOff_Tmem);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffTmem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // ---- work item: (query tile, b, kv head, head pair), longest (last) query tiles first ----
@@ -169,21 +398,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   const int b = rem / p.Hkv;
   const int h0 = kvh * p.rep + 2 * pair;
   const int nh = (2 * pair + 1 < p.rep) ? 2 : 1;
+  const bool four = p.bits[kvh] == 4;
   // the sequence's length: a query tile wholly past it writes zeros and ends
   // here, before any barrier or TMEM is set up (the decision is the CTA's own)
-  int L = p.S;
+  int Ls = p.S;
   if (p.lens != nullptr) {
-    L = p.lens[b];
-    if (L < 0 || L > p.S) {
+    Ls = p.lens[b];
+    if (Ls < 0 || Ls > p.S) {
       if (threadIdx.x == 0 && qt == 0) report(p.status, KVQ_ERR_INVALID_ARG);
-      L = min(max(L, 0), p.S);
+      Ls = min(max(Ls, 0), p.S);
     }
   }
-  if (qt * kT >= L) {
-    zero_out_tile(p, b, h0, nh, qt);
+  if (qt * kT >= Ls) {
+    zero_out_tile<D>(p, b, h0, nh, qt);
     return;
   }
-  const int q_valid = min(kT, L - qt * kT);   // query rows of this tile inside the sequence
+  const int q_valid = min(kT, Ls - qt * kT);   // query rows of this tile inside the sequence
 
   if (threadIdx.x == 0) {
     mbar_init(&bar[B_QFULL], 1);
@@ -194,7 +424,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     mbar_init(&bar[B_SFULL0], 1); mbar_init(&bar[B_SFULL1], 1);
     mbar_init(&bar[B_PFULL0], 4); mbar_init(&bar[B_PFULL1], 4);
     mbar_init(&bar[B_ORDY0], 1); mbar_init(&bar[B_ORDY1], 1);
-    mbar_init(&bar[B_DONE], 4 * nh);
+    mbar_init(&bar[B_MMADONE], 1);
+    mbar_init(&bar[B_EXIT], kExitArrivals);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&bar[B_RFULL + s], 1);
+      mbar_init(&bar[B_REMPTY + s], 4);
+    }
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -214,24 +449,51 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   // 32 x (80 + 192 + 120 + 120) = 16384, its whole register file.
 
   // number of kept key tiles (identical in every role)
-  const int kt_end = key_tile_end(p, qt, L);
+  const int kt_end = key_tile_end(p, qt, Ls);
   int n_kept = 0;
   for (int kt = 0; kt < kt_end; ++kt) n_kept += tile_kept(p, qt, kt) ? 1 : 0;
+  const uint64_t wns = p.wait_ns;
 
   if (warp < 4) {
   tc::reg_dealloc<80>();
   if (warp == 0) {
-    // ---------------- Q by TMA, then wait for the end and free TMEM ----------------
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&bar[B_QFULL], nh * kQBytes);
+    // ---------------- Q by TMA, the code stream, then free TMEM once every role is done ----------------
+    const bool issue = p.issue_limit != 0;
+    int issued = 0;
+    if (lane == 0 && issue) {
+      mbar_arrive_expect_tx(&bar[B_QFULL], nh * L::kQBytes);
       for (int h = 0; h < nh; ++h) {
         const int32_t y = ((b * p.Hq + h0 + h) * p.S) + qt * kT;
-        tma_2d_g2s(smem + kOff_Q + h * kQBytes, &p.tm_q, 0, y, &bar[B_QFULL]);
-        tma_2d_g2s(smem + kOff_Q + h * kQBytes + kT * 128, &p.tm_q, 64, y, &bar[B_QFULL]);
+#pragma unroll
+        for (int kb = 0; kb < D / 64; ++kb)
+          tma_2d_g2s(smem + L::kOffQ + h * L::kQBytes + kb * (kT * 128), &p.tm_q, 64 * kb, y, &bar[B_QFULL]);
+      }
+      const int R = D * p.bits[kvh] / 8;
+      const size_t row0 = static_cast<size_t>(b) * p.Tcap * R;
+      issued = stream_codes<D>(p, smem, bar, p.kcodes + p.plane_off[kvh] + row0, p.vcodes + p.plane_off[kvh] + row0,
+                               R, qt, kt_end);
+    }
+    issued = __shfl_sync(0xffffffffu, issued, 0);
+    // The other roles finish in bounded time: each stops at its first wait
+    // that runs out, and a role waits at most a few times per kept key tile
+    // and ring sub-chunk.  So the exit wait gets a deadline of that many limits.
+    const uint64_t deadline = wns * static_cast<uint64_t>(4 * n_kept + 2 * issued + 8);
+    const uint64_t t0 = global_ns();
+    uint32_t n = 0;
+    while (!mbar_try_wait(&bar[B_EXIT], 0)) {
+      if ((++n & 255u) == 0 && global_ns() - t0 > deadline) {
+        report(p.status, KVQ_ERR_TIMEOUT);
+        break;
       }
     }
+    // every copy into shared memory has landed before the CTA exits: the
+    // query tiles and the last copy into each ring slot (normally long since)
+    if (lane == 0 && issue) {
+      mbar_wait(&bar[B_QFULL], 0, p.status, wns);
+      for (int s = issued > kRing ? issued - kRing : 0; s < issued; ++s)
+        mbar_wait(&bar[B_RFULL + s % kRing], static_cast<uint32_t>((s / kRing) & 1), p.status, wns);
+    }
     __syncwarp();
-    mbar_wait(&bar[B_DONE], 0, p.status);
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
     return;
@@ -239,19 +501,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
   if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    if (lane != 0) return;
+    if (lane != 0) return;   // lane 0 arrives on B_EXIT for the warp
+    do {
     const uint32_t id_qk = tc::idesc_f16_f32(kT, kT, false);
-    const uint32_t id_pv = tc::idesc_f16_f32(kT, kD, true);
-    const uint32_t q_base = smem_u32(smem + kOff_Q);
-    const uint32_t k_base = smem_u32(smem + kOff_K);
-    const uint32_t v_base = smem_u32(smem + kOff_V);
-    if (!mbar_wait(&bar[B_QREADY], 0, p.status)) return;
+    const uint32_t id_pv = tc::idesc_f16_f32(kT, D, true);
+    const uint32_t q_base = smem_u32(smem + L::kOffQ);
+    const uint32_t k_base = smem_u32(smem + L::kOffK);
+    const uint32_t v_base = smem_u32(smem + L::kOffV);
+    if (!mbar_wait(&bar[B_QREADY], 0, p.status, wns)) break;
     tc::fence_after_sync();
     auto issue_qk = [&](int h, int st) {
-      const uint32_t qh = q_base + h * kQBytes;
-      const uint32_t kh = k_base + st * kQBytes;
+      const uint32_t qh = q_base + h * L::kQBytes;
+      const uint32_t kh = k_base + st * L::kQBytes;
 #pragma unroll
-      for (int s = 0; s < kD / 16; ++s) {
+      for (int s = 0; s < D / 16; ++s) {
         const uint32_t off = (s >> 2) * (kT * 128) + (s & 3) * 32;
         tc::mma_ss(tmem + h * 256, tc::smem_desc_sw128(qh + off, 16, 1024), tc::smem_desc_sw128(kh + off, 16, 1024),
                    id_qk, s > 0);
@@ -262,16 +525,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     for (int j = 0; j < n_kept && ok; ++j) {
       const int st = j & 1;
       if (j == 0) {
-        ok = mbar_wait(&bar[B_KFULL0], 0, p.status);
+        ok = mbar_wait(&bar[B_KFULL0], 0, p.status, wns);
         tc::fence_after_sync();
-        for (int h = 0; h < nh; ++h) issue_qk(h, 0);
+        for (int h = 0; h < nh && ok; ++h) issue_qk(h, 0);
       }
-      ok = ok && mbar_wait(&bar[B_VFULL0 + st], (j >> 1) & 1, p.status);
+      ok = ok && mbar_wait(&bar[B_VFULL0 + st], (j >> 1) & 1, p.status, wns);
       tc::fence_after_sync();
       for (int h = 0; h < nh && ok; ++h) {
-        ok = mbar_wait(&bar[B_PFULL0 + h], j & 1, p.status);
+        ok = mbar_wait(&bar[B_PFULL0 + h], j & 1, p.status, wns);
         tc::fence_after_sync();
-        const uint32_t vs = v_base + st * kQBytes;
+        if (!ok) break;
+        const uint32_t vs = v_base + st * L::kQBytes;
 #pragma unroll
         for (int s = 0; s < kT / 16; ++s)
           tc::mma_ts(tmem + h * 256 + 128, tmem + h * 256 + s * 8, tc::smem_desc_sw128(vs + s * 2048, kT * 128, 1024),
@@ -279,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         tc::commit(&bar[B_ORDY0 + h]);
         if (j + 1 < n_kept) {
           if (h == 0) {
-            ok = ok && mbar_wait(&bar[B_KFULL0 + ((j + 1) & 1)], ((j + 1) >> 1) & 1, p.status);
+            ok = ok && mbar_wait(&bar[B_KFULL0 + ((j + 1) & 1)], ((j + 1) >> 1) & 1, p.status, wns);
             tc::fence_after_sync();
           }
           if (ok) issue_qk(h, (j + 1) & 1);
@@ -287,20 +551,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       }
       tc::commit(&bar[B_KVEMPTY0 + st]);
     }
+    } while (0);
+    // every product issued so far has completed (a commit with none pending
+    // arrives at once) before the warp reports that it is done
+    tc::commit(&bar[B_MMADONE]);
+    mbar_wait(&bar[B_MMADONE], 0, p.status, wns);
+    tc::fence_before_sync();
+    mbar_arrive(&bar[B_EXIT]);
     return;
   }
 
-  return;   // warps 2, 3: no role
+  if (lane == 0) mbar_arrive(&bar[B_EXIT]);   // warps 2, 3: no role
+  return;
   }
 
   if (warp < 8) {
     tc::reg_alloc<192>();
     // ---------------- dequant warpgroup ----------------
-    const int wt = threadIdx.x - 128;
-    if (!mbar_wait(&bar[B_QFULL], 0, p.status)) return;
+    const int t = threadIdx.x - 128;
+    do {
+    if (!__all_sync(0xffffffffu, mbar_wait(&bar[B_QFULL], 0, p.status, wns))) break;
+    // Q to fp16 in place (exact for bf16 values in fp16 range); for a 4-bit
+    // head each 8-channel block in the order 0,4,1,5,2,6,3,7 of the K tiles
     bool finite = true;
-    for (int i = wt; i < nh * kQBytes / 16; i += 128) {
-      uint4* ptr = reinterpret_cast<uint4*>(smem + kOff_Q) + i;
+    for (int i = t; i < nh * L::kQBytes / 16; i += 128) {
+      uint4* ptr = reinterpret_cast<uint4*>(smem + L::kOffQ) + i;
       if (q_valid < kT && ((i & 1023) >> 3) >= q_valid) {   // row past the sequence's end
         *ptr = make_uint4(0u, 0u, 0u, 0u);
         continue;
@@ -313,50 +588,35 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         finite &= fabsf(lo) < 65504.0f && fabsf(hi) < 65504.0f;
         w[e] = pack_half2(lo, hi);
       }
+      if (four) {
+        const uint32_t a = prmt(w[0], w[2], 0x5410u), bb = prmt(w[0], w[2], 0x7632u);
+        const uint32_t c = prmt(w[1], w[3], 0x5410u), d = prmt(w[1], w[3], 0x7632u);
+        w[0] = a; w[1] = bb; w[2] = c; w[3] = d;
+      }
       *ptr = make_uint4(w[0], w[1], w[2], w[3]);
     }
     if (!finite) report(p.status, KVQ_ERR_NONFINITE);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar[B_QREADY]);
-
-    const size_t plane = static_cast<size_t>(kvh) * p.B * p.Tcap + static_cast<size_t>(b) * p.Tcap;
-    const uint8_t* kcodes = p.kcodes + plane * kD;
-    const uint8_t* vcodes = p.vcodes + plane * kD;
-    const uint32_t* ksz = p.ksz + plane * 4;
-    const uint32_t* vsz = p.vsz + plane * 4;
-    // two register sets: while one part (K or V of a tile) is converted, the
-    // next part's codes are already on their way from L2 / HBM.  Positions
-    // past a shorter sequence's end within its last tile read as zeros: the
-    // quantiser cleared them (codes and scale/zero words 0), so a masked score
-    // (P = 0) never meets a non-finite V_hat in the P.V product.
-    CodeRegs ra, rb;
-    int kt = next_kept(p, qt, 0, kt_end);
-    if (kt < kt_end) load_codes(ra, kcodes + static_cast<size_t>(kt) * kT * kD, ksz + kt * kT * 4, wt);
-    for (int j = 0; kt < kt_end; ++j) {
-      const int st = j & 1;
-      const int kt_next = next_kept(p, qt, kt + 1, kt_end);
-      load_codes(rb, vcodes + static_cast<size_t>(kt) * kT * kD, vsz + kt * kT * 4, wt);
-      if (j >= 2 && !mbar_wait(&bar[B_KVEMPTY0 + st], ((j >> 1) - 1) & 1, p.status)) return;
-      store_dequant(smem + kOff_K + st * kQBytes, ra, wt);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[B_KFULL0 + st]);
-      if (kt_next < kt_end)
-        load_codes(ra, kcodes + static_cast<size_t>(kt_next) * kT * kD, ksz + kt_next * kT * 4, wt);
-      store_dequant(smem + kOff_V + st * kQBytes, rb, wt);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[B_VFULL0 + st]);
-      kt = kt_next;
-    }
+    // Positions past a shorter sequence's end within its last tile read as
+    // zeros: the quantiser cleared them (codes and scale/zero words 0), so a
+    // masked score (P = 0) never meets a non-finite V_hat in the P.V product.
+    if (four) dequant_loop<D, 4>(p, smem, bar, b, kvh, qt, kt_end, t, lane);
+    else dequant_loop<D, 8>(p, smem, bar, b, kvh, qt, kt_end, t, lane);
+    } while (0);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[B_EXIT]);
     return;
   }
 
   // ---------------- softmax warpgroups ----------------
   tc::reg_dealloc<120>();
   const int h = (warp - 8) >> 2;            // head slot 0 or 1
-  if (h >= nh) return;
+  if (h >= nh) {
+    if (lane == 0) mbar_arrive(&bar[B_EXIT]);
+    return;
+  }
   const int q4 = warp & 3;                  // TMEM lane quarter
   const int r = q4 * 32 + lane;             // query row within the tile
   const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
@@ -374,14 +634,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     bool masked = p.causal && kt == qt;
     int lim = r;
     if (!p.causal) {
-      const int climit = min(kT, L - kt * kT);
+      const int climit = min(kT, Ls - kt * kT);
       masked = climit < kT;
       lim = climit - 1;
     }
-    ok = mbar_wait(&bar[B_SFULL0 + h], j & 1, p.status);
+    // a timed-out wait ends the loop for the whole warp (its TMEM accesses are warp-wide)
+    ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL0 + h], j & 1, p.status, wns));
+    if (!ok) break;
     tc::fence_after_sync();
-    // pass 1: row max
-    float mx = -INFINITY;
+    // pass 1: row max (three-input max, two chains)
+    float mxa = -INFINITY, mxb = -INFINITY;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t v[32];
@@ -389,13 +651,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       tc::wait_ld();
       if (!masked) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(v[i]));
+        for (int i = 0; i < 32; i += 4) {
+          mxa = fmax3(mxa, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+          mxb = fmax3(mxb, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+        }
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx = (c * 32 + i > lim) ? mx : fmaxf(mx, __uint_as_float(v[i]));
+        for (int i = 0; i < 32; ++i) mxa = (c * 32 + i > lim) ? mxa : fmaxf(mxa, __uint_as_float(v[i]));
       }
     }
-    const float m_tile = mx * sl2;
+    const float m_tile = fmaxf(mxa, mxb) * sl2;
     float m_use = m_run, alpha = 1.0f;
     if (m_run == -INFINITY || m_tile > m_run + kRescaleThreshold) {
       m_use = fmaxf(m_run, m_tile);
@@ -403,8 +668,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       m_run = m_use;
     }
     // pass 2: P = 2^(S*scale_log2 - m) as fp16 pairs, written over the part of S
-    // already read (columns 16c.. of P after S columns 32c.. were loaded)
-    float psum = 0.0f;
+    // already read (columns 16c.. of P after S columns 32c.. were loaded);
+    // the exponent arguments and the row sum two at a time
+    float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+    const float neg_m = -m_use;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t v[32];
@@ -413,30 +680,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       tc::wait_ld();
       if (!masked) {
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(v[i]), sl2, -m_use));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(v[i + 1]), sl2, -m_use));
-          psum += p0 + p1;
+        for (int i = 0; i < 32; i += 4) {
+          float x0, x1, x2, x3;
+          ffma2(x0, x1, __uint_as_float(v[i]), __uint_as_float(v[i + 1]), sl2, neg_m);
+          ffma2(x2, x3, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]), sl2, neg_m);
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1), p2 = fast_exp2(x2), p3 = fast_exp2(x3);
+          fadd2(s0, s1, p0, p1);
+          fadd2(s2, s3, p2, p3);
           pk[i / 2] = pack_half2(p0, p1);
+          pk[i / 2 + 1] = pack_half2(p2, p3);
         }
       } else {
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float p0 = (c * 32 + i > lim) ? 0.0f : fast_exp2(fmaf(__uint_as_float(v[i]), sl2, -m_use));
-          const float p1 = (c * 32 + i + 1 > lim) ? 0.0f : fast_exp2(fmaf(__uint_as_float(v[i + 1]), sl2, -m_use));
-          psum += p0 + p1;
+          const float p0 = (c * 32 + i > lim) ? 0.0f : fast_exp2(fmaf(__uint_as_float(v[i]), sl2, neg_m));
+          const float p1 = (c * 32 + i + 1 > lim) ? 0.0f : fast_exp2(fmaf(__uint_as_float(v[i + 1]), sl2, neg_m));
+          fadd2(s0, s1, p0, p1);
           pk[i / 2] = pack_half2(p0, p1);
         }
       }
       tc::st_32x32b_x16(s_addr + c * 16, pk);
     }
+    const float psum = (s0 + s1) + (s2 + s3);
     l_run = l_run * alpha + psum;
     // rescale O (rare): needs the previous P.V product finished
     if (__any_sync(0xffffffffu, alpha != 1.0f) && j > 0) {
-      ok = ok && mbar_wait(&bar[B_ORDY0 + h], (j - 1) & 1, p.status);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_ORDY0 + h], (j - 1) & 1, p.status, wns));
+      if (!ok) break;
       tc::fence_after_sync();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
         tc::ld_32x32b_x32(o_addr + c * 32, v);
         tc::wait_ld();
@@ -451,65 +724,70 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     if (lane == 0) mbar_arrive(&bar[B_PFULL0 + h]);
     ++j;
   }
-  // epilogue: O / l
-  if (ok && n_kept > 0) ok = mbar_wait(&bar[B_ORDY0 + h], (n_kept - 1) & 1, p.status);
+  // epilogue: O / l (skipped after a timed-out wait: the output is then unspecified)
+  if (ok && n_kept > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_ORDY0 + h], (n_kept - 1) & 1, p.status, wns));
   tc::fence_after_sync();
   // rows past the sequence's end are written as zeros
   const float inv = (l_run > 0.0f && r < q_valid) ? 1.0f / l_run : 0.0f;
   const size_t orow = (static_cast<size_t>(b) * p.Hq + h0 + h) * p.S + static_cast<size_t>(qt) * kT + r;
+  if (ok) {
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t v[32];
-    tc::ld_32x32b_x32(o_addr + c * 32, v);
-    tc::wait_ld();
-    if (p.out_dtype == KVQ_OUT_F32) {
-      float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + orow * kD + c * 32);
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t v[32];
+      tc::ld_32x32b_x32(o_addr + c * 32, v);
+      tc::wait_ld();
+      float o[32];
+      if (four) {
+        // column 8m + 2k holds channel 8m + k, column 8m + 2k + 1 channel 8m + 4 + k
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        o[i] = make_float4(__uint_as_float(v[4 * i]) * inv, __uint_as_float(v[4 * i + 1]) * inv,
-                           __uint_as_float(v[4 * i + 2]) * inv, __uint_as_float(v[4 * i + 3]) * inv);
-    } else {
-      uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + orow * kD + c * 32);
+        for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(v[(i & ~7) | ((i & 3) << 1) | ((i >> 2) & 1)]) * inv;
+      } else {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          __nv_bfloat162 t = __floats2bfloat162_rn(__uint_as_float(v[8 * i + 2 * e]) * inv,
-                                                   __uint_as_float(v[8 * i + 2 * e + 1]) * inv);
-          w[e] = *reinterpret_cast<uint32_t*>(&t);
-        }
-        o[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(v[i]) * inv;
       }
+      store_row32(p, orow * D + c * 32, o);
     }
   }
+  tc::wait_st();   // P and rescaled O stores of a loop left early have landed
   tc::fence_before_sync();
   __syncwarp();
-  if (lane == 0) mbar_arrive(&bar[B_DONE]);
+  if (lane == 0) mbar_arrive(&bar[B_EXIT]);
 }
 
-// Per device, set once under a lock: the kernel's large dynamic shared memory
-// limit, and whether it was built with the 128 registers per thread that the
-// register split above assumes.  1 = ready, -1 = not usable, 0 = not yet set.
+// Per device and head dim, set once under a lock: the kernel's large dynamic
+// shared memory limit, and whether it was built with the 128 registers per
+// thread that the register split above assumes.  1 = ready, -2 = not usable,
+// 0 = not yet set.
 std::mutex g_prep_mu;
-int g_prep[64] = {};
+int g_prep[64][2] = {};
 
+template <int D>
 int prepare_prefill_on_current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
   std::lock_guard<std::mutex> lock(g_prep_mu);
-  if (g_prep[dev] == 0) {
+  int& st = g_prep[dev][D == 128 ? 1 : 0];
+  if (st == 0) {
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, prefill_kernel) != cudaSuccess || fa.numRegs != 128) {
-      g_prep[dev] = -2;   // unsupported build
-    } else if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-               cudaSuccess) {
-      return -1;          // a CUDA error; try again on the next call
+    if (cudaFuncGetAttributes(&fa, prefill_kernel<D>) != cudaSuccess || fa.numRegs != 128) {
+      st = -2;   // unsupported build
+    } else if (cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    PLayout<D>::kBytes) != cudaSuccess) {
+      return -1;   // a CUDA error; try again on the next call
     } else {
-      g_prep[dev] = 1;
+      st = 1;
     }
   }
-  return g_prep[dev];
+  return st;
+}
+
+template <int D>
+kvq_status launch_prefill_d(const PParams& p, int64_t items, cudaStream_t stream) {
+  const int prep = prepare_prefill_on_current_device<D>();
+  if (prep == -2) return KVQ_ERR_UNSUPPORTED;
+  if (prep != 1) return KVQ_ERR_CUDA;
+  prefill_kernel<D><<<static_cast<unsigned>(items), kThreads, PLayout<D>::kBytes, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
 }  // namespace
@@ -517,9 +795,11 @@ int prepare_prefill_on_current_device() {
 kvq_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   PParams p;
   memset(&p, 0, sizeof(p));
+  const int D = a.D;
+  if (D != 64 && D != 128) return KVQ_ERR_UNSUPPORTED;
   const uint64_t qrows = static_cast<uint64_t>(a.B) * a.Hq * a.S;
   if (qrows >= (uint64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
-  if (encode_tensor_map_2d(&p.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, kD, qrows, kD * 2, 64, kT,
+  if (encode_tensor_map_2d(&p.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.q, D, qrows, D * 2, 64, kT,
                            CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
     return KVQ_ERR_CUDA;
   p.kcodes = a.k->codes;
@@ -536,15 +816,17 @@ kvq_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.nT = a.S / kT;
   p.causal = a.causal;
   p.lens = a.lens;
-  const float scale = a.softmax_scale > 0.0f ? a.softmax_scale : 1.0f / sqrtf(static_cast<float>(kD));
+  p.wait_ns = a.pol.wait_ns;
+  p.issue_limit = a.pol.issue_limit;
+  for (int h = 0; h < KVQ_MAX_HKV; ++h) {
+    p.plane_off[h] = a.layout.plane_off[h];
+    p.bits[h] = a.layout.bits[h];
+  }
+  const float scale = a.softmax_scale > 0.0f ? a.softmax_scale : 1.0f / sqrtf(static_cast<float>(D));
   p.scale_log2 = scale * 1.4426950408889634f;
-  const int prep = prepare_prefill_on_current_device();
-  if (prep == -2) return KVQ_ERR_UNSUPPORTED;
-  if (prep != 1) return KVQ_ERR_CUDA;
   const int64_t items = static_cast<int64_t>(p.nT) * a.B * a.Hkv * p.pairs;
   if (items >= (int64_t(1) << 31)) return KVQ_ERR_UNSUPPORTED;
-  prefill_kernel<<<static_cast<unsigned>(items), kThreads, kSmemBytes, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+  return D == 128 ? launch_prefill_d<128>(p, items, stream) : launch_prefill_d<64>(p, items, stream);
 }
 
 }  // namespace kvq

@@ -30,7 +30,8 @@ EXPORTS = ("kvq_cache_codes_bytes", "kvq_cache_sz_bytes", "kvq_cache_head_offset
            "kvq_decode_attention_noalloc", "kvq_decode_step", "kvq_decode_step_staging_bytes",
            "kvq_decode_step_host", "kvq_quantize_paged", "kvq_decode_attention_paged", "kvq_decode_step_paged",
            "kvq_build_tile_mask", "kvq_prefill_attention_varlen", "kvq_head_error_stats_workspace_bytes", "kvq_head_error_stats",
-           "kvq_allocate_head_bits", "kvq_status_str")
+           "kvq_allocate_head_bits", "kvq_status_str", "kvq_policy_default", "kvq_decode_attention_ex",
+           "kvq_prefill_attention_ex")
 
 
 class CBlockTable(ctypes.Structure):
@@ -41,6 +42,12 @@ class KvqError(RuntimeError):
     def __init__(self, status: int, what: str):
         super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({status})")
         self.status = status
+
+
+class CPolicy(ctypes.Structure):
+    _fields_ = [("decode_ring_tiles", ctypes.c_int32), ("decode_l2_warm_tiles", ctypes.c_int32),
+                ("decode_l2_ahead_tiles", ctypes.c_int32), ("wait_limit_us", ctypes.c_uint32),
+                ("test_issue_limit", ctypes.c_int32)]
 
 
 class CCache(ctypes.Structure):
@@ -99,6 +106,13 @@ def lib() -> ctypes.CDLL:
         L.kvq_allocate_head_bits.argtypes = [P, P, I32, I32, I32, P, P]
         L.kvq_allocate_head_bits.restype = I32
         L.kvq_status_str.argtypes = [I32]; L.kvq_status_str.restype = ctypes.c_char_p
+        PP = ctypes.POINTER(CPolicy)
+        L.kvq_policy_default.argtypes = [PP]; L.kvq_policy_default.restype = None
+        L.kvq_decode_attention_ex.argtypes = [P, CP, CP, P, I32, F32, P, I32, P, SZ, PP, P, P]
+        L.kvq_decode_attention_ex.restype = I32
+        L.kvq_prefill_attention_ex.argtypes = [P, P, P, I32, I32, I32, I32, I32, P, I32, F32, P, I32, CP, CP, P,
+                                               I32, PP, P, P]
+        L.kvq_prefill_attention_ex.restype = I32
         _LIB = L
     return _LIB
 
@@ -183,9 +197,24 @@ def decode_workspace(B: int, Hq: int, Hkv: int, D: int, device="cuda"):
     return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
 
 
+def policy(**fields) -> CPolicy:
+    """A kvq_policy: the library's defaults with the given fields replaced
+    (decode_ring_tiles, decode_l2_warm_tiles, decode_l2_ahead_tiles,
+    wait_limit_us, test_issue_limit)."""
+    p = CPolicy()
+    lib().kvq_policy_default(ctypes.byref(p))
+    for k, val in fields.items():
+        if not hasattr(p, k):
+            raise TypeError(f"kvq_policy has no field {k}")
+        setattr(p, k, int(val))
+    return p
+
+
 def decode_attention(q, k: QuantCache, v: QuantCache, seq_lens, softmax_scale: float = 0.0,
-                     out=None, out_dtype: int = OUT_F32, workspace=None, status=None, stream=None):
-    """Decode attention: q bf16 [B][Hq][D] over the caches; returns out [B][Hq][D]."""
+                     out=None, out_dtype: int = OUT_F32, workspace=None, status=None, stream=None,
+                     policy: Optional[CPolicy] = None):
+    """Decode attention: q bf16 [B][Hq][D] over the caches; returns out [B][Hq][D].
+    With a policy (see :func:`policy`) the call goes through kvq_decode_attention_ex."""
     import torch
     B, Hq, D = q.shape
     if out is None:
@@ -194,11 +223,19 @@ def decode_attention(q, k: QuantCache, v: QuantCache, seq_lens, softmax_scale: f
     if workspace is None:
         workspace = decode_workspace(B, Hq, k.Hkv, D, q.device)
     kc, vc = k.c_struct(), v.c_struct()
-    st = lib().kvq_decode_attention(q.data_ptr(), ctypes.byref(kc), ctypes.byref(vc), seq_lens.data_ptr(),
-                                    Hq, float(softmax_scale), out.data_ptr(), out_dtype,
-                                    workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                                    status.data_ptr() if status is not None else None, _stream_ptr(stream))
-    _check(st, "kvq_decode_attention")
+    status_p = status.data_ptr() if status is not None else None
+    ws_n = workspace.numel() * workspace.element_size()
+    if policy is None:
+        st = lib().kvq_decode_attention(q.data_ptr(), ctypes.byref(kc), ctypes.byref(vc), seq_lens.data_ptr(),
+                                        Hq, float(softmax_scale), out.data_ptr(), out_dtype,
+                                        workspace.data_ptr(), ws_n, status_p, _stream_ptr(stream))
+        _check(st, "kvq_decode_attention")
+    else:
+        st = lib().kvq_decode_attention_ex(q.data_ptr(), ctypes.byref(kc), ctypes.byref(vc), seq_lens.data_ptr(),
+                                           Hq, float(softmax_scale), out.data_ptr(), out_dtype,
+                                           workspace.data_ptr(), ws_n, ctypes.byref(policy), status_p,
+                                           _stream_ptr(stream))
+        _check(st, "kvq_decode_attention_ex")
     return out
 
 
@@ -422,9 +459,10 @@ def allocate_head_bits(k_stats, v_stats, n_high: int, low_bits: int = 4):
 
 def prefill_attention(q, k, v, k_cache: QuantCache, v_cache: QuantCache, softmax_scale: float = 0.0,
                       tile_mask=None, out=None, out_dtype: int = OUT_F32, status=None, stream=None,
-                      causal: bool = True, seq_lens=None):
+                      causal: bool = True, seq_lens=None, policy: Optional[CPolicy] = None):
     """Prefill (causal by default): q bf16 [B][Hq][S][D], k/v bf16 [B][Hkv][S][D]; fills the caches, returns out.
-    seq_lens (device int32 [B]): per-sequence lengths within the padded S (kvq_prefill_attention_varlen)."""
+    seq_lens (device int32 [B]): per-sequence lengths within the padded S (kvq_prefill_attention_varlen).
+    With a policy (see :func:`policy`) the call goes through kvq_prefill_attention_ex."""
     import torch
     B, Hq, S, D = q.shape
     Hkv = k.shape[1]
@@ -434,7 +472,14 @@ def prefill_attention(q, k, v, k_cache: QuantCache, v_cache: QuantCache, softmax
     kc, vc = k_cache.c_struct(), v_cache.c_struct()
     mask_p = tile_mask.data_ptr() if tile_mask is not None else None
     status_p = status.data_ptr() if status is not None else None
-    if seq_lens is None:
+    if policy is not None:
+        st = lib().kvq_prefill_attention_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, Hq, Hkv, S, D,
+                                            seq_lens.data_ptr() if seq_lens is not None else None,
+                                            1 if causal else 0, float(softmax_scale), mask_p, 128,
+                                            ctypes.byref(kc), ctypes.byref(vc), out.data_ptr(), out_dtype,
+                                            ctypes.byref(policy), status_p, _stream_ptr(stream))
+        _check(st, "kvq_prefill_attention_ex")
+    elif seq_lens is None:
         st = lib().kvq_prefill_attention(q.data_ptr(), k.data_ptr(), v.data_ptr(), B, Hq, Hkv, S, D,
                                          1 if causal else 0, float(softmax_scale), mask_p, 128,
                                          ctypes.byref(kc), ctypes.byref(vc), out.data_ptr(), out_dtype,

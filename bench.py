@@ -226,7 +226,7 @@ def run_reference(args, rank):
 
 
 def time_decode(torch, kvq, inp, dev, l2, steps, warmup, dist=None, keep=False, busy_s=0.0, sampler=None,
-                use_graph=True, paged=False):
+                use_graph=True, paged=False, policy=None):
     """Back-to-back decode steps over cache copies larger than 3x L2 together.
 
     With paged=True each copy is a pair of page pools addressed through a
@@ -273,7 +273,8 @@ def time_decode(torch, kvq, inp, dev, l2, steps, warmup, dist=None, keep=False, 
             kvq.decode_attention_paged(q, kc_i, vc_i, tables[i % n_copies], sl, inp.softmax_scale, out=out,
                                        workspace=ws, status=status)
         else:
-            kvq.decode_attention(q, kc_i, vc_i, sl, inp.softmax_scale, out=out, workspace=ws, status=status)
+            kvq.decode_attention(q, kc_i, vc_i, sl, inp.softmax_scale, out=out, workspace=ws, status=status,
+                                 policy=policy)
 
     for i in range(warmup):
         step(i)
@@ -322,8 +323,19 @@ def time_decode(torch, kvq, inp, dev, l2, steps, warmup, dist=None, keep=False, 
     if clk:
         clk.__exit__(None, None, None)
     t_total = max_over_ranks(torch, dist, t0.elapsed_time(t1) / 1e3, dev)
+    # isolated launches (each synchronised before the next): no overlap with a
+    # previous kernel, so the launch ramp and the merge tail are not hidden
+    iso = []
+    for i in range(min(steps, 10)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        iso.append(e0.elapsed_time(e1) * 1e3)
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     res = {"t_total": t_total, "bytes": nbytes, "n_copies": n_copies, "clk": clk,
+           "isolated_us": statistics.median(iso),
            "timing": "one CUDA graph of the K steps, event-timed" if graph is not None else "eager launches, event-timed"}
     if keep:
         res.update(caches=caches, q=q, sl=sl, ws=ws)
@@ -418,6 +430,58 @@ def bench_head_bits(torch, kvq, W, peaks, steps, warmup, dev):
             "outlier_heads": [int(h) for h in inp.outlier_heads],
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"], "peak_src": peaks["hbm_src"]}}
+
+
+def bench_phase_policy(torch, kvq, W, peaks, steps, warmup, dev, decode_policy):
+    """Phase-specific settings (prefill and decode tuned apart): the causal
+    prefill workload with a sparser tile mask -- 35 % of each row's candidate
+    key tiles skipped, built on the device by kvq_build_tile_mask -- and the
+    decode workload with a wider prefetch policy, each beside the defaults."""
+    import numpy as np
+    res = {}
+    inp = W.prefill_causal()
+    B, Hq, S, D = inp.B, inp.Hq, inp.S, inp.D
+    n_t = S // 128
+    todev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    q, k, v = todev(inp.q), todev(inp.k), todev(inp.v)
+    kc = kvq.empty_cache(inp.head_bits, B, S, D, device=dev)
+    vc = kvq.empty_cache(inp.head_bits, B, S, D, device=dev)
+    out = torch.empty((B, Hq, S, D), dtype=torch.bfloat16, device=dev)
+    for num, den, label in ((1, 4, "skip25_builder"), (7, 20, "skip35_builder")):
+        mask = kvq.build_tile_mask(n_t, num, den, 4, device=dev)
+        m = mask.cpu().numpy()
+        kept = int(np.tril(m, -1).sum())
+        flops = 4.0 * D * Hq * B * (kept * 128 * 128 + n_t * 128 * 129 / 2)
+        run = lambda: kvq.prefill_attention(q, k, v, kc, vc, inp.softmax_scale, mask, out=out, out_dtype=kvq.OUT_BF16)
+        for _ in range(warmup):
+            run()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            run()
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / 1e3 / steps
+        res[label] = {"skipped_share_of_row_candidates": f"{num}/{den}", "kept_below_diagonal_tiles": kept,
+                      "ms_per_step": t * 1e3, "algorithmic_flop": flops, "TFLOP/s": flops / t / 1e12,
+                      "frac_of_bf16_peak": flops / t / 1e12 / peaks["bf16_tflops"]}
+    res["prefill_speedup_35_over_25"] = res["skip25_builder"]["ms_per_step"] / res["skip35_builder"]["ms_per_step"]
+    del q, k, v, kc, vc, out
+    torch.cuda.empty_cache()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    dinp = W.decode_gqa()
+    base = time_decode(torch, kvq, dinp, dev, l2, steps, warmup)
+    pol = kvq.policy(**decode_policy)
+    wide = time_decode(torch, kvq, dinp, dev, l2, steps, warmup, policy=pol)
+    for label, d in (("decode_default_policy", base), ("decode_phase_policy", wide)):
+        avg = d["t_total"] / steps
+        res[label] = {"us_per_step": avg * 1e6, "isolated_launch_us": d["isolated_us"],
+                      "GB/s": d["bytes"] / avg / 1e9, "frac_of_hbm_peak": d["bytes"] / avg / 1e9 / peaks["hbm_gbs"]}
+    res["decode_phase_policy"]["policy"] = dict(decode_policy)
+    res["decode_speedup_policy_over_default"] = (res["decode_default_policy"]["us_per_step"] /
+                                                 res["decode_phase_policy"]["us_per_step"])
+    return res
 
 
 def bench_prefill_varlen(torch, kvq, W, peaks, steps, warmup, dev):
@@ -529,6 +593,10 @@ def main():
                     help="run only the prefill workloads (causal, non-causal) and print their JSON object")
     ap.add_argument("--only-head-bits", action="store_true",
                     help="run only the per-head bit allocation workload and print its JSON object")
+    ap.add_argument("--only-phase-policy", action="store_true",
+                    help="run only the phase-policy legs (sparser prefill mask, wider decode prefetch)")
+    ap.add_argument("--decode-policy", default="ring=4,warm=5,ahead=4",
+                    help="decode phase policy of the phase-policy leg: ring tiles, L2 warm-up tiles, L2 look-ahead")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -559,6 +627,16 @@ def main():
         if dist:
             dist.destroy_process_group()
         return
+    pol_fields = dict(kv.split("=") for kv in args.decode_policy.split(","))
+    decode_policy = {"decode_ring_tiles": int(pol_fields.get("ring", 4)),
+                     "decode_l2_warm_tiles": int(pol_fields.get("warm", 5)),
+                     "decode_l2_ahead_tiles": int(pol_fields.get("ahead", 0))}
+    if args.only_phase_policy:
+        if rank == 0:
+            print(json.dumps(bench_phase_policy(torch, kvq, W, peaks, args.steps, args.warmup, dev, decode_policy)))
+        if dist:
+            dist.destroy_process_group()
+        return
     if args.only_prefill:
         if rank == 0:
             res = bench_prefill(torch, kvq, W, peaks, args.steps, args.warmup, dev)
@@ -576,6 +654,7 @@ def main():
                     sampler=lambda: ClockSampler(local))
     clk = d["clk"]
     timing = d["timing"]
+    isolated_us = d["isolated_us"]
     caches, n_copies, q, sl, ws = d["caches"], d["n_copies"], d["q"], d["sl"], d["ws"]
     bytes_per_step = d["bytes"]
     t_total = d["t_total"]
@@ -639,6 +718,9 @@ def main():
     extras = None
     if not args.no_extras and rank == 0:
         extras = bench_extra_decodes(torch, kvq, W, peaks, dev, args.steps, args.warmup)
+    phase = None
+    if not args.no_extras and not args.no_prefill and rank == 0:
+        phase = bench_phase_policy(torch, kvq, W, peaks, max(3, min(args.steps, 10)), 3, dev, decode_policy)
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
@@ -673,6 +755,8 @@ def main():
             "prefill": prefill,
             "head_bits": head_bits,
             "other_decode_workloads": extras,
+            "phase_policy": phase,
+            "decode_isolated_launch_us": isolated_us,
         }
         print(json.dumps(line))
     if dist:

@@ -163,8 +163,9 @@ KVQ_API kvq_status kvq_decode_attention(const void* q, const kvq_cache* k, const
  *
  * q:    device bf16 [B][Hq][S][D]; k, v: device bf16 [B][Hkv][S][D];
  *       contiguous, 16-byte aligned.
- * causal 0 or 1; tile must be 128; S a multiple of 128; D == 128;
- * Hq % Hkv == 0; caches 8-bit for every head, Tcap >= S.
+ * causal 0 or 1; tile must be 128; S a multiple of 128; D 64 or 128;
+ * Hq % Hkv == 0; caches with any per-head bits (8 or 4, e.g. from
+ * kvq_allocate_head_bits), Tcap >= S.
  * tile_mask: device uint8 [nT][nT] or NULL (every tile kept); with a mask,
  *       nT * nT must stay below 2^31 (S up to 5,931,520), else
  *       KVQ_ERR_UNSUPPORTED.
@@ -406,6 +407,63 @@ KVQ_API kvq_status kvq_decode_step_paged(const void* q, const void* k_new, const
                                          int32_t Hq, float softmax_scale, void* out, int32_t out_dtype,
                                          void* workspace, size_t workspace_bytes, int32_t* dev_status,
                                          void* stream);
+
+/*
+ * kvq_policy -- per-call settings for the two phases (P4 §5.3: prefill and
+ * decode want different settings -- prefill has no history to re-read and is
+ * compute-bound, so its tile mask may skip more; decode re-reads the whole
+ * cache for every token and is memory-bound, so it gains from fetching the
+ * cache further ahead).  The prefill phase's sparsity is its tile mask
+ * (kvq_build_tile_mask's skip ratio); the decode phase's prefetch width is
+ * set here.  kvq_policy_default() fills the values every other call uses.
+ *
+ *   decode_ring_tiles     64-token tiles of K and V that each decode CTA keeps
+ *                         in flight into shared memory, 2 or 4 (default 4).
+ *   decode_l2_warm_tiles  tiles per CTA requested into L2 before the decode
+ *                         waits for the previous kernel in the stream to
+ *                         finish, 0 .. 16 (default 5).
+ *   decode_l2_ahead_tiles tiles per CTA requested into L2 ahead of the ring
+ *                         while streaming, 0 .. 16 (default 0).
+ *   wait_limit_us         every bounded wait inside the decode and prefill
+ *                         kernels gives up after this long and reports
+ *                         KVQ_ERR_TIMEOUT in dev_status, 1 .. 60,000,000
+ *                         (default 2,000,000 = 2 s).
+ *   test_issue_limit      FOR TESTS OF THE TIMEOUT PATH ONLY; negative (the
+ *                         default) = off.  Decode: each CTA's copy issuer
+ *                         streams only its first test_issue_limit tiles, so
+ *                         the waits for the rest run out.  Prefill: 0
+ *                         withholds the query load, so every role's first
+ *                         wait runs out (other values: no effect).  Nothing
+ *                         is left in flight; the call reports KVQ_ERR_TIMEOUT
+ *                         and its outputs are unspecified.
+ * An out-of-range field returns KVQ_ERR_INVALID_ARG and launches nothing.
+ */
+typedef struct kvq_policy {
+  int32_t decode_ring_tiles;
+  int32_t decode_l2_warm_tiles;
+  int32_t decode_l2_ahead_tiles;
+  uint32_t wait_limit_us;
+  int32_t test_issue_limit;
+} kvq_policy;
+
+KVQ_API void kvq_policy_default(kvq_policy* policy);
+
+/* kvq_decode_attention with a policy (NULL = kvq_policy_default). */
+KVQ_API kvq_status kvq_decode_attention_ex(const void* q, const kvq_cache* k, const kvq_cache* v,
+                                           const int32_t* seq_lens, int32_t Hq, float softmax_scale,
+                                           void* out, int32_t out_dtype,
+                                           void* workspace, size_t workspace_bytes,
+                                           const kvq_policy* policy, int32_t* dev_status, void* stream);
+
+/* kvq_prefill_attention_varlen with a policy (NULL = kvq_policy_default);
+ * seq_lens may be NULL (every sequence S long, as kvq_prefill_attention). */
+KVQ_API kvq_status kvq_prefill_attention_ex(const void* q, const void* k, const void* v,
+                                            int32_t B, int32_t Hq, int32_t Hkv, int32_t S, int32_t D,
+                                            const int32_t* seq_lens, int32_t causal, float softmax_scale,
+                                            const uint8_t* tile_mask, int32_t tile,
+                                            const kvq_cache* k_cache, const kvq_cache* v_cache,
+                                            void* out, int32_t out_dtype, const kvq_policy* policy,
+                                            int32_t* dev_status, void* stream);
 
 /* Static, human-readable name of a status code. */
 KVQ_API const char* kvq_status_str(kvq_status status);

@@ -106,9 +106,10 @@ def test_prefill_validation_without_launch(L):
     assert L.kvq_prefill_attention(a, a, a, 1, 4, 2, 200, 128, 1, 0.0, None, 128, P(k), P(v), a, 0, None, None) == 2
     assert L.kvq_prefill_attention(a, a, a, 1, 4, 2, 512, 128, 1, 0.0, None, 128, P(k), P(v), a, 0, None, None) == 1
     assert L.kvq_prefill_attention(a, a, a, 1, 3, 2, 256, 128, 1, 0.0, None, 128, P(k), P(v), a, 0, None, None) == 1
-    k4, _ = _cache([8, 4], Tcap=256)
-    v4, _ = _cache([8, 4], Tcap=256)
-    assert L.kvq_prefill_attention(a, a, a, 1, 4, 2, 256, 128, 1, 0.0, None, 128, P(k4), P(v4), a, 0, None, None) == 2
+    # head dims other than 64 and 128 are refused (4-bit and mixed per-head caches are accepted)
+    k96, _ = _cache([8, 4], Tcap=256, D=96)
+    assert L.kvq_prefill_attention(a, a, a, 1, 4, 2, 256, 96, 1, 0.0, None, 128, P(k96), P(k96), a, 0, None,
+                                   None) == 2
 
 
 def test_prefill_varlen_validation_without_launch(L):
@@ -181,3 +182,28 @@ def test_decode_step_host_validation_without_launch(L):
     assert call(st, need - 1) == 1                            # staging too small
     assert call(st + 16, need) == 1                           # staging not 256-byte aligned
     assert call(st, need, dt=3) == 1
+
+
+def test_policy_defaults_and_validation_without_launch(L):
+    """kvq_policy_default fills the values the plain calls use; an
+    out-of-range field is refused before any device work."""
+    p = kvq.CPolicy()
+    L.kvq_policy_default(ctypes.byref(p))
+    assert (p.decode_ring_tiles, p.decode_l2_warm_tiles, p.decode_l2_ahead_tiles, p.wait_limit_us,
+            p.test_issue_limit) == (4, 5, 0, 2_000_000, -1)
+    c, hb = _cache([8], B=1, Tcap=64)
+    c128, hb128 = _cache([8], B=1, Tcap=128)
+    P = ctypes.byref
+    bad = [("decode_ring_tiles", 1), ("decode_ring_tiles", 3), ("decode_ring_tiles", 5), ("decode_l2_warm_tiles", -1),
+           ("decode_l2_warm_tiles", 17), ("decode_l2_ahead_tiles", 17), ("wait_limit_us", 0),
+           ("wait_limit_us", 60_000_001)]
+    for field, val in bad:
+        q = kvq.CPolicy()
+        L.kvq_policy_default(ctypes.byref(q))
+        setattr(q, field, val)
+        st = L.kvq_decode_attention_ex(0x3000, P(c), P(c), 0x4000, 4, 0.0, 0x5000, 0, 0x6000, 1 << 20, P(q),
+                                       None, None)
+        assert st == 1, (field, val)
+        st = L.kvq_prefill_attention_ex(0x3000, 0x3000, 0x3000, 1, 4, 1, 128, 128, None, 1, 0.0, None, 128,
+                                        P(c128), P(c128), 0x5000, 0, P(q), None, None)
+        assert st == 1, (field, val)
