@@ -93,12 +93,10 @@ static bool resolve_policy(const kvq_policy* in, Policy* out) {
   // tiles, and with an even depth every slot's fills all go to one of them,
   // which then waits on each of that slot's phases in turn
   if ((in->decode_ring_tiles != 2 && in->decode_ring_tiles != 4) || in->decode_l2_warm_tiles < 0 ||
-      in->decode_l2_warm_tiles > 16 || in->decode_l2_ahead_tiles < 0 || in->decode_l2_ahead_tiles > 16 ||
-      in->wait_limit_us < 1 || in->wait_limit_us > 60000000u)
+      in->decode_l2_warm_tiles > 16 || in->wait_limit_us < 1 || in->wait_limit_us > 60000000u)
     return false;
   out->ring = in->decode_ring_tiles;
   out->l2_warm = in->decode_l2_warm_tiles;
-  out->l2_ahead = in->decode_l2_ahead_tiles;
   out->wait_ns = static_cast<uint64_t>(in->wait_limit_us) * 1000u;
   out->issue_limit = in->test_issue_limit < 0 ? -1 : in->test_issue_limit;
   return true;
@@ -132,7 +130,6 @@ void kvq_policy_default(kvq_policy* policy) {
   const Policy d{};
   policy->decode_ring_tiles = d.ring;
   policy->decode_l2_warm_tiles = d.l2_warm;
-  policy->decode_l2_ahead_tiles = d.l2_ahead;
   policy->wait_limit_us = static_cast<uint32_t>(d.wait_ns / 1000u);
   policy->test_issue_limit = d.issue_limit;
 }

@@ -85,7 +85,7 @@ static_assert(kWarps * (kConsumerRegs + kHelperRegs) == 2 * kWarps * 128, "regis
 // ring slots in shared memory; a call may keep fewer tiles in flight (its policy)
 constexpr int kStages = KVQ_DECODE_STAGES;
 constexpr int kMaxRep = 8;      // query heads per KV head
-constexpr int kMaxL2Tiles = 16; // most tiles per CTA a policy may prefetch into L2 (warm-up or look-ahead)
+constexpr int kMaxL2Tiles = 16; // most tiles per CTA a policy may warm into L2
 
 struct DParams {
   CUtensorMap tm_k8, tm_k4, tm_v8, tm_v4;
@@ -106,24 +106,25 @@ struct DParams {
   const int32_t* bt;
   int32_t bt_stride, pB, pT;
   float scale_log2;
-  // per-call policy: tiles kept in flight into shared memory (2 or kStages:
-  // an even depth, so that each ring slot is only ever filled with even or
-  // only with odd tiles and one table warp waits on all of its phases),
-  // tiles per CTA prefetched into L2 before the dependency wait and ahead of
-  // the ring while streaming (0 .. kMaxL2Tiles), the bounded-wait limit, and
-  // the test-only issue limit (tiles the copy issuer streams before it stops;
-  // negative = no limit)
-  int32_t ring, l2_warm, l2_ahead, issue_limit;
+  // per-call policy: tiles per CTA prefetched into L2 before the dependency
+  // wait (0 .. kMaxL2Tiles), the bounded-wait limit, and the test-only issue
+  // limit (tiles the copy issuer streams before it stops; negative = no
+  // limit).  The ring depth (tiles kept in flight into shared memory) is the
+  // kernel's template parameter RING.
+  int32_t l2_warm, issue_limit;
   uint64_t wait_ns;
   int32_t plane[KVQ_MAX_HKV];
   int8_t bits[KVQ_MAX_HKV];
 };
 
-// Ring slot and phase parity of the k-th tile of a CTA's range in a ring of R slots.
-__device__ __forceinline__ void ring_pos(int k, int R, int& slot, uint32_t& parity) {
-  const int q = k / R;
-  slot = k - q * R;
-  parity = static_cast<uint32_t>(q & 1);
+// Ring slot and phase parity of the k-th tile of a CTA's range in a ring of
+// RING slots.  RING is 2 or 4: even, so each slot is only ever filled with
+// even or only with odd tiles and one table warp waits on all of its phases.
+template <int RING>
+__device__ __forceinline__ void ring_pos(int k, int& slot, uint32_t& parity) {
+  static_assert(RING == 2 || RING == 4, "ring depth 2 or 4");
+  slot = k % RING;
+  parity = static_cast<uint32_t>((k / RING) & 1);
 }
 
 // Hand-off buffer from the consumer warps to the epilogue warp at a piece end.
@@ -656,8 +657,9 @@ __device__ __forceinline__ void warm_l2(const DParams& p, int lane) {
 }
 
 // PAGED: the tiles are pages of a pool found through p.bt (a separate
-// instantiation, so the contiguous kernel carries none of it)
-template <int D, bool PAGED>
+// instantiation, so the contiguous kernel carries none of it).  RING: tiles
+// kept in flight into shared memory (the policy's ring depth, 2 or kStages).
+template <int D, bool PAGED, int RING>
 __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_kernel(const __grid_constant__ DParams p) {
   using L = Smem<D>;
   constexpr int G = D / 32;
@@ -748,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
   if (w >= kWarps) {
     tc::reg_dealloc<kHelperRegs>();
     if (w == kWarps) {
-      // ---------------- TMA issuer warp: lane 0 keeps p.ring tiles in flight ----------------
+      // ---------------- TMA issuer warp: lane 0 keeps RING tiles in flight ----------------
       if (lane != 0) return;
       const uint64_t pol = l2_evict_first_policy();   // the cache is streamed once per call
       Cursor pc = locate(f0, pre, B, Hkv);
@@ -764,37 +766,14 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
           advance(pa, pre, B, Hkv);
         }
       }
-      // L2 look-ahead (policy): tiles k + 1 .. k + l2_ahead are requested
-      // into L2 before the ring has room for them, so more of the cache is on
-      // its way from HBM than the shared-memory ring holds
-      const int ahead = p.l2_ahead;
-      Cursor pf = pc;
-      int n_pf = 0;   // tiles of the range prefetched so far (tile 0 is copied at once)
-      auto prefetch_next = [&]() {
-        if (n_pf == 0) { advance(pf, pre, B, Hkv); n_pf = 1; }
-        if (n_pf >= ntiles) return;
-        const int bits_f = p.bits[pf.kvh];
-        int fb = pf.b, ft = pf.i * kTile;
-        if constexpr (PAGED) {   // a bad page id only misdirects this prefetch
-          fb = min(max(p.bt[static_cast<int64_t>(pf.b) * p.bt_stride + pf.i], 0), p.pB - 1);
-          ft = 0;
-        }
-        const int32_t frow = (p.plane[pf.kvh] * p.pB + fb) * p.pT + ft;
-        const int64_t fsz = (static_cast<int64_t>(pf.kvh) * p.pB + fb) * p.pT + ft;
-        prefetch_l2_tile_2d(bits_f == 8 ? &p.tm_k8 : &p.tm_k4, 0, frow);
-        prefetch_l2_tile_2d(bits_f == 8 ? &p.tm_v8 : &p.tm_v4, 0, frow);
-        prefetch_l2_bulk(p.k_sz + fsz * G, L::kSzBytes);
-        prefetch_l2_bulk(p.v_sz + fsz * G, L::kSzBytes);
-        advance(pf, pre, B, Hkv);
-        ++n_pf;
-      };
-      const int R = p.ring;
-      for (int k = 0; k < ntiles; ++k) {
-        if (p.issue_limit >= 0 && k >= p.issue_limit) return;   // test-only: stop streaming here
+      // test-only: the policy's issue limit stops streaming early (a bound
+      // on the loop, so the per-tile code is the same either way)
+      const int n_issue = p.issue_limit >= 0 && p.issue_limit < ntiles ? p.issue_limit : ntiles;
+      for (int k = 0; k < n_issue; ++k) {
         int slot;
         uint32_t par;
-        ring_pos(k, R, slot, par);
-        if (k >= R && !mbar_wait(&empty[slot], par ^ 1u, p.status, p.wait_ns)) return;
+        ring_pos<RING>(k, slot, par);
+        if (k >= RING && !mbar_wait(&empty[slot], par ^ 1u, p.status, p.wait_ns)) return;
         uint8_t* st = smem + slot * L::kStageBytes;
         const int bits = p.bits[pc.kvh];
         const int Rb = D * bits / 8;
@@ -827,8 +806,6 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
         bulk_g2s_hint(st + L::kOffKsz, p.k_sz + szoff * G, L::kSzBytes, bar, pol);
         bulk_g2s_hint(st + L::kOffVsz, p.v_sz + szoff * G, L::kSzBytes, bar, pol);
         advance(pc, pre, B, Hkv);
-        // keep the look-ahead l2_ahead tiles past the newest copy
-        while (ahead > 0 && n_pf < ntiles && n_pf <= k + ahead) prefetch_next();
       }
       return;
     }
@@ -841,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
       for (int kk = par; kk < ntiles; kk += 2) {
         int slot;
         uint32_t parity;
-        ring_pos(kk, p.ring, slot, parity);
+        ring_pos<RING>(kk, slot, parity);
         const bool okw = mbar_wait(&full[slot], parity, p.status, p.wait_ns);
         if (!__all_sync(0xffffffffu, okw)) return;
         uint8_t* st = smem + slot * L::kStageBytes;
@@ -925,11 +902,10 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
   int n_end = 0;
   uint32_t gphase = 0;
 
-  const int R = p.ring;
   for (int k = 0; k < ntiles;) {
     int slot, slot1 = 0;
     uint32_t parity;
-    ring_pos(k, R, slot, parity);
+    ring_pos<RING>(k, slot, parity);
     ok = ok && mbar_wait(&ready[slot], parity, p.status, p.wait_ns);
     if (!ok) break;   // a timed-out wait ends this warp (status already set)
     const uint8_t* st0 = smem + slot * L::kStageBytes;
@@ -957,7 +933,7 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
     if (!(meta.z & kFlagEnd)) {
       // the next tile belongs to the same piece: take both in one step
       uint32_t parity1;
-      ring_pos(k + 1, R, slot1, parity1);
+      ring_pos<RING>(k + 1, slot1, parity1);
       ok = ok && mbar_wait(&ready[slot1], parity1, p.status, p.wait_ns);
       if (!ok) break;
       const uint8_t* st1 = smem + slot1 * L::kStageBytes;
@@ -1042,6 +1018,9 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
   }
 }
 
+// CTAs per SM of the decode kernel on the current device (the same for both
+// ring depths: their resources are the same); sets the shared-memory limit
+// of both instantiations once per device.
 template <int D, bool PAGED>
 int ctas_per_sm() {
   static int cached[64] = {0};
@@ -1050,9 +1029,11 @@ int ctas_per_sm() {
   if (cached[dev] == 0) {
     int n = 0;
     const size_t sm = Smem<D>::bytes(64);
-    cudaFuncSetAttribute(decode_split_kernel<D, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(Smem<D>::bytes(4096)));
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<D, PAGED>, kThreads, sm) != cudaSuccess ||
+    const int lim = static_cast<int>(Smem<D>::bytes(4096));
+    cudaFuncSetAttribute(decode_split_kernel<D, PAGED, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    cudaFuncSetAttribute(decode_split_kernel<D, PAGED, kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_split_kernel<D, PAGED, kStages>, kThreads, sm) !=
+            cudaSuccess ||
         n < 1)
       n = 1;
     cached[dev] = n;
@@ -1066,8 +1047,11 @@ template <int D, bool PAGED>
 bool regs_ok() {
   static int cached = -1;
   if (cached < 0) {
-    cudaFuncAttributes fa;
-    cached = (cudaFuncGetAttributes(&fa, decode_split_kernel<D, PAGED>) == cudaSuccess && fa.numRegs == 128) ? 1 : 0;
+    cudaFuncAttributes fa, fb;
+    cached = (cudaFuncGetAttributes(&fa, decode_split_kernel<D, PAGED, 2>) == cudaSuccess && fa.numRegs == 128 &&
+              cudaFuncGetAttributes(&fb, decode_split_kernel<D, PAGED, kStages>) == cudaSuccess && fb.numRegs == 128)
+                 ? 1
+                 : 0;
   }
   return cached == 1;
 }
@@ -1076,7 +1060,7 @@ bool regs_ok() {
 // scheduled while the previous kernel of the stream drains; the kernel waits
 // for it (griddepcontrol.wait) before its first global memory access.
 template <int D, bool PAGED>
-cudaError_t launch_split(const DParams& p, int C, int B, cudaStream_t stream) {
+cudaError_t launch_split(const DParams& p, int C, int B, int ring, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(C));
   cfg.blockDim = dim3(kThreads);
@@ -1087,7 +1071,8 @@ cudaError_t launch_split(const DParams& p, int C, int B, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_split_kernel<D, PAGED>, p);
+  return ring == 2 ? cudaLaunchKernelEx(&cfg, decode_split_kernel<D, PAGED, 2>, p)
+                   : cudaLaunchKernelEx(&cfg, decode_split_kernel<D, PAGED, kStages>, p);
 }
 
 }  // namespace
@@ -1168,17 +1153,16 @@ kvq_status launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     p.plane[h] = hl.plane_idx[h];
     p.bits[h] = hl.bits[h];
   }
-  p.ring = a.pol.ring;
+  const int ring = a.pol.ring;
   p.l2_warm = a.pol.l2_warm;
-  p.l2_ahead = a.pol.l2_ahead;
   p.issue_limit = a.pol.issue_limit;
   p.wait_ns = a.pol.wait_ns;
-  if ((p.ring != 2 && p.ring != kStages) || p.l2_warm < 0 || p.l2_warm > kMaxL2Tiles || p.l2_ahead < 0 ||
-      p.l2_ahead > kMaxL2Tiles || p.wait_ns == 0)
+  if ((ring != 2 && ring != kStages) || p.l2_warm < 0 || p.l2_warm > kMaxL2Tiles || p.wait_ns == 0)
     return KVQ_ERR_INVALID_ARG;
   if (paged) (void)(D == 128 ? ctas_per_sm<128, true>() : ctas_per_sm<64, true>());   // sets its smem limit
-  const cudaError_t e = D == 128 ? (paged ? launch_split<128, true>(p, C, B, stream) : launch_split<128, false>(p, C, B, stream))
-                                 : (paged ? launch_split<64, true>(p, C, B, stream) : launch_split<64, false>(p, C, B, stream));
+  const cudaError_t e =
+      D == 128 ? (paged ? launch_split<128, true>(p, C, B, ring, stream) : launch_split<128, false>(p, C, B, ring, stream))
+               : (paged ? launch_split<64, true>(p, C, B, ring, stream) : launch_split<64, false>(p, C, B, ring, stream));
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

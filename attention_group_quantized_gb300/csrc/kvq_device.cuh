@@ -61,8 +61,25 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// A translation unit may set KVQ_TRYWAIT_HINT_NS (before including this
+// header) to let a waiting thread sleep up to that long inside try_wait
+// instead of the hardware's default, so fewer poll iterations are issued; the
+// thread still resumes when the phase completes.
+#ifndef KVQ_TRYWAIT_HINT_NS
+#define KVQ_TRYWAIT_HINT_NS 0
+#endif
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
   uint32_t ok;
+#if KVQ_TRYWAIT_HINT_NS > 0
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(phase), "n"(KVQ_TRYWAIT_HINT_NS)
+      : "memory");
+#else
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -70,6 +87,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(phase)
       : "memory");
+#endif
   return ok != 0;
 }
 

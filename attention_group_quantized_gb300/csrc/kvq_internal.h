@@ -25,7 +25,6 @@ bool resolve_layout(const kvq_cache& c, HeadLayout* out);
 struct Policy {
   int32_t ring = 4;               // decode: tiles in flight into shared memory (2 .. 4)
   int32_t l2_warm = 5;            // decode: tiles per CTA prefetched into L2 before the dependency wait
-  int32_t l2_ahead = 0;           // decode: tiles prefetched into L2 ahead of the ring while streaming
   uint64_t wait_ns = 2000000000ull;   // every bounded wait
   int32_t issue_limit = -1;       // test only: tiles (decode) / Q loads (prefill) issued before stopping
 };

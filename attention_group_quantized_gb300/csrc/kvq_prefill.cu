@@ -15,20 +15,19 @@
 // One CTA (512 threads, one per SM) computes one 128-row query tile for two
 // query heads that share a KV head, so every dequantised K/V tile feeds two
 // heads' products:
-//   warp 0      allocates TMEM, loads the bf16 Q tiles by TMA, then streams
-//               the K and V code tiles of the kept key tiles by bulk copies
-//               into a ring of 2 KB slots in shared memory (about two tile
-//               parts ahead of the dequant warpgroup), and frees TMEM last;
+//   warp 0      allocates TMEM, loads the bf16 Q tiles by TMA, and frees TMEM
+//               once every other role is done;
 //   warp 1      one thread issues every tcgen05.mma:
 //                 S_h = Q_h K^T (A, B from shared memory) and
 //                 O_h += P_h V   (P from TMEM, V from shared memory);
-//   warps 4-7   convert Q to fp16 in place, then per kept key tile read the
-//               codes from the ring (the fp16 scale/zero words by global
-//               loads a tile ahead) and write exact-rounded fp16
+//   warps 4-7   convert Q to fp16 in place, then per kept key tile load the
+//               codes and fp16 scale/zero words into registers one tile part
+//               (K or V) ahead of their use and write exact-rounded fp16
 //               K_hat = (c - z) * s and V_hat tiles in the 128-byte-swizzled
 //               layout the tensor core reads (2 stages); which row and chunk
-//               each lane takes is chosen per code format so that every
-//               8-lane phase of a 16-byte load or store covers all 32 banks;
+//               each lane takes is chosen per code format so that a warp's
+//               loads cover whole contiguous rows and every 8-lane phase of a
+//               16-byte store covers all 32 banks;
 //   warps 8-11  softmax of head 0, warps 12-15 softmax of head 1: one thread
 //               per query row reads its S row from TMEM, applies the causal
 //               rule on the diagonal tile (causal only), updates (max, sum) in
@@ -57,8 +56,7 @@ constexpr int kT = 128;           // tile edge (query rows, keys)
 constexpr int kThreads = 512;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kSub = 2048;        // bytes of one code sub-chunk: 128 dequant threads x 16 B
-constexpr int kRing = 16;         // sub-chunk slots in the code ring (32 KB)
+constexpr int kSub = 2048;        // code bytes one dequant iteration reads: 128 threads x 16 B
 
 struct PParams {
   CUtensorMap tm_q;               // bf16 [B*Hq*S][D], box [64][128], 128B swizzle
@@ -83,10 +81,7 @@ struct PParams {
 // barriers
 enum {
   B_QFULL = 0, B_QREADY, B_KFULL0, B_KFULL1, B_VFULL0, B_VFULL1, B_KVEMPTY0, B_KVEMPTY1,
-  B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_ORDY0, B_ORDY1, B_MMADONE, B_EXIT,
-  B_RFULL,                        // kRing barriers: a code slot has landed
-  B_REMPTY = B_RFULL + kRing,     // kRing barriers: the four dequant warps have read a slot
-  B_COUNT = B_REMPTY + kRing
+  B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_ORDY0, B_ORDY1, B_MMADONE, B_EXIT, B_COUNT
 };
 // Every warp but warp 0 arrives once on B_EXIT when it is done with shared
 // memory, TMEM and its asynchronous operations, on the normal path and after
@@ -100,40 +95,39 @@ struct PLayout {
   static constexpr int kOffQ = 0;                       // 2 heads
   static constexpr int kOffK = kOffQ + 2 * kQBytes;     // 2 stages
   static constexpr int kOffV = kOffK + 2 * kQBytes;     // 2 stages
-  static constexpr int kOffRing = kOffV + 2 * kQBytes;  // kRing slots of kSub bytes
-  static constexpr int kOffBar = kOffRing + kRing * kSub;
+  static constexpr int kOffBar = kOffV + 2 * kQBytes;
   static constexpr int kOffTmem = kOffBar + B_COUNT * 8;
   static constexpr int kBytes = kOffTmem + 16 + 1024;
 };
 static_assert(PLayout<128>::kBytes <= 232448, "shared memory of the D = 128 prefill");
 
 // How the dequant warpgroup walks one code tile (the K or V part of a key
-// tile) of a (D, BITS) head.  Iteration `it` reads one 2 KB sub-chunk of the
-// ring (RPI token rows of R bytes), 16 bytes per thread; a 16-byte chunk
-// holds VPC channels (16 or 32) and becomes two or four 16-byte fp16 chunks
-// of the swizzled operand tile.
+// tile) of a (D, BITS) head.  Iteration `it` covers RPI token rows of R
+// bytes (2 KB), 16 bytes per thread; a 16-byte chunk holds VPC channels (16
+// or 32) and becomes two or four 16-byte fp16 chunks of the swizzled operand
+// tile.
 template <int D, int BITS>
 struct DqFmt {
   static constexpr int R = D * BITS / 8;     // code bytes per token row
   static constexpr int RPI = kSub / R;       // rows per iteration
   static constexpr int NI = kT / RPI;        // iterations (ring sub-chunks) per part
   static constexpr int VPC = 128 / BITS;     // channels per chunk
-  static_assert(RPI * NI == kT, "whole sub-chunks per part");
+  static_assert(RPI * NI == kT, "whole iterations per part");
 };
 
-// Row (within an iteration) and chunk of the 16 bytes thread t reads.  With
-// the 128-byte swizzle, chunk x of fp16 row r sits at bank group x ^ (r & 7),
-// and the D/64 blocks of a tile are 16 KB apart (the same banks).  Per
-// format, the eight lanes of each phase take:
-//   8-bit, D 128: one half (64 B) of row r and the other half of row r + 1:
-//                 the reads cover 128 distinct bytes of banks, and the stores
-//                 (two chunks per lane) go to even chunk indices in one row
-//                 and odd ones in the other;
-//   4-bit, D 128: rows r .. r+3 (r a multiple of 4), the first 32 bytes of rows
-//                 r, r+3 and the last 32 of rows r+1, r+2 (or the other way
-//                 round): again 128 distinct bytes of banks, and each store
-//                 phase writes the four swizzle rows of a quad, once in the
-//                 low and once in the high half of the chunk index;
+// Row (within an iteration) and chunk of the 16 code bytes thread t loads.
+// A warp's 32 lanes cover whole consecutive rows (512 contiguous bytes).
+// With the 128-byte swizzle, fp16 chunk x of row r sits at bank group
+// x ^ (r & 7), and the D/64 blocks of a tile are 16 KB apart (the same
+// banks).  Per format, the eight lanes of each store phase take:
+//   8-bit, D 128: one half (64 B) of row r and the other half of row r + 1,
+//                 so the stores (two chunks per lane) go to even chunk
+//                 indices in one row and odd ones in the other;
+//   4-bit, D 128: rows r .. r+3 (r a multiple of 4), the first 32 bytes of
+//                 rows r, r+3 and the last 32 of rows r+1, r+2 (or the other
+//                 way round): each store phase writes the four swizzle rows
+//                 of a quad, once in the low and once in the high half of the
+//                 chunk index;
 //   D 64:         two (8-bit) or four (4-bit) whole consecutive rows.
 template <int D, int BITS>
 __device__ __forceinline__ void dq_lane(int t, int& row, int& c) {
@@ -196,12 +190,7 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
-// 16 bytes of shared memory at a shared-window address
-__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr));
-  return v;
-}
+// 16 bytes to a shared-window address
 __device__ __forceinline__ void sts128(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -236,41 +225,38 @@ __device__ __forceinline__ void dequant_chunk(uint32_t dst, int row, int ch0, ui
   for (int i = 0; i < OC; ++i) sts128(rowp + (((cb + i) ^ sw) << 4), o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
 }
 
-// Scale/zero words a thread needs for one part of key tile kt: one per iteration.
+// One part (K or V) of a key tile in a dequant thread's registers: its code
+// chunk and scale/zero word of every iteration.
 template <int D, int BITS>
-__device__ __forceinline__ void load_part_words(uint32_t (&w)[DqFmt<D, BITS>::NI], const uint32_t* sz, int kt, int row,
-                                                int g) {
+struct PartRegs {
+  uint4 c[DqFmt<D, BITS>::NI];
+  uint32_t w[DqFmt<D, BITS>::NI];
+};
+
+template <int D, int BITS>
+__device__ __forceinline__ void load_part(PartRegs<D, BITS>& r, const uint8_t* codes, const uint32_t* sz, int kt,
+                                          int row, int c, int g) {
   using F = DqFmt<D, BITS>;
   constexpr int G = D / 32;
 #pragma unroll
-  for (int it = 0; it < F::NI; ++it) w[it] = __ldg(sz + static_cast<size_t>(kt * kT + F::RPI * it + row) * G + g);
+  for (int it = 0; it < F::NI; ++it) {
+    const size_t tok = static_cast<size_t>(kt) * kT + F::RPI * it + row;
+    r.c[it] = __ldg(reinterpret_cast<const uint4*>(codes + tok * F::R + c * 16));
+    r.w[it] = __ldg(sz + tok * G + g);
+  }
 }
 
-// Dequantise one part (K or V) of a key tile from the code ring into an fp16
-// operand tile.  `seq` counts ring sub-chunks in the producer's order.
-// Returns false (warp-uniformly) if a ring wait ran out.
 template <int D, int BITS>
-__device__ __forceinline__ bool dequant_part(uint32_t dst, uint32_t ring, uint64_t* bar, int& seq,
-                                             const uint32_t (&words)[DqFmt<D, BITS>::NI], int row, int c, int lane,
-                                             const PParams& p) {
+__device__ __forceinline__ void store_part(uint32_t dst, const PartRegs<D, BITS>& r, int row, int c) {
   using F = DqFmt<D, BITS>;
-  const uint32_t roff = static_cast<uint32_t>(row * F::R + c * 16);
 #pragma unroll
-  for (int it = 0; it < F::NI; ++it) {
-    const int q = seq % kRing;
-    const uint32_t par = static_cast<uint32_t>((seq / kRing) & 1);
-    if (!__all_sync(0xffffffffu, mbar_wait(&bar[B_RFULL + q], par, p.status, p.wait_ns))) return false;
-    const uint4 w = lds128(ring + q * kSub + roff);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bar[B_REMPTY + q]);   // this warp's reads of the slot are done
-    dequant_chunk<BITS>(dst, F::RPI * it + row, c * F::VPC, w, words[it]);
-    ++seq;
-  }
-  return true;
+  for (int it = 0; it < F::NI; ++it) dequant_chunk<BITS>(dst, F::RPI * it + row, c * F::VPC, r.c[it], r.w[it]);
 }
 
 // Dequant warpgroup after Q: every kept key tile's K and V parts into the
-// two-stage fp16 operand tiles.
+// two-stage fp16 operand tiles.  Two register sets: while one part is
+// converted, the next part's codes are on their way from L2 / HBM.  Returns
+// early (warp-uniformly) if a wait runs out.
 template <int D, int BITS>
 __device__ __forceinline__ void dequant_loop(const PParams& p, uint8_t* smem, uint64_t* bar, int b, int kvh, int qt,
                                              int kt_end, int t, int lane) {
@@ -279,71 +265,34 @@ __device__ __forceinline__ void dequant_loop(const PParams& p, uint8_t* smem, ui
   int row, c;
   dq_lane<D, BITS>(t, row, c);
   const int g = c * F::VPC / 32;
+  const size_t base_tok = static_cast<size_t>(b) * p.Tcap;
+  const uint8_t* kcodes = p.kcodes + p.plane_off[kvh] + base_tok * F::R;
+  const uint8_t* vcodes = p.vcodes + p.plane_off[kvh] + base_tok * F::R;
   const size_t szrow = (static_cast<size_t>(kvh) * p.B + b) * p.Tcap;
   const uint32_t* ksz = p.ksz + szrow * (D / 32);
   const uint32_t* vsz = p.vsz + szrow * (D / 32);
-  const uint32_t ring = smem_u32(smem + L::kOffRing);
   const uint32_t kdst = smem_u32(smem + L::kOffK);
   const uint32_t vdst = smem_u32(smem + L::kOffV);
-  // scale/zero words one key tile ahead: `cur` for this tile, `nxt` in flight
-  uint32_t kcur[F::NI], vcur[F::NI], knxt[F::NI], vnxt[F::NI];
+  PartRegs<D, BITS> ra, rb;
   int kt = next_kept(p, qt, 0, kt_end);
-  if (kt < kt_end) {
-    load_part_words<D, BITS>(knxt, ksz, kt, row, g);
-    load_part_words<D, BITS>(vnxt, vsz, kt, row, g);
-  }
-  int seq = 0;
+  if (kt < kt_end) load_part<D, BITS>(ra, kcodes, ksz, kt, row, c, g);
   for (int j = 0; kt < kt_end; ++j) {
     const int st = j & 1;
-#pragma unroll
-    for (int it = 0; it < F::NI; ++it) {
-      kcur[it] = knxt[it];
-      vcur[it] = vnxt[it];
-    }
     const int kt_next = next_kept(p, qt, kt + 1, kt_end);
-    if (kt_next < kt_end) {
-      load_part_words<D, BITS>(knxt, ksz, kt_next, row, g);
-      load_part_words<D, BITS>(vnxt, vsz, kt_next, row, g);
-    }
+    load_part<D, BITS>(rb, vcodes, vsz, kt, row, c, g);
     if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bar[B_KVEMPTY0 + st], ((j >> 1) - 1) & 1, p.status, p.wait_ns)))
       return;
-    if (!dequant_part<D, BITS>(kdst + st * L::kQBytes, ring, bar, seq, kcur, row, c, lane, p)) return;
+    store_part<D, BITS>(kdst + st * L::kQBytes, ra, row, c);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar[B_KFULL0 + st]);
-    if (!dequant_part<D, BITS>(vdst + st * L::kQBytes, ring, bar, seq, vcur, row, c, lane, p)) return;
+    if (kt_next < kt_end) load_part<D, BITS>(ra, kcodes, ksz, kt_next, row, c, g);
+    store_part<D, BITS>(vdst + st * L::kQBytes, rb, row, c);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar[B_VFULL0 + st]);
     kt = kt_next;
   }
-}
-
-// Warp 0's producer loop (one thread): the K and V code parts of every kept
-// key tile, in 2 KB sub-chunks, into the ring.  Returns the number of
-// sub-chunks issued (it stops early if a wait for a free slot runs out).
-template <int D>
-__device__ __forceinline__ int stream_codes(const PParams& p, uint8_t* smem, uint64_t* bar, const uint8_t* kplane,
-                                            const uint8_t* vplane, int R, int qt, int kt_end) {
-  using L = PLayout<D>;
-  const int part_bytes = kT * R;
-  const int nsub = part_bytes / kSub;
-  int seq = 0;
-  for (int kt = next_kept(p, qt, 0, kt_end); kt < kt_end; kt = next_kept(p, qt, kt + 1, kt_end)) {
-    for (int part = 0; part < 2; ++part) {
-      const uint8_t* src = (part ? vplane : kplane) + static_cast<size_t>(kt) * part_bytes;
-      for (int s = 0; s < nsub; ++s) {
-        const int q = seq % kRing;
-        const int round = seq / kRing;
-        if (round > 0 && !mbar_wait(&bar[B_REMPTY + q], static_cast<uint32_t>((round - 1) & 1), p.status, p.wait_ns))
-          return seq;
-        mbar_arrive_expect_tx(&bar[B_RFULL + q], kSub);
-        bulk_g2s(smem + L::kOffRing + q * kSub, src + s * kSub, kSub, &bar[B_RFULL + q]);
-        ++seq;
-      }
-    }
-  }
-  return seq;
 }
 
 // Zeros in the output rows of this work item (a query tile past its sequence's end).
@@ -426,10 +375,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     mbar_init(&bar[B_ORDY0], 1); mbar_init(&bar[B_ORDY1], 1);
     mbar_init(&bar[B_MMADONE], 1);
     mbar_init(&bar[B_EXIT], kExitArrivals);
-    for (int s = 0; s < kRing; ++s) {
-      mbar_init(&bar[B_RFULL + s], 1);
-      mbar_init(&bar[B_REMPTY + s], 4);
-    }
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -457,9 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
   if (warp < 4) {
   tc::reg_dealloc<80>();
   if (warp == 0) {
-    // ---------------- Q by TMA, the code stream, then free TMEM once every role is done ----------------
+    // ---------------- Q by TMA, then free TMEM once every role is done ----------------
     const bool issue = p.issue_limit != 0;
-    int issued = 0;
     if (lane == 0 && issue) {
       mbar_arrive_expect_tx(&bar[B_QFULL], nh * L::kQBytes);
       for (int h = 0; h < nh; ++h) {
@@ -468,16 +412,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         for (int kb = 0; kb < D / 64; ++kb)
           tma_2d_g2s(smem + L::kOffQ + h * L::kQBytes + kb * (kT * 128), &p.tm_q, 64 * kb, y, &bar[B_QFULL]);
       }
-      const int R = D * p.bits[kvh] / 8;
-      const size_t row0 = static_cast<size_t>(b) * p.Tcap * R;
-      issued = stream_codes<D>(p, smem, bar, p.kcodes + p.plane_off[kvh] + row0, p.vcodes + p.plane_off[kvh] + row0,
-                               R, qt, kt_end);
     }
-    issued = __shfl_sync(0xffffffffu, issued, 0);
+    __syncwarp();
     // The other roles finish in bounded time: each stops at its first wait
-    // that runs out, and a role waits at most a few times per kept key tile
-    // and ring sub-chunk.  So the exit wait gets a deadline of that many limits.
-    const uint64_t deadline = wns * static_cast<uint64_t>(4 * n_kept + 2 * issued + 8);
+    // that runs out, and a role waits at most a few times per kept key tile.
+    // So the exit wait gets a deadline of that many limits.
+    const uint64_t deadline = wns * static_cast<uint64_t>(4 * n_kept + 8);
     const uint64_t t0 = global_ns();
     uint32_t n = 0;
     while (!mbar_try_wait(&bar[B_EXIT], 0)) {
@@ -486,13 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         break;
       }
     }
-    // every copy into shared memory has landed before the CTA exits: the
-    // query tiles and the last copy into each ring slot (normally long since)
-    if (lane == 0 && issue) {
-      mbar_wait(&bar[B_QFULL], 0, p.status, wns);
-      for (int s = issued > kRing ? issued - kRing : 0; s < issued; ++s)
-        mbar_wait(&bar[B_RFULL + s % kRing], static_cast<uint32_t>((s / kRing) & 1), p.status, wns);
-    }
+    // the query copy has landed before the CTA can exit (normally long since)
+    if (lane == 0 && issue) mbar_wait(&bar[B_QFULL], 0, p.status, wns);
     __syncwarp();
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);

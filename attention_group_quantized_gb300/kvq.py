@@ -46,8 +46,7 @@ class KvqError(RuntimeError):
 
 class CPolicy(ctypes.Structure):
     _fields_ = [("decode_ring_tiles", ctypes.c_int32), ("decode_l2_warm_tiles", ctypes.c_int32),
-                ("decode_l2_ahead_tiles", ctypes.c_int32), ("wait_limit_us", ctypes.c_uint32),
-                ("test_issue_limit", ctypes.c_int32)]
+                ("wait_limit_us", ctypes.c_uint32), ("test_issue_limit", ctypes.c_int32)]
 
 
 class CCache(ctypes.Structure):
@@ -199,8 +198,7 @@ def decode_workspace(B: int, Hq: int, Hkv: int, D: int, device="cuda"):
 
 def policy(**fields) -> CPolicy:
     """A kvq_policy: the library's defaults with the given fields replaced
-    (decode_ring_tiles, decode_l2_warm_tiles, decode_l2_ahead_tiles,
-    wait_limit_us, test_issue_limit)."""
+    (decode_ring_tiles, decode_l2_warm_tiles, wait_limit_us, test_issue_limit)."""
     p = CPolicy()
     lib().kvq_policy_default(ctypes.byref(p))
     for k, val in fields.items():

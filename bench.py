@@ -471,16 +471,16 @@ def bench_phase_policy(torch, kvq, W, peaks, steps, warmup, dev, decode_policy):
     torch.cuda.empty_cache()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     dinp = W.decode_gqa()
-    base = time_decode(torch, kvq, dinp, dev, l2, steps, warmup)
-    pol = kvq.policy(**decode_policy)
-    wide = time_decode(torch, kvq, dinp, dev, l2, steps, warmup, policy=pol)
-    for label, d in (("decode_default_policy", base), ("decode_phase_policy", wide)):
+    variants = (("decode_ring2", {"decode_ring_tiles": 2}), ("decode_default", {}),
+                ("decode_policy", dict(decode_policy)))
+    for label, fields in variants:
+        d = time_decode(torch, kvq, dinp, dev, l2, steps, warmup, policy=kvq.policy(**fields) if fields else None)
         avg = d["t_total"] / steps
-        res[label] = {"us_per_step": avg * 1e6, "isolated_launch_us": d["isolated_us"],
+        res[label] = {"policy": fields or "defaults (ring 4, L2 warm-up 5)",
+                      "us_per_step": avg * 1e6, "isolated_launch_us": d["isolated_us"],
                       "GB/s": d["bytes"] / avg / 1e9, "frac_of_hbm_peak": d["bytes"] / avg / 1e9 / peaks["hbm_gbs"]}
-    res["decode_phase_policy"]["policy"] = dict(decode_policy)
-    res["decode_speedup_policy_over_default"] = (res["decode_default_policy"]["us_per_step"] /
-                                                 res["decode_phase_policy"]["us_per_step"])
+        del d
+    res["decode_speedup_policy_over_default"] = res["decode_default"]["us_per_step"] / res["decode_policy"]["us_per_step"]
     return res
 
 
@@ -595,8 +595,8 @@ def main():
                     help="run only the per-head bit allocation workload and print its JSON object")
     ap.add_argument("--only-phase-policy", action="store_true",
                     help="run only the phase-policy legs (sparser prefill mask, wider decode prefetch)")
-    ap.add_argument("--decode-policy", default="ring=4,warm=5,ahead=4",
-                    help="decode phase policy of the phase-policy leg: ring tiles, L2 warm-up tiles, L2 look-ahead")
+    ap.add_argument("--decode-policy", default="ring=4,warm=10",
+                    help="decode policy timed beside the defaults in the phase-policy leg: ring tiles, L2 warm-up tiles")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -629,8 +629,7 @@ def main():
         return
     pol_fields = dict(kv.split("=") for kv in args.decode_policy.split(","))
     decode_policy = {"decode_ring_tiles": int(pol_fields.get("ring", 4)),
-                     "decode_l2_warm_tiles": int(pol_fields.get("warm", 5)),
-                     "decode_l2_ahead_tiles": int(pol_fields.get("ahead", 0))}
+                     "decode_l2_warm_tiles": int(pol_fields.get("warm", 5))}
     if args.only_phase_policy:
         if rank == 0:
             print(json.dumps(bench_phase_policy(torch, kvq, W, peaks, args.steps, args.warmup, dev, decode_policy)))

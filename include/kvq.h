@@ -422,8 +422,6 @@ KVQ_API kvq_status kvq_decode_step_paged(const void* q, const void* k_new, const
  *   decode_l2_warm_tiles  tiles per CTA requested into L2 before the decode
  *                         waits for the previous kernel in the stream to
  *                         finish, 0 .. 16 (default 5).
- *   decode_l2_ahead_tiles tiles per CTA requested into L2 ahead of the ring
- *                         while streaming, 0 .. 16 (default 0).
  *   wait_limit_us         every bounded wait inside the decode and prefill
  *                         kernels gives up after this long and reports
  *                         KVQ_ERR_TIMEOUT in dev_status, 1 .. 60,000,000
@@ -441,7 +439,6 @@ KVQ_API kvq_status kvq_decode_step_paged(const void* q, const void* k_new, const
 typedef struct kvq_policy {
   int32_t decode_ring_tiles;
   int32_t decode_l2_warm_tiles;
-  int32_t decode_l2_ahead_tiles;
   uint32_t wait_limit_us;
   int32_t test_issue_limit;
 } kvq_policy;

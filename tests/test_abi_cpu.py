@@ -189,13 +189,12 @@ def test_policy_defaults_and_validation_without_launch(L):
     out-of-range field is refused before any device work."""
     p = kvq.CPolicy()
     L.kvq_policy_default(ctypes.byref(p))
-    assert (p.decode_ring_tiles, p.decode_l2_warm_tiles, p.decode_l2_ahead_tiles, p.wait_limit_us,
-            p.test_issue_limit) == (4, 5, 0, 2_000_000, -1)
+    assert (p.decode_ring_tiles, p.decode_l2_warm_tiles, p.wait_limit_us, p.test_issue_limit) == (4, 5, 2_000_000, -1)
     c, hb = _cache([8], B=1, Tcap=64)
     c128, hb128 = _cache([8], B=1, Tcap=128)
     P = ctypes.byref
     bad = [("decode_ring_tiles", 1), ("decode_ring_tiles", 3), ("decode_ring_tiles", 5), ("decode_l2_warm_tiles", -1),
-           ("decode_l2_warm_tiles", 17), ("decode_l2_ahead_tiles", 17), ("wait_limit_us", 0),
+           ("decode_l2_warm_tiles", 17), ("wait_limit_us", 0),
            ("wait_limit_us", 60_000_001)]
     for field, val in bad:
         q = kvq.CPolicy()

@@ -124,7 +124,10 @@ def test_allocation_prefill_then_decode(kvq):
     quantises into the allocated cache and attends it, and a decode of a new
     query over the same cache: each against the oracle."""
     B, Hq, H, D, S = 2, 16, 8, 128, 512
-    sens = W.make_sensitivity("alloc_prefill", 93, B, H, D, S, [2, 5], lens=[S, S])
+    # outlier channels x4: the allocation still singles out heads 2 and 5, and
+    # the prefill's fp16 K_hat operand (one rounding of (c - z) s) keeps the
+    # score error well inside the tolerance (it grows with |q| |k|)
+    sens = W.make_sensitivity("alloc_prefill", 93, B, H, D, S, [2, 5], outlier_mult=4.0, lens=[S, S])
     ks = kvq.head_error_stats(U.to_dev_bf16(sens.k), 4)
     vs = kvq.head_error_stats(U.to_dev_bf16(sens.v), 4)
     bits, _ = kvq.allocate_head_bits(ks, vs, 2)

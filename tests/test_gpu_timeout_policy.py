@@ -109,9 +109,8 @@ def test_prefill_policy_without_fault_injection_matches_plain_call(kvq):
     assert torch.equal(outs[0], outs[1])
 
 
-POLICIES = [dict(decode_ring_tiles=2), dict(decode_l2_warm_tiles=0),
-            dict(decode_l2_warm_tiles=16), dict(decode_l2_ahead_tiles=1), dict(decode_l2_ahead_tiles=4),
-            dict(decode_l2_ahead_tiles=16, decode_l2_warm_tiles=16), dict(decode_ring_tiles=2, decode_l2_ahead_tiles=8)]
+POLICIES = [dict(decode_ring_tiles=2), dict(decode_l2_warm_tiles=0), dict(decode_l2_warm_tiles=16),
+            dict(decode_ring_tiles=2, decode_l2_warm_tiles=10)]
 
 
 @pytest.fixture(scope="module")
