@@ -180,6 +180,18 @@ __device__ __forceinline__ uint32_t swz(int row, int byte) {
   return row * 32 + ((((byte >> 4) ^ ((row >> 2) & 1)) << 4) | (byte & 15));
 }
 
+// (d0, d1) += (a, a) * (b0, b1) as one two-wide fp32 instruction
+__device__ __forceinline__ void ffma2_b(float& d0, float& d1, float a, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %2};\n\t"
+      "mov.b64 rb, {%3, %4};\n\t"
+      "mov.b64 rd, {%0, %1};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rd;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a), "f"(b0), "f"(b1));
+}
+
 using split::Cursor;
 using split::advance;
 using split::locate;
@@ -307,10 +319,11 @@ __device__ __forceinline__ void qk_tile(float (&S)[4], const uint32_t (&qa)[D / 
                   qa[2 * grp + 1][0], qa[2 * grp + 1][1]);
       }
       const float4 sz = kt[grp * 32];   // tokens g and g + 8
-      acc[0] = fmaf(sz.x, c[0], fmaf(-sz.y, qs[grp][0], acc[0]));
-      acc[1] = fmaf(sz.x, c[1], fmaf(-sz.y, qs[grp][1], acc[1]));
-      acc[2] = fmaf(sz.z, c[2], fmaf(-sz.w, qs[grp][0], acc[2]));
-      acc[3] = fmaf(sz.z, c[3], fmaf(-sz.w, qs[grp][1], acc[3]));
+      // the lane's two heads at once (same rounding as two scalar FMAs)
+      ffma2_b(acc[0], acc[1], -sz.y, qs[grp][0], qs[grp][1]);
+      ffma2_b(acc[0], acc[1], sz.x, c[0], c[1]);
+      ffma2_b(acc[2], acc[3], -sz.w, qs[grp][0], qs[grp][1]);
+      ffma2_b(acc[2], acc[3], sz.z, c[2], c[3]);
     }
   }
 #pragma unroll
