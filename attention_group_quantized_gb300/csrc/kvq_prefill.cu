@@ -17,9 +17,17 @@
 // heads' products:
 //   warp 0      allocates TMEM, loads the bf16 Q tiles by TMA, and frees TMEM
 //               once every other role is done;
-//   warp 1      one thread issues every tcgen05.mma:
+//   warps 1, 2  one thread each issues head h = warp - 1's tcgen05.mma:
 //                 S_h = Q_h K^T (A, B from shared memory) and
 //                 O_h += P_h V   (P from TMEM, V from shared memory);
+//               the heads' products touch disjoint TMEM columns, so each
+//               head's chain (S_h, softmax, P_h V, next S_h) runs on its own
+//               and the two take turns: head 0's block (P_0 V, next S_0),
+//               then head 1's, so that one head's softmax runs while the
+//               other's products occupy the tensor pipe; an issuing thread
+//               stalls at the pipe's rate, and the turn hand-over replaces the
+//               gap a single issuer leaves while it checks the next head's
+//               barriers;
 //   warps 4-7   convert Q to fp16 in place, then per kept key tile load the
 //               codes and fp16 scale/zero words into registers one tile part
 //               (K or V) ahead of their use and write exact-rounded fp16
@@ -81,7 +89,7 @@ struct PParams {
 // barriers
 enum {
   B_QFULL = 0, B_QREADY, B_KFULL0, B_KFULL1, B_VFULL0, B_VFULL1, B_KVEMPTY0, B_KVEMPTY1,
-  B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_ORDY0, B_ORDY1, B_MMADONE, B_EXIT, B_COUNT
+  B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_ORDY0, B_ORDY1, B_MMADONE, B_TURN0, B_TURN1, B_EXIT, B_COUNT
 };
 // Every warp but warp 0 arrives once on B_EXIT when it is done with shared
 // memory, TMEM and its asynchronous operations, on the normal path and after
@@ -369,11 +377,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     mbar_init(&bar[B_QREADY], 4);
     mbar_init(&bar[B_KFULL0], 4); mbar_init(&bar[B_KFULL1], 4);
     mbar_init(&bar[B_VFULL0], 4); mbar_init(&bar[B_VFULL1], 4);
-    mbar_init(&bar[B_KVEMPTY0], 1); mbar_init(&bar[B_KVEMPTY1], 1);
+    mbar_init(&bar[B_KVEMPTY0], nh); mbar_init(&bar[B_KVEMPTY1], nh);
     mbar_init(&bar[B_SFULL0], 1); mbar_init(&bar[B_SFULL1], 1);
     mbar_init(&bar[B_PFULL0], 4); mbar_init(&bar[B_PFULL1], 4);
     mbar_init(&bar[B_ORDY0], 1); mbar_init(&bar[B_ORDY1], 1);
-    mbar_init(&bar[B_MMADONE], 1);
+    mbar_init(&bar[B_MMADONE], nh);
+    mbar_init(&bar[B_TURN0], 1); mbar_init(&bar[B_TURN1], 1);
     mbar_init(&bar[B_EXIT], kExitArrivals);
     fence_barrier_init();
   }
@@ -434,69 +443,105 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     return;
   }
 
-  if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane != 0) return;   // lane 0 arrives on B_EXIT for the warp
-    do {
+  if (warp == 1 || warp == 2) {
+    // ---------------- MMA issuers, one warp per head ----------------
+    // Every lane runs the waits (their outcome is made warp-uniform) and the
+    // descriptor arithmetic; the elected lane -- lane 0, the lowest of a
+    // converged warp -- issues the products, their commits and the turn
+    // hand-overs, so every commit tracks every product of this head.
+    const int h = warp - 1;
+    if (h >= nh) {
+      if (lane == 0) mbar_arrive(&bar[B_EXIT]);
+      return;
+    }
     const uint32_t id_qk = tc::idesc_f16_f32(kT, kT, false);
     const uint32_t id_pv = tc::idesc_f16_f32(kT, D, true);
-    const uint32_t q_base = smem_u32(smem + L::kOffQ);
+    const uint32_t qh = smem_u32(smem + L::kOffQ) + h * L::kQBytes;
     const uint32_t k_base = smem_u32(smem + L::kOffK);
     const uint32_t v_base = smem_u32(smem + L::kOffV);
-    if (!mbar_wait(&bar[B_QREADY], 0, p.status, wns)) break;
-    tc::fence_after_sync();
-    auto issue_qk = [&](int h, int st) {
-      const uint32_t qh = q_base + h * L::kQBytes;
+    const uint32_t d_s = tmem + h * 256, d_o = d_s + 128;
+    auto wait_all = [&](int which, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(&bar[which], parity, p.status, wns));
+    };
+    // S_h = Q_h K^T over the K tile in stage st (elected lane)
+    auto issue_qk = [&](int st) {
       const uint32_t kh = k_base + st * L::kQBytes;
+      tc::mma_ss<false>(d_s, tc::smem_desc_sw128(qh, 16, 1024), tc::smem_desc_sw128(kh, 16, 1024), id_qk);
 #pragma unroll
-      for (int s = 0; s < D / 16; ++s) {
+      for (int s = 1; s < D / 16; ++s) {
         const uint32_t off = (s >> 2) * (kT * 128) + (s & 3) * 32;
-        tc::mma_ss(tmem + h * 256, tc::smem_desc_sw128(qh + off, 16, 1024), tc::smem_desc_sw128(kh + off, 16, 1024),
-                   id_qk, s > 0);
+        tc::mma_ss<true>(d_s, tc::smem_desc_sw128(qh + off, 16, 1024), tc::smem_desc_sw128(kh + off, 16, 1024), id_qk);
       }
       tc::commit(&bar[B_SFULL0 + h]);
     };
-    bool ok = true;
+    // O_h (+)= P_h V over the V tile in stage st (elected lane)
+    auto issue_pv = [&](int st, bool first) {
+      const uint32_t vs = v_base + st * L::kQBytes;
+      const uint64_t v0 = tc::smem_desc_sw128(vs, kT * 128, 1024);
+      if (first) tc::mma_ts<false>(d_o, d_s, v0, id_pv);
+      else tc::mma_ts<true>(d_o, d_s, v0, id_pv);
+#pragma unroll
+      for (int s = 1; s < kT / 16; ++s)
+        tc::mma_ts<true>(d_o, d_s + s * 8, tc::smem_desc_sw128(vs + s * 2048, kT * 128, 1024), id_pv);
+    };
+    // Turns: block b = -1 is Q.K^T of tile 0, block b >= 0 is P.V of tile b
+    // and Q.K^T of tile b + 1.  With two heads, head 0 issues block b after
+    // head 1's block b - 1 (completion b of B_TURN0) and head 1 after head 0's
+    // block b (completion b + 1 of B_TURN1).
+    const bool turns = nh == 2;
+    auto take_turn = [&](int blk) -> bool {
+      if (!turns || (h == 0 && blk < 0)) return true;
+      return h == 0 ? wait_all(B_TURN0, blk & 1) : wait_all(B_TURN1, (blk + 1) & 1);
+    };
+    auto pass_turn = [&]() {
+      if (turns) mbar_arrive(&bar[h == 0 ? B_TURN1 : B_TURN0]);
+    };
+    bool ok = wait_all(B_QREADY, 0) && (n_kept == 0 || (wait_all(B_KFULL0, 0) && take_turn(-1)));
+    tc::fence_after_sync();
+    if (ok && n_kept > 0) {
+      if (tc::elect_one()) {
+        issue_qk(0);
+        pass_turn();
+      }
+      __syncwarp();
+    }
     for (int j = 0; j < n_kept && ok; ++j) {
       const int st = j & 1;
-      if (j == 0) {
-        ok = mbar_wait(&bar[B_KFULL0], 0, p.status, wns);
-        tc::fence_after_sync();
-        for (int h = 0; h < nh && ok; ++h) issue_qk(h, 0);
-      }
-      ok = ok && mbar_wait(&bar[B_VFULL0 + st], (j >> 1) & 1, p.status, wns);
+      ok = wait_all(B_VFULL0 + st, (j >> 1) & 1) && wait_all(B_PFULL0 + h, j & 1) && take_turn(j);
+      if (!ok) break;
       tc::fence_after_sync();
-      for (int h = 0; h < nh && ok; ++h) {
-        ok = mbar_wait(&bar[B_PFULL0 + h], j & 1, p.status, wns);
-        tc::fence_after_sync();
-        if (!ok) break;
-        const uint32_t vs = v_base + st * L::kQBytes;
-#pragma unroll
-        for (int s = 0; s < kT / 16; ++s)
-          tc::mma_ts(tmem + h * 256 + 128, tmem + h * 256 + s * 8, tc::smem_desc_sw128(vs + s * 2048, kT * 128, 1024),
-                     id_pv, (j > 0 || s > 0) ? 1u : 0u);
+      if (tc::elect_one()) {
+        issue_pv(st, j == 0);
         tc::commit(&bar[B_ORDY0 + h]);
-        if (j + 1 < n_kept) {
-          if (h == 0) {
-            ok = ok && mbar_wait(&bar[B_KFULL0 + ((j + 1) & 1)], ((j + 1) >> 1) & 1, p.status, wns);
-            tc::fence_after_sync();
-          }
-          if (ok) issue_qk(h, (j + 1) & 1);
-        }
+        // this head is done with the stage: its Q.K^T of tile j was issued
+        // before this P.V (an issuer's products complete in issue order)
+        tc::commit(&bar[B_KVEMPTY0 + st]);
       }
-      tc::commit(&bar[B_KVEMPTY0 + st]);
+      __syncwarp();
+      if (j + 1 < n_kept) {
+        // the next K tile is written once both heads' P.V of tile j - 1 are
+        // done; this head's P.V queued above covers most of that wait
+        ok = wait_all(B_KFULL0 + ((j + 1) & 1), ((j + 1) >> 1) & 1);
+        if (!ok) break;
+        tc::fence_after_sync();
+      }
+      if (tc::elect_one()) {
+        if (j + 1 < n_kept) issue_qk((j + 1) & 1);
+        pass_turn();
+      }
+      __syncwarp();
     }
-    } while (0);
-    // every product issued so far has completed (a commit with none pending
-    // arrives at once) before the warp reports that it is done
-    tc::commit(&bar[B_MMADONE]);
-    mbar_wait(&bar[B_MMADONE], 0, p.status, wns);
+    // every product this warp issued has completed (a commit with none
+    // pending arrives at once) before the warp reports that it is done
+    if (tc::elect_one()) tc::commit(&bar[B_MMADONE]);
+    __syncwarp();
+    wait_all(B_MMADONE, 0);
     tc::fence_before_sync();
-    mbar_arrive(&bar[B_EXIT]);
+    if (lane == 0) mbar_arrive(&bar[B_EXIT]);
     return;
   }
 
-  if (lane == 0) mbar_arrive(&bar[B_EXIT]);   // warps 2, 3: no role
+  if (lane == 0) mbar_arrive(&bar[B_EXIT]);   // warp 3: no role
   return;
   }
 
