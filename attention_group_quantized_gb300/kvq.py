@@ -314,7 +314,12 @@ def decode_step_host(q_host, k_new_host, v_new_host, k: QuantCache, v: QuantCach
 class DecodeStepHost:
     """A decode_step_host call with its host buffers, staging, workspace and stream bound once,
     for serving loops that run it every token: ``run(k, v)`` enqueues one step on the caches
-    given (their C views are cached) with little Python work per call."""
+    given with little Python work per call.
+
+    Every argument but the two caches is converted to its C type once; the call goes through a
+    second handle on the same library function without ctypes argument conversion (the
+    converted values are passed as they are), and each cache's C view is reused while the cache
+    object and its buffers are unchanged."""
 
     def __init__(self, q_host, k_new_host, v_new_host, seq_lens, out_host, softmax_scale: float = 0.0,
                  out_dtype: int = OUT_F32, staging=None, workspace=None, status=None, stream=None,
@@ -324,15 +329,33 @@ class DecodeStepHost:
         self.staging = staging if staging is not None else decode_step_staging(B, Hq, Hkv, D, out_dtype, device)
         self.workspace = workspace if workspace is not None else decode_workspace(B, Hq, Hkv, D, device)
         self._keep = (q_host, k_new_host, v_new_host, seq_lens, out_host, status, stream)
-        self._head = (q_host.data_ptr(), k_new_host.data_ptr(), v_new_host.data_ptr())
-        self._tail = (seq_lens.data_ptr(), Hq, float(softmax_scale), out_host.data_ptr(), out_dtype,
-                      self.staging.data_ptr(), self.staging.numel(), self.workspace.data_ptr(),
-                      self.workspace.numel() * self.workspace.element_size(),
-                      status.data_ptr() if status is not None else None, _stream_ptr(stream))
-        self._fn = lib().kvq_decode_step_host
+        P, I32, F32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+        self._head = (P(q_host.data_ptr()), P(k_new_host.data_ptr()), P(v_new_host.data_ptr()))
+        self._tail = (P(seq_lens.data_ptr()), I32(Hq), F32(float(softmax_scale)), P(out_host.data_ptr()),
+                      I32(out_dtype), P(self.staging.data_ptr()), SZ(self.staging.numel()),
+                      P(self.workspace.data_ptr()), SZ(self.workspace.numel() * self.workspace.element_size()),
+                      P(status.data_ptr() if status is not None else None), P(_stream_ptr(stream)))
+        lib()   # loads the library and checks its exports
+        raw = ctypes.CDLL(LIB_PATH).kvq_decode_step_host
+        raw.restype = ctypes.c_int32
+        self._fn = raw
+        self._views = {}
+
+    def _view(self, c: QuantCache):
+        """byref of the cache's C view, reused while the cache object, the buffer objects it holds
+        and its shape fields are the same (a buffer resized in place needs a new call object)."""
+        hit = self._views.get(id(c))
+        if (hit is not None and hit[0] is c and hit[1] is c.codes and hit[2] is c.sz and hit[3] is c.head_bits
+                and hit[4] == (c.B, c.Hkv, c.Tcap, c.D)):
+            return hit[5]
+        ref = ctypes.byref(c.c_struct())
+        if len(self._views) > 64:
+            self._views.clear()
+        self._views[id(c)] = (c, c.codes, c.sz, c.head_bits, (c.B, c.Hkv, c.Tcap, c.D), ref)
+        return ref
 
     def run(self, k: QuantCache, v: QuantCache):
-        st = self._fn(*self._head, ctypes.byref(k.c_struct()), ctypes.byref(v.c_struct()), *self._tail)
+        st = self._fn(*self._head, self._view(k), self._view(v), *self._tail)
         if st != KVQ_OK:
             raise KvqError(st, "kvq_decode_step_host")
 

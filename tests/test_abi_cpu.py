@@ -206,3 +206,49 @@ def test_policy_defaults_and_validation_without_launch(L):
         st = L.kvq_prefill_attention_ex(0x3000, 0x3000, 0x3000, 1, 4, 1, 128, 128, None, 1, 0.0, None, 128,
                                         P(c128), P(c128), 0x5000, 0, P(q), None, None)
         assert st == 1, (field, val)
+
+
+class _FakeBuf:
+    """Stands in for a tensor: an address and a size, never dereferenced (the call fails first)."""
+
+    def __init__(self, ptr, n=0, shape=()):
+        self.ptr, self.n, self.shape = ptr, n, shape
+
+    def data_ptr(self):
+        return self.ptr
+
+    def numel(self):
+        return self.n
+
+    def element_size(self):
+        return 1
+
+
+class _FakeStream:
+    cuda_stream = None
+
+
+def test_prepared_decode_step_host_marshals_its_arguments(L):
+    """DecodeStepHost converts every argument once and calls through a handle
+    without ctypes conversion: a staging buffer one byte short must come back
+    as INVALID_ARG, one of the exact size must pass that check and fail only
+    at the first CUDA call (no GPU here), and a second run reuses the caches'
+    C views."""
+    B, Hq, Hkv, D = 1, 8, 2, 128
+    need = L.kvq_decode_step_staging_bytes(B, Hq, Hkv, D, 0)
+    mk = lambda: kvq.QuantCache(_FakeBuf(0x100000), _FakeBuf(0x200000), np.array([8, 8], np.int8), B, Hkv, 128, D)
+    k, v = mk(), mk()
+    q, kn = _FakeBuf(0x10000, shape=(B, Hq, D)), _FakeBuf(0x11000, shape=(B, Hkv, D))
+    args = (q, kn, _FakeBuf(0x12000), _FakeBuf(0x5000), _FakeBuf(0x13000))
+    short = kvq.DecodeStepHost(*args, 0.1, staging=_FakeBuf(0x20000, need - 1), workspace=_FakeBuf(0x7000, 1 << 20),
+                               stream=_FakeStream())
+    with pytest.raises(kvq.KvqError) as e:
+        short.run(k, v)
+    assert e.value.status == 1
+    exact = kvq.DecodeStepHost(*args, 0.1, staging=_FakeBuf(0x20000, need), workspace=_FakeBuf(0x7000, 1 << 20),
+                               stream=_FakeStream())
+    for _ in range(2):
+        with pytest.raises(kvq.KvqError) as e:
+            exact.run(k, v)
+        assert e.value.status not in (0, 1)
+    assert len(exact._views) == 2

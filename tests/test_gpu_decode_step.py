@@ -217,7 +217,10 @@ def test_decode_step_host_prepared_call_matches_the_function():
         h_out = torch.zeros((inp.B, inp.Hq, inp.D), dtype=torch.float32).pin_memory()
         sl = torch.from_numpy(inp.seq_lens).cuda()
         if use_obj:
-            kvq.DecodeStepHost(h_q, h_k, h_v, sl, h_out, inp.softmax_scale, status=status).run(kc, vc)
+            # twice: the second call rewrites the same token and reuses the caches' C views
+            obj = kvq.DecodeStepHost(h_q, h_k, h_v, sl, h_out, inp.softmax_scale, status=status)
+            obj.run(kc, vc)
+            obj.run(kc, vc)
         else:
             kvq.decode_step_host(h_q, h_k, h_v, kc, vc, sl, h_out, inp.softmax_scale, status=status)
         torch.cuda.synchronize()
