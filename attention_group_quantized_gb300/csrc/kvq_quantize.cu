@@ -65,6 +65,13 @@ struct QParams {
 constexpr float kRoundAdd = 12582912.0f;
 constexpr int kRoundAddBits = 0x4B400000;
 
+// max(a, b, c), NaN if any input is NaN (three-input form, sm_100 and later)
+__device__ __forceinline__ float fmax3_nan(float a, float b, float c) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ float rcp_approx(float s) {
   float r;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
@@ -200,11 +207,13 @@ __device__ __forceinline__ void quarter_values(const uint16_t* src, int v, F f) 
 // values as loaded by load_group from src; the codes go to cdst (32 bytes for
 // 8-bit, 16 for 4-bit) and the fp16 (scale, zero) word to *szw.
 // Fast path, per pair of values: m = fl(x * r + C) holds rne(x * r) + z in its
-// low mantissa bits, u = m - C = rne(x * r), d = x - u * s exact; the code is
-// the specification's wherever |d| < s / 2 (then u is the integer nearest
-// x / s) and no code is clamped (group_clamps).  A quarter with some |d| at
-// least s / 2 (a tie, or u one step off), or a NaN (the sum of the d's), or a
-// clamped group, is redone with code_exact and stored 8 codes at a time.
+// low mantissa bits (C's low byte is zero, so a code 0 .. qmax is m's low byte
+// or nibble, gathered by byte permutes), u = m - C = rne(x * r), d = x - u * s
+// exact; the code is the specification's wherever |d| < s / 2 (then u is the
+// integer nearest x / s) and no code is clamped (group_clamps).  A quarter
+// with some |d| at least s / 2 (a tie, or u one step off) or a NaN (the
+// quarter's largest |d| is then NaN), or a clamped group, is redone with
+// code_exact and stored 8 codes at a time.
 __device__ __forceinline__ void quantize_group(const uint32_t (&w)[16], const uint16_t* src, int bits,
                                                uint8_t* cdst, uint32_t* szw, int32_t* status) {
   const GroupParams gp = group_params(w, bits);
@@ -218,28 +227,33 @@ __device__ __forceinline__ void quantize_group(const uint32_t (&w)[16], const ui
   } else {
     const float2 r2 = make_float2(gp.rcp, gp.rcp), c2 = make_float2(gp.C, gp.C);
     const float2 nc2 = make_float2(-gp.C, -gp.C), ns2 = make_float2(-gp.sf, -gp.sf);
-    float2 dsum = make_float2(0.0f, 0.0f);
     const float hs = 0.5f * gp.sf;
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
+      // the largest |d| of the quarter; a NaN anywhere makes it NaN
       float dmax = 0.0f;
+      uint32_t mb[8];   // bits of m: C = z + 1.5 * 2^23 has a zero low byte, so the code is in the low bits
 #pragma unroll
-      for (int k = 4 * v; k < 4 * v + 4; ++k) {
-        const float2 x2 = bf16x2_to_float2(w[k]);
+      for (int kk = 0; kk < 4; ++kk) {
+        const float2 x2 = bf16x2_to_float2(w[4 * v + kk]);
         const float2 m2 = __ffma2_rn(x2, r2, c2);
         const float2 d2 = __ffma2_rn(__fadd2_rn(m2, nc2), ns2, x2);
-        dsum = __fadd2_rn(dsum, d2);
-        dmax = fmaxf(dmax, fmaxf(fabsf(d2.x), fabsf(d2.y)));
-        const uint32_t c0 = static_cast<uint32_t>(__float_as_int(m2.x) - kRoundAddBits);
-        const uint32_t c1 = static_cast<uint32_t>(__float_as_int(m2.y) - kRoundAddBits);
-        const int i = 2 * k;
-        if (bits == 8) packed[i >> 2] |= (c0 | (c1 << 8)) << (8 * (i & 3));
-        else packed[i >> 3] |= (c0 | (c1 << 4)) << (4 * (i & 7));
+        dmax = fmax3_nan(dmax, fabsf(d2.x), fabsf(d2.y));
+        mb[2 * kk] = __float_as_uint(m2.x);
+        mb[2 * kk + 1] = __float_as_uint(m2.y);
       }
-      redo |= (dmax < hs ? 0u : 1u) << v;
+      if (bits == 8) {   // low bytes of four m's per word
+        packed[2 * v] = prmt(prmt(mb[0], mb[1], 0x0040u), prmt(mb[2], mb[3], 0x0040u), 0x5410u);
+        packed[2 * v + 1] = prmt(prmt(mb[4], mb[5], 0x0040u), prmt(mb[6], mb[7], 0x0040u), 0x5410u);
+      } else {           // low nibbles of eight m's, the first in bits 0-3
+        uint32_t b[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) b[j] = (mb[2 * j] & 0x0Fu) | ((mb[2 * j + 1] << 4) & 0xF0u);
+        packed[v] = prmt(prmt(b[0], b[1], 0x0040u), prmt(b[2], b[3], 0x0040u), 0x5410u);
+      }
+      redo |= (dmax < hs ? 0u : 1u) << v;   // false for a NaN
     }
-    const float dtot = __fadd_rn(dsum.x, dsum.y);
-    if (dtot != dtot || group_clamps(gp)) redo = 0xFu;
+    if (group_clamps(gp)) redo = 0xFu;
   }
   if (redo == 0u) {
     uint4* dst = reinterpret_cast<uint4*>(cdst);
