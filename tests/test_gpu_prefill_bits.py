@@ -149,3 +149,35 @@ def test_allocation_prefill_then_decode(kvq):
     vd = U.oracle_quantize(sens.v, bits)[3]
     ref = O.decode_attention(qd, kd, vd, np.full(B, S), inp.softmax_scale)
     U.assert_close(out.cpu().numpy(), ref, "decode after prefill over allocated bits")
+
+
+JUMPS = [(128 + 70, "tile1_chunk2"), (256 + 5, "tile2_chunk0"), (256 + 100, "tile2_chunk3")]
+
+
+@pytest.mark.parametrize("causal", [True, False], ids=["causal", "noncausal"])
+@pytest.mark.parametrize("tok", [t for t, _ in JUMPS], ids=[n for _, n in JUMPS])
+def test_prefill_running_max_jumps(kvq, causal, tok):
+    """One key token of large values in the middle of a later key tile: in
+    the rows whose score against it is large the tile's max exceeds the running
+    max by far more than the rescale threshold, so the running max moves in
+    the middle of the sequence and the O accumulated so far is rescaled (after
+    the previous P.V product has finished); in those rows that key then
+    dominates, so an unrescaled O would show at full weight.  Every row
+    against the oracle, over an 8-bit and a 4-bit KV head.  (The key's values
+    are chosen so that the fp16 K operand holds them exactly: with ordinary
+    bf16 values of that size the operand's rounding alone moves such scores by
+    percents, and the check would measure that instead of the rescale.)"""
+    inp = W.make_prefill("max_jump", 95, 1, 4, 2, 128, 512, mask_seed=None)
+    kf = (inp.k.astype(np.uint32) << 16).view(np.float32).copy()
+    # The large key: per 32-channel group, integers n spanning exactly the code
+    # range ([-128, 127] at 8 bits, [-8, 7] at 4) times a power of two, so the
+    # group's scale is that power of two and its dequantised values are exact
+    # in fp16 -- the scores against it then carry no operand rounding.
+    rng = np.random.default_rng(96)
+    for h, (lo, hi, step) in enumerate(((-128, 127, 0.5), (-8, 7, 8.0))):
+        n = rng.integers(lo, hi + 1, size=(128,)).astype(np.float64)
+        n[0::32], n[1::32] = lo, hi
+        kf[0, h, tok] = (n * step).astype(np.float32)
+    inp.k = (kf.view(np.uint32) >> 16).astype(np.uint16)
+    got, kc, vc = _run(kvq, inp, [8, 4], causal=causal)
+    _check(inp, [8, 4], got, kc, vc, causal=causal)
