@@ -324,8 +324,12 @@ def time_decode(torch, kvq, inp, dev, l2, steps, warmup, dist=None, keep=False, 
         clk.__exit__(None, None, None)
     t_total = max_over_ranks(torch, dist, t0.elapsed_time(t1) / 1e3, dev)
     # isolated launches (each synchronised before the next): no overlap with a
-    # previous kernel, so the launch ramp and the merge tail are not hidden
-    iso = []
+    # previous kernel, so the launch ramp and the merge tail are not hidden.
+    # iso: events around the call, so the host's enqueue (the GPU idles
+    # meanwhile) is included; iso_dev: a spin kernel queued first keeps the
+    # GPU busy while the call is enqueued, so the events bracket the device
+    # work of the launch alone
+    iso, iso_dev = [], []
     for i in range(min(steps, 10)):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -333,9 +337,16 @@ def time_decode(torch, kvq, inp, dev, l2, steps, warmup, dist=None, keep=False, 
         e1.record(stream)
         torch.cuda.synchronize()
         iso.append(e0.elapsed_time(e1) * 1e3)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(200000)   # about 0.1 ms of device spin
+        e0.record(stream)
+        step(i + 1)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        iso_dev.append(e0.elapsed_time(e1) * 1e3)
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     res = {"t_total": t_total, "bytes": nbytes, "n_copies": n_copies, "clk": clk,
-           "isolated_us": statistics.median(iso),
+           "isolated_us": statistics.median(iso), "isolated_device_us": statistics.median(iso_dev),
            "timing": "one CUDA graph of the K steps, event-timed" if graph is not None else "eager launches, event-timed"}
     if keep:
         res.update(caches=caches, q=q, sl=sl, ws=ws)
@@ -478,6 +489,7 @@ def bench_phase_policy(torch, kvq, W, peaks, steps, warmup, dev, decode_policy):
         avg = d["t_total"] / steps
         res[label] = {"policy": fields or "defaults (ring 4, L2 warm-up 5)",
                       "us_per_step": avg * 1e6, "isolated_launch_us": d["isolated_us"],
+                      "isolated_device_us": d["isolated_device_us"],
                       "GB/s": d["bytes"] / avg / 1e9, "frac_of_hbm_peak": d["bytes"] / avg / 1e9 / peaks["hbm_gbs"]}
         del d
     res["decode_speedup_policy_over_default"] = res["decode_default"]["us_per_step"] / res["decode_policy"]["us_per_step"]
@@ -654,6 +666,7 @@ def main():
     clk = d["clk"]
     timing = d["timing"]
     isolated_us = d["isolated_us"]
+    isolated_dev_us = d["isolated_device_us"]
     caches, n_copies, q, sl, ws = d["caches"], d["n_copies"], d["q"], d["sl"], d["ws"]
     bytes_per_step = d["bytes"]
     t_total = d["t_total"]
@@ -756,6 +769,7 @@ def main():
             "other_decode_workloads": extras,
             "phase_policy": phase,
             "decode_isolated_launch_us": isolated_us,
+            "decode_isolated_device_us": isolated_dev_us,
         }
         print(json.dumps(line))
     if dist:
