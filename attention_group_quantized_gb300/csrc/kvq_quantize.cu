@@ -61,9 +61,9 @@ struct QParams {
 
 // 1.5 * 2^23: adding it to a float of magnitude below 2^22 rounds that value
 // to the nearest integer (ties to even) -- floats in [2^23, 2^24) are spaced
-// 1 apart -- and leaves the integer in the low mantissa bits.
+// 1 apart -- and leaves the integer in the low mantissa bits (its bit pattern
+// 0x4B400000 has a zero low byte).
 constexpr float kRoundAdd = 12582912.0f;
-constexpr int kRoundAddBits = 0x4B400000;
 
 // max(a, b, c), NaN if any input is NaN (three-input form, sm_100 and later)
 __device__ __forceinline__ float fmax3_nan(float a, float b, float c) {
@@ -119,8 +119,8 @@ __device__ __forceinline__ void load_group(uint32_t (&w)[16], const uint16_t* sr
 // s = round-up(range / qmax) (one IEEE division), the zero point
 // z = clamp(rne(-lo / s), 0, qmax) (rne_div), and the fast path's constants.
 // Non-finite input: an infinity makes the range, hence the scale, infinite; a
-// NaN is dropped by the min/max but shows in the fast path's remainders (or,
-// in an otherwise all-zero group, in group_has_nan).
+// NaN is dropped by the min/max but shows in the fast path's largest remainder
+// (or, in an otherwise all-zero group, in group_has_nan).
 struct GroupParams {
   __half scale_h;   // 1 when the range is 0
   float mn, mx;     // the group's min and max (before widening)
