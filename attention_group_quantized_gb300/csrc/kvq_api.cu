@@ -143,6 +143,7 @@ const char* kvq_status_str(kvq_status s) {
     case KVQ_ERR_WORKSPACE: return "workspace missing or too small";
     case KVQ_ERR_TIMEOUT: return "device wait timed out";
     case KVQ_ERR_NONFINITE: return "non-finite input or fp16 overflow";
+    case KVQ_ERR_BOUNDS: return "device index check failed (debug build)";
   }
   return "unknown status";
 }

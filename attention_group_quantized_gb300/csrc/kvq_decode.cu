@@ -413,7 +413,9 @@ __device__ __forceinline__ void load_words(uint32_t (&w)[G], const uint32_t* src
   }
 }
 
+template <int D>
 __device__ __forceinline__ void store_out4(const DParams& p, int64_t i, float4 v) {
+  if (!KVQ_IN_RANGE(i >= 0 && i + 4 <= static_cast<int64_t>(p.B) * p.Hq * D, p.status)) return;
   if (p.out_dtype == KVQ_OUT_F32) {
     *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + i) = v;
   } else {
@@ -464,6 +466,10 @@ __device__ __forceinline__ void segment_end(const DParams& p, const EpiBuf<D>* e
   const bool whole = c0 == c1;
   const int64_t orow0 = (static_cast<int64_t>(cb) * p.Hq + ckvh * rep) * D;
   const int64_t slot = static_cast<int64_t>(seg) + blockIdx.x;
+  // debug build: the segment's counter and this piece's workspace slot exist
+  // (slots = segments + split CTAs); a failed check writes no partial
+  const int64_t n_slots = static_cast<int64_t>(p.B) * Hkv + p.num_ctas;
+  const bool slot_ok = KVQ_IN_RANGE(seg < p.B * Hkv && slot < n_slots && c1 < p.num_ctas, p.status);
   for (int i4 = tid; i4 < rep * (D / 4); i4 += nthr) {
     const int h = i4 / (D / 4), ch = (i4 % (D / 4)) * 4;
     float M = -INFINITY;
@@ -484,8 +490,8 @@ __device__ __forceinline__ void segment_end(const DParams& p, const EpiBuf<D>* e
     const float inv = any ? 1.0f / Lsum : 0.0f;
     o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
     if (whole) {
-      store_out4(p, orow0 + static_cast<int64_t>(h) * D + ch, o);
-    } else {
+      store_out4<D>(p, orow0 + static_cast<int64_t>(h) * D + ch, o);
+    } else if (slot_ok) {
       *reinterpret_cast<float4*>(p.ws_o + (slot * rep + h) * D + ch) = o;
       if (ch == 0) p.ws_lse[slot * rep + h] = any ? M + __log2f(Lsum) : -INFINITY;
     }
@@ -500,7 +506,7 @@ __device__ __forceinline__ void segment_end(const DParams& p, const EpiBuf<D>* e
   // own arrivals, before the group's reads below
   if (tid == 0) {
     const int np = c1 - c0 + 1;   // every split CTA owns at least one tile
-    *flag = (atom_add_acq_rel_gpu(p.ws_cnt + seg, 1) + 1 == np) ? 1 : 0;
+    *flag = (slot_ok && atom_add_acq_rel_gpu(p.ws_cnt + seg, 1) + 1 == np) ? 1 : 0;
   }
   sync();
   if (*flag != 1) return;
@@ -538,7 +544,7 @@ __device__ __forceinline__ void segment_end(const DParams& p, const EpiBuf<D>* e
     }
     const float inv = Lsum > 0.0f ? 1.0f / Lsum : 0.0f;
     acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
-    store_out4(p, orow0 + static_cast<int64_t>(h) * D + ch, acc);
+    store_out4<D>(p, orow0 + static_cast<int64_t>(h) * D + ch, acc);
   }
   if (tid == 0) p.ws_cnt[seg] = 0;   // ready for the next call
 }
@@ -658,11 +664,13 @@ __device__ __forceinline__ void warm_l2(const DParams& p, int lane) {
   const int bits = p.bits[kvh];
   int pb = bs, pt = i * kTile;
   if constexpr (PAGED) {   // (a stale or bad page id only misdirects this prefetch)
+    if (!KVQ_IN_RANGE(i < p.bt_stride, p.status)) return;
     pb = min(max(p.bt[static_cast<int64_t>(bs) * p.bt_stride + i], 0), p.pB - 1);
     pt = 0;
   }
   const int32_t row0 = (p.plane[kvh] * p.pB + pb) * p.pT + pt;
   const int64_t szoff = (static_cast<int64_t>(kvh) * p.pB + pb) * p.pT + pt;
+  if (!KVQ_IN_RANGE(kvh < p.Hkv && szoff + kTile <= static_cast<int64_t>(p.Hkv) * p.pB * p.pT, p.status)) return;
   prefetch_l2_tile_2d(bits == 8 ? &p.tm_k8 : &p.tm_k4, 0, row0);
   prefetch_l2_tile_2d(bits == 8 ? &p.tm_v8 : &p.tm_v4, 0, row0);
   prefetch_l2_bulk(p.k_sz + szoff * G, Smem<D>::kSzBytes);
@@ -775,7 +783,8 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
       for (int j = 0; j < kStages; ++j) {
         pg[j] = 0;
         if (PAGED && j < ntiles) {
-          pg[j] = p.bt[static_cast<int64_t>(pa.b) * p.bt_stride + pa.i];
+          pg[j] = KVQ_IN_RANGE(pa.b < p.B && pa.i < p.bt_stride, p.status)
+                      ? p.bt[static_cast<int64_t>(pa.b) * p.bt_stride + pa.i] : 0;
           advance(pa, pre, B, Hkv);
         }
       }
@@ -797,7 +806,8 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
           for (int j = 0; j + 1 < kStages; ++j) pg[j] = pg[j + 1];
           pg[kStages - 1] = 0;
           if (k + kStages < ntiles) {
-            pg[kStages - 1] = p.bt[static_cast<int64_t>(pa.b) * p.bt_stride + pa.i];
+            pg[kStages - 1] = KVQ_IN_RANGE(pa.b < p.B && pa.i < p.bt_stride, p.status)
+                                  ? p.bt[static_cast<int64_t>(pa.b) * p.bt_stride + pa.i] : 0;
             advance(pa, pre, B, Hkv);
           }
           if (pb < 0 || pb >= p.pB) {   // a page outside the pool: report, read page 0 instead
@@ -807,13 +817,21 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
           pt = 0;
         }
         const int32_t row0 = (p.plane[pc.kvh] * p.pB + pb) * p.pT + pt;
-        const int64_t szoff = (static_cast<int64_t>(pc.kvh) * p.pB + pb) * p.pT + pt;
+        int64_t szoff = (static_cast<int64_t>(pc.kvh) * p.pB + pb) * p.pT + pt;
+        // debug build: the tile's rows inside its code plane, its scale/zero
+        // words and queries inside their buffers (a failed check reads the
+        // buffers' first entries instead)
+        (void)KVQ_IN_RANGE(row0 >= 0 && row0 + kTile <= (p.plane[pc.kvh] + 1) * p.pB * p.pT, p.status);
+        if (!KVQ_IN_RANGE(szoff >= 0 && szoff + kTile <= static_cast<int64_t>(p.Hkv) * p.pB * p.pT, p.status))
+          szoff = 0;
         uint64_t* bar = &full[slot];
         const bool first = pc.i == 0 || k == 0;
         const uint32_t qbytes = first ? static_cast<uint32_t>(p.rep * D * 2) : 0u;
+        int64_t qoff = (static_cast<int64_t>(pc.b) * p.Hq + pc.kvh * p.rep) * D;
+        if (!KVQ_IN_RANGE(qoff >= 0 && qoff + p.rep * D <= static_cast<int64_t>(p.B) * p.Hq * D, p.status)) qoff = 0;
         mbar_arrive_expect_tx(bar, 2 * kTile * Rb + 2 * L::kSzBytes + qbytes);
         if (first)
-          bulk_g2s(st + L::kOffQ, p.q + (static_cast<int64_t>(pc.b) * p.Hq + pc.kvh * p.rep) * D, qbytes, bar);
+          bulk_g2s(st + L::kOffQ, p.q + qoff, qbytes, bar);
         tma_2d_g2s_hint(st + L::kOffK, bits == 8 ? &p.tm_k8 : &p.tm_k4, 0, row0, bar, pol);
         tma_2d_g2s_hint(st + L::kOffV, bits == 8 ? &p.tm_v8 : &p.tm_v4, 0, row0, bar, pol);
         bulk_g2s_hint(st + L::kOffKsz, p.k_sz + szoff * G, L::kSzBytes, bar, pol);

@@ -21,6 +21,22 @@ __device__ __forceinline__ void report(int32_t* status, int32_t code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
 
+// Index checks of the debug build (libkvq_debug.so, compiled with
+// KVQ_DEBUG=1): KVQ_IN_RANGE(cond, status) is cond there -- and a false cond
+// reports KVQ_ERR_BOUNDS, the caller then skipping the access -- and the
+// constant true in the shipped library, so the checks cost nothing there.
+// They stand in for a memory checker: a check that fails never faults, it
+// only records the first failure in the status word.
+__device__ __forceinline__ bool debug_in_range(bool ok, int32_t* status) {
+  if (!ok) report(status, KVQ_ERR_BOUNDS);
+  return ok;
+}
+#if defined(KVQ_DEBUG) && KVQ_DEBUG
+#define KVQ_IN_RANGE(cond, status) (::kvq::debug_in_range((cond), (status)))
+#else
+#define KVQ_IN_RANGE(cond, status) (static_cast<void>(sizeof((cond) ? 1 : 0)), true)   // unevaluated
+#endif
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -83,6 +83,7 @@ struct PParams {
   uint64_t wait_ns;               // bounded-wait limit
   int32_t issue_limit;            // test only: 0 withholds the query load (every first wait then runs out)
   int64_t plane_off[KVQ_MAX_HKV]; // byte offset of each KV head's code plane
+  int64_t codes_bytes;            // size of each code buffer (the debug build's index checks)
   int8_t bits[KVQ_MAX_HKV];       // 8 or 4 per KV head
 };
 
@@ -241,16 +242,26 @@ struct PartRegs {
   uint32_t w[DqFmt<D, BITS>::NI];
 };
 
+// (cend, send, status: the ends of the code and scale/zero buffers for the
+// debug build's index checks; a failed check loads zeros instead)
 template <int D, int BITS>
 __device__ __forceinline__ void load_part(PartRegs<D, BITS>& r, const uint8_t* codes, const uint32_t* sz, int kt,
-                                          int row, int c, int g) {
+                                          int row, int c, int g, const uint8_t* cend, const uint32_t* send,
+                                          int32_t* status) {
   using F = DqFmt<D, BITS>;
   constexpr int G = D / 32;
 #pragma unroll
   for (int it = 0; it < F::NI; ++it) {
     const size_t tok = static_cast<size_t>(kt) * kT + F::RPI * it + row;
-    r.c[it] = __ldg(reinterpret_cast<const uint4*>(codes + tok * F::R + c * 16));
-    r.w[it] = __ldg(sz + tok * G + g);
+    const uint8_t* cp = codes + tok * F::R + c * 16;
+    const uint32_t* sp = sz + tok * G + g;
+    if (KVQ_IN_RANGE(cp + 16 <= cend && sp < send, status)) {
+      r.c[it] = __ldg(reinterpret_cast<const uint4*>(cp));
+      r.w[it] = __ldg(sp);
+    } else {
+      r.c[it] = make_uint4(0u, 0u, 0u, 0u);
+      r.w[it] = 0u;
+    }
   }
 }
 
@@ -279,22 +290,27 @@ __device__ __forceinline__ void dequant_loop(const PParams& p, uint8_t* smem, ui
   const size_t szrow = (static_cast<size_t>(kvh) * p.B + b) * p.Tcap;
   const uint32_t* ksz = p.ksz + szrow * (D / 32);
   const uint32_t* vsz = p.vsz + szrow * (D / 32);
+  const int64_t sz_words = static_cast<int64_t>(p.Hkv) * p.B * p.Tcap * (D / 32);
+  const uint8_t* kcend = p.kcodes + p.codes_bytes;
+  const uint8_t* vcend = p.vcodes + p.codes_bytes;
+  const uint32_t* ksend = p.ksz + sz_words;
+  const uint32_t* vsend = p.vsz + sz_words;
   const uint32_t kdst = smem_u32(smem + L::kOffK);
   const uint32_t vdst = smem_u32(smem + L::kOffV);
   PartRegs<D, BITS> ra, rb;
   int kt = next_kept(p, qt, 0, kt_end);
-  if (kt < kt_end) load_part<D, BITS>(ra, kcodes, ksz, kt, row, c, g);
+  if (kt < kt_end) load_part<D, BITS>(ra, kcodes, ksz, kt, row, c, g, kcend, ksend, p.status);
   for (int j = 0; kt < kt_end; ++j) {
     const int st = j & 1;
     const int kt_next = next_kept(p, qt, kt + 1, kt_end);
-    load_part<D, BITS>(rb, vcodes, vsz, kt, row, c, g);
+    load_part<D, BITS>(rb, vcodes, vsz, kt, row, c, g, vcend, vsend, p.status);
     if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(&bar[B_KVEMPTY0 + st], ((j >> 1) - 1) & 1, p.status, p.wait_ns)))
       return;
     store_part<D, BITS>(kdst + st * L::kQBytes, ra, row, c);
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar[B_KFULL0 + st]);
-    if (kt_next < kt_end) load_part<D, BITS>(ra, kcodes, ksz, kt_next, row, c, g);
+    if (kt_next < kt_end) load_part<D, BITS>(ra, kcodes, ksz, kt_next, row, c, g, kcend, ksend, p.status);
     store_part<D, BITS>(vdst + st * L::kQBytes, rb, row, c);
     fence_proxy_async_smem();
     __syncwarp();
@@ -309,6 +325,8 @@ __device__ __forceinline__ void zero_out_tile(const PParams& p, int b, int h0, i
   const size_t row0 = (static_cast<size_t>(b) * p.Hq + h0) * p.S + static_cast<size_t>(qt) * kT;
   const int esz = p.out_dtype == KVQ_OUT_F32 ? 4 : 2;
   const int vec_per_row = D * esz / 16;
+  if (!KVQ_IN_RANGE(row0 + static_cast<size_t>(nh - 1) * p.S + kT <= static_cast<size_t>(p.B) * p.Hq * p.S, p.status))
+    return;
   for (int h = 0; h < nh; ++h) {
     uint4* base =
         reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + (row0 + static_cast<size_t>(h) * p.S) * D * esz);
@@ -317,7 +335,9 @@ __device__ __forceinline__ void zero_out_tile(const PParams& p, int b, int h0, i
 }
 
 // 32 output values of one row (TMEM columns 32c .. 32c+31, times inv) to global memory.
+template <int D>
 __device__ __forceinline__ void store_row32(const PParams& p, size_t off, const float (&o)[32]) {
+  if (!KVQ_IN_RANGE(off + 32 <= static_cast<size_t>(p.B) * p.Hq * p.S * D, p.status)) return;
   if (p.out_dtype == KVQ_OUT_F32) {
     float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + off);
 #pragma unroll
@@ -725,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(v[i]) * inv;
       }
-      store_row32(p, orow * D + c * 32, o);
+      store_row32<D>(p, orow * D + c * 32, o);
     }
   }
   tc::wait_st();   // P and rescaled O stores of a loop left early have landed
@@ -798,6 +818,7 @@ kvq_status launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.lens = a.lens;
   p.wait_ns = a.pol.wait_ns;
   p.issue_limit = a.pol.issue_limit;
+  p.codes_bytes = kvq_cache_codes_bytes(a.k);
   for (int h = 0; h < KVQ_MAX_HKV; ++h) {
     p.plane_off[h] = a.layout.plane_off[h];
     p.bits[h] = a.layout.bits[h];

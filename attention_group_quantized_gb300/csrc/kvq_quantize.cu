@@ -55,9 +55,17 @@ struct QParams {
   int32_t* status;
   int32_t B, Hkv, Tcap, t0, nt;
   int64_t rows;
+  int64_t codes_bytes;      // size of the code buffer (the debug build's index checks)
   int64_t plane_off[KVQ_MAX_HKV];
   int8_t bits[KVQ_MAX_HKV];
 };
+
+// Debug build: a group's codes (nbytes from byte offset off) and its
+// scale/zero word (index si) inside their buffers.
+__device__ __forceinline__ bool group_dst_ok(int64_t off, int nbytes, int64_t si, int64_t codes_bytes,
+                                             int64_t sz_words, int32_t* status) {
+  return KVQ_IN_RANGE(off >= 0 && off + nbytes <= codes_bytes && si >= 0 && si < sz_words, status);
+}
 
 // 1.5 * 2^23: adding it to a float of magnitude below 2^22 rounds that value
 // to the nearest integer (ties to even) -- floats in [2^23, 2^24) are spaced
@@ -373,17 +381,21 @@ __global__ void __launch_bounds__(256, KVQ_QUANT_MIN_BLOCKS) quantize_kernel(con
     if constexpr (LENS) {
       const int len = min(max(p.lens[b], 0), p.Tcap);
       if (p.t0 + t >= len) {
-        if (p.t0 + t < ((len + 127) & ~127)) {
-          uint4* dst = reinterpret_cast<uint4*>(p.codes + p.plane_off[h] + pos * (D * bits / 8) + g * (32 * bits / 8));
+        const int64_t off = p.plane_off[h] + pos * (D * bits / 8) + g * (32 * bits / 8);
+        const int64_t si = (static_cast<int64_t>(h) * p.B * p.Tcap + pos) * G + g;
+        if (p.t0 + t < ((len + 127) & ~127) &&
+            group_dst_ok(off, 4 * bits, si, p.codes_bytes, static_cast<int64_t>(p.Hkv) * p.B * p.Tcap * G, p.status)) {
+          uint4* dst = reinterpret_cast<uint4*>(p.codes + off);
           dst[0] = make_uint4(0u, 0u, 0u, 0u);
           if (bits == 8) dst[1] = make_uint4(0u, 0u, 0u, 0u);
-          p.sz[(static_cast<int64_t>(h) * p.B * p.Tcap + pos) * G + g] = 0u;
+          p.sz[si] = 0u;
         }
         continue;
       }
     }
     if constexpr (PAGED) {
       const int tl = p.t0 + t;
+      if (!KVQ_IN_RANGE(tl / 64 < p.bt_stride, p.status)) continue;
       const int page = p.bt[static_cast<int64_t>(b) * p.bt_stride + tl / 64];
       if (page < 0 || page >= p.B) {   // a page outside the pool: report, write nothing
         if (g == 0) report(p.status, KVQ_ERR_INVALID_ARG);
@@ -391,11 +403,14 @@ __global__ void __launch_bounds__(256, KVQ_QUANT_MIN_BLOCKS) quantize_kernel(con
       }
       pos = static_cast<int64_t>(page) * 64 + tl % 64;
     }
+    const int64_t off = p.plane_off[h] + pos * (D * bits / 8) + g * (32 * bits / 8);
+    const int64_t si = (static_cast<int64_t>(h) * p.B * p.Tcap + pos) * G + g;
+    if (!group_dst_ok(off, 4 * bits, si, p.codes_bytes, static_cast<int64_t>(p.Hkv) * p.B * p.Tcap * G, p.status))
+      continue;
     uint32_t w[16];
     const uint16_t* src = p.x + b * p.sx_b + h * p.sx_h + t * p.sx_t + g * 32;
     load_group(w, src);
-    quantize_group(w, src, bits, p.codes + p.plane_off[h] + pos * (D * bits / 8) + g * (32 * bits / 8),
-                   p.sz + (static_cast<int64_t>(h) * p.B * p.Tcap + pos) * G + g, p.status);
+    quantize_group(w, src, bits, p.codes + off, p.sz + si, p.status);
   }
 }
 
@@ -414,6 +429,7 @@ struct AParams {
   int32_t* status;
   int32_t B, Hkv, Tcap;     // storage: B sequences (or pages) of Tcap tokens
   int32_t nseq, cap;        // sequences and their capacity in tokens
+  int64_t codes_bytes;      // size of each code buffer (the debug build's index checks)
   int64_t plane_off[KVQ_MAX_HKV];
   int8_t bits[KVQ_MAX_HKV];
 };
@@ -445,6 +461,7 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ APa
     const int bits = p.bits[h];
     int64_t pos = static_cast<int64_t>(b) * p.Tcap + len - 1;
     if constexpr (PAGED) {
+      if (!KVQ_IN_RANGE((len - 1) / 64 < p.bt_stride, p.status)) continue;
       const int page = p.bt[static_cast<int64_t>(b) * p.bt_stride + (len - 1) / 64];
       if (page < 0 || page >= p.B) {
         if (job == 0 && h == 0 && g == 0) report(p.status, KVQ_ERR_INVALID_ARG);
@@ -452,11 +469,14 @@ __global__ void __launch_bounds__(256) append_kernel(const __grid_constant__ APa
       }
       pos = static_cast<int64_t>(page) * 64 + (len - 1) % 64;
     }
+    const int64_t off = p.plane_off[h] + pos * (D * bits / 8) + g * (32 * bits / 8);
+    const int64_t si = (static_cast<int64_t>(h) * p.B * p.Tcap + pos) * G + g;
+    if (!group_dst_ok(off, 4 * bits, si, p.codes_bytes, static_cast<int64_t>(p.Hkv) * p.B * p.Tcap * G, p.status))
+      continue;
     uint32_t w[16];
     const uint16_t* src = p.x[job] + bh * D + g * 32;
     load_group(w, src);
-    quantize_group(w, src, bits, p.codes[job] + p.plane_off[h] + pos * (D * bits / 8) + g * (32 * bits / 8),
-                   p.sz[job] + (static_cast<int64_t>(h) * p.B * p.Tcap + pos) * G + g, p.status);
+    quantize_group(w, src, bits, p.codes[job] + off, p.sz[job] + si, p.status);
   }
 }
 
@@ -591,6 +611,7 @@ cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t stream) {
   if (p.lens != nullptr && p.bt != nullptr) return cudaErrorInvalidValue;
   p.rows = static_cast<int64_t>(a.bt != nullptr ? a.bt_B : a.B) * a.Hkv * a.nt;
   if (p.rows >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // rows are indexed in 32 bits
+  p.codes_bytes = a.layout.off4 + static_cast<int64_t>(a.layout.n4) * a.B * a.Tcap * (a.D / 2);
   p.div_nt = FastDiv::make(static_cast<uint32_t>(a.nt));
   p.div_hkv = FastDiv::make(static_cast<uint32_t>(a.Hkv));
   for (int h = 0; h < KVQ_MAX_HKV; ++h) {
@@ -628,6 +649,7 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
   p.bt = a.bt;
   p.bt_stride = a.bt_max_pages;
   p.nseq = a.bt != nullptr ? a.bt_B : a.B;
+  p.codes_bytes = a.layout.off4 + static_cast<int64_t>(a.layout.n4) * a.B * a.Tcap * (a.D / 2);
   p.cap = a.bt != nullptr ? a.bt_max_pages * 64 : a.Tcap;
   for (int h = 0; h < KVQ_MAX_HKV; ++h) {
     p.plane_off[h] = a.layout.plane_off[h];

@@ -15,10 +15,12 @@ import numpy as np
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libkvq.so")
+# the same kernels built with KVQ_DEBUG=1 (device index checks; see build.py)
+DEBUG_LIB_PATH = os.path.join(HERE, "libkvq_debug.so")
 
 KVQ_OK = 0
 STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error",
-                4: "workspace", 5: "timeout", 6: "non-finite"}
+                4: "workspace", 5: "timeout", 6: "non-finite", 7: "index check (debug build)"}
 OUT_F32 = 0
 OUT_BF16 = 1
 GROUP = 32

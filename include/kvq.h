@@ -50,7 +50,8 @@ typedef enum kvq_status {
   KVQ_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
   KVQ_ERR_WORKSPACE = 4,     /* workspace missing or too small */
   KVQ_ERR_TIMEOUT = 5,       /* (device) a bounded wait gave up */
-  KVQ_ERR_NONFINITE = 6      /* (device) non-finite input or fp16 overflow */
+  KVQ_ERR_NONFINITE = 6,     /* (device) non-finite input or fp16 overflow */
+  KVQ_ERR_BOUNDS = 7         /* (device, libkvq_debug.so only) an index check failed; the access was skipped */
 } kvq_status;
 
 #define KVQ_GROUP 32          /* channels per quantisation group (P4 §3.2) */

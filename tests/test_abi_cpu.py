@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_status_strings(L):
-    for s in range(7):
+    for s in range(8):
         assert L.kvq_status_str(s)
     assert L.kvq_status_str(99) == b"unknown status"
 
@@ -252,3 +252,17 @@ def test_prepared_decode_step_host_marshals_its_arguments(L):
             exact.run(k, v)
         assert e.value.status not in (0, 1)
     assert len(exact._views) == 2
+
+
+def test_debug_library_exports_every_declared_symbol(L):
+    """libkvq_debug.so (the kernels with index checks) is a drop-in: same exports,
+    and the status it adds has its own string."""
+    if not os.path.exists(kvq.DEBUG_LIB_PATH):
+        from attention_group_quantized_gb300 import build
+        build.build(debug=True)
+    D = ctypes.CDLL(kvq.DEBUG_LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(D, name), name
+    D.kvq_status_str.restype = ctypes.c_char_p
+    assert D.kvq_status_str(7) == b"device index check failed (debug build)"
+    assert L.kvq_status_str(7) == D.kvq_status_str(7)
