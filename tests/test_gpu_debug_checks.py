@@ -7,8 +7,8 @@ loads and output rows; the quantiser's and the append's code and word stores --
 and a failed check reports KVQ_ERR_BOUNDS (7) in the status word instead of
 touching memory.  Representative calls run on both libraries: the debug build's
 status must stay 0 and its results must be byte-identical to the shipped
-library's (the checks change no arithmetic).  This stands in for a memory
-checker, which this GPU pool does not offer.
+library's (the checks change no arithmetic).  It stands in for a memory
+checker, with checks that record a status rather than stop the kernel.
 """
 import contextlib
 
