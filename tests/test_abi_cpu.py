@@ -266,3 +266,13 @@ def test_debug_library_exports_every_declared_symbol(L):
     D.kvq_status_str.restype = ctypes.c_char_p
     assert D.kvq_status_str(7) == b"device index check failed (debug build)"
     assert L.kvq_status_str(7) == D.kvq_status_str(7)
+
+
+def test_decode_refuses_more_sequences_than_its_length_table(L):
+    """4097 sequences: KVQ_ERR_UNSUPPORTED before any launch (the decode kernel's
+    shared-memory length table holds 4096)."""
+    k, hk = _cache([8], B=4097, Tcap=64)
+    v, hv = _cache([8], B=4097, Tcap=64)
+    P = ctypes.byref
+    st = L.kvq_decode_attention(0x10000, P(k), P(v), 0x5000, 8, 0.0, 0x20000, 0, 0x30000, 1 << 30, None, None)
+    assert st == 2

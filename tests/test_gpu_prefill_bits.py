@@ -83,6 +83,7 @@ CASES = [
     ("d64_mixed_noncausal", 85, 2, 4, 2, 64, 384, [4, 8], False, ("full", 7)),
     ("mixed_noncausal_d128", 86, 1, 8, 2, 128, 384, [8, 4], False, None),
     ("int4_mha_d128", 90, 1, 2, 2, 128, 256, [4, 4], True, None),
+    ("max_64_kv_heads_d64", 97, 1, 64, 64, 64, 256, [8, 4] * 32, True, ("causal", 11)),
 ]
 
 

@@ -87,6 +87,10 @@ SMALL = [
     ("d64_int4_gqa2", 15, 2, 8, 4, 64, 256, [31, 255], "4"),
     ("edge_lengths", 16, 9, 8, 1, 128, 192, [0, 1, 31, 33, 63, 64, 65, 127, 192], "8"),
     ("many_sequences", 17, 40, 4, 1, 128, 256, list(np.random.default_rng(0).integers(0, 257, 40)), "mixed"),
+    # at the limits: 4096 sequences (the most the decode's length table holds),
+    # 8 query heads per KV head; and 64 KV heads (the most a cache may have)
+    ("max_4096_sequences", 18, 4096, 8, 1, 64, 64, list(np.random.default_rng(1).integers(0, 65, 4096)), "8"),
+    ("max_64_kv_heads", 19, 2, 64, 64, 128, 128, [128, 70], "mixed"),
 ]
 # GQA ratios 3, 5, 6 and 7 (the MMA's 8 head columns partly unused), both head
 # dims and both bit-widths, with a ragged tail in every case
