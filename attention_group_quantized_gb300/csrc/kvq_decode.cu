@@ -313,9 +313,10 @@ __device__ __forceinline__ void qk_tile(float (&S)[4], const uint32_t (&qa)[D / 
                   qa[2 * grp + 1][0], qa[2 * grp + 1][1]);
       } else {
         const uint32_t w0 = r[2 * gg], w1 = r[2 * gg + 1];
-        mma_16816_z(c, nib_biased(w0), nib_biased(w1), nib_biased(w0 >> 4), nib_biased(w1 >> 4), qa[2 * grp][0],
+        const uint32_t w08 = w0 >> 8, w18 = w1 >> 8;
+        mma_16816_z(c, nib_biased(w0), nib_biased(w1), nib_hi_biased(w0), nib_hi_biased(w1), qa[2 * grp][0],
                     qa[2 * grp][1]);
-        mma_16816(c, nib_biased(w0 >> 8), nib_biased(w1 >> 8), nib_biased(w0 >> 12), nib_biased(w1 >> 12),
+        mma_16816(c, nib_biased(w08), nib_biased(w18), nib_hi_biased(w08), nib_hi_biased(w18),
                   qa[2 * grp + 1][0], qa[2 * grp + 1][1]);
       }
       const float4 sz = kt[grp * 32];   // tokens g and g + 8
@@ -370,9 +371,9 @@ __device__ __forceinline__ void pv_tile(float (&O)[D / 16][4], float (&Z)[2][4],
     } else {
       // matrices of ldmatrix (gi = grp/2): (group 2gi, tok 0-7), (2gi+1, 0-7), (2gi, 8-15), (2gi+1, 8-15)
       const uint32_t lo = rv4[grp >> 1][grp & 1], hi = rv4[grp >> 1][2 + (grp & 1)];
-      mma_16816(O[2 * grp + 0], nib_biased(lo), nib_biased(lo >> 4), nib_biased(hi), nib_biased(hi >> 4), b0, b1);
-      mma_16816(O[2 * grp + 1], nib_biased(lo >> 8), nib_biased(lo >> 12), nib_biased(hi >> 8),
-                nib_biased(hi >> 12), b0, b1);
+      const uint32_t lo8 = lo >> 8, hi8 = hi >> 8;
+      mma_16816(O[2 * grp + 0], nib_biased(lo), nib_hi_biased(lo), nib_biased(hi), nib_hi_biased(hi), b0, b1);
+      mma_16816(O[2 * grp + 1], nib_biased(lo8), nib_hi_biased(lo8), nib_biased(hi8), nib_hi_biased(hi8), b0, b1);
     }
     const uint32_t za = g == grp ? zown.x : 0u;
     const uint32_t zb = g == grp ? zown.y : 0u;

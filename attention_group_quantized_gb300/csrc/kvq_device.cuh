@@ -269,6 +269,20 @@ __device__ __forceinline__ uint32_t bytes13_biased(uint32_t w) { return prmt(w, 
 // nibbles at bits [0,4) and [16,20) of w -> half2(1024 + lo, 1024 + hi)
 __device__ __forceinline__ uint32_t nib_biased(uint32_t w) { return (w & 0x000F000Fu) | 0x64006400u; }
 
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b), *reinterpret_cast<__half2*>(&c));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// The fp16 pair (1024 + n, 1024 + n') of the nibbles at bits 4-7 and 20-23,
+// without a shift: masked in place the word is the pair (1024 + 16 n, ...),
+// and x / 16 + 960 = 1024 + n, every step exact (one FMA on the FMA pipe
+// instead of a shift on the ALU pipe).  nib_hi_biased(w) == nib_biased(w >> 4).
+constexpr uint32_t kHalf2Sixteenth = 0x2C002C00u;   // (1/16, 1/16)
+__device__ __forceinline__ uint32_t nib_hi_biased(uint32_t w) {
+  return hfma2_u32((w & 0x00F000F0u) | 0x64006400u, kHalf2Sixteenth, 0x63806380u /* (960, 960) */);
+}
+
 __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
   __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);

@@ -212,6 +212,8 @@ __device__ __forceinline__ void dequant_chunk(uint32_t dst, int row, int ch0, ui
   constexpr int OC = BITS == 8 ? 2 : 4;
   const uint32_t zb = zero_biased2(word);
   const uint32_t s2 = (word & 0xFFFFu) | (word << 16);
+  // 4-bit high nibbles: c - z = (1024 + 16 c) / 16 - 64 - z in one exact FMA
+  const uint32_t mz = hsub2_u32(0x63806380u /* (960, 960) */, zb);   // -(64 + z), exact
   const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
   uint32_t o[4 * OC];
 #pragma unroll
@@ -222,10 +224,11 @@ __device__ __forceinline__ void dequant_chunk(uint32_t dst, int row, int ch0, ui
       o[2 * i + 1] = hmul2_u32(hsub2_u32(bytes23_biased(wv[i]), zb), s2);
     } else {
       // channels 8i .. 8i + 7 in the order 0,4,1,5,2,6,3,7
+      const uint32_t w8 = wv[i] >> 8;
       o[4 * i + 0] = hmul2_u32(hsub2_u32(nib_biased(wv[i]), zb), s2);
-      o[4 * i + 1] = hmul2_u32(hsub2_u32(nib_biased(wv[i] >> 4), zb), s2);
-      o[4 * i + 2] = hmul2_u32(hsub2_u32(nib_biased(wv[i] >> 8), zb), s2);
-      o[4 * i + 3] = hmul2_u32(hsub2_u32(nib_biased(wv[i] >> 12), zb), s2);
+      o[4 * i + 1] = hmul2_u32(hfma2_u32((wv[i] & 0x00F000F0u) | 0x64006400u, kHalf2Sixteenth, mz), s2);
+      o[4 * i + 2] = hmul2_u32(hsub2_u32(nib_biased(w8), zb), s2);
+      o[4 * i + 3] = hmul2_u32(hfma2_u32((w8 & 0x00F000F0u) | 0x64006400u, kHalf2Sixteenth, mz), s2);
     }
   }
   const int kb = ch0 >> 6, cb = (ch0 & 63) >> 3, sw = row & 7;
