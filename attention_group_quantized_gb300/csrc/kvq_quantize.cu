@@ -505,6 +505,9 @@ template <int D>
 __global__ void __launch_bounds__(kStatThreads, kStatBlocksPerSM) head_stats_kernel(const __grid_constant__ SParams p) {
   constexpr int G = D / 32;
   const int h = blockIdx.y;
+  // the reduction launched after this kernel may be scheduled now; it waits
+  // for this grid's completion before reading the partial sums
+  grid_launch_dependents();
   const int64_t n = static_cast<int64_t>(p.B) * p.T * G;
   // (error, norm) summed in fp32 with Kahan's compensation (sum - comp is the
   // running total), widened to fp64 once for the block's reduction
@@ -557,6 +560,7 @@ __global__ void __launch_bounds__(kStatThreads, kStatBlocksPerSM) head_stats_ker
 // One warp per head: stats[h] = the sum of part[h][0 .. chunks) in a fixed order.
 __global__ void __launch_bounds__(32) head_stats_reduce(const double* part, int chunks, double* stats) {
   const int h = blockIdx.x, lane = threadIdx.x;
+  grid_dependency_wait();   // launched as a dependent of head_stats_kernel
   double e = 0.0, m = 0.0;
   for (int c = lane; c < chunks; c += 32) {
     e += part[(static_cast<int64_t>(h) * chunks + c) * 2];
@@ -595,8 +599,19 @@ cudaError_t launch_head_stats(const HeadStatsArgs& a, cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>(p.chunks), static_cast<unsigned>(a.H));
   if (a.D == 128) head_stats_kernel<128><<<grid, kStatThreads, 0, stream>>>(p);
   else head_stats_kernel<64><<<grid, kStatThreads, 0, stream>>>(p);
-  head_stats_reduce<<<static_cast<unsigned>(a.H), 32, 0, stream>>>(a.part, p.chunks, a.stats);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // the fixed-order sum, launched while the statistics kernel still runs
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.H));
+  cfg.blockDim = dim3(32);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, head_stats_reduce, static_cast<const double*>(a.part), p.chunks, a.stats);
 }
 
 cudaError_t launch_quantize(const QuantizeArgs& a, cudaStream_t stream) {
