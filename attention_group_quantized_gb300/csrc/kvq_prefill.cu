@@ -645,20 +645,37 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_SFULL0 + h], j & 1, p.status, wns));
     if (!ok) break;
     tc::fence_after_sync();
-    // pass 1: row max (three-input max, two chains)
+    // pass 1: row max (three-input max, two chains).  Unmasked tiles keep the
+    // next 32-column chunk's TMEM load in flight while a chunk is reduced
+    // (two register buffers), so only the first load's latency is exposed.
     float mxa = -INFINITY, mxb = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t v[32];
-      tc::ld_32x32b_x32(s_addr + c * 32, v);
-      tc::wait_ld();
-      if (!masked) {
+    if (!masked) {
+      uint32_t va[32], vb[32];
+      auto mx_chunk = [&](const uint32_t (&v)[32]) {
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
           mxa = fmax3(mxa, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
           mxb = fmax3(mxb, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
         }
-      } else {
+      };
+      tc::ld_32x32b_x32(s_addr, va);
+      tc::wait_ld(va);
+      tc::ld_32x32b_x32(s_addr + 32, vb);
+      mx_chunk(va);
+      tc::wait_ld(vb);
+      tc::ld_32x32b_x32(s_addr + 64, va);
+      mx_chunk(vb);
+      tc::wait_ld(va);
+      tc::ld_32x32b_x32(s_addr + 96, vb);
+      mx_chunk(va);
+      tc::wait_ld(vb);
+      mx_chunk(vb);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tc::ld_32x32b_x32(s_addr + c * 32, v);
+        tc::wait_ld(v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) mxa = (c * 32 + i > lim) ? mxa : fmaxf(mxa, __uint_as_float(v[i]));
       }
@@ -675,13 +692,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     // the exponent arguments and the row sum two at a time
     float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
     const float neg_m = -m_use;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t v[32];
-      uint32_t pk[16];
-      tc::ld_32x32b_x32(s_addr + c * 32, v);
-      tc::wait_ld();
-      if (!masked) {
+    if (!masked) {
+      // P of chunk c goes to columns 16c.. (S columns already read); the next
+      // chunk's load is in flight meanwhile, as in pass 1
+      uint32_t va[32], vb[32];
+      auto p_chunk = [&](const uint32_t (&v)[32], int c) {
+        uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
           float x0, x1, x2, x3;
@@ -693,7 +709,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           pk[i / 2] = pack_half2(p0, p1);
           pk[i / 2 + 1] = pack_half2(p2, p3);
         }
-      } else {
+        tc::st_32x32b_x16(s_addr + c * 16, pk);
+      };
+      tc::ld_32x32b_x32(s_addr, va);
+      tc::wait_ld(va);
+      tc::ld_32x32b_x32(s_addr + 32, vb);
+      p_chunk(va, 0);
+      tc::wait_ld(vb);
+      tc::ld_32x32b_x32(s_addr + 64, va);
+      p_chunk(vb, 1);
+      tc::wait_ld(va);
+      tc::ld_32x32b_x32(s_addr + 96, vb);
+      p_chunk(va, 2);
+      tc::wait_ld(vb);
+      p_chunk(vb, 3);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        uint32_t pk[16];
+        tc::ld_32x32b_x32(s_addr + c * 32, v);
+        tc::wait_ld(v);
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           const float p0 = (c * 32 + i > lim) ? 0.0f : fast_exp2(fmaf(__uint_as_float(v[i]), sl2, neg_m));
@@ -701,8 +737,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           fadd2(s0, s1, p0, p1);
           pk[i / 2] = pack_half2(p0, p1);
         }
+        tc::st_32x32b_x16(s_addr + c * 16, pk);
       }
-      tc::st_32x32b_x16(s_addr + c * 16, pk);
     }
     const float psum = (s0 + s1) + (s2 + s3);
     l_run = l_run * alpha + psum;
