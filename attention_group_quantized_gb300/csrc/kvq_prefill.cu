@@ -90,7 +90,8 @@ struct PParams {
 // barriers
 enum {
   B_QFULL = 0, B_QREADY, B_KFULL0, B_KFULL1, B_VFULL0, B_VFULL1, B_KVEMPTY0, B_KVEMPTY1,
-  B_SFULL0, B_SFULL1, B_PFULL0, B_PFULL1, B_ORDY0, B_ORDY1, B_MMADONE, B_TURN0, B_TURN1, B_EXIT, B_COUNT
+  B_SFULL0, B_SFULL1, B_PHALF0, B_PHALF1, B_PFULL0, B_PFULL1, B_ORDY0, B_ORDY1, B_MMADONE, B_TURN0, B_TURN1,
+  B_EXIT, B_COUNT
 };
 // Every warp but warp 0 arrives once on B_EXIT when it is done with shared
 // memory, TMEM and its asynchronous operations, on the normal path and after
@@ -402,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     mbar_init(&bar[B_VFULL0], 4); mbar_init(&bar[B_VFULL1], 4);
     mbar_init(&bar[B_KVEMPTY0], nh); mbar_init(&bar[B_KVEMPTY1], nh);
     mbar_init(&bar[B_SFULL0], 1); mbar_init(&bar[B_SFULL1], 1);
+    mbar_init(&bar[B_PHALF0], 4); mbar_init(&bar[B_PHALF1], 4);
     mbar_init(&bar[B_PFULL0], 4); mbar_init(&bar[B_PFULL1], 4);
     mbar_init(&bar[B_ORDY0], 1); mbar_init(&bar[B_ORDY1], 1);
     mbar_init(&bar[B_MMADONE], nh);
@@ -497,14 +499,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       }
       tc::commit(&bar[B_SFULL0 + h]);
     };
-    // O_h (+)= P_h V over the V tile in stage st (elected lane)
-    auto issue_pv = [&](int st, bool first) {
+    // O_h (+)= P_h V over half `hf` of the V tile in stage st, keys
+    // 64 hf .. 64 hf + 63 (elected lane); P's first half is written first
+    auto issue_pv = [&](int st, bool first, int hf) {
       const uint32_t vs = v_base + st * L::kQBytes;
-      const uint64_t v0 = tc::smem_desc_sw128(vs, kT * 128, 1024);
-      if (first) tc::mma_ts<false>(d_o, d_s, v0, id_pv);
-      else tc::mma_ts<true>(d_o, d_s, v0, id_pv);
+      if (hf == 0) {
+        const uint64_t v0 = tc::smem_desc_sw128(vs, kT * 128, 1024);
+        if (first) tc::mma_ts<false>(d_o, d_s, v0, id_pv);
+        else tc::mma_ts<true>(d_o, d_s, v0, id_pv);
+      }
 #pragma unroll
-      for (int s = 1; s < kT / 16; ++s)
+      for (int s = hf == 0 ? 1 : kT / 32; s < (hf + 1) * (kT / 32); ++s)
         tc::mma_ts<true>(d_o, d_s + s * 8, tc::smem_desc_sw128(vs + s * 2048, kT * 128, 1024), id_pv);
     };
     // Turns: block b = -1 is Q.K^T of tile 0, block b >= 0 is P.V of tile b
@@ -530,11 +535,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
     for (int j = 0; j < n_kept && ok; ++j) {
       const int st = j & 1;
-      ok = wait_all(B_VFULL0 + st, (j >> 1) & 1) && wait_all(B_PFULL0 + h, j & 1) && take_turn(j);
+      ok = wait_all(B_VFULL0 + st, (j >> 1) & 1) && wait_all(B_PHALF0 + h, j & 1) && take_turn(j);
+      if (!ok) break;
+      tc::fence_after_sync();
+      if (tc::elect_one()) issue_pv(st, j == 0, 0);   // while the softmax writes P's second half
+      __syncwarp();
+      ok = wait_all(B_PFULL0 + h, j & 1);
       if (!ok) break;
       tc::fence_after_sync();
       if (tc::elect_one()) {
-        issue_pv(st, j == 0);
+        issue_pv(st, false, 1);
         tc::commit(&bar[B_ORDY0 + h]);
         // this head is done with the stage: its Q.K^T of tile j was issued
         // before this P.V (an issuer's products complete in issue order)
@@ -687,6 +697,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       alpha = (m_run == -INFINITY) ? 0.0f : fast_exp2(m_run - m_use);
       m_run = m_use;
     }
+    // rescale O (rare) before any P.V of this tile is issued: the previous
+    // P.V has finished (it was issued before the Q.K^T that made this S, and
+    // an issuer's products complete in order), so the wait returns at once
+    if (__any_sync(0xffffffffu, alpha != 1.0f) && j > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_ORDY0 + h], (j - 1) & 1, p.status, wns));
+      if (!ok) break;
+      tc::fence_after_sync();
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tc::ld_32x32b_x32(o_addr + c * 32, v);
+        tc::wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+        tc::st_32x32b_x32(o_addr + c * 32, v);
+      }
+    }
+    // P's first half (keys 0-63, and any rescaled O) is stored: the issuer
+    // may start this tile's P.V on it while the second half is computed
+    auto p_half = [&]() {
+      tc::wait_st();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[B_PHALF0 + h]);
+    };
     // pass 2: P = 2^(S*scale_log2 - m) as fp16 pairs, written over the part of S
     // already read (columns 16c.. of P after S columns 32c.. were loaded);
     // the exponent arguments and the row sum two at a time
@@ -718,6 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       tc::wait_ld(vb);
       tc::ld_32x32b_x32(s_addr + 64, va);
       p_chunk(vb, 1);
+      p_half();
       tc::wait_ld(va);
       tc::ld_32x32b_x32(s_addr + 96, vb);
       p_chunk(va, 2);
@@ -738,25 +774,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           pk[i / 2] = pack_half2(p0, p1);
         }
         tc::st_32x32b_x16(s_addr + c * 16, pk);
+        if (c == 1) p_half();
       }
     }
     const float psum = (s0 + s1) + (s2 + s3);
     l_run = l_run * alpha + psum;
-    // rescale O (rare): needs the previous P.V product finished
-    if (__any_sync(0xffffffffu, alpha != 1.0f) && j > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar[B_ORDY0 + h], (j - 1) & 1, p.status, wns));
-      if (!ok) break;
-      tc::fence_after_sync();
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tc::ld_32x32b_x32(o_addr + c * 32, v);
-        tc::wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-        tc::st_32x32b_x32(o_addr + c * 32, v);
-      }
-    }
     tc::wait_st();
     tc::fence_before_sync();
     __syncwarp();
