@@ -17,9 +17,11 @@
 // heads' products:
 //   warp 0      allocates TMEM, loads the bf16 Q tiles by TMA, and frees TMEM
 //               once every other role is done;
-//   warps 1, 2  one thread each issues head h = warp - 1's tcgen05.mma:
+//   warps 1, 2  one elected lane each issues head h = warp - 1's tcgen05.mma:
 //                 S_h = Q_h K^T (A, B from shared memory) and
-//                 O_h += P_h V   (P from TMEM, V from shared memory);
+//                 O_h += P_h V   (P from TMEM, V from shared memory), its
+//                 first two products (keys 0-31) as soon as the softmax has
+//                 stored that chunk of P, the rest once all of P is stored;
 //               the heads' products touch disjoint TMEM columns, so each
 //               head's chain (S_h, softmax, P_h V, next S_h) runs on its own
 //               and the two take turns: head 0's block (P_0 V, next S_0),
@@ -37,10 +39,12 @@
 //               loads cover whole contiguous rows and every 8-lane phase of a
 //               16-byte store covers all 32 banks;
 //   warps 8-11  softmax of head 0, warps 12-15 softmax of head 1: one thread
-//               per query row reads its S row from TMEM, applies the causal
-//               rule on the diagonal tile (causal only), updates (max, sum) in
-//               the log2 domain with two-wide fp32 arithmetic, writes P (fp16)
-//               back over S, and at the end scales O by 1 / sum and stores it.
+//               per query row reads its S row from TMEM (two passes of four
+//               32-column loads, the next load in flight while a chunk is
+//               worked on), applies the causal rule on the diagonal tile
+//               (causal only), updates (max, sum) in the log2 domain with
+//               two-wide fp32 arithmetic, writes P (fp16) back over S, and at
+//               the end scales O by 1 / sum and stores it.
 // TMEM (512 columns): S_0 [0,128) O_0 [128,128+D) S_1 [256,384) O_1 [384,384+D).
 // The running max is only moved (and O rescaled) when it grows by more than
 // 2^8, so P stays <= 256 and rescales are rare; the final division uses the
@@ -90,7 +94,7 @@ struct PParams {
 // barriers
 enum {
   B_QFULL = 0, B_QREADY, B_KFULL0, B_KFULL1, B_VFULL0, B_VFULL1, B_KVEMPTY0, B_KVEMPTY1,
-  B_SFULL0, B_SFULL1, B_PHALF0, B_PHALF1, B_PFULL0, B_PFULL1, B_ORDY0, B_ORDY1, B_MMADONE, B_TURN0, B_TURN1,
+  B_SFULL0, B_SFULL1, B_PFIRST0, B_PFIRST1, B_PFULL0, B_PFULL1, B_ORDY0, B_ORDY1, B_MMADONE, B_TURN0, B_TURN1,
   B_EXIT, B_COUNT
 };
 // Every warp but warp 0 arrives once on B_EXIT when it is done with shared
@@ -403,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     mbar_init(&bar[B_VFULL0], 4); mbar_init(&bar[B_VFULL1], 4);
     mbar_init(&bar[B_KVEMPTY0], nh); mbar_init(&bar[B_KVEMPTY1], nh);
     mbar_init(&bar[B_SFULL0], 1); mbar_init(&bar[B_SFULL1], 1);
-    mbar_init(&bar[B_PHALF0], 4); mbar_init(&bar[B_PHALF1], 4);
+    mbar_init(&bar[B_PFIRST0], 4); mbar_init(&bar[B_PFIRST1], 4);
     mbar_init(&bar[B_PFULL0], 4); mbar_init(&bar[B_PFULL1], 4);
     mbar_init(&bar[B_ORDY0], 1); mbar_init(&bar[B_ORDY1], 1);
     mbar_init(&bar[B_MMADONE], nh);
@@ -499,8 +503,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       }
       tc::commit(&bar[B_SFULL0 + h]);
     };
-    // O_h (+)= P_h V over half `hf` of the V tile in stage st, keys
-    // 64 hf .. 64 hf + 63 (elected lane); P's first half is written first
+    // O_h (+)= P_h V over part `hf` of the V tile in stage st (elected lane):
+    // keys 0-31, as soon as the softmax has stored that much of P, then keys
+    // 32-127
     auto issue_pv = [&](int st, bool first, int hf) {
       const uint32_t vs = v_base + st * L::kQBytes;
       if (hf == 0) {
@@ -509,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         else tc::mma_ts<true>(d_o, d_s, v0, id_pv);
       }
 #pragma unroll
-      for (int s = hf == 0 ? 1 : kT / 32; s < (hf + 1) * (kT / 32); ++s)
+      for (int s = hf == 0 ? 1 : 2; s < (hf == 0 ? 2 : kT / 16); ++s)
         tc::mma_ts<true>(d_o, d_s + s * 8, tc::smem_desc_sw128(vs + s * 2048, kT * 128, 1024), id_pv);
     };
     // Turns: block b = -1 is Q.K^T of tile 0, block b >= 0 is P.V of tile b
@@ -535,10 +540,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     }
     for (int j = 0; j < n_kept && ok; ++j) {
       const int st = j & 1;
-      ok = wait_all(B_VFULL0 + st, (j >> 1) & 1) && wait_all(B_PHALF0 + h, j & 1) && take_turn(j);
+      ok = wait_all(B_VFULL0 + st, (j >> 1) & 1) && wait_all(B_PFIRST0 + h, j & 1) && take_turn(j);
       if (!ok) break;
       tc::fence_after_sync();
-      if (tc::elect_one()) issue_pv(st, j == 0, 0);   // while the softmax writes P's second half
+      if (tc::elect_one()) issue_pv(st, j == 0, 0);   // while the softmax writes the rest of P
       __syncwarp();
       ok = wait_all(B_PFULL0 + h, j & 1);
       if (!ok) break;
@@ -714,13 +719,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         tc::st_32x32b_x32(o_addr + c * 32, v);
       }
     }
-    // P's first half (keys 0-63, and any rescaled O) is stored: the issuer
-    // may start this tile's P.V on it while the second half is computed
-    auto p_half = [&]() {
+    // P's first chunk (keys 0-31, and any rescaled O) is stored: the issuer
+    // may start this tile's P.V on it while the rest is computed
+    auto p_first = [&]() {
       tc::wait_st();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[B_PHALF0 + h]);
+      if (lane == 0) mbar_arrive(&bar[B_PFIRST0 + h]);
     };
     // pass 2: P = 2^(S*scale_log2 - m) as fp16 pairs, written over the part of S
     // already read (columns 16c.. of P after S columns 32c.. were loaded);
@@ -750,10 +755,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       tc::wait_ld(va);
       tc::ld_32x32b_x32(s_addr + 32, vb);
       p_chunk(va, 0);
+      p_first();
       tc::wait_ld(vb);
       tc::ld_32x32b_x32(s_addr + 64, va);
       p_chunk(vb, 1);
-      p_half();
       tc::wait_ld(va);
       tc::ld_32x32b_x32(s_addr + 96, vb);
       p_chunk(va, 2);
@@ -774,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
           pk[i / 2] = pack_half2(p0, p1);
         }
         tc::st_32x32b_x16(s_addr + c * 16, pk);
-        if (c == 1) p_half();
+        if (c == 0) p_first();
       }
     }
     const float psum = (s0 + s1) + (s2 + s3);
