@@ -725,20 +725,32 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
   // start early.
   grid_dependency_wait();
   grid_launch_dependents();
-  for (int b = tid; b < B; b += blockDim.x) {
+  // The lengths, clamped into the cache, and per-sequence tile counts with
+  // their prefix sums.  Up to 32 sequences, warp 0 alone loads and scans them
+  // (one block barrier after the wait); more are loaded by all threads first.
+  auto load_len = [&](int b) {
     int L0 = p.seq_lens[b];
     if (L0 < 0 || L0 > p.Tcap) {
       report(p.status, KVQ_ERR_INVALID_ARG);
       L0 = L0 < 0 ? 0 : p.Tcap;
     }
-    lens[b] = L0;
+    return L0;
+  };
+  const bool small_b = B <= 32;
+  if (!small_b) {
+    for (int b = tid; b < B; b += blockDim.x) lens[b] = load_len(b);
+    __syncthreads();
   }
-  __syncthreads();
-  if (w == 0) {  // per-sequence tile counts and their prefix sums
+  if (w == 0) {
     int carry = 0;
     for (int b0 = 0; b0 < B; b0 += 32) {
       const int b = b0 + lane;
-      int n = b < B ? (lens[b] + kTile - 1) / kTile : 0;
+      int len = 0;
+      if (b < B) {
+        len = small_b ? load_len(b) : lens[b];
+        if (small_b) lens[b] = len;
+      }
+      int n = (len + kTile - 1) / kTile;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int v = __shfl_up_sync(0xffffffffu, n, o);
@@ -756,8 +768,14 @@ __global__ void __launch_bounds__(kThreads, KVQ_DECODE_MIN_BLOCKS) decode_split_
   // least one tile, and a segment's pieces are those of CTAs c0 .. c1
   const int C = N < p.num_ctas ? static_cast<int>(N) : p.num_ctas;
   const bool in_split = static_cast<int>(blockIdx.x) < C;
-  const int64_t f0 = in_split ? N * blockIdx.x / C : 0;
-  const int64_t f1 = in_split ? N * (blockIdx.x + 1) / C : 0;
+  // N c / C in 32 bits when the product fits (a 64-bit division is a long
+  // software sequence on this critical path)
+  auto cut = [&](int c) -> int64_t {
+    const int64_t nc = N * c;
+    return nc <= 0xFFFFFFFFll ? static_cast<int64_t>(static_cast<uint32_t>(nc) / static_cast<uint32_t>(C)) : nc / C;
+  };
+  const int64_t f0 = in_split ? cut(blockIdx.x) : 0;
+  const int64_t f1 = in_split ? cut(blockIdx.x + 1) : 0;
   const int ntiles = static_cast<int>(f1 - f0);
   if (ntiles <= 0) {
     if (w == 0) zero_empty_rows<D>(p, lens, lane);

@@ -39,8 +39,15 @@ __device__ __forceinline__ Cursor locate(int64_t f, const int32_t* pre, int B, i
   const int64_t off = f - static_cast<int64_t>(Hkv) * pre[b];
   Cursor c;
   c.b = b;
-  c.kvh = static_cast<int>(off / n);
-  c.i = static_cast<int>(off % n);
+  // off < Hkv * n: a 32-bit division unless that exceeds 32 bits
+  if (off <= 0xFFFFFFFFll) {
+    const uint32_t o32 = static_cast<uint32_t>(off), q = o32 / static_cast<uint32_t>(n);
+    c.kvh = static_cast<int>(q);
+    c.i = static_cast<int>(o32 - q * static_cast<uint32_t>(n));
+  } else {
+    c.kvh = static_cast<int>(off / n);
+    c.i = static_cast<int>(off % n);
+  }
   return c;
 }
 
