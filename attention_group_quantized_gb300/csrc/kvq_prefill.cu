@@ -433,8 +433,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 
   // number of kept key tiles (identical in every role)
   const int kt_end = key_tile_end(p, qt, Ls);
-  int n_kept = 0;
-  for (int kt = 0; kt < kt_end; ++kt) n_kept += tile_kept(p, qt, kt) ? 1 : 0;
+  int n_kept = kt_end;
+  if (p.tile_mask != nullptr) {
+    // 16 mask bytes per load where the row allows it; the diagonal counts as
+    // kept whatever its byte says
+    const uint8_t* row = p.tile_mask + static_cast<size_t>(qt) * p.nT;
+    n_kept = 0;
+    int kt = 0;
+    if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
+      for (; kt + 16 <= kt_end; kt += 16) {
+        const uint4 m4 = *reinterpret_cast<const uint4*>(row + kt);
+        const uint32_t w4[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)   // bytes that are not zero: their top bit after adding 0x7F to the low seven
+          n_kept += __popc((((w4[i] & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | w4[i]) & 0x80808080u);
+      }
+    }
+    for (; kt < kt_end; ++kt) n_kept += row[kt] != 0 ? 1 : 0;
+    if (qt < kt_end && row[qt] == 0) ++n_kept;
+  }
   const uint64_t wns = p.wait_ns;
 
   if (warp < 4) {
