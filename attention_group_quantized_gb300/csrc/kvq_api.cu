@@ -1,6 +1,8 @@
 // kvq_api.cu -- the C ABI of libkvq: argument validation, cache layout,
-// tensor-map encoding and dispatch to the kernels.  Nothing here allocates
-// device memory or synchronises; every launch goes to the caller's stream.
+// tensor-map encoding and dispatch to the kernels.  Nothing here synchronises
+// or allocates device memory (apart from the driver's own resources for the
+// graphs that replay repeated host-buffer decode steps, at most 16 per
+// process); every launch goes to the caller's stream.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -345,6 +347,105 @@ static kvq_status decode_step_impl(const void* q, const void* q_src, size_t q_by
                      dev_status, stream);
 }
 
+// ---- repeated decode steps replayed from a CUDA graph ----
+// A serving loop issues the same step every token: the same buffers, caches
+// and scalars, only the contents (lengths, new rows, cache codes) change, and
+// the kernels read those at run time.  The second call with a given key
+// captures the step's launches on an internal stream into a graph; every
+// later call with that key launches the graph (one launch call, no
+// tensor-map encoding).  The key holds every value the launches are built
+// from: the device, each pointer and size argument, both caches' fields and
+// their per-head bit widths.  At most kStepGraphs graphs are kept, for the
+// life of the process; further keys run their launches directly.
+namespace {
+
+constexpr size_t kStepGraphs = 16;
+constexpr size_t kStepSeen = 32;
+
+struct StepGraph {
+  std::vector<uint8_t> key;
+  cudaGraphExec_t exec;
+};
+
+std::mutex g_step_mu;
+std::vector<StepGraph> g_step_graphs;
+std::vector<std::vector<uint8_t>> g_step_seen;   // keys met once, oldest first
+cudaStream_t g_capture_stream[64] = {};
+
+void key_put(std::vector<uint8_t>& key, const void* p, size_t n) {
+  const uint8_t* b = static_cast<const uint8_t*>(p);
+  key.insert(key.end(), b, b + n);
+}
+template <class T>
+void key_val(std::vector<uint8_t>& key, T v) {
+  key_put(key, &v, sizeof(v));
+}
+void key_cache(std::vector<uint8_t>& key, const kvq_cache* c) {
+  key_val(key, c->codes);
+  key_val(key, c->sz);
+  key_val(key, c->head_bits);
+  key_val(key, c->B);
+  key_val(key, c->Hkv);
+  key_val(key, c->Tcap);
+  key_val(key, c->D);
+  if (c->head_bits != nullptr && c->Hkv > 0 && c->Hkv <= KVQ_MAX_HKV) key_put(key, c->head_bits, c->Hkv);
+}
+
+// Runs `launch(stream)` directly, or replays it from its graph (see above).
+// A stream that is itself being captured gets the launches directly.
+template <class F>
+kvq_status launch_or_replay(std::vector<uint8_t>& key, cudaStream_t stream, F&& launch) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  int dev = -1;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone ||
+      cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return launch(stream);
+  }
+  key_val(key, dev);
+  std::lock_guard<std::mutex> lock(g_step_mu);
+  for (const StepGraph& g : g_step_graphs)
+    if (g.key == key) return cudaGraphLaunch(g.exec, stream) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+  auto seen = std::find(g_step_seen.begin(), g_step_seen.end(), key);
+  if (seen == g_step_seen.end() || g_step_graphs.size() >= kStepGraphs) {
+    // first time (or no room): launch directly and remember the key
+    if (seen == g_step_seen.end() && g_step_graphs.size() < kStepGraphs) {
+      if (g_step_seen.size() >= kStepSeen) g_step_seen.erase(g_step_seen.begin());
+      g_step_seen.push_back(key);
+    }
+    return launch(stream);
+  }
+  g_step_seen.erase(seen);
+  if (g_capture_stream[dev] == nullptr &&
+      cudaStreamCreateWithFlags(&g_capture_stream[dev], cudaStreamNonBlocking) != cudaSuccess) {
+    g_capture_stream[dev] = nullptr;
+    cudaGetLastError();
+    return launch(stream);
+  }
+  cudaStream_t cap = g_capture_stream[dev];
+  if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaGetLastError();
+    return launch(stream);
+  }
+  const kvq_status r = launch(cap);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(cap, &graph);
+  cudaGraphExec_t exec = nullptr;
+  const bool made = r == KVQ_OK && ec == cudaSuccess && graph != nullptr &&
+                    cudaGraphInstantiate(&exec, graph, 0) == cudaSuccess;
+  if (graph != nullptr) cudaGraphDestroy(graph);
+  if (!made) {
+    cudaGetLastError();
+    // a rejected argument is rejected again without launching; anything
+    // else runs directly
+    return r != KVQ_OK ? r : launch(stream);
+  }
+  g_step_graphs.push_back(StepGraph{key, exec});
+  return cudaGraphLaunch(exec, stream) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+}  // namespace
+
 extern "C" {
 
 kvq_status kvq_decode_step(const void* q, const void* k_new, const void* v_new, const kvq_cache* k,
@@ -412,9 +513,27 @@ kvq_status kvq_decode_step_host(const void* q_host, const void* k_new_host, cons
   void* p_k = p_q ? pinned_device_view(k_new_host) : nullptr;
   void* p_v = p_k ? pinned_device_view(v_new_host) : nullptr;
   void* p_o = p_v ? pinned_device_view(out_host) : nullptr;
-  if (p_o != nullptr && aligned16(p_q) && aligned16(p_k) && aligned16(p_v) && aligned16(p_o))
-    return decode_step_impl(d_q, p_q, qb, p_k, p_v, k, v, nullptr, seq_lens, Hq, softmax_scale, p_o, out_dtype,
-                            workspace, workspace_bytes, dev_status, stream);
+  if (p_o != nullptr && aligned16(p_q) && aligned16(p_k) && aligned16(p_v) && aligned16(p_o)) {
+    if (v == nullptr) return KVQ_ERR_INVALID_ARG;
+    std::vector<uint8_t> key;
+    key.reserve(192);
+    for (const void* ptr : {static_cast<const void*>(d_q), static_cast<const void*>(p_q),
+                            static_cast<const void*>(p_k), static_cast<const void*>(p_v),
+                            static_cast<const void*>(p_o), static_cast<const void*>(seq_lens), static_cast<const void*>(workspace),
+                            static_cast<const void*>(dev_status)})
+      key_val(key, ptr);
+    key_val(key, qb);
+    key_val(key, workspace_bytes);
+    key_val(key, Hq);
+    key_val(key, softmax_scale);
+    key_val(key, out_dtype);
+    key_cache(key, k);
+    key_cache(key, v);
+    return launch_or_replay(key, s, [&](cudaStream_t ls) {
+      return decode_step_impl(d_q, p_q, qb, p_k, p_v, k, v, nullptr, seq_lens, Hq, softmax_scale, p_o, out_dtype,
+                              workspace, workspace_bytes, dev_status, ls);
+    });
+  }
   // pageable memory: asynchronous copies through the staging buffer
   if (cudaMemcpyAsync(d_q, q_host, qb, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(d_k, k_new_host, kvb, cudaMemcpyHostToDevice, s) != cudaSuccess ||

@@ -342,6 +342,15 @@ KVQ_API size_t kvq_decode_step_staging_bytes(int32_t B, int32_t Hq, int32_t Hkv,
  * `stream` and the call returns once it is enqueued; out_host holds the
  * result after the caller synchronises the stream, and the host inputs and
  * `staging` must stay untouched until then.
+ * Repeated steps (pinned buffers): the second call whose arguments all match
+ * an earlier call's -- every pointer and size, Hq, softmax_scale, out_dtype,
+ * both caches' fields and per-head bit widths, the current device -- captures
+ * the two launches into a CUDA graph on an internal stream, and every later
+ * matching call launches that graph on `stream` (one launch call, no
+ * tensor-map encoding).  The kernels read the lengths, the new rows and the
+ * caches at run time, so those may change between calls.  Up to 16 graphs
+ * are kept for the life of the process; other steps launch directly, and so
+ * does any call on a stream that is being captured.
  * staging: device scratch of >= kvq_decode_step_staging_bytes(B, Hq, Hkv, D,
  * out_dtype) bytes, 256-byte aligned.  The caches, seq_lens, workspace and
  * dev_status are device memory as in kvq_decode_step.

@@ -228,3 +228,70 @@ def test_decode_step_host_prepared_call_matches_the_function():
         _check(inp, kc, vc, h_out.numpy(), 0)
         outs.append(h_out.numpy().copy())
     assert np.array_equal(outs[0], outs[1])
+
+
+def test_decode_step_host_repeated_steps_replay_fresh_contents():
+    """A serving loop: the same pinned buffers, lengths tensor and caches every
+    step, with new contents each time.  From the third identical call on, the
+    library launches a graph captured on the second; every step must still
+    see that step's lengths, query and new rows.  Two cache pairs take turns,
+    so two graphs are kept side by side.  Each output is checked against the
+    oracle and against kvq_decode_step on device copies of the same inputs
+    (byte for byte: the same kernels on the same data)."""
+    kvq = _kvq()
+    n_steps = 6
+    T_final = [90, 131, 8]
+    pairs = []
+    for seed in (41, 42):
+        inp = W.make_decode(f"step_replay_{seed}", seed, 3, 8, 2, 128, 192, lens=T_final, bits="mixed",
+                            outliers_per_head=2, outlier_head_mult=8.0)
+        start = [L - n_steps for L in T_final]
+        pre_k, pre_v = inp.k.copy(), inp.v.copy()
+        for b, L0 in enumerate(start):
+            pre_k[b, :, L0:] = 0
+            pre_v[b, :, L0:] = 0
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        caches = []
+        for copy in range(2):   # [0]: the host-buffer step, [1]: the device-buffer reference
+            kc = kvq.empty_cache(inp.head_bits, inp.B, inp.Tcap, inp.D)
+            vc = kvq.empty_cache(inp.head_bits, inp.B, inp.Tcap, inp.D)
+            kvq.quantize(U.to_dev_bf16(pre_k), kc, 0, st)
+            kvq.quantize(U.to_dev_bf16(pre_v), vc, 0, st)
+            caches.append((kc, vc))
+        bf = lambda shape: torch.zeros(shape, dtype=torch.bfloat16).pin_memory()
+        h_q, h_k, h_v = bf((inp.B, inp.Hq, inp.D)), bf((inp.B, inp.Hkv, inp.D)), bf((inp.B, inp.Hkv, inp.D))
+        h_out = torch.zeros((inp.B, inp.Hq, inp.D), dtype=torch.float32).pin_memory()
+        sl = torch.zeros(inp.B, dtype=torch.int32, device="cuda")
+        call = kvq.DecodeStepHost(h_q, h_k, h_v, sl, h_out, inp.softmax_scale, status=st)
+        deq_k = U.oracle_quantize(inp.k, inp.head_bits)[3]
+        deq_v = U.oracle_quantize(inp.v, inp.head_bits)[3]
+        pairs.append(dict(inp=inp, start=start, caches=caches, h=(h_q, h_k, h_v, h_out), sl=sl, call=call,
+                          st=st, deq=(deq_k, deq_v), rng=np.random.default_rng(seed + 100)))
+    as_bf16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    for s in range(n_steps):
+        for pi, P in enumerate(pairs):
+            inp = P["inp"]
+            B = inp.B
+            lens = np.array([L0 + s + 1 for L0 in P["start"]], dtype=np.int32)
+            q = W._draw_bf16(P["rng"], (B, inp.Hq, inp.D))
+            k_new = np.stack([inp.k[b, :, lens[b] - 1] for b in range(B)])
+            v_new = np.stack([inp.v[b, :, lens[b] - 1] for b in range(B)])
+            h_q, h_k, h_v, h_out = P["h"]
+            h_q.copy_(as_bf16(q))
+            h_k.copy_(as_bf16(k_new))
+            h_v.copy_(as_bf16(v_new))
+            h_out.fill_(7.0)
+            P["sl"].copy_(torch.from_numpy(lens))
+            P["call"].run(*P["caches"][0])
+            ref_out = kvq.decode_step(U.to_dev_bf16(q), U.to_dev_bf16(k_new), U.to_dev_bf16(v_new),
+                                      *P["caches"][1], torch.from_numpy(lens).cuda(), inp.softmax_scale,
+                                      status=P["st"])
+            torch.cuda.synchronize()
+            assert int(P["st"].item()) == 0, (s, pi)
+            got = h_out.numpy().copy()
+            assert np.array_equal(got, ref_out.cpu().numpy()), (s, pi)
+            ref = O.decode_attention(q, P["deq"][0], P["deq"][1], lens, inp.softmax_scale)
+            U.assert_close(got, ref, f"replayed step {s} pair {pi}")
+    for P in pairs:
+        kc, vc = P["caches"][0]
+        assert torch.equal(kc.codes, P["caches"][1][0].codes) and torch.equal(vc.sz, P["caches"][1][1].sz)
