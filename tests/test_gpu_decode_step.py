@@ -295,3 +295,114 @@ def test_decode_step_host_repeated_steps_replay_fresh_contents():
     for P in pairs:
         kc, vc = P["caches"][0]
         assert torch.equal(kc.codes, P["caches"][1][0].codes) and torch.equal(vc.sz, P["caches"][1][1].sz)
+
+
+def _as_bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+
+
+def _host_step_buffers(inp):
+    bf = lambda shape: torch.zeros(shape, dtype=torch.bfloat16).pin_memory()
+    h_q, h_k, h_v = bf((inp.B, inp.Hq, inp.D)), bf((inp.B, inp.Hkv, inp.D)), bf((inp.B, inp.Hkv, inp.D))
+    h_out = torch.zeros((inp.B, inp.Hq, inp.D), dtype=torch.float32).pin_memory()
+    return h_q, h_k, h_v, h_out
+
+
+def test_decode_step_host_replay_follows_bit_widths_changed_in_place():
+    """The cache's per-head bit widths are part of what a replayed step was
+    built from: after the widths change in place (same host array, same
+    buffers, re-quantised contents) the next calls must use the new layout."""
+    kvq = _kvq()
+    lens = [100, 37]
+    inp = W.make_decode("step_rebits", 43, 2, 8, 2, 128, 128, lens=lens, bits="8",
+                        outliers_per_head=2, outlier_head_mult=8.0)
+    kc = kvq.empty_cache([8, 8], inp.B, inp.Tcap, inp.D)
+    vc = kvq.empty_cache([8, 8], inp.B, inp.Tcap, inp.D)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    h_q, h_k, h_v, h_out = _host_step_buffers(inp)
+    sl = torch.from_numpy(np.asarray(lens, np.int32)).cuda()
+    call = kvq.DecodeStepHost(h_q, h_k, h_v, sl, h_out, inp.softmax_scale, status=st)
+    k_new = np.stack([inp.k[b, :, lens[b] - 1] for b in range(inp.B)])
+    v_new = np.stack([inp.v[b, :, lens[b] - 1] for b in range(inp.B)])
+    h_q.copy_(_as_bf16(inp.q)); h_k.copy_(_as_bf16(k_new)); h_v.copy_(_as_bf16(v_new))
+    for bits in ([8, 8], [8, 4]):
+        kc.head_bits[:] = bits
+        vc.head_bits[:] = bits
+        hb = np.asarray(bits, np.int8)
+        kvq.quantize(U.to_dev_bf16(inp.k), kc, 0, st)
+        kvq.quantize(U.to_dev_bf16(inp.v), vc, 0, st)
+        deq_k = U.oracle_quantize(inp.k, hb)[3]
+        deq_v = U.oracle_quantize(inp.v, hb)[3]
+        ref = O.decode_attention(inp.q, deq_k, deq_v, np.asarray(lens, np.int32), inp.softmax_scale)
+        for s in range(4):   # direct, captured, then replayed
+            h_out.fill_(7.0)
+            call.run(kc, vc)
+            torch.cuda.synchronize()
+            assert int(st.item()) == 0, (bits, s)
+            U.assert_close(h_out.numpy().copy(), ref, f"bits {bits} call {s}")
+
+
+def test_decode_step_host_inside_a_captured_graph():
+    """A call on a stream that is itself being captured launches its kernels
+    into that capture (the library keeps no graph of its own for it); the
+    caller's graph then replays the step with each step's contents."""
+    kvq = _kvq()
+    n_steps = 3
+    T_final = [66, 20]
+    inp = W.make_decode("step_in_graph", 44, 2, 8, 2, 128, 128, lens=T_final, bits="mixed",
+                        outliers_per_head=2, outlier_head_mult=8.0)
+    start = [L - n_steps for L in T_final]
+    pre_k, pre_v = inp.k.copy(), inp.v.copy()
+    for b, L0 in enumerate(start):
+        pre_k[b, :, L0:] = 0
+        pre_v[b, :, L0:] = 0
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    caches = []
+    for _ in range(2):   # [0]: replayed through the caller's graph, [1]: kvq_decode_step reference
+        kc = kvq.empty_cache(inp.head_bits, inp.B, inp.Tcap, inp.D)
+        vc = kvq.empty_cache(inp.head_bits, inp.B, inp.Tcap, inp.D)
+        kvq.quantize(U.to_dev_bf16(pre_k), kc, 0, st)
+        kvq.quantize(U.to_dev_bf16(pre_v), vc, 0, st)
+        caches.append((kc, vc))
+    torch.cuda.synchronize()
+    h_q, h_k, h_v, h_out = _host_step_buffers(inp)
+    sl = torch.zeros(inp.B, dtype=torch.int32, device="cuda")
+    cap = torch.cuda.Stream()
+    call = kvq.DecodeStepHost(h_q, h_k, h_v, sl, h_out, inp.softmax_scale, status=st, stream=cap)
+    rng = np.random.default_rng(45)
+    steps = []
+    for s in range(n_steps):
+        lens = np.array([L0 + s + 1 for L0 in start], dtype=np.int32)
+        q = W._draw_bf16(rng, (inp.B, inp.Hq, inp.D))
+        k_new = np.stack([inp.k[b, :, lens[b] - 1] for b in range(inp.B)])
+        v_new = np.stack([inp.v[b, :, lens[b] - 1] for b in range(inp.B)])
+        steps.append((lens, q, k_new, v_new))
+
+    def load(step):
+        lens, q, k_new, v_new = step
+        h_q.copy_(_as_bf16(q)); h_k.copy_(_as_bf16(k_new)); h_v.copy_(_as_bf16(v_new))
+        h_out.fill_(7.0)
+        sl.copy_(torch.from_numpy(lens))
+        torch.cuda.synchronize()
+
+    # one plain call first (the step-0 token, which the first replay writes again)
+    load(steps[0])
+    with torch.cuda.stream(cap):
+        call.run(*caches[0])
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        call.run(*caches[0])
+    deq_k = U.oracle_quantize(inp.k, inp.head_bits)[3]
+    deq_v = U.oracle_quantize(inp.v, inp.head_bits)[3]
+    for s, step in enumerate(steps):
+        lens, q, k_new, v_new = step
+        load(step)
+        graph.replay()
+        ref_out = kvq.decode_step(U.to_dev_bf16(q), U.to_dev_bf16(k_new), U.to_dev_bf16(v_new), *caches[1],
+                                  torch.from_numpy(lens).cuda(), inp.softmax_scale, status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0, s
+        got = h_out.numpy().copy()
+        assert np.array_equal(got, ref_out.cpu().numpy()), s
+        U.assert_close(got, O.decode_attention(q, deq_k, deq_v, lens, inp.softmax_scale), f"graph step {s}")
