@@ -157,6 +157,12 @@ def _cpu_entry(r: dict) -> dict:
     return {"value": r["value"], "unit": r["unit"], "cores": r["cores"], "kind": "oracle", "sample": r["sample"]}
 
 
+def _p95(xs):
+    """95th percentile of a few samples (nearest rank)."""
+    ys = sorted(xs)
+    return ys[min(len(ys) - 1, int(0.95 * len(ys) + 0.5) - 1)] if ys else float("nan")
+
+
 def max_over_ranks(torch, dist, value: float, device) -> float:
     """The largest of every rank's value (the job's time is its slowest rank's)."""
     if not dist:
@@ -568,6 +574,7 @@ def bench_prefill(torch, kvq, W, peaks, steps, warmup, dev, causal=True):
     t = statistics.mean(times)
     tf = flops / t / 1e12
     res = {"workload": inp.name, "value": tf, "unit": "TFLOP/s", "ms_per_step": t * 1e3,
+           "ms_median": statistics.median(times) * 1e3, "ms_p95": _p95(times) * 1e3,
            "algorithmic_flop": flops,
            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                         "frac": tf / peaks["bf16_tflops"], "peak_src": peaks["bf16_src"],
@@ -712,6 +719,7 @@ def main():
                "h2d_bytes_per_step": int(h_q.numel() * 2 + h_k.numel() * 2 + h_v.numel() * 2),
                "d2h_bytes_per_step": int(h_out.numel() * 2),
                "ms_per_step": te / args.steps * 1e3,
+               "us_median": statistics.median(et) * 1e6, "us_p95": _p95(et) * 1e6,
                "step": "one kvq_decode_step_host call from pinned host buffers: the append launch reads the "
                        "new K/V rows and q over the host link (quantise-on-write of K and V, q staged), the decode "
                        "launch writes the bf16 output into host memory; a repeated step's two launches are "
