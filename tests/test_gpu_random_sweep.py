@@ -1,0 +1,128 @@
+"""Seeded random configurations of quantise + decode and of prefill against
+the oracle: batch, query/KV head counts (every GQA ratio the calls accept),
+head dim, capacity, ragged lengths (0, 1, tile edges), per-head bit widths,
+masks, causal and non-causal, varlen and output dtype all drawn from the
+case's seed, at sizes where the oracle checks every output row.
+
+Codes, scales and zero points must equal the oracle's bit for bit;
+outputs must satisfy |o - ref| <= 2e-3 + 2e-3 |ref| (plus half a bf16 ulp
+of the result for bf16 output).
+"""
+import os
+
+import numpy as np
+import pytest
+
+from oracle import kvq_oracle as O
+import kvq_workloads as W
+from tests import kvq_testutil as U
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+# cases per test (more with KVQ_SWEEP_CASES for a longer search)
+N_CASES = int(os.environ.get("KVQ_SWEEP_CASES", "24"))
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from attention_group_quantized_gb300 import kvq as K
+    K.lib()
+    return K
+
+
+def _lens(rng, B, cap, tile):
+    """Ragged lengths with the edge cases mixed in: 0, 1, a tile edge, the capacity."""
+    special = [min(x, cap) for x in (0, 1, tile - 1, tile, tile + 1, cap)]
+    return [int(rng.choice(special)) if rng.random() < 0.5 else int(rng.integers(1, cap + 1)) for _ in range(B)]
+
+
+def _check_caches(kc, vc, inp, head_bits, lens):
+    for cache, x in ((kc, inp.k), (vc, inp.v)):
+        planes, scale, zero = U.read_cache(cache, inp.Tcap if hasattr(inp, "Tcap") else inp.S)
+        o_planes, o_scale, o_zero, deq = U.oracle_quantize(x, head_bits)
+        for b, L in enumerate(lens):
+            for h in range(len(head_bits)):
+                assert np.array_equal(planes[h][b, :L], o_planes[h][b, :L]), (b, h)
+            assert np.array_equal(scale[b, :, :L].view(np.uint16), o_scale[b, :, :L].view(np.uint16)), b
+            assert np.array_equal(zero[b, :, :L].view(np.uint16), o_zero[b, :, :L].view(np.uint16)), b
+
+
+@pytest.mark.parametrize("seed", range(N_CASES))
+def test_random_quantize_and_decode(kvq, seed):
+    rng = np.random.default_rng(1000 + seed)
+    B = int(rng.integers(1, 5))
+    Hkv = int(rng.choice([1, 2, 3, 4]))
+    rep = int(rng.choice([1, 2, 3, 4, 5, 8]))
+    D = int(rng.choice([64, 128]))
+    Tcap = 64 * int(rng.integers(1, 9))
+    lens = _lens(rng, B, Tcap, 64)
+    bits = str(rng.choice(["8", "4", "mixed"]))
+    out_dtype = int(rng.integers(0, 2))
+    inp = W.make_decode(f"sweep_decode_{seed}", 2000 + seed, B, Hkv * rep, Hkv, D, Tcap, lens=lens, bits=bits,
+                        outliers_per_head=int(rng.integers(0, 3)), outlier_head_mult=8.0)
+    kc = kvq.empty_cache(inp.head_bits, B, Tcap, D)
+    vc = kvq.empty_cache(inp.head_bits, B, Tcap, D)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq.quantize(U.to_dev_bf16(inp.k), kc, 0, st)
+    kvq.quantize(U.to_dev_bf16(inp.v), vc, 0, st)
+    out = kvq.decode_attention(U.to_dev_bf16(inp.q), kc, vc, torch.tensor(lens, dtype=torch.int32, device="cuda"),
+                               inp.softmax_scale, out_dtype=out_dtype, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    _check_caches(kc, vc, inp, inp.head_bits, [Tcap] * B)
+    deq_k = U.oracle_quantize(inp.k, inp.head_bits)[3]
+    deq_v = U.oracle_quantize(inp.v, inp.head_bits)[3]
+    ref = O.decode_attention(inp.q, deq_k, deq_v, np.asarray(lens, np.int32), inp.softmax_scale)
+    U.assert_close(out.float().cpu().numpy(), ref, f"sweep decode {seed} B{B} Hkv{Hkv} rep{rep} D{D} "
+                   f"T{Tcap} lens{lens} bits {list(inp.head_bits)}", out_bf16=out_dtype == 1)
+
+
+@pytest.mark.parametrize("seed", range(N_CASES))
+def test_random_prefill(kvq, seed):
+    rng = np.random.default_rng(3000 + seed)
+    B = int(rng.integers(1, 4))
+    Hkv = int(rng.choice([1, 2, 3]))
+    rep = int(rng.choice([1, 2, 3, 4, 5]))
+    D = int(rng.choice([64, 128]))
+    n_t = int(rng.integers(1, 5))
+    S = 128 * n_t
+    causal = bool(rng.random() < 0.6)
+    head_bits = np.asarray([8 if rng.random() < 0.5 else 4 for _ in range(Hkv)], np.int8)
+    varlen = bool(rng.random() < 0.5)
+    lens = _lens(rng, B, S, 128) if varlen else [S] * B
+    mask_kind = str(rng.choice(["none", "random"]))
+    out_dtype = int(rng.integers(0, 2))
+    inp = W.make_prefill(f"sweep_prefill_{seed}", 4000 + seed, B, Hkv * rep, Hkv, D, S, mask_seed=None)
+    if mask_kind == "random":
+        inp.tile_mask = (rng.random((n_t, n_t)) < 0.6).astype(np.uint8)
+    kc = kvq.empty_cache(head_bits, B, S, D)
+    vc = kvq.empty_cache(head_bits, B, S, D)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mask = torch.from_numpy(inp.tile_mask).cuda() if inp.tile_mask is not None else None
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda") if varlen else None
+    out = kvq.prefill_attention(U.to_dev_bf16(inp.q), U.to_dev_bf16(inp.k), U.to_dev_bf16(inp.v), kc, vc,
+                                inp.softmax_scale, mask, out_dtype=out_dtype, status=st, causal=causal, seq_lens=sl)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = out.float().cpu().numpy()
+    what = (f"sweep prefill {seed} B{B} Hkv{Hkv} rep{rep} D{D} S{S} causal={causal} lens{lens} "
+            f"mask={mask_kind} bits {list(head_bits)}")
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert np.all(got[b] == 0), what
+            continue
+        o_planes, o_scale, o_zero, kd = U.oracle_quantize(inp.k[b:b + 1, :, :L], head_bits)
+        vd = U.oracle_quantize(inp.v[b:b + 1, :, :L], head_bits)[3]
+        planes, scale, zero = U.read_cache(kc, L)
+        for h in range(Hkv):
+            assert np.array_equal(planes[h][b], o_planes[h][0]), (what, b, h)
+        assert np.array_equal(scale[b].view(np.uint16), o_scale[0].view(np.uint16)), (what, b)
+        assert np.array_equal(zero[b].view(np.uint16), o_zero[0].view(np.uint16)), (what, b)
+        for h in range(inp.Hq):
+            ref = O.prefill_rows(inp.q[b:b + 1, :, :L], kd, vd, 0, h, np.arange(L), inp.tile_mask,
+                                 inp.softmax_scale, causal=causal)
+            U.assert_close(got[b, h, :L], ref, f"{what} b={b} h={h}", out_bf16=out_dtype == 1)
+        assert np.all(got[b, :, L:] == 0), what
