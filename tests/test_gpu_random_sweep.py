@@ -126,3 +126,60 @@ def test_random_prefill(kvq, seed):
                                  inp.softmax_scale, causal=causal)
             U.assert_close(got[b, h, :L], ref, f"{what} b={b} h={h}", out_bf16=out_dtype == 1)
         assert np.all(got[b, :, L:] == 0), what
+
+
+@pytest.mark.parametrize("seed", range(N_CASES))
+def test_random_paged_decode_and_step(kvq, seed):
+    """Paged decode through a random block table (byte-equal to the contiguous
+    decode of the same data), then one decode step on contiguous caches whose
+    new-token rows held other values."""
+    rng = np.random.default_rng(5000 + seed)
+    B = int(rng.integers(1, 6))
+    Hkv = int(rng.choice([1, 2, 4]))
+    rep = int(rng.choice([1, 2, 4, 8]))
+    D = int(rng.choice([64, 128]))
+    max_pages = int(rng.integers(1, 6))
+    Tcap = 64 * max_pages
+    lens = [max(L, 1) for L in _lens(rng, B, Tcap, 64)]   # a step appends at len - 1
+    bits = str(rng.choice(["8", "4", "mixed"]))
+    inp = W.make_decode(f"sweep_paged_{seed}", 6000 + seed, B, Hkv * rep, Hkv, D, Tcap, lens=lens, bits=bits,
+                        outliers_per_head=int(rng.integers(0, 3)), outlier_head_mult=8.0)
+    what = f"sweep paged/step {seed} B{B} Hkv{Hkv} rep{rep} D{D} T{Tcap} lens{lens} bits {list(inp.head_bits)}"
+    n_pages = B * max_pages + int(rng.integers(0, 8))
+    table = rng.permutation(n_pages)[:B * max_pages].reshape(B, max_pages).astype(np.int32)
+    bt = torch.from_numpy(table).cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kp = kvq.empty_page_pool(inp.head_bits, n_pages, D)
+    vp = kvq.empty_page_pool(inp.head_bits, n_pages, D)
+    kvq.quantize_paged(U.to_dev_bf16(inp.k), kp, bt, 0, st)
+    kvq.quantize_paged(U.to_dev_bf16(inp.v), vp, bt, 0, st)
+    kc = kvq.empty_cache(inp.head_bits, B, Tcap, D)
+    vc = kvq.empty_cache(inp.head_bits, B, Tcap, D)
+    kvq.quantize(U.to_dev_bf16(inp.k), kc, 0, st)
+    kvq.quantize(U.to_dev_bf16(inp.v), vc, 0, st)
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    q = U.to_dev_bf16(inp.q)
+    paged = kvq.decode_attention_paged(q, kp, vp, bt, sl, inp.softmax_scale, status=st)
+    contiguous = kvq.decode_attention(q, kc, vc, sl, inp.softmax_scale, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, what
+    assert torch.equal(paged, contiguous), what
+    deq_k = U.oracle_quantize(inp.k, inp.head_bits)[3]
+    deq_v = U.oracle_quantize(inp.v, inp.head_bits)[3]
+    ref = O.decode_attention(inp.q, deq_k, deq_v, np.asarray(lens, np.int32), inp.softmax_scale)
+    U.assert_close(paged.cpu().numpy(), ref, what)
+    # the step: caches quantised from inputs whose row len - 1 held other values
+    stale_k, stale_v = inp.k.copy(), inp.v.copy()
+    for b, L in enumerate(lens):
+        for x in (stale_k, stale_v):
+            f = (rng.standard_normal((Hkv, D)) * 3.0).astype(np.float32)
+            x[b, :, L - 1] = (f.view(np.uint32) >> 16).astype(np.uint16)
+    kvq.quantize(U.to_dev_bf16(stale_k), kc, 0, st)
+    kvq.quantize(U.to_dev_bf16(stale_v), vc, 0, st)
+    k_new = np.stack([inp.k[b, :, lens[b] - 1] for b in range(B)])
+    v_new = np.stack([inp.v[b, :, lens[b] - 1] for b in range(B)])
+    out = kvq.decode_step(q, U.to_dev_bf16(k_new), U.to_dev_bf16(v_new), kc, vc, sl, inp.softmax_scale, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, what
+    assert torch.equal(out, contiguous), what   # the same cache contents as the contiguous decode above
+    _check_caches(kc, vc, inp, inp.head_bits, lens)
