@@ -374,7 +374,48 @@ def bench_extra_decodes(torch, kvq, W, peaks, dev, steps, warmup):
                          "frac_of_hbm_peak": round(gbs / peaks["hbm_gbs"], 4), "bytes_per_step": d["bytes"]}
         del d
         torch.cuda.empty_cache()
+    res["decode_tiny_with_quantize"] = time_tiny_with_quantize(torch, kvq, W, dev, steps, warmup)
     return res
+
+
+def time_tiny_with_quantize(torch, kvq, W, dev, steps, warmup):
+    """decode_tiny as its configuration states it: each step quantises the 512-token K and V into the
+    caches and then decodes (three launches), steps back to back in one CUDA graph."""
+    import numpy as np
+    inp = W.decode_tiny()
+    todev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    k, v, q = todev(inp.k), todev(inp.v), todev(inp.q)
+    kc = kvq.empty_cache(inp.head_bits, inp.B, inp.Tcap, inp.D, device=dev)
+    vc = kvq.empty_cache(inp.head_bits, inp.B, inp.Tcap, inp.D, device=dev)
+    sl = torch.from_numpy(inp.seq_lens).to(dev)
+    out = torch.empty((inp.B, inp.Hq, inp.D), dtype=torch.float32, device=dev)
+    ws = kvq.decode_workspace(inp.B, inp.Hq, inp.Hkv, inp.D, dev)
+
+    def step():
+        kvq.quantize(k, kc)
+        kvq.quantize(v, vc)
+        kvq.decode_attention(q, kc, vc, sl, inp.softmax_scale, out=out, workspace=ws)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(steps):
+            step()
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / steps
+    kv_bytes = 2 * inp.B * inp.Hkv * inp.Tcap * (inp.D + 4 * inp.D // 32)
+    q_bytes = 2 * (2 * inp.B * inp.Hkv * inp.Tcap * inp.D) + kv_bytes
+    return {"us_per_step": round(us, 2), "launches_per_step": 3,
+            "bytes_per_step": {"quantize": q_bytes, "decode": kv_bytes},
+            "note": "latency workload: quantise K and V (bf16 in, codes and scale/zero words out), then decode"}
 
 
 def bench_quantize(torch, kvq, inp, peaks, steps, warmup, dev):
