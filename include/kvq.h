@@ -15,9 +15,11 @@
  *
  * Conventions for every call:
  *   - Ownership: the caller owns every buffer.  The library never allocates or
- *     frees memory, never synchronises, and launches only on `stream`
- *     (a cudaStream_t; NULL = the legacy default stream).  All calls are
- *     asynchronous with respect to the host.
+ *     frees the caller's memory, never synchronises, and launches only on
+ *     `stream` (a cudaStream_t; NULL = the legacy default stream).  All calls
+ *     are asynchronous with respect to the host.  The one exception to "no
+ *     allocation" is kvq_decode_step_host, which keeps up to 16 CUDA graphs
+ *     (driver resources) to replay repeated steps; see that call.
  *   - Errors: argument problems are detected on the host; the call returns a
  *     status and launches nothing.  A failed launch returns KVQ_ERR_CUDA.
  *   - Device status: conditions only the device can see (non-finite input,
