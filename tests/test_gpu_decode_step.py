@@ -406,3 +406,35 @@ def test_decode_step_host_inside_a_captured_graph():
         got = h_out.numpy().copy()
         assert np.array_equal(got, ref_out.cpu().numpy()), s
         U.assert_close(got, O.decode_attention(q, deq_k, deq_v, lens, inp.softmax_scale), f"graph step {s}")
+
+
+def test_decode_step_host_more_repeated_steps_than_kept_graphs():
+    """More distinct repeated steps than the library keeps graphs for (16 per
+    process): the steps beyond that launch directly, and every result stays
+    byte-equal to kvq_decode_step on device copies of the same inputs."""
+    kvq = _kvq()
+    lens = [77, 128]
+    inp = W.make_decode("step_many_keys", 46, 2, 8, 2, 128, 128, lens=lens, bits="mixed",
+                        outliers_per_head=2, outlier_head_mult=8.0)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kc = kvq.empty_cache(inp.head_bits, inp.B, inp.Tcap, inp.D)
+    vc = kvq.empty_cache(inp.head_bits, inp.B, inp.Tcap, inp.D)
+    kvq.quantize(U.to_dev_bf16(inp.k), kc, 0, st)
+    kvq.quantize(U.to_dev_bf16(inp.v), vc, 0, st)
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    k_new = np.stack([inp.k[b, :, lens[b] - 1] for b in range(inp.B)])
+    v_new = np.stack([inp.v[b, :, lens[b] - 1] for b in range(inp.B)])
+    ref = kvq.decode_step(U.to_dev_bf16(inp.q), U.to_dev_bf16(k_new), U.to_dev_bf16(v_new), kc, vc, sl,
+                          inp.softmax_scale, status=st).cpu().numpy()
+    calls = []
+    for i in range(20):   # 20 distinct argument sets (own host buffers each)
+        h_q, h_k, h_v, h_out = _host_step_buffers(inp)
+        h_q.copy_(_as_bf16(inp.q)); h_k.copy_(_as_bf16(k_new)); h_v.copy_(_as_bf16(v_new))
+        calls.append((kvq.DecodeStepHost(h_q, h_k, h_v, sl, h_out, inp.softmax_scale, status=st), h_out))
+    for rnd in range(3):   # direct, captured (while there is room), replayed
+        for i, (call, h_out) in enumerate(calls):
+            h_out.fill_(7.0)
+            call.run(kc, vc)
+            torch.cuda.synchronize()
+            assert int(st.item()) == 0, (rnd, i)
+            assert np.array_equal(h_out.numpy(), ref), (rnd, i)
