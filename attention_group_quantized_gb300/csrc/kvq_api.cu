@@ -4,6 +4,7 @@
 // graphs that replay repeated host-buffer decode steps, at most 16 per
 // process); every launch goes to the caller's stream.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <cudaTypedefs.h>
@@ -15,16 +16,18 @@
 
 namespace kvq {
 
+// (Per-device values cached in atomics: host threads may race to fill an
+// entry, and they all store the same value.)
 int device_sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cached[dev] == 0) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
