@@ -183,3 +183,43 @@ def test_random_paged_decode_and_step(kvq, seed):
     assert int(st.item()) == 0, what
     assert torch.equal(out, contiguous), what   # the same cache contents as the contiguous decode above
     _check_caches(kc, vc, inp, inp.head_bits, lens)
+
+
+@pytest.mark.parametrize("seed", range(N_CASES))
+def test_random_head_error_stats_and_allocation(kvq, seed):
+    """Per-head error statistics (fixed summation order: the same bytes twice)
+    against the oracle, and the host allocator's choice from those statistics
+    against the oracle's allocation rule applied to the same statistics (near
+    ties between heads could order differently from the oracle's own
+    statistics within the 1e-5 tolerance)."""
+    rng = np.random.default_rng(7000 + seed)
+    B = int(rng.integers(1, 4))
+    H = int(rng.integers(1, 9))
+    D = int(rng.choice([64, 128]))
+    T = 64 * int(rng.integers(1, 9))
+    bits = int(rng.choice([4, 8]))
+    outliers = sorted(int(h) for h in rng.choice(H, int(rng.integers(0, H + 1)), replace=False))
+    ragged = bool(rng.random() < 0.5)
+    lens = _lens(rng, B, T, 64) if ragged else "full"
+    weighted = bool(rng.random() < 0.5)
+    inp = W.make_sensitivity(f"sweep_stats_{seed}", 8000 + seed, B, H, D, T, outliers, lens=lens, weights=weighted)
+    what = f"sweep stats {seed} B{B} H{H} D{D} T{T} bits{bits} outliers{outliers} lens{lens} weighted={weighted}"
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    sl = torch.from_numpy(inp.seq_lens).cuda() if ragged else None
+    w = torch.from_numpy(inp.weights).cuda() if weighted else None
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = []
+    for x in (inp.k, inp.v):
+        a = kvq.head_error_stats(dev(x), bits, seq_lens=sl, weights=w, status=st).cpu().numpy()
+        b = kvq.head_error_stats(dev(x), bits, seq_lens=sl, weights=w, status=st).cpu().numpy()
+        want = O.head_error_stats(x, bits, inp.seq_lens if ragged else None, inp.weights)
+        assert np.array_equal(a, b), what
+        assert np.allclose(a, want, rtol=1e-5, atol=1e-30), (what, a, want)
+        got.append((a, want))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, what
+    n_high = int(rng.integers(0, H + 1))
+    hb, _ = kvq.allocate_head_bits(torch.from_numpy(got[0][0]), torch.from_numpy(got[1][0]), n_high=n_high,
+                                   low_bits=4)
+    o_bits = O.allocate_head_bits(O.head_sensitivity(got[0][0], got[1][0]), n_high, 4)
+    assert np.array_equal(np.asarray(hb), np.asarray(o_bits)), (what, hb, o_bits)
