@@ -223,3 +223,18 @@ def test_random_head_error_stats_and_allocation(kvq, seed):
                                    low_bits=4)
     o_bits = O.allocate_head_bits(O.head_sensitivity(got[0][0], got[1][0]), n_high, 4)
     assert np.array_equal(np.asarray(hb), np.asarray(o_bits)), (what, hb, o_bits)
+
+
+@pytest.mark.parametrize("seed", range(N_CASES))
+def test_random_tile_mask(kvq, seed):
+    """The device mask builder against the oracle, bit for bit, over random grid
+    sizes (a single tile up to 700 tiles a side), skip ratios (none to all of the
+    candidates) and 64-bit seeds."""
+    rng = np.random.default_rng(9000 + seed)
+    nT = int(rng.choice([1, 2, 3, int(rng.integers(4, 129)), int(rng.integers(129, 701))]))
+    den = int(rng.integers(1, 21))
+    num = int(rng.integers(0, den + 1))
+    mseed = int(rng.integers(0, 1 << 62)) * 4 + int(rng.integers(0, 4))
+    got = kvq.build_tile_mask(nT, num, den, mseed).cpu().numpy()
+    torch.cuda.synchronize()
+    assert np.array_equal(got, O.build_tile_mask(nT, num, den, mseed)), (nT, num, den, mseed)
