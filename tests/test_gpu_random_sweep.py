@@ -238,3 +238,52 @@ def test_random_tile_mask(kvq, seed):
     got = kvq.build_tile_mask(nT, num, den, mseed).cpu().numpy()
     torch.cuda.synchronize()
     assert np.array_equal(got, O.build_tile_mask(nT, num, den, mseed)), (nT, num, den, mseed)
+
+
+@pytest.mark.parametrize("seed", range(N_CASES))
+def test_random_strided_quantize_into_a_window(kvq, seed):
+    """Quantise-on-write of a strided view (sequence, head or token strides
+    padded, or the head and token axes swapped in memory) into positions
+    [t0, t0 + nt) of a cache: those rows bit-exact against the oracle, every
+    other row of the cache untouched."""
+    rng = np.random.default_rng(11000 + seed)
+    B = int(rng.integers(1, 4))
+    Hkv = int(rng.integers(1, 5))
+    D = int(rng.choice([64, 128]))
+    Tcap = 64 * int(rng.integers(1, 5))
+    t0 = int(rng.integers(0, Tcap))
+    nt = int(rng.integers(1, Tcap - t0 + 1))
+    head_bits = np.asarray([8 if rng.random() < 0.5 else 4 for _ in range(Hkv)], np.int8)
+    full = W.make_decode(f"sweep_quant_{seed}", 12000 + seed, B, Hkv, Hkv, D, nt, lens="full",
+                         outliers_per_head=int(rng.integers(0, 3)), outlier_head_mult=8.0).k   # [B][Hkv][nt][D]
+    layout = str(rng.choice(["contiguous", "padded", "heads_inner"]))
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    if layout == "contiguous":
+        xv = dev(full)
+    elif layout == "padded":   # every stride padded by a multiple of 8 elements
+        pad = dev(np.zeros((B, Hkv + 1, nt + 3, D + 8 * int(rng.integers(1, 3))), np.uint16))
+        pad[:, :Hkv, :nt, :D] = dev(full)
+        xv = pad[:, :Hkv, :nt, :D]
+    else:                      # memory order [B][T][Hkv][D]
+        xv = dev(np.ascontiguousarray(full.transpose(0, 2, 1, 3))).permute(0, 2, 1, 3)
+    kc = kvq.empty_cache(head_bits, B, Tcap, D)
+    kc.codes.fill_(0x5A)
+    kc.sz.fill_(0x1234567)
+    codes0, sz0 = kc.codes.clone(), kc.sz.clone()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq.quantize(xv, kc, t0, st)
+    torch.cuda.synchronize()
+    what = f"sweep quantize {seed} B{B} Hkv{Hkv} D{D} Tcap{Tcap} t0={t0} nt={nt} {layout} bits {list(head_bits)}"
+    assert int(st.item()) == 0, what
+    planes, scale, zero = U.read_cache(kc, Tcap)
+    p0, s0, z0 = U.read_cache(kvq.QuantCache(codes0, sz0, head_bits, B, Hkv, Tcap, D), Tcap)
+    o_planes, o_scale, o_zero, _ = U.oracle_quantize(full, head_bits)
+    for h in range(Hkv):
+        assert np.array_equal(planes[h][:, t0:t0 + nt], o_planes[h]), (what, h)
+        assert np.array_equal(planes[h][:, :t0], p0[h][:, :t0]), (what, h)
+        assert np.array_equal(planes[h][:, t0 + nt:], p0[h][:, t0 + nt:]), (what, h)
+    assert np.array_equal(scale[:, :, t0:t0 + nt].view(np.uint16), o_scale.view(np.uint16)), what
+    assert np.array_equal(zero[:, :, t0:t0 + nt].view(np.uint16), o_zero.view(np.uint16)), what
+    for a, b in ((scale, s0), (zero, z0)):
+        assert np.array_equal(a[:, :, :t0].view(np.uint16), b[:, :, :t0].view(np.uint16)), what
+        assert np.array_equal(a[:, :, t0 + nt:].view(np.uint16), b[:, :, t0 + nt:].view(np.uint16)), what
